@@ -1,0 +1,309 @@
+"""Plain, slow, float64 oracle of the gpt-oss-style routed MoE expert chain.
+
+TEST INFRASTRUCTURE ONLY. Nothing in the library imports this module; only
+the tests, the smoke check and the benchmark's CPU-baseline leg do.
+
+What it computes, and where each step is defined:
+
+* MXFP4 weights: 32-element blocks of E2M1 codes sharing one E8M0 exponent
+  byte ("dasLLAMA: dig the last two board reds green", section "gpt-oss: mx4
+  kernels to the lab-winning shape": the 16-value E2M1 table and the E8M0
+  exponent decode). A value is E2M1[q] * 2**(s - 127). Inside a block, byte i
+  holds element i in its low nibble and element i + 16 in its high nibble
+  (the low/high nibble split of the mx4 dot in "dasLLAMA gpt-oss arc", commit
+  "dot_mx4q8_template rewritten in plain das").
+* Router: logits over the E experts, the top k taken (descending logit,
+  lower expert index first on equal logits), then a softmax over the k taken.
+* Bucket: a CSR of the T*k (token, slot) assignments grouped by expert, each
+  expert's row range padded to a tile height, with the padded prefix
+  ``basep`` ("dasLLAMA gpt-oss arc", Metal fusion lane commit, third bullet:
+  the prefix folded into MetalMoeBucket, bit-identical CSR).
+* Expert FFN: gate and up projections with bias (the bias seeds the
+  accumulator in the pages' kernels, Metal fusion lane commit, first bullet;
+  here it is simply added), swiglu_oai, down projection with bias.
+* Combine: the router-weighted sum over the k slots, in slot order
+  ("dasLLAMA gpt-oss arc", fused MoE expert chain commit: stage 1 sums the
+  experts' down rows "in slot order").
+
+Readings where the pages are silent are listed in the design doc; the ones that
+change arithmetic are noted beside the function that takes them.
+
+Every function here is pinned by a test in tests/test_oracle_pins.py against
+something other than itself (the printed E2M1 table, math.ldexp, brute force
+in oracle/brute.py, closed forms and invariants).
+"""
+
+from __future__ import annotations
+
+import math
+from typing import Dict, Optional, Tuple
+
+import numpy as np
+
+SWIGLU_ALPHA = 1.702
+SWIGLU_LIMIT = 7.0
+
+
+# ----------------------------------------------------------------------------
+# MXFP4 element and scale decoding
+# ----------------------------------------------------------------------------
+
+def e2m1_value(code: int) -> float:
+    """Value of a 4-bit E2M1 code: 1 sign bit, 2 exponent bits (bias 1), 1 mantissa bit.
+
+    Exponent field 0 is subnormal (m * 0.5). Code 8 is negative zero.
+    """
+    code = int(code) & 0xF
+    sign = -1.0 if code & 0x8 else 1.0
+    e = (code >> 1) & 0x3
+    m = code & 0x1
+    if e == 0:
+        mag = 0.5 * m
+    else:
+        mag = 2.0 ** (e - 1) * (1.0 + 0.5 * m)
+    return sign * mag
+
+
+E2M1_LUT = np.array([e2m1_value(c) for c in range(16)], dtype=np.float64)
+
+
+def e8m0_value(s: int) -> float:
+    """Value of an E8M0 scale byte: 2**(s - 127); byte 255 is NaN."""
+    s = int(s)
+    if s == 255:
+        return float("nan")
+    return math.ldexp(1.0, s - 127)
+
+
+E8M0_LUT = np.array([e8m0_value(s) for s in range(256)], dtype=np.float64)
+
+
+def dequant_mxfp4(qs: np.ndarray, sc: np.ndarray) -> np.ndarray:
+    """Dequantise an MXFP4 matrix stored as planes qs [R, C/2] and sc [R, C/32] to float64 [R, C]."""
+    qs = np.asarray(qs, dtype=np.uint8)
+    sc = np.asarray(sc, dtype=np.uint8)
+    R, half = qs.shape
+    C = half * 2
+    nb = C // 32
+    assert sc.shape == (R, nb)
+    blocks = qs.reshape(R, nb, 16)
+    low = E2M1_LUT[blocks & 0x0F]          # block elements 0..15
+    high = E2M1_LUT[blocks >> 4]           # block elements 16..31
+    vals = np.concatenate([low, high], axis=2)  # [R, nb, 32]
+    vals = vals * E8M0_LUT[sc][:, :, None]
+    return vals.reshape(R, C)
+
+
+# ----------------------------------------------------------------------------
+# Router: logits, top-k, softmax over the selected k
+# ----------------------------------------------------------------------------
+
+def router_logits(x: np.ndarray, w_router: np.ndarray, b_router: Optional[np.ndarray]) -> np.ndarray:
+    """l[t, e] = sum_i x[t, i] * Wr[e, i] + br[e], in float64 from the float32 inputs."""
+    l = np.asarray(x, np.float64) @ np.asarray(w_router, np.float64).T
+    if b_router is not None:
+        l = l + np.asarray(b_router, np.float64)[None, :]
+    return l
+
+
+def topk_softmax(logits: np.ndarray, k: int) -> Tuple[np.ndarray, np.ndarray]:
+    """Top-k experts per token (descending logit, lower index first on ties), then softmax over them.
+
+    Returns ids int32 [T, k] in slot order and weights float64 [T, k].
+    """
+    logits = np.asarray(logits, np.float64)
+    T, E = logits.shape
+    ids = np.empty((T, k), dtype=np.int32)
+    w = np.empty((T, k), dtype=np.float64)
+    for t in range(T):
+        order = sorted(range(E), key=lambda e: (-logits[t, e], e))[:k]
+        ids[t] = order
+        sel = logits[t, order]
+        ex = np.exp(sel - sel[0])  # sel[0] is the largest
+        w[t] = ex / ex.sum()
+    return ids, w
+
+
+# ----------------------------------------------------------------------------
+# Bucket: CSR grouped by expert with a tile-padded prefix
+# ----------------------------------------------------------------------------
+
+def bucket_max_rows(T: int, k: int, E: int, tile: int) -> int:
+    """Worst-case padded row count T*k + E*(tile-1), rounded up to a whole tile."""
+    n = T * k + E * (tile - 1)
+    return ((n + tile - 1) // tile) * tile
+
+
+def bucket_csr(ids: np.ndarray, E: int, tile: int) -> Dict[str, np.ndarray]:
+    """CSR of the (token, slot) assignments grouped by expert.
+
+    counts[e]      number of assignments to expert e
+    basep[e]       padded prefix: sum over e' < e of ceil(counts[e']/tile)*tile; basep[E] = mpad
+    rows[p]        for p in [basep[e], basep[e] + counts[e]): the assignment index t*k + j,
+                   in ascending order; -1 for pad rows and for every p >= mpad
+    inv[t*k + j]   the row position p of that assignment (-1 if its id is out of range)
+    """
+    ids = np.asarray(ids, dtype=np.int64)
+    T, k = ids.shape
+    flat = ids.reshape(-1)
+    counts = np.zeros(E, dtype=np.int32)
+    for a in range(T * k):
+        e = flat[a]
+        if 0 <= e < E:
+            counts[e] += 1
+    basep = np.zeros(E + 1, dtype=np.int32)
+    for e in range(E):
+        basep[e + 1] = basep[e] + ((counts[e] + tile - 1) // tile) * tile
+    rows = np.full(bucket_max_rows(T, k, E, tile), -1, dtype=np.int32)
+    inv = np.full(T * k, -1, dtype=np.int32)
+    fill = np.zeros(E, dtype=np.int64)
+    for a in range(T * k):
+        e = flat[a]
+        if 0 <= e < E:
+            p = basep[e] + fill[e]
+            rows[p] = a
+            inv[a] = p
+            fill[e] += 1
+    return dict(counts=counts, basep=basep, rows=rows, inv=inv)
+
+
+# ----------------------------------------------------------------------------
+# Activation
+# ----------------------------------------------------------------------------
+
+def sigmoid(z: np.ndarray) -> np.ndarray:
+    """Logistic function evaluated without overflow: 1/(1+e^-z) for z >= 0, e^z/(1+e^z) otherwise."""
+    z = np.asarray(z, np.float64)
+    out = np.empty_like(z)
+    pos = z >= 0
+    out[pos] = 1.0 / (1.0 + np.exp(-z[pos]))
+    ez = np.exp(z[~pos])
+    out[~pos] = ez / (1.0 + ez)
+    return out
+
+
+def swiglu_oai(g: np.ndarray, u: np.ndarray, alpha: float = SWIGLU_ALPHA,
+               limit: float = SWIGLU_LIMIT) -> np.ndarray:
+    """min(g, limit) * sigmoid(alpha * min(g, limit)) * (clamp(u, -limit, limit) + 1)."""
+    g = np.minimum(np.asarray(g, np.float64), limit)
+    u = np.clip(np.asarray(u, np.float64), -limit, limit)
+    return g * sigmoid(alpha * g) * (u + 1.0)
+
+
+# ----------------------------------------------------------------------------
+# bfloat16 rounding (operand precision of the prefill rail's tensor-core MMAs)
+# ----------------------------------------------------------------------------
+
+def round_bf16(a: np.ndarray) -> np.ndarray:
+    """Round to the nearest bfloat16 (ties to even), returned as float64.
+
+    The value is first taken to float32 (the operands arrive as float32 in
+    this layer), then its low 16 bits are rounded away.
+    """
+    f = np.asarray(a, dtype=np.float32)
+    bits = f.view(np.uint32).astype(np.uint64)
+    lsb = (bits >> 16) & 1
+    rounded = (bits + 0x7FFF + lsb) & 0xFFFF0000
+    nan = np.isnan(f)
+    out = rounded.astype(np.uint32).view(np.float32).astype(np.float64)
+    out[nan] = np.nan
+    return out
+
+
+# ----------------------------------------------------------------------------
+# Projections and the expert FFN
+# ----------------------------------------------------------------------------
+
+def mxfp4_gemv(qs: np.ndarray, sc: np.ndarray, x: np.ndarray, bias: Optional[np.ndarray]) -> np.ndarray:
+    """out = W x + bias for one MXFP4 matrix W [R, C] and vector(s) x [..., C]."""
+    W = dequant_mxfp4(qs, sc)
+    out = np.asarray(x, np.float64) @ W.T
+    if bias is not None:
+        out = out + np.asarray(bias, np.float64)
+    return out
+
+
+def expert_ffn(x_rows: np.ndarray, Wg: np.ndarray, bg, Wu: np.ndarray, bu, Wd: np.ndarray, bd,
+               operands: str = "f64") -> np.ndarray:
+    """One expert on a batch of token rows, with dequantised float64 weights.
+
+    g = Wg x + bg, u = Wu x + bu, h = swiglu_oai(g, u), o = Wd h + bd.
+    With operands="bf16" the token rows and h are rounded to bfloat16 before
+    their projections (the prefill rail's MMA operand precision); the weights
+    are exact in bfloat16 already.
+    """
+    x = np.asarray(x_rows, np.float64)
+    if operands == "bf16":
+        x = round_bf16(x)
+    g = x @ Wg.T + (0.0 if bg is None else np.asarray(bg, np.float64))
+    u = x @ Wu.T + (0.0 if bu is None else np.asarray(bu, np.float64))
+    h = swiglu_oai(g, u)
+    if operands == "bf16":
+        h = round_bf16(h)
+    return h @ Wd.T + (0.0 if bd is None else np.asarray(bd, np.float64))
+
+
+class ExpertCache:
+    """Dequantises each expert's three matrices on first use (float64)."""
+
+    def __init__(self, layer: Dict[str, np.ndarray]):
+        self.layer = layer
+        self._cache: Dict[int, Tuple[np.ndarray, np.ndarray, np.ndarray]] = {}
+
+    def __call__(self, e: int):
+        if e not in self._cache:
+            L = self.layer
+            self._cache[e] = (dequant_mxfp4(L["g_qs"][e], L["g_sc"][e]),
+                              dequant_mxfp4(L["u_qs"][e], L["u_sc"][e]),
+                              dequant_mxfp4(L["d_qs"][e], L["d_sc"][e]))
+        return self._cache[e]
+
+
+def moe_layer(layer: Dict[str, np.ndarray], x: np.ndarray, k: int, token_idx=None,
+              operands: str = "f64", ids: Optional[np.ndarray] = None,
+              weights: Optional[np.ndarray] = None, cache: Optional[ExpertCache] = None):
+    """The full layer for the tokens in ``token_idx`` (all tokens by default).
+
+    Returns (y [n, D] float64, ids [T, k], weights [T, k], logits [T, E]).
+    ``ids``/``weights`` may be given to evaluate the experts under a fixed
+    routing (used when a near-tie makes the routing ambiguous).
+    """
+    x = np.asarray(x, np.float32)
+    T = x.shape[0]
+    logits = router_logits(x, layer["w_router"], layer.get("b_router"))
+    if ids is None:
+        ids, weights = topk_softmax(logits, k)
+    if token_idx is None:
+        token_idx = np.arange(T)
+    cache = cache or ExpertCache(layer)
+    D = layer["d_qs"].shape[1]
+    y = np.zeros((len(token_idx), D), dtype=np.float64)
+    for n, t in enumerate(token_idx):
+        for j in range(k):  # slot order
+            e = int(ids[t, j])
+            Wg, Wu, Wd = cache(e)
+            o = expert_ffn(x[t:t + 1], Wg, layer["bg"][e], Wu, layer["bu"][e], Wd, layer["bd"][e],
+                           operands=operands)[0]
+            y[n] += float(weights[t, j]) * o
+    return y, ids, weights, logits
+
+
+# ----------------------------------------------------------------------------
+# Comparison helpers used by the tests
+# ----------------------------------------------------------------------------
+
+def rownorm_rel_err(y: np.ndarray, y_ref: np.ndarray, floor: float = 1e-3) -> np.ndarray:
+    """Per row t: max_c |y - y_ref| / max(max_c |y_ref|, floor)."""
+    y = np.asarray(y, np.float64)
+    y_ref = np.asarray(y_ref, np.float64)
+    num = np.abs(y - y_ref).max(axis=-1)
+    den = np.maximum(np.abs(y_ref).max(axis=-1), floor)
+    return num / den
+
+
+def routing_margins(logits: np.ndarray, k: int) -> np.ndarray:
+    """Smallest gap, per token, among the sorted top k+1 logits (the tie guard of the router test)."""
+    s = -np.sort(-np.asarray(logits, np.float64), axis=1)
+    kk = min(k + 1, s.shape[1])
+    gaps = s[:, :kk - 1] - s[:, 1:kk]
+    return gaps.min(axis=1) if gaps.shape[1] else np.full(s.shape[0], np.inf)

@@ -1,0 +1,151 @@
+"""Negative controls for the oracle's pins: a planted mistake must turn the pin red.
+
+Each mutation is built on the CPU from a copy of an oracle function; the
+oracle module itself is never modified.
+"""
+
+import numpy as np
+
+from oracle import moe_oracle as O
+from tests.test_oracle_pins import (
+    check_bias_linearity,
+    check_bucket_vs_brute,
+    check_dequant_vs_brute,
+    check_e2m1,
+    check_layer_vs_brute,
+    check_swiglu_points,
+    check_topk_vs_brute,
+)
+
+
+def test_pins_pass_on_the_real_oracle():
+    assert check_e2m1(O.e2m1_value)
+    assert check_dequant_vs_brute(O.dequant_mxfp4)
+    assert check_topk_vs_brute(O.topk_softmax)
+    assert check_bucket_vs_brute(O.bucket_csr)
+    assert check_swiglu_points(O.swiglu_oai)
+
+
+def test_e2m1_subnormal_mistake_is_caught():
+    def bad(code):  # treats exponent field 0 as normal
+        code &= 0xF
+        sign = -1.0 if code & 8 else 1.0
+        e, m = (code >> 1) & 3, code & 1
+        return sign * 2.0 ** (e - 1) * (1 + 0.5 * m)
+    assert not check_e2m1(bad)
+
+
+def test_swapped_nibbles_are_caught():
+    def bad(qs, sc):
+        swapped = ((qs & 0x0F) << 4) | (qs >> 4)
+        return O.dequant_mxfp4(swapped.astype(np.uint8), sc)
+    assert not check_dequant_vs_brute(bad)
+
+
+def test_interleaved_nibbles_are_caught():
+    # Reading low/high nibbles as adjacent columns (2i, 2i+1) instead of (i, i+16).
+    def bad(qs, sc):
+        R, half = qs.shape
+        lo = O.E2M1_LUT[qs & 0x0F]
+        hi = O.E2M1_LUT[qs >> 4]
+        vals = np.stack([lo, hi], axis=-1).reshape(R, half * 2)
+        return vals * np.repeat(O.E8M0_LUT[sc], 32, axis=1)
+    assert not check_dequant_vs_brute(bad)
+
+
+def test_scale_off_by_one_is_caught():
+    def bad(qs, sc):
+        return O.dequant_mxfp4(qs, sc) * 2.0
+    assert not check_dequant_vs_brute(bad)
+
+
+def test_tie_break_mistake_is_caught():
+    def bad(logits, k):
+        T, E = logits.shape
+        ids = np.empty((T, k), np.int32)
+        w = np.empty((T, k))
+        for t in range(T):
+            order = sorted(range(E), key=lambda e: (-logits[t, e], -e))[:k]  # higher index first
+            ids[t] = order
+            ex = np.exp(logits[t, order] - logits[t, order[0]])
+            w[t] = ex / ex.sum()
+        return ids, w
+    assert not check_topk_vs_brute(bad)
+
+
+def test_softmax_over_all_experts_is_caught():
+    def bad(logits, k):
+        ids, _ = O.topk_softmax(logits, k)
+        ex = np.exp(logits - logits.max(axis=1, keepdims=True))
+        full = ex / ex.sum(axis=1, keepdims=True)
+        return ids, np.take_along_axis(full, ids.astype(np.int64), axis=1)
+    assert not check_topk_vs_brute(bad)
+
+
+def test_unpadded_prefix_is_caught():
+    def bad(ids, E, tile):
+        out = O.bucket_csr(ids, E, 1)  # forgets the tile padding
+        mr = O.bucket_max_rows(ids.shape[0], ids.shape[1], E, tile)
+        rows = np.full(mr, -1, np.int32)
+        rows[:len(out["rows"])] = out["rows"][:mr]
+        out["rows"] = rows
+        return out
+    assert not check_bucket_vs_brute(bad)
+
+
+def test_descending_bucket_order_is_caught():
+    def bad(ids, E, tile):
+        out = O.bucket_csr(ids, E, tile)
+        rows = out["rows"].copy()
+        for e in range(E):
+            s, n = out["basep"][e], out["counts"][e]
+            rows[s:s + n] = rows[s:s + n][::-1]
+        out["rows"] = rows
+        return out
+    assert not check_bucket_vs_brute(bad)
+
+
+def test_swiglu_missing_plus_one_is_caught():
+    def bad(g, u):
+        g = np.minimum(g, 7.0)
+        return g * O.sigmoid(1.702 * g) * np.clip(u, -7, 7)
+    assert not check_swiglu_points(bad)
+
+
+def test_swiglu_two_sided_gate_clamp_is_caught():
+    def bad(g, u):
+        g = np.clip(g, -7.0, 7.0)
+        return g * O.sigmoid(1.702 * g) * (np.clip(u, -7, 7) + 1)
+    assert not check_swiglu_points(bad)
+
+
+def test_dropped_down_bias_is_caught():
+    def bad(layer, x, k, **kw):
+        L = dict(layer)
+        L["bd"] = np.zeros_like(layer["bd"])
+        return O.moe_layer(L, x, k, **kw)
+    assert not check_bias_linearity(bad)
+    assert not check_layer_vs_brute(bad)
+
+
+def test_transposed_down_projection_is_caught():
+    # Uses the down matrix as if stored [F, D] (square shapes make it type-check).
+    def bad(layer, x, k, **kw):
+        L = dict(layer)
+        E = layer["d_qs"].shape[0]
+        full = np.stack([O.dequant_mxfp4(layer["d_qs"][e], layer["d_sc"][e]).T for e in range(E)])
+
+        class Cache(O.ExpertCache):
+            def __call__(self, e):
+                g, u, _ = super().__call__(e)
+                return g, u, full[e]
+        return O.moe_layer(L, x, k, cache=Cache(L), **kw)
+    assert not check_layer_vs_brute(bad)
+
+
+def test_unweighted_combine_is_caught():
+    def bad(layer, x, k, **kw):
+        y, ids, w, logits = O.moe_layer(layer, x, k, **kw)
+        y2, _, _, _ = O.moe_layer(layer, x, k, ids=ids, weights=np.ones_like(w))
+        return y2, ids, w, logits
+    assert not check_layer_vs_brute(bad)

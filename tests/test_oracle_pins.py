@@ -1,0 +1,372 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Each check is a plain function taking the oracle functions it exercises as
+arguments, so tests/test_oracle_mutations.py can hand it a copy with a planted
+mistake and see it fail.
+"""
+
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import brute
+from oracle import moe_oracle as O
+from synthetic import make_layer, spec_for
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def load_e2m1_golden():
+    vals = {}
+    with open(os.path.join(GOLDEN, "e2m1_table.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            c, v = line.split()
+            vals[int(c)] = float(v)
+    assert sorted(vals) == list(range(16))
+    return vals
+
+
+def tiny_planes(rng, R, C, s_lo=120, s_hi=130):
+    qs = rng.integers(0, 256, size=(R, C // 2), dtype=np.uint8)
+    sc = rng.integers(s_lo, s_hi + 1, size=(R, C // 32), dtype=np.uint8)
+    return qs, sc
+
+
+# ---------------------------------------------------------------------------
+# reusable checks (return True when the pin holds)
+# ---------------------------------------------------------------------------
+
+def check_e2m1(e2m1_value):
+    gold = load_e2m1_golden()
+    for c in range(16):
+        v = e2m1_value(c)
+        if v != gold[c] or math.copysign(1.0, v) != math.copysign(1.0, gold[c]):
+            return False
+    return True
+
+
+def check_dequant_vs_brute(dequant, seed=0):
+    rng = np.random.default_rng(seed)
+    for R, C in [(3, 32), (5, 64), (2, 96)]:
+        qs, sc = tiny_planes(rng, R, C)
+        ref = np.array(brute.dequant(qs.tolist(), sc.tolist()))
+        got = dequant(qs, sc)
+        if got.shape != ref.shape or not np.array_equal(got, ref):
+            return False
+    return True
+
+
+def check_topk_vs_brute(topk_softmax, seed=1):
+    rng = np.random.default_rng(seed)
+    for E, k in [(4, 2), (6, 3), (5, 5), (8, 1)]:
+        # integer-valued logits make exact ties frequent
+        logits = rng.integers(-3, 4, size=(40, E)).astype(np.float64)
+        logits[::3] += rng.standard_normal((len(logits[::3]), E))
+        ids, w = topk_softmax(logits, k)
+        for t in range(len(logits)):
+            bid, bw = brute.topk(logits[t].tolist(), k)
+            if list(ids[t]) != bid or not np.allclose(w[t], bw, rtol=1e-14, atol=0):
+                return False
+    return True
+
+
+def check_bucket_vs_brute(bucket_csr, seed=2):
+    rng = np.random.default_rng(seed)
+    for T, k, E, tile in [(8, 2, 4, 4), (13, 3, 5, 16), (1, 4, 32, 128), (40, 4, 6, 1), (0, 2, 3, 4)]:
+        ids = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]) if T else \
+            np.zeros((0, k), np.int64)
+        got = bucket_csr(ids, E, tile)
+        counts, basep, rows, inv = brute.bucket(ids.tolist(), E, tile, k=k)
+        mpad = basep[-1]
+        if list(got["counts"]) != counts or list(got["basep"]) != basep:
+            return False
+        if list(got["rows"][:mpad]) != rows or not np.all(got["rows"][mpad:] == -1):
+            return False
+        if list(got["inv"]) != inv:
+            return False
+    return True
+
+
+def check_swiglu_points(swiglu_oai):
+    a = O.SWIGLU_ALPHA
+    sig = lambda z: 1.0 / (1.0 + math.exp(-z))  # noqa: E731  (z >= 0 here)
+    cases = [
+        # (g, u, expected)
+        (9.0, 0.5, 7.0 * sig(7.0 * a) * 1.5),        # g clamped at 7 from above
+        (7.0, 100.0, 7.0 * sig(7.0 * a) * 8.0),      # u clamped at +7
+        (0.0, 3.0, 0.0),                              # g = 0 -> 0
+        (2.5, -1.0, 0.0),                             # u = -1 -> 0
+        (1.0, -50.0, 1.0 * sig(a) * -6.0),           # u clamped at -7 -> factor -6
+        (1.0, 0.0, sig(a)),                           # plain point
+        (-0.5, 2.0, -0.5 * (1.0 - sig(0.5 * a)) * 3.0),
+    ]
+    for g, u, exp in cases:
+        got = float(swiglu_oai(np.array([g]), np.array([u]))[0])
+        if not math.isclose(got, exp, rel_tol=1e-14, abs_tol=1e-300):
+            return False
+    # very negative g: tends to -0, never NaN
+    got = swiglu_oai(np.array([-1e4, -800.0]), np.array([0.0, 5.0]))
+    if np.any(np.isnan(got)) or np.any(np.abs(got) > 1e-300):
+        return False
+    return True
+
+
+def check_layer_vs_brute(moe_layer, seed_layer=0):
+    spec = spec_for(0)
+    L = make_layer(spec, layer=seed_layer)
+    y, ids, w, _ = moe_layer(L, L["x"], spec.k)
+    by, bids, bw = brute.layer(L, L["x"], spec.k)
+    if [list(r) for r in ids] != bids:
+        return False
+    by = np.array(by)
+    return bool(np.max(O.rownorm_rel_err(y, by, floor=1e-300)) < 1e-12)
+
+
+def check_bias_linearity(moe_layer):
+    spec = spec_for(0)
+    L = make_layer(spec, layer=3)
+    L0 = dict(L)
+    L0["bd"] = np.zeros_like(L["bd"])
+    y1, ids, w, _ = moe_layer(L, L["x"], spec.k)
+    y0, _, _, _ = moe_layer(L0, L["x"], spec.k)
+    expect = np.einsum("tj,tjd->td", w, L["bd"].astype(np.float64)[ids])
+    return bool(np.allclose(y1 - y0, expect, rtol=1e-9, atol=1e-12 * np.abs(y1).max()))
+
+
+# ---------------------------------------------------------------------------
+# tests
+# ---------------------------------------------------------------------------
+
+def test_e2m1_matches_printed_table():
+    assert check_e2m1(O.e2m1_value)
+    assert np.array_equal(O.E2M1_LUT, np.array([load_e2m1_golden()[c] for c in range(16)]))
+
+
+def test_e8m0_exhaustive():
+    # 2**(s-127) against math.ldexp, and against the float32 exponent-field bitcast
+    # (s << 23) that the pages' ALU decode uses, for every byte 1..254; byte 0 is
+    # the float32 denormal 2**-127 (bit pattern 0x00400000); 255 is NaN.
+    for s in range(255):
+        v = O.e8m0_value(s)
+        assert v == math.ldexp(1.0, s - 127)
+        bits = (s << 23) if s >= 1 else 0x00400000
+        f32 = np.array([bits], dtype=np.uint32).view(np.float32)[0]
+        assert float(f32) == v
+    assert math.isnan(O.e8m0_value(255))
+
+
+def test_dequant_matches_brute_force():
+    assert check_dequant_vs_brute(O.dequant_mxfp4)
+
+
+def test_dequant_nibble_layout_closed_form():
+    # One row, one block: byte i = (code_hi << 4) | code_lo with chosen codes.
+    qs = np.zeros((1, 16), np.uint8)
+    qs[0, 0] = (7 << 4) | 1      # col 0 -> 0.5, col 16 -> 6
+    qs[0, 5] = (10 << 4) | 3     # col 5 -> 1.5, col 21 -> -1
+    qs[0, 15] = (0 << 4) | 15    # col 15 -> -6, col 31 -> 0
+    sc = np.array([[128]], np.uint8)   # scale 2
+    W = O.dequant_mxfp4(qs, sc)[0]
+    expect = np.zeros(32)
+    expect[0], expect[16] = 1.0, 12.0
+    expect[5], expect[21] = 3.0, -2.0
+    expect[15], expect[31] = -12.0, 0.0
+    assert np.array_equal(W, expect)
+
+
+def test_router_logits_match_loops():
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((3, 7)).astype(np.float32)
+    wr = rng.standard_normal((4, 7)).astype(np.float32)
+    br = rng.standard_normal(4).astype(np.float32)
+    got = O.router_logits(x, wr, br)
+    for t in range(3):
+        for e in range(4):
+            ref = sum(float(x[t, i]) * float(wr[e, i]) for i in range(7)) + float(br[e])
+            assert math.isclose(got[t, e], ref, rel_tol=1e-13, abs_tol=1e-13)
+
+
+def test_topk_matches_brute_force():
+    assert check_topk_vs_brute(O.topk_softmax)
+
+
+def test_topk_invariants():
+    rng = np.random.default_rng(6)
+    logits = rng.standard_normal((200, 32)) * 5
+    ids, w = O.topk_softmax(logits, 4)
+    assert np.allclose(w.sum(axis=1), 1.0, rtol=0, atol=1e-15)
+    assert np.all(np.diff(w, axis=1) <= 0)
+    assert all(len(set(r)) == 4 for r in ids.tolist())
+    # the chosen logits are the 4 largest
+    assert np.allclose(np.sort(logits, axis=1)[:, ::-1][:, :4], np.take_along_axis(logits, ids, 1))
+
+
+def test_topk_all_equal_k_equals_E():
+    ids, w = O.topk_softmax(np.zeros((3, 5)), 5)
+    assert np.array_equal(ids, np.tile(np.arange(5), (3, 1)))
+    assert np.array_equal(w, np.full((3, 5), 0.2))
+
+
+def test_bucket_matches_brute_force():
+    assert check_bucket_vs_brute(O.bucket_csr)
+
+
+@pytest.mark.parametrize("tile", [1, 4, 16, 128])
+def test_bucket_invariants(tile):
+    rng = np.random.default_rng(7)
+    T, k, E = 300, 4, 32
+    logits = rng.standard_normal((T, E))
+    logits[:, :2] += 3.0  # skew
+    ids, _ = O.topk_softmax(logits, k)
+    b = O.bucket_csr(ids, E, tile)
+    counts, basep, rows, inv = b["counts"], b["basep"], b["rows"], b["inv"]
+    assert counts.sum() == T * k
+    assert np.all(basep % tile == 0) and np.all(np.diff(basep) >= 0)
+    assert basep[E] == sum(-(-c // tile) * tile for c in counts)
+    live = rows[rows >= 0]
+    # every token appears exactly k times
+    assert np.array_equal(np.bincount(live // k, minlength=T), np.full(T, k))
+    for e in range(E):
+        seg = rows[basep[e]:basep[e + 1]]
+        n = counts[e]
+        assert np.all(seg[n:] == -1)
+        assert np.all(np.diff(seg[:n]) > 0)
+        assert np.all(ids.reshape(-1)[seg[:n]] == e)
+    assert np.all(rows[basep[E]:] == -1)
+    assert np.array_equal(rows[inv], np.arange(T * k))
+    assert len(rows) == O.bucket_max_rows(T, k, E, tile)
+
+
+def test_bucket_token_permutation():
+    # Permuting the tokens permutes the bucket contents accordingly.
+    rng = np.random.default_rng(8)
+    T, k, E = 50, 3, 7
+    ids = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)])
+    perm = rng.permutation(T)
+    a = O.bucket_csr(ids, E, 4)
+    b = O.bucket_csr(ids[perm], E, 4)
+    assert np.array_equal(a["counts"], b["counts"]) and np.array_equal(a["basep"], b["basep"])
+    for e in range(E):
+        s, n = a["basep"][e], a["counts"][e]
+        ra = a["rows"][s:s + n]
+        rb = b["rows"][s:s + n]
+        mapped = sorted(perm[r // k] * k + r % k for r in rb)  # b's token i is a's token perm[i]
+        assert list(ra) == mapped
+
+
+def test_swiglu_closed_form_points():
+    assert check_swiglu_points(O.swiglu_oai)
+
+
+def test_sigmoid_extremes():
+    s = O.sigmoid(np.array([-1000.0, -30.0, 0.0, 30.0, 1000.0]))
+    assert not np.any(np.isnan(s))
+    assert s[0] == 0.0 and s[2] == 0.5 and s[4] == 1.0
+    assert math.isclose(s[1], math.exp(-30) / (1 + math.exp(-30)), rel_tol=1e-15)
+
+
+def test_round_bf16_closed_form():
+    cases = [
+        (1.0, 1.0),
+        (1.0 + 2.0 ** -8, 1.0),                        # halfway, ties to even (down)
+        (1.0 + 3 * 2.0 ** -8, 1.0 + 2.0 ** -6),        # halfway, ties to even (up)
+        (1.0 + 2.0 ** -8 + 2.0 ** -20, 1.0 + 2.0 ** -7),  # just above halfway
+        (-(1.0 + 2.0 ** -8 + 2.0 ** -20), -(1.0 + 2.0 ** -7)),
+        (3.0, 3.0),
+        (2.0 ** -133, 2.0 ** -133),                    # smallest bf16 subnormal is kept
+        (0.0, 0.0),
+    ]
+    for a, e in cases:
+        assert O.round_bf16(np.array([a]))[0] == e, a
+    assert math.isnan(O.round_bf16(np.array([float("nan")]))[0])
+    # every float32 with zero low half is a fixed point
+    rng = np.random.default_rng(9)
+    bits = (rng.integers(0, 2 ** 16, size=1000, dtype=np.uint32) << 16).astype(np.uint32)
+    v = bits.view(np.float32)
+    v = v[np.isfinite(v)]
+    assert np.array_equal(O.round_bf16(v), v.astype(np.float64))
+
+
+def test_layer_matches_brute_force():
+    assert check_layer_vs_brute(O.moe_layer)
+
+
+def test_one_hot_routing_is_dense_ffn():
+    # A router margin of 100 on one expert gives weight 1 (to float64 rounding)
+    # on it; with k=1 the layer is exactly that expert's dense FFN.
+    spec = spec_for(0)
+    L = make_layer(spec, layer=1)
+    E, D = spec.E, spec.D
+    L = dict(L)
+    L["w_router"] = np.zeros((E, D), np.float32)
+    L["b_router"] = np.zeros(E, np.float32)
+    L["b_router"][2] = 100.0
+    x = L["x"][:3]
+    y, ids, w, _ = O.moe_layer(L, x, 1)
+    assert np.all(ids[:, 0] == 2) and np.all(w == 1.0)
+    Wg = brute.dequant(L["g_qs"][2].tolist(), L["g_sc"][2].tolist())
+    Wu = brute.dequant(L["u_qs"][2].tolist(), L["u_sc"][2].tolist())
+    Wd = brute.dequant(L["d_qs"][2].tolist(), L["d_sc"][2].tolist())
+    for t in range(3):
+        xt = [float(v) for v in x[t]]
+        g = brute.matvec(Wg, xt, L["bg"][2])
+        u = brute.matvec(Wu, xt, L["bu"][2])
+        h = [brute.swiglu(a, b) for a, b in zip(g, u)]
+        o = brute.matvec(Wd, h, L["bd"][2])
+        assert np.max(O.rownorm_rel_err(y[t], np.array(o), floor=1e-300)) < 1e-12
+    # with k=2 the margin still puts weight ~1 on expert 2 (the other weight is e^-100)
+    y2, ids2, w2, _ = O.moe_layer(L, x, 2)
+    assert np.all(ids2[:, 0] == 2) and np.all(w2[:, 1] < 1e-40)
+    assert np.max(O.rownorm_rel_err(y2, y, floor=1e-300)) < 1e-12
+
+
+def test_identical_experts_give_dense_ffn_whatever_the_routing():
+    spec = spec_for(0)
+    L = dict(make_layer(spec, layer=2))
+    for key in ["g_qs", "g_sc", "u_qs", "u_sc", "d_qs", "d_sc", "bg", "bu", "bd"]:
+        L[key] = np.repeat(L[key][:1], spec.E, axis=0)
+    y, ids, w, _ = O.moe_layer(L, L["x"], spec.k)
+    assert len(set(ids.reshape(-1).tolist())) > 1  # routing really varies
+    Wg = O.dequant_mxfp4(L["g_qs"][0], L["g_sc"][0])
+    Wu = O.dequant_mxfp4(L["u_qs"][0], L["u_sc"][0])
+    Wd = O.dequant_mxfp4(L["d_qs"][0], L["d_sc"][0])
+    dense = O.expert_ffn(L["x"], Wg, L["bg"][0], Wu, L["bu"][0], Wd, L["bd"][0])
+    assert np.max(O.rownorm_rel_err(y, dense, floor=1e-300)) < 1e-12
+
+
+def test_bias_linearity():
+    assert check_bias_linearity(O.moe_layer)
+
+
+def test_gate_up_bias_enters_before_activation():
+    # With zero gate/up weights, g = bg and u = bu exactly, so h = swiglu(bg, bu).
+    spec = spec_for(0)
+    L = dict(make_layer(spec, layer=4))
+    L["g_qs"] = np.zeros_like(L["g_qs"])
+    L["u_qs"] = np.zeros_like(L["u_qs"])
+    L["bg"] = np.full_like(L["bg"], 0.75)
+    L["bu"] = np.full_like(L["bu"], -0.25)
+    y, ids, w, _ = O.moe_layer(L, L["x"], spec.k)
+    h = O.swiglu_oai(np.full(spec.F, 0.75), np.full(spec.F, -0.25))
+    for t in range(spec.T):
+        exp = np.zeros(spec.D)
+        for j in range(spec.k):
+            e = ids[t, j]
+            exp += w[t, j] * (O.dequant_mxfp4(L["d_qs"][e], L["d_sc"][e]) @ h + L["bd"][e])
+        assert np.max(O.rownorm_rel_err(y[t], exp, floor=1e-300)) < 1e-12
+
+
+def test_bf16_operand_variant_stays_close():
+    # The bf16-operand reading of the prefill rail differs from the float64 layer by
+    # bf16 rounding of x and h only: well inside the prefill tolerance 2e-2.
+    spec = spec_for(0)
+    L = make_layer(spec, layer=0)
+    y64, _, _, _ = O.moe_layer(L, L["x"], spec.k)
+    ybf, _, _, _ = O.moe_layer(L, L["x"], spec.k, operands="bf16")
+    err = O.rownorm_rel_err(ybf, y64)
+    assert np.all(err < 2e-2) and np.all(err > 0)
