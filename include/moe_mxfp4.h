@@ -1,0 +1,272 @@
+/*
+ * moe_mxfp4.h -- C ABI of the GB300 (sm_103a) MXFP4 routed mixture-of-experts
+ * expert chain: router top-k, expert bucketing, MXFP4 projections with the
+ * gpt-oss swiglu, and the router-weighted combine.
+ *
+ * The method follows three dasLLAMA pull-request pages:
+ *  - "dasLLAMA gpt-oss arc: idot dot migrations, Metal fusion lane, fused MoE
+ *    expert chain, fleet boards": the Metal fusion-lane commit (bias-seeded
+ *    MetalMoeMulMmMx4, the MetalSwigluOaiPf ghost-row exit, the prefix folded
+ *    into MetalMoeBucket) and the fused MoE expert chain commit (gate+up rows,
+ *    bias, activation, then down rows, bias and the weighted sum in slot order).
+ *  - "dasLLAMA: dig the last two board reds green -- lcpp-shape mx4 kernels +
+ *    GPU PLE pre-step", section "gpt-oss: mx4 kernels to the lab-winning
+ *    shape": the routed-expert MXFP4 GEMV (MetalMoeGemvMx4), the 16-value
+ *    E2M1 table and the ALU E8M0 decode.
+ *  - "dasLLAMA: M5 pp deep-dense - board v8", section "Claims - stated, not
+ *    tested": 128-row tiles for the MoE tensor pair.
+ *
+ * Conventions for every entry point:
+ *  - Pointers are DEVICE pointers owned by the caller unless stated otherwise.
+ *    The library allocates no memory and keeps no state except one status
+ *    word per device (moe_get_status).
+ *  - Work is enqueued on `stream` and the call returns without waiting for it.
+ *    No call below synchronises the host except moe_get_status.
+ *  - Return value: MOE_OK, or a negative code. MOE_EINVAL means an argument
+ *    was rejected on the host before anything was enqueued. MOE_ECUDA means a
+ *    CUDA runtime call failed (moe_last_cuda_error gives its cudaError_t).
+ *    MOE_EUNSUPPORTED means the shape or the device is outside what the
+ *    kernels handle (the kernels are built for sm_103a only).
+ *  - Data errors found on the device (an expert id outside [0, E), a pipeline
+ *    wait that timed out) never trap: they set bits in the device status word.
+ *
+ * MXFP4 storage: a matrix W[R][C] (C a multiple of 32) is two planes, both
+ * row-major: the nibble plane qs[R][C/2] (uint8) and the exponent plane
+ * sc[R][C/32] (uint8, E8M0). Block b of a row covers columns 32b..32b+31 and
+ * is held in bytes 16b..16b+15 of the row; byte i holds column 32b+i in its
+ * low nibble and column 32b+16+i in its high nibble. The value is
+ * E2M1[q] * 2^(s-127), E2M1 = {0, .5, 1, 1.5, 2, 3, 4, 6, -0, -.5, -1, -1.5,
+ * -2, -3, -4, -6}; s = 255 decodes to NaN. Expert matrices are stacked:
+ * qs[E][R][C/2], sc[E][R][C/32]. Planes must be 16-byte aligned.
+ */
+#ifndef MOE_MXFP4_H
+#define MOE_MXFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes ---- */
+#define MOE_OK 0
+#define MOE_EINVAL (-1)
+#define MOE_ECUDA (-2)
+#define MOE_EUNSUPPORTED (-3)
+
+/* ---- device status bits (moe_get_status) ---- */
+#define MOE_STATUS_BAD_EXPERT_ID 0x1 /* an id outside [0, E) reached a kernel */
+#define MOE_STATUS_WAIT_TIMEOUT 0x2  /* a pipeline wait gave up; outputs are invalid */
+
+/* ---- activation element types ---- */
+#define MOE_DTYPE_F32 0
+#define MOE_DTYPE_BF16 1
+
+/* ---- grouped-GEMM epilogues ---- */
+#define MOE_EPI_STORE_BF16 0       /* out[p][r] = bf16(acc)                       */
+#define MOE_EPI_SWIGLU_BF16 1      /* out[p][r] = bf16(swiglu_oai(acc1, acc2))     */
+#define MOE_EPI_SCATTER_WEIGHTED 2 /* out[t][r] += weights[a] * acc, a = rows[p]   */
+
+/* ---- layer rails ---- */
+#define MOE_RAIL_AUTO 0       /* GEMV rail when T <= MOE_GEMV_MAX_T, grouped GEMM otherwise */
+#define MOE_RAIL_GEMV 1
+#define MOE_RAIL_GROUPED_MM 2
+#define MOE_GEMV_MAX_T 8
+
+/* Bucket tile height of the grouped-GEMM rail (rows per tensor-core tile). */
+#define MOE_MM_TILE 128
+
+/*
+ * moe_bucket_max_rows -- length of the `rows` array of moe_bucket: the
+ * worst-case padded row count T*k + E*(tile-1), rounded up to a whole tile.
+ * Returns 0 for invalid arguments. Host only.
+ */
+size_t moe_bucket_max_rows(int T, int k, int E, int tile);
+
+/*
+ * moe_ffn_workspace_bytes -- bytes of device workspace moe_ffn_layer needs
+ * for the given shape and rail (MOE_RAIL_AUTO resolves as moe_ffn_layer
+ * does). Returns 0 for invalid arguments. Host only.
+ */
+size_t moe_ffn_workspace_bytes(int T, int D, int F, int E, int k, int rail);
+
+/*
+ * moe_route_topk -- router logits, top-k, softmax over the k selected.
+ *   logits[t][e] = sum_i x[t][i] * w_router[e][i] + b_router[e]   (fp32)
+ *   ids[t][0..k-1]: the k largest logits of token t in descending order,
+ *                   lower expert index first on equal logits (slot order)
+ *   weights[t][j] = exp(l_j - l_0) / sum_m exp(l_m - l_0) over the k selected
+ * x: float [T][D]; w_router: float [E][D]; b_router: float [E] or NULL;
+ * logits: float [T][E] (output); ids: int32 [T][k]; weights: float [T][k].
+ * Requires 1 <= k <= E <= 256, D a multiple of 4, T >= 0 (T = 0 is a no-op).
+ * The selection on the pages is implicit (the router produces the "ids" that
+ * the MoE kernels consume, E = 32, k = 4); top-k then softmax over the k is
+ * the gpt-oss router.
+ */
+int moe_route_topk(const float* x, int T, int D, const float* w_router, const float* b_router,
+                   int E, int k, float* logits, int32_t* ids, float* weights, cudaStream_t stream);
+
+/*
+ * moe_bucket -- CSR of the T*k (token, slot) assignments grouped by expert,
+ * with each expert's row range padded to `tile` rows (MetalMoeBucket with
+ * MetalMoePrefix folded in: each expert's block computes its own padded
+ * base in-block; "dasLLAMA gpt-oss arc", Metal fusion lane commit, third
+ * bullet). One kernel; the result is deterministic and bit-exact:
+ *   counts[e]  = number of assignments with ids == e                 int32 [E]
+ *   basep[e]   = sum_{e' < e} ceil(counts[e']/tile)*tile; basep[E] = mpad   int32 [E+1]
+ *   rows[p]    = t*k + j for p in [basep[e], basep[e]+counts[e]), ascending;
+ *                -1 at every other p < moe_bucket_max_rows(T, k, E, tile)
+ *   inv[t*k+j] = the row p holding that assignment, -1 if its id is invalid int32 [T*k]
+ * ids: int32 [T][k]. Ids outside [0, E) are skipped and set
+ * MOE_STATUS_BAD_EXPERT_ID. Requires 1 <= k, 1 <= E <= 1024, 1 <= tile <= 1024.
+ */
+int moe_bucket(const int32_t* ids, int T, int k, int E, int tile, int32_t* counts, int32_t* basep,
+               int32_t* rows, int32_t* inv, cudaStream_t stream);
+
+/*
+ * moe_mxfp4_gemv -- n independent MXFP4 matrix-vector products with bias
+ * (the routed-expert GEMV, MetalMoeGemvMx4, of "dasLLAMA: dig the last two
+ * board reds green", section "gpt-oss: mx4 kernels to the lab-winning shape").
+ *   out[i][r] = sum_c W[experts[i]][r][c] * x_i[c] + bias[experts[i]][r]
+ * W: stacked MXFP4 planes w_qs [E][R][C/2], w_sc [E][R][C/32]; experts: int32
+ * [n]; x_i = x + i * x_stride (floats; x_stride = 0 uses one vector for all
+ * i); bias: float [E][R] or NULL; out: float [n][R]. fp32 accumulation.
+ * Requires C a multiple of 32, x_stride a multiple of 4. An expert id outside
+ * [0, E) gives a zero row and sets MOE_STATUS_BAD_EXPERT_ID.
+ */
+int moe_mxfp4_gemv(const uint8_t* w_qs, const uint8_t* w_sc, int E, int R, int C,
+                   const int32_t* experts, int n, const float* x, int64_t x_stride,
+                   const float* bias, float* out, cudaStream_t stream);
+
+/*
+ * moe_swiglu_oai -- h = min(g, limit) * sigmoid(alpha * min(g, limit))
+ *                       * (clamp(u, -limit, limit) + 1)
+ * elementwise over n floats (gpt-oss uses alpha = 1.702, limit = 7). h is
+ * float (h_dtype MOE_DTYPE_F32) or bfloat16 (MOE_DTYPE_BF16, rounded to
+ * nearest even). The sigmoid is evaluated without overflow for any g.
+ */
+int moe_swiglu_oai(const float* g, const float* u, void* h, int64_t n, int h_dtype, float alpha,
+                   float limit, cudaStream_t stream);
+
+/*
+ * moe_gather_rows_bf16 -- activation rows of the grouped GEMM in bucket order:
+ *   xg[p][:] = bf16(x[rows[p] / k][:]) for p < basep[E] with rows[p] >= 0,
+ *   xg[p][:] = 0 for pad rows p < basep[E]; rows p >= basep[E] are not written.
+ * x: float [T][D]; rows/basep from moe_bucket; xg: bf16 [max_rows][D].
+ * If y_zero is not NULL, y_zero[0 .. T*D) is also set to 0 (the scatter
+ * epilogue accumulates into it). Requires D a multiple of 8.
+ */
+int moe_gather_rows_bf16(const float* x, int T, int D, int k, const int32_t* rows,
+                         const int32_t* basep, int E, int max_rows, uint16_t* xg, float* y_zero,
+                         cudaStream_t stream);
+
+/*
+ * moe_mxfp4_grouped_mm -- per-expert MXFP4 GEMM over the bucket rows on the
+ * tcgen05 tensor cores (MetalMoeMulMmMx4; "dasLLAMA gpt-oss arc", Metal
+ * fusion lane commit). For every expert e and every live bucket row p in
+ * [basep[e], basep[e] + counts[e]):
+ *   acc[p][r]  = bias[e][r] + sum_c W[e][r][c] * a[p][c]       (r < R)
+ *   acc2[p][r] = bias2[e][r] + sum_c W2[e][r][c] * a[p][c]     (MOE_EPI_SWIGLU_BF16 only)
+ * bf16 x bf16 products, fp32 accumulation in tensor memory; the bias seeds
+ * the accumulator (NULL bias: the accumulator starts at zero). Then:
+ *   MOE_EPI_STORE_BF16:        out (bf16 [max_rows][out_ld]) row p = bf16(acc[p])
+ *   MOE_EPI_SWIGLU_BF16:       out row p = bf16(swiglu_oai(acc[p], acc2[p]; alpha, limit))
+ *   MOE_EPI_SCATTER_WEIGHTED:  out (float [T][out_ld]) row rows[p]/k += weights[rows[p]] * acc[p]
+ *                              (atomic adds: the order of the k contributions is not fixed)
+ * Pad rows and rows past basep[E] are neither computed nor written; tiles
+ * past basep[E] exit at once. a: bf16 [max_rows][C] in bucket order (see
+ * moe_gather_rows_bf16), max_rows = moe_bucket_max_rows(., ., E, MOE_MM_TILE);
+ * basep must be padded to MOE_MM_TILE. Requires C a multiple of 64 with
+ * C <= 4096, R a multiple of 8, out_ld >= R and a multiple of 8.
+ */
+int moe_mxfp4_grouped_mm(const uint8_t* w_qs, const uint8_t* w_sc, const float* bias,
+                         const uint8_t* w2_qs, const uint8_t* w2_sc, const float* bias2, int E,
+                         int R, int C, const uint16_t* a, const int32_t* counts,
+                         const int32_t* basep, const int32_t* rows, int max_rows, int k,
+                         const float* weights, int epilogue, float alpha, float limit, void* out,
+                         int64_t out_ld, cudaStream_t stream);
+
+/*
+ * moe_expert_gateup_swiglu -- stage 0 of the fused decode expert chain ("dasLLAMA
+ * gpt-oss arc", fused MoE expert chain commit: gate+up rows + bias + activation
+ * per expert row span), the GEMV rail's first expert kernel. For every expert e
+ * with counts[e] > 0 and every assignment a = rows[p], p in [basep[e],
+ * basep[e] + counts[e]), with t = a / k:
+ *   h[a] = swiglu_oai(Wg[e] x_t + bg[e], Wu[e] x_t + bu[e]; alpha, limit)
+ * Each weight row is streamed once for all of the expert's tokens. x: float
+ * [T][D]; gate/up planes [E][F][D/2], [E][F][D/32]; bg, bu [E][F] or NULL;
+ * counts/basep/rows: moe_bucket output (any tile); h: float [T*k][F] in the
+ * block-pair order read by moe_expert_down_combine (within each 32-float group
+ * of a row, values are interleaved as the MXFP4 nibble pairs (i, i+16) and the
+ * group's 16-byte quads are permuted by the group index); treat it as opaque.
+ * Requires 1 <= T <= MOE_GEMV_MAX_T, k <= 8, D and F multiples of 64, <= 4096.
+ */
+int moe_expert_gateup_swiglu(const uint8_t* g_qs, const uint8_t* g_sc, const float* bg,
+                             const uint8_t* u_qs, const uint8_t* u_sc, const float* bu, int E,
+                             int F, int D, int T, int k, const float* x, const int32_t* counts,
+                             const int32_t* basep, const int32_t* rows, float alpha, float limit,
+                             float* h, cudaStream_t stream);
+
+/*
+ * moe_expert_down_combine -- stage 1 of the fused decode expert chain: every
+ * expert's down rows, bias, and the router-weighted sum in slot order, per
+ * output row span:
+ *   y[t][c] = sum_{j=0..k-1} weights[t][j] * (Wd[ids[t][j]][c] . h[t*k+j] + bd[ids[t][j]][c])
+ * summed for j = 0, 1, ..., k-1 in that order (deterministic). h: output of
+ * moe_expert_gateup_swiglu; ids, weights: float/int32 [T][k]; down planes
+ * [E][D][F/2], [E][D][F/32]; bd [E][D] or NULL; y: float [T][D], overwritten.
+ * Same limits as moe_expert_gateup_swiglu.
+ */
+int moe_expert_down_combine(const uint8_t* d_qs, const uint8_t* d_sc, const float* bd, int E, int D,
+                            int F, int T, int k, const float* h, const int32_t* ids,
+                            const float* weights, const int32_t* counts, const int32_t* basep,
+                            const int32_t* rows, float* y, cudaStream_t stream);
+
+/*
+ * moe_ffn_layer -- the whole routed-expert chain for T tokens:
+ *   route (moe_route_topk) -> bucket -> gate/up projections with bias and
+ *   swiglu_oai -> down projection with bias -> router-weighted combine in
+ *   slot order.
+ *   y[t] = sum_j weights[t][j] * (Wd[e] h_j + bd[e]),  e = ids[t][j],
+ *   h_j  = swiglu_oai(Wg[e] x_t + bg[e], Wu[e] x_t + bu[e])  (alpha 1.702, limit 7)
+ * Rails: MOE_RAIL_GEMV (T <= MOE_GEMV_MAX_T) streams the touched experts'
+ * weights through fp32 CUDA-core GEMVs (gate/up + swiglu fused, down + bias +
+ * slot-order combine fused; deterministic). MOE_RAIL_GROUPED_MM runs the
+ * tcgen05 grouped GEMM with bf16 operands (x and h rounded to bf16), the
+ * swiglu fused into the gate/up epilogue and the weighted scatter fused into
+ * the down epilogue. MOE_RAIL_AUTO picks GEMV for T <= MOE_GEMV_MAX_T.
+ * x: float [T][D]; w_router [E][D]; b_router [E] or NULL; gate/up planes
+ * [E][F][D/2], [E][F][D/32]; down planes [E][D][F/2], [E][D][F/32]; biases
+ * bg, bu [E][F], bd [E][D] (each may be NULL); y: float [T][D], overwritten.
+ * ids_out [T][k] and weights_out [T][k] receive the routing if not NULL.
+ * workspace: device memory of at least moe_ffn_workspace_bytes(T, D, F, E, k,
+ * rail) bytes, 256-byte aligned; its contents on entry do not matter.
+ * Requires D, F multiples of 64 (grouped rail: also <= 4096), 1 <= k <= E <= 256.
+ */
+int moe_ffn_layer(const float* x, int T, int D, int F, int E, int k, const float* w_router,
+                  const float* b_router, const uint8_t* g_qs, const uint8_t* g_sc, const float* bg,
+                  const uint8_t* u_qs, const uint8_t* u_sc, const float* bu, const uint8_t* d_qs,
+                  const uint8_t* d_sc, const float* bd, int rail, void* workspace,
+                  size_t workspace_bytes, float* y, int32_t* ids_out, float* weights_out,
+                  cudaStream_t stream);
+
+/*
+ * moe_get_status -- waits for `stream`, then reads and clears the calling
+ * device's status word (MOE_STATUS_* bits set by kernels since the last
+ * read) into *status. This is the one call that synchronises.
+ */
+int moe_get_status(cudaStream_t stream, int* status);
+
+/* moe_last_cuda_error -- the cudaError_t of the last MOE_ECUDA in this thread. */
+int moe_last_cuda_error(void);
+
+/* moe_kernel_launches -- number of kernels this library enqueued from this process (a counter). */
+uint64_t moe_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_MXFP4_H */

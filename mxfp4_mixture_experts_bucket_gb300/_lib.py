@@ -1,0 +1,188 @@
+"""ctypes binding of libmoe_mxfp4.so: the C ABI of include/moe_mxfp4.h, same names.
+
+Argument marshalling only. Tensors are passed as raw pointers (torch tensors
+by ``data_ptr()``), streams default to torch's current CUDA stream. Every
+kernel runs inside the library; if the library is missing this module raises
+at import time instead of falling back to anything else.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmoe_mxfp4.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "moe_mxfp4.h")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'` "
+        "or `python -m mxfp4_mixture_experts_bucket_gb300.build`")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+# ---- constants mirrored from the header ----
+MOE_OK = 0
+MOE_EINVAL = -1
+MOE_ECUDA = -2
+MOE_EUNSUPPORTED = -3
+MOE_STATUS_BAD_EXPERT_ID = 0x1
+MOE_STATUS_WAIT_TIMEOUT = 0x2
+MOE_DTYPE_F32 = 0
+MOE_DTYPE_BF16 = 1
+MOE_EPI_STORE_BF16 = 0
+MOE_EPI_SWIGLU_BF16 = 1
+MOE_EPI_SCATTER_WEIGHTED = 2
+MOE_RAIL_AUTO = 0
+MOE_RAIL_GEMV = 1
+MOE_RAIL_GROUPED_MM = 2
+MOE_GEMV_MAX_T = 8
+MOE_MM_TILE = 128
+
+P = ctypes.c_void_p
+I = ctypes.c_int
+I64 = ctypes.c_int64
+F = ctypes.c_float
+SZ = ctypes.c_size_t
+
+_SIGS = {
+    "moe_bucket_max_rows": (SZ, [I, I, I, I]),
+    "moe_ffn_workspace_bytes": (SZ, [I, I, I, I, I, I]),
+    "moe_route_topk": (I, [P, I, I, P, P, I, I, P, P, P, P]),
+    "moe_bucket": (I, [P, I, I, I, I, P, P, P, P, P]),
+    "moe_mxfp4_gemv": (I, [P, P, I, I, I, P, I, P, I64, P, P, P]),
+    "moe_swiglu_oai": (I, [P, P, P, I64, I, F, F, P]),
+    "moe_gather_rows_bf16": (I, [P, I, I, I, P, P, I, I, P, P, P]),
+    "moe_mxfp4_grouped_mm": (I, [P, P, P, P, P, P, I, I, I, P, P, P, P, I, I, P, I, F, F, P, I64, P]),
+    "moe_expert_gateup_swiglu": (I, [P, P, P, P, P, P, I, I, I, I, I, P, P, P, P, F, F, P, P]),
+    "moe_expert_down_combine": (I, [P, P, P, I, I, I, I, I, P, P, P, P, P, P, P, P]),
+    "moe_ffn_layer": (I, [P, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, I, P, SZ, P, P, P, P]),
+    "moe_get_status": (I, [P, ctypes.POINTER(ctypes.c_int)]),
+    "moe_last_cuda_error": (I, []),
+    "moe_kernel_launches": (ctypes.c_uint64, []),
+}
+
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+
+def declared_functions():
+    """Names of the functions include/moe_mxfp4.h declares."""
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)))
+
+
+class MoeError(RuntimeError):
+    pass
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if hasattr(t, "data_ptr"):
+        return t.data_ptr()
+    if hasattr(t, "ctypes"):  # numpy array (host memory): only for host-side argument checks
+        return t.ctypes.data
+    raise TypeError(f"cannot pass {type(t)} as a pointer")
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if hasattr(s, "cuda_stream"):
+        return s.cuda_stream
+    return s
+
+
+def check(rc: int, what: str = "call"):
+    if rc != MOE_OK:
+        extra = f" (cudaError {moe_last_cuda_error()})" if rc == MOE_ECUDA else ""
+        raise MoeError(f"{what} returned {rc}{extra}")
+    return rc
+
+
+# ---- thin wrappers, same names and argument order as the C ABI ----
+
+def moe_bucket_max_rows(T, k, E, tile):
+    return _lib.moe_bucket_max_rows(T, k, E, tile)
+
+
+def moe_ffn_workspace_bytes(T, D, F, E, k, rail=MOE_RAIL_AUTO):
+    return _lib.moe_ffn_workspace_bytes(T, D, F, E, k, rail)
+
+
+def moe_route_topk(x, T, D, w_router, b_router, E, k, logits, ids, weights, stream=None):
+    return _lib.moe_route_topk(_ptr(x), T, D, _ptr(w_router), _ptr(b_router), E, k, _ptr(logits),
+                               _ptr(ids), _ptr(weights), _stream(stream))
+
+
+def moe_bucket(ids, T, k, E, tile, counts, basep, rows, inv, stream=None):
+    return _lib.moe_bucket(_ptr(ids), T, k, E, tile, _ptr(counts), _ptr(basep), _ptr(rows), _ptr(inv),
+                           _stream(stream))
+
+
+def moe_mxfp4_gemv(w_qs, w_sc, E, R, C, experts, n, x, x_stride, bias, out, stream=None):
+    return _lib.moe_mxfp4_gemv(_ptr(w_qs), _ptr(w_sc), E, R, C, _ptr(experts), n, _ptr(x), x_stride,
+                               _ptr(bias), _ptr(out), _stream(stream))
+
+
+def moe_swiglu_oai(g, u, h, n, h_dtype, alpha=1.702, limit=7.0, stream=None):
+    return _lib.moe_swiglu_oai(_ptr(g), _ptr(u), _ptr(h), n, h_dtype, alpha, limit, _stream(stream))
+
+
+def moe_gather_rows_bf16(x, T, D, k, rows, basep, E, max_rows, xg, y_zero=None, stream=None):
+    return _lib.moe_gather_rows_bf16(_ptr(x), T, D, k, _ptr(rows), _ptr(basep), E, max_rows, _ptr(xg),
+                                     _ptr(y_zero), _stream(stream))
+
+
+def moe_mxfp4_grouped_mm(w_qs, w_sc, bias, w2_qs, w2_sc, bias2, E, R, C, a, counts, basep, rows,
+                         max_rows, k, weights, epilogue, alpha, limit, out, out_ld, stream=None):
+    return _lib.moe_mxfp4_grouped_mm(_ptr(w_qs), _ptr(w_sc), _ptr(bias), _ptr(w2_qs), _ptr(w2_sc),
+                                     _ptr(bias2), E, R, C, _ptr(a), _ptr(counts), _ptr(basep),
+                                     _ptr(rows), max_rows, k, _ptr(weights), epilogue, alpha, limit,
+                                     _ptr(out), out_ld, _stream(stream))
+
+
+def moe_expert_gateup_swiglu(g_qs, g_sc, bg, u_qs, u_sc, bu, E, F, D, T, k, x, counts, basep, rows,
+                             alpha, limit, h, stream=None):
+    return _lib.moe_expert_gateup_swiglu(_ptr(g_qs), _ptr(g_sc), _ptr(bg), _ptr(u_qs), _ptr(u_sc),
+                                         _ptr(bu), E, F, D, T, k, _ptr(x), _ptr(counts), _ptr(basep),
+                                         _ptr(rows), alpha, limit, _ptr(h), _stream(stream))
+
+
+def moe_expert_down_combine(d_qs, d_sc, bd, E, D, F, T, k, h, ids, weights, counts, basep, rows, y,
+                            stream=None):
+    return _lib.moe_expert_down_combine(_ptr(d_qs), _ptr(d_sc), _ptr(bd), E, D, F, T, k, _ptr(h),
+                                        _ptr(ids), _ptr(weights), _ptr(counts), _ptr(basep),
+                                        _ptr(rows), _ptr(y), _stream(stream))
+
+
+def moe_ffn_layer(x, T, D, F, E, k, w_router, b_router, g_qs, g_sc, bg, u_qs, u_sc, bu, d_qs, d_sc,
+                  bd, rail, workspace, workspace_bytes, y, ids_out=None, weights_out=None,
+                  stream=None):
+    return _lib.moe_ffn_layer(_ptr(x), T, D, F, E, k, _ptr(w_router), _ptr(b_router), _ptr(g_qs),
+                              _ptr(g_sc), _ptr(bg), _ptr(u_qs), _ptr(u_sc), _ptr(bu), _ptr(d_qs),
+                              _ptr(d_sc), _ptr(bd), rail, _ptr(workspace), workspace_bytes, _ptr(y),
+                              _ptr(ids_out), _ptr(weights_out), _stream(stream))
+
+
+def moe_get_status(stream=None):
+    v = ctypes.c_int(0)
+    rc = _lib.moe_get_status(_stream(stream), ctypes.byref(v))
+    return rc, v.value
+
+
+def moe_last_cuda_error():
+    return _lib.moe_last_cuda_error()
+
+
+def moe_kernel_launches():
+    return _lib.moe_kernel_launches()

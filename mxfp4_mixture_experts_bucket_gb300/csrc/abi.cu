@@ -1,0 +1,438 @@
+// Exported C ABI (include/moe_mxfp4.h): argument checks on the host, workspace
+// carving, and the launch sequence of each entry point on the caller's stream.
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "../../include/moe_mxfp4.h"
+#include "moe_internal.h"
+
+namespace moe {
+
+__device__ int g_status_word;  // MOE_STATUS_* bits, one per device
+
+static std::atomic<uint64_t> g_launches{0};
+static thread_local int t_last_cuda_error = 0;
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool probed = false;
+  bool supported = false;
+  int sms = 0;
+  int* status = nullptr;
+};
+
+std::mutex g_dev_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+// Probes the current device once: architecture, SM count, status-word address.
+int current_device(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) {
+    t_last_cuda_error = (int)err;
+    return MOE_ECUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return MOE_EUNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.probed) {
+    int major = 0, minor = 0, sms = 0;
+    if ((err = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (err = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) {
+      t_last_cuda_error = (int)err;
+      return MOE_ECUDA;
+    }
+    void* p = nullptr;
+    if ((err = cudaGetSymbolAddress(&p, g_status_word)) != cudaSuccess) {
+      t_last_cuda_error = (int)err;
+      return MOE_ECUDA;
+    }
+    d.supported = (major == 10 && minor == 3);
+    d.sms = sms;
+    d.status = static_cast<int*>(p);
+    d.probed = true;
+  }
+  if (!d.supported) return MOE_EUNSUPPORTED;
+  *out = &d;
+  return MOE_OK;
+}
+
+int cuda_status(cudaError_t err) {
+  if (err == cudaSuccess) return MOE_OK;
+  t_last_cuda_error = (int)err;
+  return MOE_ECUDA;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+size_t max_rows_of(int T, int k, int E, int tile) {
+  const size_t n = (size_t)T * k + (size_t)E * (tile - 1);
+  return round_up(n, (size_t)tile);
+}
+
+int resolve_rail(int T, int rail) {
+  if (rail == MOE_RAIL_AUTO) return T <= MOE_GEMV_MAX_T ? MOE_RAIL_GEMV : MOE_RAIL_GROUPED_MM;
+  return rail;
+}
+
+struct Workspace {
+  float* logits;
+  int32_t* ids;
+  float* w;
+  int32_t* counts;
+  int32_t* basep;
+  int32_t* rows;
+  int32_t* inv;
+  float* h;        // GEMV rail: [T*k][F] pair-swizzled
+  uint16_t* xg;    // grouped rail: [max_rows][D] bf16
+  uint16_t* hg;    // grouped rail: [max_rows][F] bf16
+  size_t max_rows;
+};
+
+// Lays the workspace out from `base` (nullptr: size only). Returns total bytes.
+size_t layout_workspace(int T, int D, int F, int E, int k, int rail, char* base, Workspace* ws) {
+  const int tile = (rail == MOE_RAIL_GEMV) ? 1 : MOE_MM_TILE;
+  const size_t mr = max_rows_of(T, k, E, tile);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    char* p = base ? base + off : nullptr;
+    off = round_up(off + bytes, 256);
+    return p;
+  };
+  Workspace w{};
+  w.logits = reinterpret_cast<float*>(take((size_t)T * E * 4));
+  w.ids = reinterpret_cast<int32_t*>(take((size_t)T * k * 4));
+  w.w = reinterpret_cast<float*>(take((size_t)T * k * 4));
+  w.counts = reinterpret_cast<int32_t*>(take((size_t)E * 4));
+  w.basep = reinterpret_cast<int32_t*>(take((size_t)(E + 1) * 4));
+  w.rows = reinterpret_cast<int32_t*>(take(mr * 4));
+  w.inv = reinterpret_cast<int32_t*>(take((size_t)T * k * 4));
+  if (rail == MOE_RAIL_GEMV) {
+    w.h = reinterpret_cast<float*>(take((size_t)T * k * F * 4));
+  } else {
+    w.xg = reinterpret_cast<uint16_t*>(take(mr * D * 2));
+    w.hg = reinterpret_cast<uint16_t*>(take(mr * F * 2));
+  }
+  w.max_rows = mr;
+  if (ws) *ws = w;
+  return off;
+}
+
+}  // namespace
+
+int device_sm_count() {
+  DeviceInfo* d = nullptr;
+  if (current_device(&d) != MOE_OK) return 1;
+  return d->sms;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+#define MOE_REQUIRE(cond)              \
+  do {                                 \
+    if (!(cond)) return MOE_EINVAL;    \
+  } while (0)
+
+extern "C" {
+
+size_t moe_bucket_max_rows(int T, int k, int E, int tile) {
+  if (T < 0 || k < 1 || E < 1 || tile < 1) return 0;
+  return max_rows_of(T, k, E, tile);
+}
+
+size_t moe_ffn_workspace_bytes(int T, int D, int F, int E, int k, int rail) {
+  if (T < 0 || D < 1 || F < 1 || E < 1 || k < 1 || k > E) return 0;
+  rail = resolve_rail(T, rail);
+  if (rail != MOE_RAIL_GEMV && rail != MOE_RAIL_GROUPED_MM) return 0;
+  return layout_workspace(T, D, F, E, k, rail, nullptr, nullptr);
+}
+
+int moe_route_topk(const float* x, int T, int D, const float* w_router, const float* b_router,
+                   int E, int k, float* logits, int32_t* ids, float* weights, cudaStream_t stream) {
+  MOE_REQUIRE(T >= 0 && D >= 4 && D % 4 == 0);
+  MOE_REQUIRE(E >= 1 && E <= 256 && k >= 1 && k <= E && k <= 32);
+  if (T == 0) return MOE_OK;
+  MOE_REQUIRE(x && w_router && logits && ids && weights);
+  MOE_REQUIRE(aligned(x, 16) && aligned(w_router, 16));
+  DeviceInfo* d = nullptr;
+  int rc = current_device(&d);
+  if (rc != MOE_OK) return rc;
+  Launch L{stream, false};
+  rc = cuda_status(launch_router_logits(x, T, D, w_router, b_router, E, logits, L));
+  if (rc != MOE_OK) return rc;
+  L.pdl = true;
+  return cuda_status(launch_topk_softmax(logits, T, E, k, ids, weights, L));
+}
+
+int moe_bucket(const int32_t* ids, int T, int k, int E, int tile, int32_t* counts, int32_t* basep,
+               int32_t* rows, int32_t* inv, cudaStream_t stream) {
+  MOE_REQUIRE(T >= 0 && k >= 1 && E >= 1 && E <= 1024 && tile >= 1 && tile <= 1024);
+  MOE_REQUIRE(counts && basep && rows && (T == 0 || (ids && inv)));
+  MOE_REQUIRE((size_t)T * k + (size_t)E * tile < (size_t)1 << 30);
+  DeviceInfo* d = nullptr;
+  int rc = current_device(&d);
+  if (rc != MOE_OK) return rc;
+  Launch L{stream, false};
+  const int mr = (int)max_rows_of(T, k, E, tile);
+  return cuda_status(launch_bucket(ids, T, k, E, tile, mr, counts, basep, rows, inv, d->status, L));
+}
+
+int moe_mxfp4_gemv(const uint8_t* w_qs, const uint8_t* w_sc, int E, int R, int C,
+                   const int32_t* experts, int n, const float* x, int64_t x_stride,
+                   const float* bias, float* out, cudaStream_t stream) {
+  MOE_REQUIRE(E >= 1 && R >= 1 && C >= 32 && C % 32 == 0 && n >= 0 && x_stride >= 0);
+  MOE_REQUIRE(x_stride % 4 == 0);
+  if (n == 0) return MOE_OK;
+  if (C > 4096) return MOE_EUNSUPPORTED;
+  MOE_REQUIRE(w_qs && w_sc && experts && x && out);
+  MOE_REQUIRE(aligned(w_qs, 16) && aligned(x, 16));
+  DeviceInfo* d = nullptr;
+  int rc = current_device(&d);
+  if (rc != MOE_OK) return rc;
+  Launch L{stream, false};
+  return cuda_status(
+      launch_mxfp4_gemv(w_qs, w_sc, E, R, C, experts, n, x, x_stride, bias, out, d->status, L));
+}
+
+int moe_swiglu_oai(const float* g, const float* u, void* h, int64_t n, int h_dtype, float alpha,
+                   float limit, cudaStream_t stream) {
+  MOE_REQUIRE(n >= 0 && (h_dtype == MOE_DTYPE_F32 || h_dtype == MOE_DTYPE_BF16));
+  if (n == 0) return MOE_OK;
+  MOE_REQUIRE(g && u && h);
+  DeviceInfo* d = nullptr;
+  int rc = current_device(&d);
+  if (rc != MOE_OK) return rc;
+  Launch L{stream, false};
+  return cuda_status(launch_swiglu(g, u, h, n, h_dtype, alpha, limit, L));
+}
+
+int moe_gather_rows_bf16(const float* x, int T, int D, int k, const int32_t* rows,
+                         const int32_t* basep, int E, int max_rows, uint16_t* xg, float* y_zero,
+                         cudaStream_t stream) {
+  MOE_REQUIRE(T >= 0 && D >= 8 && D % 8 == 0 && k >= 1 && E >= 1 && max_rows >= 0);
+  MOE_REQUIRE(rows && basep && xg && (T == 0 || x));
+  MOE_REQUIRE(aligned(x, 16) && aligned(xg, 16) && aligned(y_zero, 16));
+  DeviceInfo* d = nullptr;
+  int rc = current_device(&d);
+  if (rc != MOE_OK) return rc;
+  Launch L{stream, false};
+  return cuda_status(launch_gather_bf16(x, T, D, k, rows, basep, E, max_rows, xg, y_zero, L));
+}
+
+int moe_mxfp4_grouped_mm(const uint8_t* w_qs, const uint8_t* w_sc, const float* bias,
+                         const uint8_t* w2_qs, const uint8_t* w2_sc, const float* bias2, int E,
+                         int R, int C, const uint16_t* a, const int32_t* counts,
+                         const int32_t* basep, const int32_t* rows, int max_rows, int k,
+                         const float* weights, int epilogue, float alpha, float limit, void* out,
+                         int64_t out_ld, cudaStream_t stream) {
+  MOE_REQUIRE(E >= 1 && E <= 1024 && R >= 1 && C >= 64 && k >= 1 && max_rows >= 0);
+  MOE_REQUIRE(epilogue == MOE_EPI_STORE_BF16 || epilogue == MOE_EPI_SWIGLU_BF16 ||
+              epilogue == MOE_EPI_SCATTER_WEIGHTED);
+  MOE_REQUIRE(max_rows % MOE_MM_TILE == 0);
+  if (C % 64 != 0 || C > 4096 || R % 8 != 0) return MOE_EUNSUPPORTED;
+  MOE_REQUIRE(out_ld >= R && out_ld % 8 == 0);
+  MOE_REQUIRE(w_qs && w_sc && a && counts && basep && rows && out);
+  MOE_REQUIRE(aligned(w_qs, 16) && aligned(w_sc, 16) && aligned(a, 16));
+  if (epilogue == MOE_EPI_SWIGLU_BF16) {
+    MOE_REQUIRE(w2_qs && w2_sc && aligned(w2_qs, 16) && aligned(w2_sc, 16));
+  }
+  if (epilogue == MOE_EPI_SCATTER_WEIGHTED) MOE_REQUIRE(weights != nullptr);
+  if (max_rows == 0) return MOE_OK;
+  DeviceInfo* d = nullptr;
+  int rc = current_device(&d);
+  if (rc != MOE_OK) return rc;
+  GroupedMMArgs g{};
+  g.w_qs[0] = w_qs;
+  g.w_sc[0] = w_sc;
+  g.bias[0] = bias;
+  g.w_qs[1] = w2_qs;
+  g.w_sc[1] = w2_sc;
+  g.bias[1] = bias2;
+  g.nmat = (epilogue == MOE_EPI_SWIGLU_BF16) ? 2 : 1;
+  g.E = E;
+  g.R = R;
+  g.C = C;
+  g.a = a;
+  g.counts = counts;
+  g.basep = basep;
+  g.rows = rows;
+  g.max_rows = max_rows;
+  g.k = k;
+  g.weights = weights;
+  g.epilogue = epilogue;
+  g.alpha = alpha;
+  g.limit = limit;
+  g.out = out;
+  g.out_ld = out_ld;
+  g.status = d->status;
+  Launch L{stream, false};
+  return cuda_status(launch_grouped_mm(g, L));
+}
+
+int moe_expert_gateup_swiglu(const uint8_t* g_qs, const uint8_t* g_sc, const float* bg,
+                             const uint8_t* u_qs, const uint8_t* u_sc, const float* bu, int E,
+                             int F, int D, int T, int k, const float* x, const int32_t* counts,
+                             const int32_t* basep, const int32_t* rows, float alpha, float limit,
+                             float* h, cudaStream_t stream) {
+  MOE_REQUIRE(T >= 0 && T <= MOE_GEMV_MAX_T && k >= 1 && k <= 8 && E >= 1 && E <= 256);
+  MOE_REQUIRE(D >= 64 && F >= 64 && D % 64 == 0 && F % 64 == 0);
+  if (D > 4096 || F > 4096) return MOE_EUNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  MOE_REQUIRE(g_qs && g_sc && u_qs && u_sc && x && counts && basep && rows && h);
+  MOE_REQUIRE(aligned(g_qs, 16) && aligned(u_qs, 16) && aligned(x, 16) && aligned(h, 16));
+  DeviceInfo* d = nullptr;
+  int rc = current_device(&d);
+  if (rc != MOE_OK) return rc;
+  Launch L{stream, false};
+  return cuda_status(launch_gemv_gateup_swiglu(g_qs, g_sc, bg, u_qs, u_sc, bu, E, F, D, T, k, x,
+                                               counts, basep, rows, alpha, limit, h, L));
+}
+
+int moe_expert_down_combine(const uint8_t* d_qs, const uint8_t* d_sc, const float* bd, int E, int D,
+                            int F, int T, int k, const float* h, const int32_t* ids,
+                            const float* weights, const int32_t* counts, const int32_t* basep,
+                            const int32_t* rows, float* y, cudaStream_t stream) {
+  MOE_REQUIRE(T >= 0 && T <= MOE_GEMV_MAX_T && k >= 1 && k <= 8 && E >= 1 && E <= 256);
+  MOE_REQUIRE(D >= 64 && F >= 64 && D % 64 == 0 && F % 64 == 0);
+  if (D > 4096 || F > 4096) return MOE_EUNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  MOE_REQUIRE(d_qs && d_sc && h && ids && weights && counts && basep && rows && y);
+  MOE_REQUIRE(aligned(d_qs, 16) && aligned(h, 16));
+  DeviceInfo* d = nullptr;
+  int rc = current_device(&d);
+  if (rc != MOE_OK) return rc;
+  Launch L{stream, false};
+  return cuda_status(launch_gemv_down_combine(d_qs, d_sc, bd, E, D, F, T, k, h, ids, weights, counts,
+                                              basep, rows, y, L));
+}
+
+int moe_ffn_layer(const float* x, int T, int D, int F, int E, int k, const float* w_router,
+                  const float* b_router, const uint8_t* g_qs, const uint8_t* g_sc, const float* bg,
+                  const uint8_t* u_qs, const uint8_t* u_sc, const float* bu, const uint8_t* d_qs,
+                  const uint8_t* d_sc, const float* bd, int rail, void* workspace,
+                  size_t workspace_bytes, float* y, int32_t* ids_out, float* weights_out,
+                  cudaStream_t stream) {
+  MOE_REQUIRE(T >= 0 && D >= 64 && F >= 64 && D % 64 == 0 && F % 64 == 0);
+  MOE_REQUIRE(E >= 1 && E <= 256 && k >= 1 && k <= E && k <= 32);
+  rail = resolve_rail(T, rail);
+  MOE_REQUIRE(rail == MOE_RAIL_GEMV || rail == MOE_RAIL_GROUPED_MM);
+  if (rail == MOE_RAIL_GEMV) {
+    MOE_REQUIRE(T <= MOE_GEMV_MAX_T && k <= 8);
+    if (D > 4096 || F > 4096) return MOE_EUNSUPPORTED;
+  } else {
+    if (D > 4096 || F > 4096) return MOE_EUNSUPPORTED;
+  }
+  if (T == 0) return MOE_OK;
+  MOE_REQUIRE(x && w_router && g_qs && g_sc && u_qs && u_sc && d_qs && d_sc && y && workspace);
+  MOE_REQUIRE(aligned(x, 16) && aligned(w_router, 16) && aligned(y, 16) && aligned(workspace, 256));
+  MOE_REQUIRE(aligned(g_qs, 16) && aligned(u_qs, 16) && aligned(d_qs, 16));
+  MOE_REQUIRE(aligned(g_sc, 16) && aligned(u_sc, 16) && aligned(d_sc, 16));
+  const size_t need = layout_workspace(T, D, F, E, k, rail, nullptr, nullptr);
+  MOE_REQUIRE(workspace_bytes >= need);
+  DeviceInfo* d = nullptr;
+  int rc = current_device(&d);
+  if (rc != MOE_OK) return rc;
+  Workspace ws;
+  layout_workspace(T, D, F, E, k, rail, static_cast<char*>(workspace), &ws);
+  int32_t* ids = ids_out ? ids_out : ws.ids;
+  float* wts = weights_out ? weights_out : ws.w;
+  const float alpha = 1.702f, limit = 7.0f;
+
+  Launch L{stream, false};
+  rc = cuda_status(launch_router_logits(x, T, D, w_router, b_router, E, ws.logits, L));
+  if (rc != MOE_OK) return rc;
+  L.pdl = true;
+  rc = cuda_status(launch_topk_softmax(ws.logits, T, E, k, ids, wts, L));
+  if (rc != MOE_OK) return rc;
+  const int tile = (rail == MOE_RAIL_GEMV) ? 1 : MOE_MM_TILE;
+  rc = cuda_status(launch_bucket(ids, T, k, E, tile, (int)ws.max_rows, ws.counts, ws.basep, ws.rows,
+                                 ws.inv, d->status, L));
+  if (rc != MOE_OK) return rc;
+  if (rail == MOE_RAIL_GEMV) {
+    rc = cuda_status(launch_gemv_gateup_swiglu(g_qs, g_sc, bg, u_qs, u_sc, bu, E, F, D, T, k, x,
+                                               ws.counts, ws.basep, ws.rows, alpha, limit, ws.h, L));
+    if (rc != MOE_OK) return rc;
+    return cuda_status(launch_gemv_down_combine(d_qs, d_sc, bd, E, D, F, T, k, ws.h, ids, wts,
+                                                ws.counts, ws.basep, ws.rows, y, L));
+  }
+  rc = cuda_status(launch_gather_bf16(x, T, D, k, ws.rows, ws.basep, E, (int)ws.max_rows, ws.xg, y, L));
+  if (rc != MOE_OK) return rc;
+  GroupedMMArgs g{};
+  g.w_qs[0] = g_qs;
+  g.w_sc[0] = g_sc;
+  g.bias[0] = bg;
+  g.w_qs[1] = u_qs;
+  g.w_sc[1] = u_sc;
+  g.bias[1] = bu;
+  g.nmat = 2;
+  g.E = E;
+  g.R = F;
+  g.C = D;
+  g.a = ws.xg;
+  g.counts = ws.counts;
+  g.basep = ws.basep;
+  g.rows = ws.rows;
+  g.max_rows = (int)ws.max_rows;
+  g.k = k;
+  g.weights = wts;
+  g.epilogue = MOE_EPI_SWIGLU_BF16;
+  g.alpha = alpha;
+  g.limit = limit;
+  g.out = ws.hg;
+  g.out_ld = F;
+  g.status = d->status;
+  rc = cuda_status(launch_grouped_mm(g, L));
+  if (rc != MOE_OK) return rc;
+  GroupedMMArgs gd = g;
+  gd.w_qs[0] = d_qs;
+  gd.w_sc[0] = d_sc;
+  gd.bias[0] = bd;
+  gd.w_qs[1] = nullptr;
+  gd.w_sc[1] = nullptr;
+  gd.bias[1] = nullptr;
+  gd.nmat = 1;
+  gd.R = D;
+  gd.C = F;
+  gd.a = ws.hg;
+  gd.epilogue = MOE_EPI_SCATTER_WEIGHTED;
+  gd.out = y;
+  gd.out_ld = D;
+  return cuda_status(launch_grouped_mm(gd, L));
+}
+
+int moe_get_status(cudaStream_t stream, int* status) {
+  MOE_REQUIRE(status != nullptr);
+  DeviceInfo* d = nullptr;
+  int rc = current_device(&d);
+  if (rc != MOE_OK) return rc;
+  cudaError_t err = cudaStreamSynchronize(stream);
+  if (err != cudaSuccess) return cuda_status(err);
+  int v = 0;
+  if ((err = cudaMemcpy(&v, d->status, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_status(err);
+  const int zero = 0;
+  if ((err = cudaMemcpy(d->status, &zero, sizeof(int), cudaMemcpyHostToDevice)) != cudaSuccess)
+    return cuda_status(err);
+  *status = v;
+  return MOE_OK;
+}
+
+int moe_last_cuda_error(void) { return t_last_cuda_error; }
+
+uint64_t moe_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

@@ -1,0 +1,180 @@
+// Shared device helpers for the MXFP4 routed-MoE kernels (sm_103a only).
+//
+// MXFP4 storage (the library's layout): a matrix W[R, C] is a nibble plane
+// qs[R][C/2] and an exponent plane sc[R][C/32]. Block b of a row covers
+// columns 32b..32b+31 in bytes 16b..16b+15; byte i holds column 32b+i in its
+// low nibble and column 32b+16+i in its high nibble. A value is
+// E2M1[q] * 2^(s-127) ("dasLLAMA: dig the last two board reds green",
+// section "gpt-oss: mx4 kernels to the lab-winning shape": 16-value E2M1
+// table, E8M0 exponent computed in the ALU as a float bit pattern).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// status word
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void set_status(int* status, int bits) {
+  if (status) atomicOr(status, bits);
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------------------
+// E8M0 and E2M1 decode
+// ---------------------------------------------------------------------------
+
+// 2^(s-127) built directly as an fp32 bit pattern: exponent field s for
+// s = 1..254, the denormal 2^-127 for s = 0, NaN for s = 255.
+__device__ __forceinline__ float e8m0_to_f32(uint32_t s) {
+  uint32_t bits = (s == 0u) ? 0x00400000u : ((s == 255u) ? 0x7FC00000u : (s << 23));
+  return __uint_as_float(bits);
+}
+
+// One byte holding two E2M1 codes -> f16x2 (low nibble -> low half). Exact.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t word, int byte_idx) {
+  uint32_t r;
+  switch (byte_idx) {
+    case 0:
+      asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %1;\n cvt.rn.f16x2.e2m1x2 %0, b0;\n}"
+          : "=r"(r) : "r"(word));
+      break;
+    case 1:
+      asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %1;\n cvt.rn.f16x2.e2m1x2 %0, b1;\n}"
+          : "=r"(r) : "r"(word));
+      break;
+    case 2:
+      asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %1;\n cvt.rn.f16x2.e2m1x2 %0, b2;\n}"
+          : "=r"(r) : "r"(word));
+      break;
+    default:
+      asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %1;\n cvt.rn.f16x2.e2m1x2 %0, b3;\n}"
+          : "=r"(r) : "r"(word));
+      break;
+  }
+  return r;
+}
+
+__device__ __forceinline__ float2 f16x2_to_float2(uint32_t h) {
+  __half2 v = *reinterpret_cast<__half2*>(&h);
+  return __half22float2(v);
+}
+
+// Packed fp32 FMA on two lanes (Blackwell f32x2 datapath).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  uint64_t ra, rb, rc, rd;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rc) : "f"(c.x), "f"(c.y));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+  float2 d;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+  return d;
+}
+
+// ---------------------------------------------------------------------------
+// Pair-swizzled float vectors used by the decode (GEMV) rail.
+//
+// A length-C vector v is stored as C/32 groups of 8 float4. Group b holds the
+// pairs (v[32b+i], v[32b+16+i]) for i = 0..15, two pairs per float4: float4 j
+// holds pairs 2j and 2j+1 as (v[32b+2j], v[32b+16+2j], v[32b+2j+1],
+// v[32b+16+2j+1]), and sits at position j ^ (b & 7) inside its group so that
+// eight lanes reading eight consecutive groups hit distinct shared-memory
+// banks. The pair order matches the byte order of an MXFP4 block.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int pairswz_offset(int c) {
+  int b = c >> 5, i = c & 31;
+  int p = i & 15, slot = i >> 4;
+  int j = p >> 1;
+  int phys = (b << 3) + (j ^ (b & 7));
+  return (phys << 2) + ((p & 1) << 1) + slot;
+}
+
+// Loads the group of block b of a pair-swizzled vector into registers, in
+// logical float4 order (pairs 2j, 2j+1 in xv[j]).
+__device__ __forceinline__ void load_pair_group(const float4* __restrict__ vec, int b, float4 (&xv)[8]) {
+  const float4* grp = vec + (b << 3);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) xv[j] = grp[j ^ (b & 7)];
+}
+
+// Dot of one MXFP4 block (16 nibble bytes, unscaled E2M1 values) with the
+// block's pairs of a vector (xv from load_pair_group). fp32 products and sums.
+__device__ __forceinline__ float mx_block_dot(uint4 q, const float4 (&xv)[8]) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    // bytes 4m..4m+3 of the block are pairs 4m..4m+3 -> xv[2m], xv[2m+1]
+    const float4 xa = xv[2 * m];
+    const float4 xb = xv[2 * m + 1];
+    const float2 v0 = f16x2_to_float2(e2m1x2_to_f16x2(w[m], 0));
+    const float2 v1 = f16x2_to_float2(e2m1x2_to_f16x2(w[m], 1));
+    const float2 v2 = f16x2_to_float2(e2m1x2_to_f16x2(w[m], 2));
+    const float2 v3 = f16x2_to_float2(e2m1x2_to_f16x2(w[m], 3));
+    acc0 = ffma2(v0, make_float2(xa.x, xa.y), acc0);
+    acc1 = ffma2(v1, make_float2(xa.z, xa.w), acc1);
+    acc0 = ffma2(v2, make_float2(xb.x, xb.y), acc0);
+    acc1 = ffma2(v3, make_float2(xb.z, xb.w), acc1);
+  }
+  return (acc0.x + acc1.x) + (acc0.y + acc1.y);
+}
+
+// ---------------------------------------------------------------------------
+// swiglu_oai
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float sigmoid_f(float z) {
+  // 1/(1+e^-z) for z >= 0 and e^z/(1+e^z) otherwise: never inf/inf.
+  if (z >= 0.f) return 1.f / (1.f + __expf(-z));
+  const float ez = __expf(z);
+  return ez / (1.f + ez);
+}
+
+__device__ __forceinline__ float swiglu_oai_f(float g, float u, float alpha, float limit) {
+  g = fminf(g, limit);
+  u = fminf(fmaxf(u, -limit), limit);
+  return g * sigmoid_f(alpha * g) * (u + 1.f);
+}
+
+// ---------------------------------------------------------------------------
+// warp helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t ldg_nc_u8(const uint8_t* p) {
+  uint16_t r;
+  asm volatile("ld.global.nc.u8 %0, [%1];" : "=h"(r) : "l"(p));
+  return (uint32_t)r;
+}
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+}  // namespace moe

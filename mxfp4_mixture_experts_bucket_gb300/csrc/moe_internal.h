@@ -1,0 +1,116 @@
+// Internal (non-exported) launchers shared between the library's translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+// Epilogue ids of the grouped GEMM (same values as the public MOE_EPI_* macros).
+constexpr int MOE_EPI_STORE_BF16_ID = 0;
+constexpr int MOE_EPI_SWIGLU_BF16_ID = 1;
+constexpr int MOE_EPI_SCATTER_WEIGHTED_ID = 2;
+
+struct Launch {
+  cudaStream_t stream = nullptr;
+  bool pdl = false;  // programmatic dependent launch on the previous kernel in the stream
+};
+
+// Counts every kernel the library enqueues (defined in abi.cu).
+void count_launch();
+int device_sm_count();
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, Launch L,
+                          Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = L.stream;
+  cudaLaunchAttribute attr[1];
+  cfg.numAttrs = 0;
+  if (L.pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  count_launch();
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+// Raises a kernel's dynamic shared-memory limit once per device (the value only grows).
+template <typename K>
+cudaError_t ensure_smem_limit(K kern, size_t bytes) {
+  static int set_bytes[64] = {0};
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev >= 0 && dev < 64 && set_bytes[dev] >= (int)bytes) return cudaSuccess;
+  err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (err == cudaSuccess && dev >= 0 && dev < 64) set_bytes[dev] = (int)bytes;
+  return err;
+}
+
+// ---- route_bucket.cu ----
+cudaError_t launch_router_logits(const float* x, int T, int D, const float* wr, const float* br,
+                                 int E, float* logits, Launch L);
+cudaError_t launch_topk_softmax(const float* logits, int T, int E, int k, int32_t* ids, float* w,
+                                Launch L);
+cudaError_t launch_bucket(const int32_t* ids, int T, int k, int E, int tile, int max_rows,
+                          int32_t* counts, int32_t* basep, int32_t* rows, int32_t* inv,
+                          int* status, Launch L);
+cudaError_t launch_gather_bf16(const float* x, int T, int D, int k, const int32_t* rows,
+                               const int32_t* basep, int E, int max_rows, uint16_t* xg,
+                               float* y_zero, Launch L);
+
+// ---- gemv.cu ----
+cudaError_t launch_mxfp4_gemv(const uint8_t* qs, const uint8_t* sc, int E, int R, int C,
+                              const int32_t* experts, int n, const float* x, int64_t x_stride,
+                              const float* bias, float* out, int* status, Launch L);
+cudaError_t launch_swiglu(const float* g, const float* u, void* h, int64_t n, int h_dtype,
+                          float alpha, float limit, Launch L);
+// Decode rail: gate/up projections + bias + swiglu for the bucketed assignments.
+// h is written pair-swizzled, one row of F floats per assignment t*k+j.
+cudaError_t launch_gemv_gateup_swiglu(const uint8_t* g_qs, const uint8_t* g_sc, const float* bg,
+                                      const uint8_t* u_qs, const uint8_t* u_sc, const float* bu,
+                                      int E, int F, int D, int T, int k, const float* x,
+                                      const int32_t* counts, const int32_t* basep,
+                                      const int32_t* rows, float alpha, float limit, float* h,
+                                      Launch L);
+// Decode rail: down projection + bias + router-weighted combine in slot order.
+cudaError_t launch_gemv_down_combine(const uint8_t* d_qs, const uint8_t* d_sc, const float* bd,
+                                     int E, int D, int F, int T, int k, const float* h,
+                                     const int32_t* ids, const float* w, const int32_t* counts,
+                                     const int32_t* basep, const int32_t* rows, float* y,
+                                     Launch L);
+size_t gemv_gateup_smem_bytes(int T, int D);
+size_t gemv_down_smem_bytes(int T, int k, int F);
+
+// ---- grouped_mm.cu ----
+struct GroupedMMArgs {
+  const uint8_t* w_qs[2];
+  const uint8_t* w_sc[2];
+  const float* bias[2];
+  int nmat;  // 1 or 2
+  int E, R, C;
+  const uint16_t* a;  // bf16 [max_rows][C]
+  const int32_t* counts;
+  const int32_t* basep;
+  const int32_t* rows;
+  int max_rows;
+  int k;
+  const float* weights;
+  int epilogue;
+  float alpha, limit;
+  void* out;
+  int64_t out_ld;
+  int* status;
+};
+// Returns cudaErrorInvalidValue for unsupported shapes (checked by the caller first).
+cudaError_t launch_grouped_mm(const GroupedMMArgs& args, Launch L);
+
+}  // namespace moe

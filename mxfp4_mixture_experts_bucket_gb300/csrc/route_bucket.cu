@@ -1,0 +1,308 @@
+// Router (logits, top-k, softmax over the k) and the single-kernel expert bucket.
+//
+// The bucket follows the Metal fusion lane of "dasLLAMA gpt-oss arc" (third
+// bullet of the fusion commit): the serial one-threadgroup prefix walk is
+// folded into the bucket kernel, each expert's block computing its own padded
+// base in-block and publishing basep[e]; the resulting CSR is bit-identical
+// to the two-pass one.
+#include "moe_common.cuh"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// Router logits: logits[t][e] = x[t] . wr[e] + br[e]
+// Each block computes TT tokens x EG experts; every dot product is spread over
+// G = 128 / (TT*EG) consecutive threads (float4 loads, shuffle / smem reduce).
+// ---------------------------------------------------------------------------
+template <int TT, int EG>
+__global__ void __launch_bounds__(128) router_logits_kernel(const float* __restrict__ x, int T, int D,
+                                                            const float* __restrict__ wr,
+                                                            const float* __restrict__ br, int E,
+                                                            float* __restrict__ logits) {
+  pdl_launch_dependents();
+  pdl_wait();
+  constexpr int NDOT = TT * EG;
+  constexpr int G = 128 / NDOT;
+  static_assert(G * NDOT == 128, "threads per dot");
+  const int tid = threadIdx.x;
+  const int d = tid / G;   // which dot of this block
+  const int gi = tid % G;  // thread within the dot's group
+  const int t = blockIdx.x * TT + d / EG;
+  const int e = blockIdx.y * EG + d % EG;
+  const bool live = (t < T) && (e < E);
+  float acc = 0.f;
+  if (live) {
+    const float4* xr = reinterpret_cast<const float4*>(x + (size_t)t * D);
+    const float4* wrr = reinterpret_cast<const float4*>(wr + (size_t)e * D);
+    const int n4 = D >> 2;
+    float a0 = 0.f, a1 = 0.f;
+    int i = gi;
+    for (; i + G < n4; i += 2 * G) {
+      const float4 xa = xr[i], wa = wrr[i];
+      const float4 xb = xr[i + G], wb = wrr[i + G];
+      a0 = fmaf(xa.x, wa.x, a0); a0 = fmaf(xa.y, wa.y, a0);
+      a0 = fmaf(xa.z, wa.z, a0); a0 = fmaf(xa.w, wa.w, a0);
+      a1 = fmaf(xb.x, wb.x, a1); a1 = fmaf(xb.y, wb.y, a1);
+      a1 = fmaf(xb.z, wb.z, a1); a1 = fmaf(xb.w, wb.w, a1);
+    }
+    for (; i < n4; i += G) {
+      const float4 xa = xr[i], wa = wrr[i];
+      a0 = fmaf(xa.x, wa.x, a0); a0 = fmaf(xa.y, wa.y, a0);
+      a0 = fmaf(xa.z, wa.z, a0); a0 = fmaf(xa.w, wa.w, a0);
+    }
+    acc = a0 + a1;
+  }
+  if constexpr (G <= 32) {
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (gi == 0 && live) logits[(size_t)t * E + e] = acc + (br ? br[e] : 0.f);
+  } else {
+    __shared__ float part[4];
+    acc = warp_sum(acc);
+    if ((tid & 31) == 0) part[tid >> 5] = acc;
+    __syncthreads();
+    if (gi == 0 && live) {
+      float s = 0.f;
+      for (int w = 0; w < G / 32; ++w) s += part[d * (G / 32) + w];
+      logits[(size_t)t * E + e] = s + (br ? br[e] : 0.f);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Top-k then softmax over the k selected; one warp per token.
+// Order: descending logit, lower expert index first on equal logits.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
+  return (va > vb) || (va == vb && ia < ib);
+}
+
+__global__ void __launch_bounds__(256) topk_softmax_kernel(const float* __restrict__ logits, int T,
+                                                           int E, int k, int32_t* __restrict__ ids,
+                                                           float* __restrict__ w) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  constexpr int MAXPER = 8;  // E <= 256
+  float v[MAXPER];
+  const float* lt = logits + (size_t)t * E;
+#pragma unroll
+  for (int q = 0; q < MAXPER; ++q) {
+    const int e = lane + 32 * q;
+    float val = (e < E) ? lt[e] : -INFINITY;
+    if (val != val) val = -INFINITY;  // NaN never wins
+    v[q] = val;
+  }
+  uint32_t taken = 0;  // bit q: expert lane+32q already selected
+  float top0 = 0.f, sum = 0.f, my_ex = 0.f;  // lane j keeps exp(l_j - l_0) of slot j (k <= 32)
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int q = 0; q < MAXPER; ++q) {
+      const int e = lane + 32 * q;
+      if (e < E && !((taken >> q) & 1u) && better(v[q], e, bv, bi)) {
+        bv = v[q];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (better(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (j == 0) top0 = bv;
+    const float ex = expf(bv - top0);
+    sum += ex;
+    if (lane == j) {
+      my_ex = ex;
+      ids[(size_t)t * k + j] = bi;
+    }
+  }
+  if (lane < k) w[(size_t)t * k + lane] = my_ex / sum;
+}
+
+// ---------------------------------------------------------------------------
+// Bucket: one block per expert. Each block histograms all ids, derives its own
+// padded base with a warp reduction over the lower experts, then compacts its
+// assignments in ascending order with ballot/popc warp scans.
+// ---------------------------------------------------------------------------
+constexpr int kBucketThreads = 512;
+
+__global__ void __launch_bounds__(kBucketThreads) bucket_kernel(const int32_t* __restrict__ ids, int n,
+                                                                int E, int tile, int max_rows,
+                                                                int32_t* __restrict__ counts,
+                                                                int32_t* __restrict__ basep,
+                                                                int32_t* __restrict__ rows,
+                                                                int32_t* __restrict__ inv,
+                                                                int* status) {
+  pdl_launch_dependents();
+  pdl_wait();
+  extern __shared__ int hist[];  // [E]
+  __shared__ int s_wtot[kBucketThreads / 32];
+  __shared__ int s_base, s_mpad;
+  const int e = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < E; i += kBucketThreads) hist[i] = 0;
+  __syncthreads();
+  for (int a = tid; a < n; a += kBucketThreads) {
+    const int id = ids[a];
+    if (id >= 0 && id < E) {
+      atomicAdd(&hist[id], 1);
+    } else if (e == 0) {
+      set_status(status, 0x1);
+      inv[a] = -1;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int below = 0, all = 0;
+    for (int i = lane; i < E; i += 32) {
+      const int padded = ((hist[i] + tile - 1) / tile) * tile;
+      all += padded;
+      if (i < e) below += padded;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      below += __shfl_xor_sync(0xffffffffu, below, o);
+      all += __shfl_xor_sync(0xffffffffu, all, o);
+    }
+    if (lane == 0) {
+      s_base = below;
+      s_mpad = all;
+      counts[e] = hist[e];
+      basep[e] = below;
+      if (e == E - 1) basep[E] = all;
+    }
+  }
+  __syncthreads();
+  const int base = s_base;
+  const int mine = hist[e];
+  // stable compaction of the assignments that chose expert e
+  int running = 0;
+  for (int c0 = 0; c0 < n; c0 += kBucketThreads) {
+    const int a = c0 + tid;
+    const bool match = (a < n) && (ids[a] == e);
+    const uint32_t ballot = __ballot_sync(0xffffffffu, match);
+    if (lane == 0) s_wtot[warp] = __popc(ballot);
+    __syncthreads();
+    int before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < kBucketThreads / 32; ++w) {
+      const int c = s_wtot[w];
+      before += (w < warp) ? c : 0;
+      total += c;
+    }
+    if (match) {
+      const int p = base + running + before + __popc(ballot & ((1u << lane) - 1u));
+      rows[p] = a;
+      inv[a] = p;
+    }
+    running += total;
+    __syncthreads();
+  }
+  // pad rows of this expert's last tile
+  const int padded = ((mine + tile - 1) / tile) * tile;
+  for (int p = base + mine + tid; p < base + padded; p += kBucketThreads) rows[p] = -1;
+  // tail past mpad
+  if (e == E - 1)
+    for (int p = s_mpad + tid; p < max_rows; p += kBucketThreads) rows[p] = -1;
+}
+
+// ---------------------------------------------------------------------------
+// Gather token rows into bucket order as bf16 (the grouped GEMM's B operand),
+// zero pad rows, and optionally zero y. One warp per bucket row.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) gather_bf16_kernel(const float* __restrict__ x, int T, int D,
+                                                          int k, const int32_t* __restrict__ rows,
+                                                          const int32_t* __restrict__ basep, int E,
+                                                          uint16_t* __restrict__ xg,
+                                                          float* __restrict__ y_zero) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int warp_global = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int nwarps = gridDim.x * 8;
+  const int mpad = basep[E];
+  const int n4 = D >> 2;
+  for (int p = warp_global; p < mpad; p += nwarps) {
+    const int a = rows[p];
+    uint2* dst = reinterpret_cast<uint2*>(xg + (size_t)p * D);
+    if (a >= 0) {
+      const float4* src = reinterpret_cast<const float4*>(x + (size_t)(a / k) * D);
+      for (int i = lane; i < n4; i += 32) {
+        const float4 v = src[i];
+        __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+        uint2 o;
+        o.x = *reinterpret_cast<uint32_t*>(&lo);
+        o.y = *reinterpret_cast<uint32_t*>(&hi);
+        dst[i] = o;
+      }
+    } else {
+      for (int i = lane; i < n4; i += 32) dst[i] = make_uint2(0u, 0u);
+    }
+  }
+  if (y_zero) {
+    float4* y4 = reinterpret_cast<float4*>(y_zero);
+    const size_t ny = (size_t)T * D / 4;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < ny;
+         i += (size_t)gridDim.x * blockDim.x)
+      y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------
+cudaError_t launch_router_logits(const float* x, int T, int D, const float* wr, const float* br,
+                                 int E, float* logits, Launch L) {
+  if (T <= 0) return cudaSuccess;
+  if (T == 1) {
+    dim3 grid(1, E);
+    return launch_kernel(router_logits_kernel<1, 1>, grid, dim3(128), 0, L, x, T, D, wr, br, E,
+                         logits);
+  }
+  if (T <= 8) {
+    dim3 grid((T + 3) / 4, (E + 3) / 4);
+    return launch_kernel(router_logits_kernel<4, 4>, grid, dim3(128), 0, L, x, T, D, wr, br, E,
+                         logits);
+  }
+  dim3 grid((T + 7) / 8, (E + 7) / 8);
+  return launch_kernel(router_logits_kernel<8, 8>, grid, dim3(128), 0, L, x, T, D, wr, br, E,
+                       logits);
+}
+
+cudaError_t launch_topk_softmax(const float* logits, int T, int E, int k, int32_t* ids, float* w,
+                                Launch L) {
+  if (T <= 0) return cudaSuccess;
+  return launch_kernel(topk_softmax_kernel, dim3((T + 7) / 8), dim3(256), 0, L, logits, T, E, k,
+                       ids, w);
+}
+
+cudaError_t launch_bucket(const int32_t* ids, int T, int k, int E, int tile, int max_rows,
+                          int32_t* counts, int32_t* basep, int32_t* rows, int32_t* inv,
+                          int* status, Launch L) {
+  return launch_kernel(bucket_kernel, dim3(E), dim3(kBucketThreads), sizeof(int) * (size_t)E, L,
+                       ids, T * k, E, tile, max_rows, counts, basep, rows, inv, status);
+}
+
+cudaError_t launch_gather_bf16(const float* x, int T, int D, int k, const int32_t* rows,
+                               const int32_t* basep, int E, int max_rows, uint16_t* xg,
+                               float* y_zero, Launch L) {
+  int blocks = (max_rows + 7) / 8;
+  const int cap = device_sm_count() * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return launch_kernel(gather_bf16_kernel, dim3(blocks), dim3(256), 0, L, x, T, D, k, rows, basep,
+                       E, xg, y_zero);
+}
+
+}  // namespace moe

@@ -1,0 +1,69 @@
+"""A routed MXFP4 MoE layer object: device weights + workspace around moe_ffn_layer.
+
+Marshalling only: every step of the layer runs in libmoe_mxfp4.so. PyTorch
+provides device memory and the stream.
+"""
+
+from __future__ import annotations
+
+from typing import Dict, Optional
+
+import torch
+
+from . import _lib
+
+_WEIGHT_KEYS = ("w_router", "b_router", "g_qs", "g_sc", "u_qs", "u_sc", "d_qs", "d_sc",
+                "bg", "bu", "bd")
+
+
+class MoeLayer:
+    """Holds one layer's weights on a CUDA device and runs it through the C ABI.
+
+    weights: dict with w_router [E, D] f32, b_router [E] f32 (optional),
+    g_qs/u_qs [E, F, D/2] u8, g_sc/u_sc [E, F, D/32] u8, d_qs [E, D, F/2] u8,
+    d_sc [E, D, F/32] u8, bg/bu [E, F] f32, bd [E, D] f32 (biases optional).
+    Host (numpy or torch CPU) arrays are copied to `device` once.
+    """
+
+    def __init__(self, weights: Dict[str, object], k: int, device="cuda"):
+        self.device = torch.device(device)
+        self.w: Dict[str, Optional[torch.Tensor]] = {}
+        for key in _WEIGHT_KEYS:
+            v = weights.get(key)
+            if v is None:
+                self.w[key] = None
+                continue
+            t = v if isinstance(v, torch.Tensor) else torch.from_numpy(v)
+            self.w[key] = t.to(self.device).contiguous()
+        self.E, self.D = self.w["w_router"].shape
+        self.F = self.w["g_qs"].shape[1]
+        self.k = k
+        self._ws: Dict[int, torch.Tensor] = {}
+
+    def workspace(self, T: int, rail: int) -> torch.Tensor:
+        n = _lib.moe_ffn_workspace_bytes(T, self.D, self.F, self.E, self.k, rail)
+        if n == 0 and T > 0:
+            raise _lib.MoeError("invalid shape for moe_ffn_workspace_bytes")
+        key = (n, rail)
+        buf = self._ws.get(key)
+        if buf is None:
+            buf = torch.empty(max(n, 256), dtype=torch.uint8, device=self.device)
+            self._ws[key] = buf
+        return buf
+
+    def forward(self, x: torch.Tensor, rail: int = _lib.MOE_RAIL_AUTO, out: Optional[torch.Tensor] = None,
+                ids_out: Optional[torch.Tensor] = None, weights_out: Optional[torch.Tensor] = None,
+                stream=None) -> torch.Tensor:
+        T = x.shape[0]
+        if out is None:
+            out = torch.empty((T, self.D), dtype=torch.float32, device=self.device)
+        ws = self.workspace(T, rail)
+        w = self.w
+        rc = _lib.moe_ffn_layer(x, T, self.D, self.F, self.E, self.k, w["w_router"], w["b_router"],
+                                w["g_qs"], w["g_sc"], w["bg"], w["u_qs"], w["u_sc"], w["bu"],
+                                w["d_qs"], w["d_sc"], w["bd"], rail, ws, ws.numel(), out, ids_out,
+                                weights_out, stream)
+        _lib.check(rc, "moe_ffn_layer")
+        return out
+
+    __call__ = forward

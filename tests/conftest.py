@@ -28,3 +28,14 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def moe():
+    """The built library's binding (builds libmoe_mxfp4.so first if needed)."""
+    import __graft_entry__ as g
+
+    g.build()
+    import mxfp4_mixture_experts_bucket_gb300 as pkg
+
+    return pkg
