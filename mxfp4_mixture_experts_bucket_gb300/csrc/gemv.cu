@@ -377,12 +377,14 @@ cudaError_t launch_gemv_gateup_swiglu(const uint8_t* g_qs, const uint8_t* g_sc, 
                                       Launch L) {
   if (T <= 0) return cudaSuccess;
   const size_t smem = gemv_gateup_smem_bytes(T, D);
-  const dim3 grid(device_sm_count() * 2);
+  const int sms = device_sm_count();
+  dim3 grid(sms);
   const int nbl = ((D >> 5) + 31) / 32;
   cudaError_t err;
 #define MOE_GU_CASE(N)                                                                           \
   case N:                                                                                        \
     if ((err = set_smem(gemv_gateup_swiglu_kernel<N>, smem)) != cudaSuccess) return err;         \
+    grid = dim3(sms * resident_blocks_per_sm(gemv_gateup_swiglu_kernel<N>, kGemvThreads, smem));  \
     return launch_kernel(gemv_gateup_swiglu_kernel<N>, grid, dim3(kGemvThreads), smem, L, g_qs,  \
                          g_sc, bg, u_qs, u_sc, bu, E, F, D, T, k, x, counts, basep, rows, alpha, \
                          limit, h);
@@ -405,12 +407,14 @@ cudaError_t launch_gemv_down_combine(const uint8_t* d_qs, const uint8_t* d_sc, c
   if (T <= 0) return cudaSuccess;
   const size_t smem = gemv_down_smem_bytes(T, k, F);
   const int h_in_smem = smem > 0 ? 1 : 0;
-  const dim3 grid(device_sm_count() * 2);
+  const int sms = device_sm_count();
+  dim3 grid(sms);
   const int nbl = ((F >> 5) + 31) / 32;
   cudaError_t err;
 #define MOE_DN_CASE(N)                                                                           \
   case N:                                                                                        \
     if ((err = set_smem(gemv_down_combine_kernel<N>, smem)) != cudaSuccess) return err;          \
+    grid = dim3(sms * resident_blocks_per_sm(gemv_down_combine_kernel<N>, kGemvThreads, smem));   \
     return launch_kernel(gemv_down_combine_kernel<N>, grid, dim3(kGemvThreads), smem, L, d_qs,   \
                          d_sc, bd, E, D, F, T, k, h, ids, w, counts, basep, rows, h_in_smem, y);
   switch (nbl) {

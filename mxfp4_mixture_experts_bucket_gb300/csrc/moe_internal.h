@@ -55,6 +55,22 @@ cudaError_t ensure_smem_limit(K kern, size_t bytes) {
   return err;
 }
 
+// Resident blocks per SM of a kernel at a block size and dynamic shared memory,
+// remembered per device for the last shared-memory size asked.
+template <typename K>
+int resident_blocks_per_sm(K kern, int threads, size_t smem) {
+  static int last_smem[64];
+  static int last_val[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (last_val[dev] > 0 && last_smem[dev] == (int)smem) return last_val[dev];
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem) != cudaSuccess || n < 1) n = 1;
+  last_smem[dev] = (int)smem;
+  last_val[dev] = n;
+  return n;
+}
+
 // ---- route_bucket.cu ----
 cudaError_t launch_router_logits(const float* x, int T, int D, const float* wr, const float* br,
                                  int E, float* logits, Launch L);
