@@ -3,7 +3,9 @@
 #include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include <cuda_runtime.h>
 
@@ -136,6 +138,39 @@ int device_sm_count() {
   DeviceInfo* d = nullptr;
   if (current_device(&d) != MOE_OK) return 1;
   return d->sms;
+}
+
+namespace {
+std::mutex g_fn_mu;
+std::map<std::pair<const void*, int>, size_t> g_smem_set;
+std::map<std::tuple<const void*, int, int, size_t>, int> g_resident;
+}  // namespace
+
+cudaError_t ensure_smem_limit_fn(const void* kern, size_t bytes) {
+  if (bytes == 0) return cudaSuccess;
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  std::lock_guard<std::mutex> lock(g_fn_mu);
+  auto key = std::make_pair(kern, dev);
+  auto it = g_smem_set.find(key);
+  if (it != g_smem_set.end() && it->second >= bytes) return cudaSuccess;
+  err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (err == cudaSuccess) g_smem_set[key] = bytes;
+  return err;
+}
+
+int resident_blocks_per_sm_fn(const void* kern, int threads, size_t smem) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+  std::lock_guard<std::mutex> lock(g_fn_mu);
+  auto key = std::make_tuple(kern, dev, threads, smem);
+  auto it = g_resident.find(key);
+  if (it != g_resident.end()) return it->second;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem) != cudaSuccess || n < 1) n = 1;
+  g_resident[key] = n;
+  return n;
 }
 
 }  // namespace moe

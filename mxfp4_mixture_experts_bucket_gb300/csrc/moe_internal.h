@@ -41,34 +41,21 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
-// Raises a kernel's dynamic shared-memory limit once per device (the value only grows).
+// Raises a kernel's dynamic shared-memory limit to at least `bytes` (static
+// plus dynamic may exceed the 48 KB default even when `bytes` alone does not).
+// Remembered per (kernel, device); defined in abi.cu.
+cudaError_t ensure_smem_limit_fn(const void* kern, size_t bytes);
+// Resident blocks per SM of a kernel at a block size and dynamic shared memory,
+// remembered per (kernel, device, threads, bytes); defined in abi.cu.
+int resident_blocks_per_sm_fn(const void* kern, int threads, size_t smem);
+
 template <typename K>
 cudaError_t ensure_smem_limit(K kern, size_t bytes) {
-  static int set_bytes[64] = {0};
-  if (bytes <= 48 * 1024) return cudaSuccess;
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
-  if (dev >= 0 && dev < 64 && set_bytes[dev] >= (int)bytes) return cudaSuccess;
-  err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-  if (err == cudaSuccess && dev >= 0 && dev < 64) set_bytes[dev] = (int)bytes;
-  return err;
+  return ensure_smem_limit_fn(reinterpret_cast<const void*>(kern), bytes);
 }
-
-// Resident blocks per SM of a kernel at a block size and dynamic shared memory,
-// remembered per device for the last shared-memory size asked.
 template <typename K>
 int resident_blocks_per_sm(K kern, int threads, size_t smem) {
-  static int last_smem[64];
-  static int last_val[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-  if (last_val[dev] > 0 && last_smem[dev] == (int)smem) return last_val[dev];
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem) != cudaSuccess || n < 1) n = 1;
-  last_smem[dev] = (int)smem;
-  last_val[dev] = n;
-  return n;
+  return resident_blocks_per_sm_fn(reinterpret_cast<const void*>(kern), threads, smem);
 }
 
 // ---- route_bucket.cu ----
