@@ -154,13 +154,18 @@ int moe_swiglu_oai(const float* g, const float* u, void* h, int64_t n, int h_dty
  * moe_gather_rows_bf16 -- activation rows of the grouped GEMM in bucket order:
  *   xg[p][:] = bf16(x[rows[p] / k][:]) for p < basep[E] with rows[p] >= 0,
  *   xg[p][:] = 0 for pad rows p < basep[E]; rows p >= basep[E] are not written.
- * x: float [T][D]; rows/basep from moe_bucket; xg: bf16 [max_rows][D].
+ * If xg_lo is not NULL it receives the rounding remainders in the same rows,
+ * xg_lo[p][c] = bf16(x - float(xg[p][c])), so that xg + xg_lo carries 16
+ * significant bits of x (the layer uses this split for its gate/up GEMM: with
+ * weights of large E8M0 scale, rounding x alone to bf16 moves g and u by whole
+ * units near the swiglu clamp knees). Rounding is to nearest even.
+ * x: float [T][D]; rows/basep from moe_bucket; xg, xg_lo: bf16 [max_rows][D].
  * If y_zero is not NULL, y_zero[0 .. T*D) is also set to 0 (the scatter
  * epilogue accumulates into it). Requires D a multiple of 8.
  */
 int moe_gather_rows_bf16(const float* x, int T, int D, int k, const int32_t* rows,
-                         const int32_t* basep, int E, int max_rows, uint16_t* xg, float* y_zero,
-                         cudaStream_t stream);
+                         const int32_t* basep, int E, int max_rows, uint16_t* xg, uint16_t* xg_lo,
+                         float* y_zero, cudaStream_t stream);
 
 /*
  * moe_mxfp4_grouped_mm -- per-expert MXFP4 GEMM over the bucket rows on the
@@ -169,7 +174,9 @@ int moe_gather_rows_bf16(const float* x, int T, int D, int k, const int32_t* row
  * [basep[e], basep[e] + counts[e]):
  *   acc[p][r]  = bias[e][r] + sum_c W[e][r][c] * a[p][c]       (r < R)
  *   acc2[p][r] = bias2[e][r] + sum_c W2[e][r][c] * a[p][c]     (MOE_EPI_SWIGLU_BF16 only)
- * bf16 x bf16 products, fp32 accumulation in tensor memory; the bias seeds
+ * where a[p][c] is the bf16 row, or a[p][c] + a_lo[p][c] when a_lo is not NULL
+ * (a second MMA per step on the low parts, accumulating into the same tensor
+ * memory). bf16 x bf16 products, fp32 accumulation in tensor memory; the bias seeds
  * the accumulator (NULL bias: the accumulator starts at zero). Then:
  *   MOE_EPI_STORE_BF16:        out (bf16 [max_rows][out_ld]) row p = bf16(acc[p])
  *   MOE_EPI_SWIGLU_BF16:       out row p = bf16(swiglu_oai(acc[p], acc2[p]; alpha, limit))
@@ -183,10 +190,10 @@ int moe_gather_rows_bf16(const float* x, int T, int D, int k, const int32_t* row
  */
 int moe_mxfp4_grouped_mm(const uint8_t* w_qs, const uint8_t* w_sc, const float* bias,
                          const uint8_t* w2_qs, const uint8_t* w2_sc, const float* bias2, int E,
-                         int R, int C, const uint16_t* a, const int32_t* counts,
-                         const int32_t* basep, const int32_t* rows, int max_rows, int k,
-                         const float* weights, int epilogue, float alpha, float limit, void* out,
-                         int64_t out_ld, cudaStream_t stream);
+                         int R, int C, const uint16_t* a, const uint16_t* a_lo,
+                         const int32_t* counts, const int32_t* basep, const int32_t* rows,
+                         int max_rows, int k, const float* weights, int epilogue, float alpha,
+                         float limit, void* out, int64_t out_ld, cudaStream_t stream);
 
 /*
  * moe_expert_gateup_swiglu -- stage 0 of the fused decode expert chain ("dasLLAMA
@@ -234,9 +241,9 @@ int moe_expert_down_combine(const uint8_t* d_qs, const uint8_t* d_sc, const floa
  * Rails: MOE_RAIL_GEMV (T <= MOE_GEMV_MAX_T) streams the touched experts'
  * weights through fp32 CUDA-core GEMVs (gate/up + swiglu fused, down + bias +
  * slot-order combine fused; deterministic). MOE_RAIL_GROUPED_MM runs the
- * tcgen05 grouped GEMM with bf16 operands (x and h rounded to bf16), the
- * swiglu fused into the gate/up epilogue and the weighted scatter fused into
- * the down epilogue. MOE_RAIL_AUTO picks GEMV for T <= MOE_GEMV_MAX_T.
+ * tcgen05 grouped GEMM with bf16 MMAs (x enters gate/up split into bf16 high
+ * and low parts, h enters down rounded to bf16), the swiglu fused into the
+ * gate/up epilogue and the weighted scatter fused into the down epilogue. MOE_RAIL_AUTO picks GEMV for T <= MOE_GEMV_MAX_T.
  * x: float [T][D]; w_router [E][D]; b_router [E] or NULL; gate/up planes
  * [E][F][D/2], [E][F][D/32]; down planes [E][D][F/2], [E][D][F/32]; biases
  * bg, bu [E][F], bd [E][D] (each may be NULL); y: float [T][D], overwritten.

@@ -54,8 +54,8 @@ _SIGS = {
     "moe_bucket": (I, [P, I, I, I, I, P, P, P, P, P]),
     "moe_mxfp4_gemv": (I, [P, P, I, I, I, P, I, P, I64, P, P, P]),
     "moe_swiglu_oai": (I, [P, P, P, I64, I, F, F, P]),
-    "moe_gather_rows_bf16": (I, [P, I, I, I, P, P, I, I, P, P, P]),
-    "moe_mxfp4_grouped_mm": (I, [P, P, P, P, P, P, I, I, I, P, P, P, P, I, I, P, I, F, F, P, I64, P]),
+    "moe_gather_rows_bf16": (I, [P, I, I, I, P, P, I, I, P, P, P, P]),
+    "moe_mxfp4_grouped_mm": (I, [P, P, P, P, P, P, I, I, I, P, P, P, P, P, I, I, P, I, F, F, P, I64, P]),
     "moe_expert_gateup_swiglu": (I, [P, P, P, P, P, P, I, I, I, I, I, P, P, P, P, F, F, P, P]),
     "moe_expert_down_combine": (I, [P, P, P, I, I, I, I, I, P, P, P, P, P, P, P, P]),
     "moe_ffn_layer": (I, [P, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, I, P, SZ, P, P, P, P]),
@@ -138,15 +138,15 @@ def moe_swiglu_oai(g, u, h, n, h_dtype, alpha=1.702, limit=7.0, stream=None):
     return _lib.moe_swiglu_oai(_ptr(g), _ptr(u), _ptr(h), n, h_dtype, alpha, limit, _stream(stream))
 
 
-def moe_gather_rows_bf16(x, T, D, k, rows, basep, E, max_rows, xg, y_zero=None, stream=None):
+def moe_gather_rows_bf16(x, T, D, k, rows, basep, E, max_rows, xg, xg_lo=None, y_zero=None, stream=None):
     return _lib.moe_gather_rows_bf16(_ptr(x), T, D, k, _ptr(rows), _ptr(basep), E, max_rows, _ptr(xg),
-                                     _ptr(y_zero), _stream(stream))
+                                     _ptr(xg_lo), _ptr(y_zero), _stream(stream))
 
 
-def moe_mxfp4_grouped_mm(w_qs, w_sc, bias, w2_qs, w2_sc, bias2, E, R, C, a, counts, basep, rows,
+def moe_mxfp4_grouped_mm(w_qs, w_sc, bias, w2_qs, w2_sc, bias2, E, R, C, a, a_lo, counts, basep, rows,
                          max_rows, k, weights, epilogue, alpha, limit, out, out_ld, stream=None):
     return _lib.moe_mxfp4_grouped_mm(_ptr(w_qs), _ptr(w_sc), _ptr(bias), _ptr(w2_qs), _ptr(w2_sc),
-                                     _ptr(bias2), E, R, C, _ptr(a), _ptr(counts), _ptr(basep),
+                                     _ptr(bias2), E, R, C, _ptr(a), _ptr(a_lo), _ptr(counts), _ptr(basep),
                                      _ptr(rows), max_rows, k, _ptr(weights), epilogue, alpha, limit,
                                      _ptr(out), out_ld, _stream(stream))
 

@@ -98,7 +98,8 @@ struct Workspace {
   int32_t* rows;
   int32_t* inv;
   float* h;        // GEMV rail: [T*k][F] pair-swizzled
-  uint16_t* xg;    // grouped rail: [max_rows][D] bf16
+  uint16_t* xg;    // grouped rail: [max_rows][D] bf16, high parts of x
+  uint16_t* xg_lo; // grouped rail: [max_rows][D] bf16, low parts of x
   uint16_t* hg;    // grouped rail: [max_rows][F] bf16
   size_t max_rows;
 };
@@ -125,6 +126,7 @@ size_t layout_workspace(int T, int D, int F, int E, int k, int rail, char* base,
     w.h = reinterpret_cast<float*>(take((size_t)T * k * F * 4));
   } else {
     w.xg = reinterpret_cast<uint16_t*>(take(mr * D * 2));
+    w.xg_lo = reinterpret_cast<uint16_t*>(take(mr * D * 2));
     w.hg = reinterpret_cast<uint16_t*>(take(mr * F * 2));
   }
   w.max_rows = mr;
@@ -256,24 +258,24 @@ int moe_swiglu_oai(const float* g, const float* u, void* h, int64_t n, int h_dty
 }
 
 int moe_gather_rows_bf16(const float* x, int T, int D, int k, const int32_t* rows,
-                         const int32_t* basep, int E, int max_rows, uint16_t* xg, float* y_zero,
-                         cudaStream_t stream) {
+                         const int32_t* basep, int E, int max_rows, uint16_t* xg, uint16_t* xg_lo,
+                         float* y_zero, cudaStream_t stream) {
   MOE_REQUIRE(T >= 0 && D >= 8 && D % 8 == 0 && k >= 1 && E >= 1 && max_rows >= 0);
   MOE_REQUIRE(rows && basep && xg && (T == 0 || x));
-  MOE_REQUIRE(aligned(x, 16) && aligned(xg, 16) && aligned(y_zero, 16));
+  MOE_REQUIRE(aligned(x, 16) && aligned(xg, 16) && aligned(xg_lo, 16) && aligned(y_zero, 16));
   DeviceInfo* d = nullptr;
   int rc = current_device(&d);
   if (rc != MOE_OK) return rc;
   Launch L{stream, false};
-  return cuda_status(launch_gather_bf16(x, T, D, k, rows, basep, E, max_rows, xg, y_zero, L));
+  return cuda_status(launch_gather_bf16(x, T, D, k, rows, basep, E, max_rows, xg, xg_lo, y_zero, L));
 }
 
 int moe_mxfp4_grouped_mm(const uint8_t* w_qs, const uint8_t* w_sc, const float* bias,
                          const uint8_t* w2_qs, const uint8_t* w2_sc, const float* bias2, int E,
-                         int R, int C, const uint16_t* a, const int32_t* counts,
-                         const int32_t* basep, const int32_t* rows, int max_rows, int k,
-                         const float* weights, int epilogue, float alpha, float limit, void* out,
-                         int64_t out_ld, cudaStream_t stream) {
+                         int R, int C, const uint16_t* a, const uint16_t* a_lo,
+                         const int32_t* counts, const int32_t* basep, const int32_t* rows,
+                         int max_rows, int k, const float* weights, int epilogue, float alpha,
+                         float limit, void* out, int64_t out_ld, cudaStream_t stream) {
   MOE_REQUIRE(E >= 1 && E <= 1024 && R >= 1 && C >= 64 && k >= 1 && max_rows >= 0);
   MOE_REQUIRE(epilogue == MOE_EPI_STORE_BF16 || epilogue == MOE_EPI_SWIGLU_BF16 ||
               epilogue == MOE_EPI_SCATTER_WEIGHTED);
@@ -281,7 +283,7 @@ int moe_mxfp4_grouped_mm(const uint8_t* w_qs, const uint8_t* w_sc, const float* 
   if (C % 64 != 0 || C > 4096 || R % 8 != 0) return MOE_EUNSUPPORTED;
   MOE_REQUIRE(out_ld >= R && out_ld % 8 == 0);
   MOE_REQUIRE(w_qs && w_sc && a && counts && basep && rows && out);
-  MOE_REQUIRE(aligned(w_qs, 16) && aligned(w_sc, 16) && aligned(a, 16));
+  MOE_REQUIRE(aligned(w_qs, 16) && aligned(w_sc, 16) && aligned(a, 16) && aligned(a_lo, 16));
   if (epilogue == MOE_EPI_SWIGLU_BF16) {
     MOE_REQUIRE(w2_qs && w2_sc && aligned(w2_qs, 16) && aligned(w2_sc, 16));
   }
@@ -302,6 +304,7 @@ int moe_mxfp4_grouped_mm(const uint8_t* w_qs, const uint8_t* w_sc, const float* 
   g.R = R;
   g.C = C;
   g.a = a;
+  g.a_lo = a_lo;
   g.counts = counts;
   g.basep = basep;
   g.rows = rows;
@@ -404,7 +407,8 @@ int moe_ffn_layer(const float* x, int T, int D, int F, int E, int k, const float
     return cuda_status(launch_gemv_down_combine(d_qs, d_sc, bd, E, D, F, T, k, ws.h, ids, wts,
                                                 ws.counts, ws.basep, ws.rows, y, L));
   }
-  rc = cuda_status(launch_gather_bf16(x, T, D, k, ws.rows, ws.basep, E, (int)ws.max_rows, ws.xg, y, L));
+  rc = cuda_status(launch_gather_bf16(x, T, D, k, ws.rows, ws.basep, E, (int)ws.max_rows, ws.xg,
+                                      ws.xg_lo, y, L));
   if (rc != MOE_OK) return rc;
   GroupedMMArgs g{};
   g.w_qs[0] = g_qs;
@@ -418,6 +422,7 @@ int moe_ffn_layer(const float* x, int T, int D, int F, int E, int k, const float
   g.R = F;
   g.C = D;
   g.a = ws.xg;
+  g.a_lo = ws.xg_lo;  // gate/up on split activations: x = hi + lo (16 significant bits)
   g.counts = ws.counts;
   g.basep = ws.basep;
   g.rows = ws.rows;
@@ -443,6 +448,7 @@ int moe_ffn_layer(const float* x, int T, int D, int F, int E, int k, const float
   gd.R = D;
   gd.C = F;
   gd.a = ws.hg;
+  gd.a_lo = nullptr;  // h enters the down projection as plain bf16
   gd.epilogue = MOE_EPI_SCATTER_WEIGHTED;
   gd.out = y;
   gd.out_ld = D;

@@ -29,8 +29,8 @@ namespace mm {
 constexpr int BM = 128;  // weight rows per tile (MMA M)
 constexpr int BN = 128;  // bucket rows per tile (CSR tile height, MMA N <= BN)
 constexpr int BK = 64;   // reduction columns per stage (one 128-byte bf16 row)
-constexpr int OS = 3;    // operand stages (A tiles + B tile)
-constexpr int RS = 4;    // raw MXFP4 stages
+constexpr int MAX_OS = 3;  // operand stages (A tiles + B tiles); 2 for gate/up with split activations
+constexpr int RS = 4;      // raw MXFP4 stages
 constexpr int kThreads = 320;
 constexpr int kDqThreads = 256;  // warps 2..9
 constexpr int kATile = BM * BK * 2;  // 16 KB
@@ -53,18 +53,26 @@ struct Params {
   int box_rows;  // rows of one weight TMA box: min(BM, R)
 };
 
+// Operand stages: three, except gate+up with split (hi+lo) activations, whose
+// two A tiles and two B tiles per stage only fit shared memory twice.
+template <int NMAT, bool SPLIT>
+struct StageCfg {
+  static constexpr int OS = (NMAT == 2 && SPLIT) ? 2 : 3;
+  static constexpr int NB = SPLIT ? 2 : 1;  // B tiles per stage (activation hi, lo)
+};
+
 struct Layout {
   uint32_t a, b, raw, sc, bars, misc, total;
   uint32_t sc_stride;  // bytes per matrix
 };
 
-__host__ __device__ inline Layout make_layout(int nmat, int C) {
+__host__ __device__ inline Layout make_layout(int nmat, int C, int os, int nb) {
   Layout L;
   uint32_t off = 0;
   L.a = off;
-  off += OS * nmat * kATile;
+  off += os * nmat * kATile;
   L.b = off;
-  off += OS * kBTile;
+  off += os * nb * kBTile;
   L.raw = off;
   off += RS * nmat * kRawTile;
   L.sc = off;
@@ -82,9 +90,9 @@ __host__ __device__ inline Layout make_layout(int nmat, int C) {
 constexpr int kRawFull = 0;
 constexpr int kRawEmpty = kRawFull + RS;
 constexpr int kAFull = kRawEmpty + RS;
-constexpr int kBFull = kAFull + OS;
-constexpr int kOpEmpty = kBFull + OS;
-constexpr int kAccFull = kOpEmpty + OS;
+constexpr int kBFull = kAFull + MAX_OS;
+constexpr int kOpEmpty = kBFull + MAX_OS;
+constexpr int kAccFull = kOpEmpty + MAX_OS;
 constexpr int kScFull = kAccFull + 1;
 constexpr int kBiasReady = kScFull + 1;
 constexpr int kNumBars = kBiasReady + 1;
@@ -116,10 +124,13 @@ __device__ __forceinline__ void dequant_block_bf16(uint4 q, float scale, uint32_
   }
 }
 
-template <int NMAT, int EPI>
+template <int NMAT, int EPI, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_mm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
-                      const __grid_constant__ CUtensorMap tm_a, const Params p) {
+                      const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_alo,
+                      const Params p) {
+  constexpr int OS = StageCfg<NMAT, SPLIT>::OS;
+  constexpr int NB = StageCfg<NMAT, SPLIT>::NB;
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -148,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rows_here = min(BM, p.R - m0);
   const bool seeded = (p.bias[0] != nullptr) || (NMAT == 2 && p.bias[1] != nullptr);
 
-  const Layout L = make_layout(NMAT, p.C);
+  const Layout L = make_layout(NMAT, p.C, OS, NB);
   const uint32_t sbase = tc::smem_u32(smem);
   const uint32_t sA = sbase + L.a, sB = sbase + L.b, sRaw = sbase + L.raw;
   const uint8_t* scs = smem + L.sc;
@@ -199,13 +210,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::prefetch_tmap(&tm_w0);
       if (NMAT == 2) tc::prefetch_tmap(&tm_w1);
       tc::prefetch_tmap(&tm_a);
+      if (SPLIT) tc::prefetch_tmap(&tm_alo);
       const uint32_t sc_bytes = (uint32_t)(rows_here * nbc);
       tc::mbar_expect_tx(bar(kScFull), NMAT * sc_bytes);
       for (int mat = 0; mat < NMAT; ++mat)
         tc::bulk_load(sbase + L.sc + mat * L.sc_stride,
                       p.w_sc[mat] + ((size_t)e * p.R + m0) * nbc, sc_bytes, bar(kScFull));
       const uint32_t raw_bytes = (uint32_t)(NMAT * p.box_rows * (BK / 2));
-      const uint32_t b_bytes = (uint32_t)(nchunk * 32 * BK * 2);
+      const uint32_t b_bytes = (uint32_t)(NB * nchunk * 32 * BK * 2);
       int raw_issued = 0, b_issued = 0;
       for (int ks = 0; ks < nk; ++ks) {
         const int rs = ks % RS, rn = ks / RS;
@@ -220,9 +232,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int os = ks % OS, on = ks / OS;
         if (on > 0 && !tc::mbar_wait(bar(kOpEmpty + os), (on - 1) & 1, s_abort)) { fail(); break; }
         tc::mbar_expect_tx(bar(kBFull + os), b_bytes);
-        for (int c = 0; c < nchunk; ++c)
-          tc::tma_load_2d(sB + os * kBTile + c * (32 * BK * 2), &tm_a, ks * BK, tile_row0 + 32 * c,
-                          bar(kBFull + os));
+        for (int c = 0; c < nchunk; ++c) {
+          tc::tma_load_2d(sB + (os * NB) * kBTile + c * (32 * BK * 2), &tm_a, ks * BK,
+                          tile_row0 + 32 * c, bar(kBFull + os));
+          if (SPLIT)
+            tc::tma_load_2d(sB + (os * NB + 1) * kBTile + c * (32 * BK * 2), &tm_alo, ks * BK,
+                            tile_row0 + 32 * c, bar(kBFull + os));
+        }
         b_issued = ks + 1;
       }
       if (*s_abort) {
@@ -258,8 +274,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t ad = tc::sw128_kmajor_desc(sA + (os * NMAT + mat) * kATile + kk * 32);
-            const uint64_t bd = tc::sw128_kmajor_desc(sB + os * kBTile + kk * 32);
-            tc::mma_bf16(tmem + mat * 128, ad, bd, idesc, (ks > 0 || kk > 0 || seeded) ? 1u : 0u);
+#pragma unroll
+            for (int hl = 0; hl < NB; ++hl) {  // activation hi part, then its lo part
+              const uint64_t bd = tc::sw128_kmajor_desc(sB + (os * NB + hl) * kBTile + kk * 32);
+              tc::mma_bf16(tmem + mat * 128, ad, bd, idesc,
+                           (ks > 0 || kk > 0 || hl > 0 || seeded) ? 1u : 0u);
+            }
           }
         }
         tc::mma_commit(bar(kOpEmpty + os));
@@ -408,15 +428,25 @@ static bool make_act_map(CUtensorMap* tm, const uint16_t* a, int rows, int C) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NMAT, int EPI>
+template <int NMAT, int EPI, bool SPLIT>
 static cudaError_t launch_mm(const GroupedMMArgs& g, const CUtensorMap& t0, const CUtensorMap& t1,
-                             const CUtensorMap& ta, const mm::Params& prm, Launch L) {
-  const mm::Layout lay = mm::make_layout(NMAT, g.C);
-  cudaError_t err = ensure_smem_limit(mm::grouped_mm_kernel<NMAT, EPI>, lay.total);
+                             const CUtensorMap& ta, const CUtensorMap& talo, const mm::Params& prm,
+                             Launch L) {
+  using C = mm::StageCfg<NMAT, SPLIT>;
+  const mm::Layout lay = mm::make_layout(NMAT, g.C, C::OS, C::NB);
+  cudaError_t err = ensure_smem_limit(mm::grouped_mm_kernel<NMAT, EPI, SPLIT>, lay.total);
   if (err != cudaSuccess) return err;
   dim3 grid((g.R + mm::BM - 1) / mm::BM, g.max_rows / mm::BN);
-  return launch_kernel(mm::grouped_mm_kernel<NMAT, EPI>, grid, dim3(mm::kThreads), lay.total, L, t0,
-                       t1, ta, prm);
+  return launch_kernel(mm::grouped_mm_kernel<NMAT, EPI, SPLIT>, grid, dim3(mm::kThreads), lay.total,
+                       L, t0, t1, ta, talo, prm);
+}
+
+template <int NMAT, int EPI>
+static cudaError_t launch_mm_split(const GroupedMMArgs& g, const CUtensorMap& t0,
+                                   const CUtensorMap& t1, const CUtensorMap& ta,
+                                   const CUtensorMap& talo, const mm::Params& prm, Launch L) {
+  if (g.a_lo) return launch_mm<NMAT, EPI, true>(g, t0, t1, ta, talo, prm, L);
+  return launch_mm<NMAT, EPI, false>(g, t0, t1, ta, talo, prm, L);
 }
 
 cudaError_t launch_grouped_mm(const GroupedMMArgs& g, Launch L) {
@@ -432,6 +462,8 @@ cudaError_t launch_grouped_mm(const GroupedMMArgs& g, Launch L) {
     t1 = t0;
   }
   if (!make_act_map(&ta, g.a, g.max_rows, g.C)) return cudaErrorInvalidValue;
+  CUtensorMap talo = ta;
+  if (g.a_lo && !make_act_map(&talo, g.a_lo, g.max_rows, g.C)) return cudaErrorInvalidValue;
   mm::Params prm;
   prm.w_sc[0] = g.w_sc[0];
   prm.w_sc[1] = g.nmat == 2 ? g.w_sc[1] : g.w_sc[0];
@@ -453,11 +485,12 @@ cudaError_t launch_grouped_mm(const GroupedMMArgs& g, Launch L) {
   prm.box_rows = box_rows;
   if (g.nmat == 2) {
     if (g.epilogue != MOE_EPI_SWIGLU_BF16_ID) return cudaErrorInvalidValue;
-    return launch_mm<2, MOE_EPI_SWIGLU_BF16_ID>(g, t0, t1, ta, prm, L);
+    return launch_mm_split<2, MOE_EPI_SWIGLU_BF16_ID>(g, t0, t1, ta, talo, prm, L);
   }
-  if (g.epilogue == MOE_EPI_STORE_BF16_ID) return launch_mm<1, MOE_EPI_STORE_BF16_ID>(g, t0, t1, ta, prm, L);
+  if (g.epilogue == MOE_EPI_STORE_BF16_ID)
+    return launch_mm_split<1, MOE_EPI_STORE_BF16_ID>(g, t0, t1, ta, talo, prm, L);
   if (g.epilogue == MOE_EPI_SCATTER_WEIGHTED_ID)
-    return launch_mm<1, MOE_EPI_SCATTER_WEIGHTED_ID>(g, t0, t1, ta, prm, L);
+    return launch_mm_split<1, MOE_EPI_SCATTER_WEIGHTED_ID>(g, t0, t1, ta, talo, prm, L);
   return cudaErrorInvalidValue;
 }
 

@@ -68,7 +68,7 @@ cudaError_t launch_bucket(const int32_t* ids, int T, int k, int E, int tile, int
                           int* status, Launch L);
 cudaError_t launch_gather_bf16(const float* x, int T, int D, int k, const int32_t* rows,
                                const int32_t* basep, int E, int max_rows, uint16_t* xg,
-                               float* y_zero, Launch L);
+                               uint16_t* xg_lo, float* y_zero, Launch L);
 
 // ---- gemv.cu ----
 cudaError_t launch_mxfp4_gemv(const uint8_t* qs, const uint8_t* sc, int E, int R, int C,
@@ -100,7 +100,8 @@ struct GroupedMMArgs {
   const float* bias[2];
   int nmat;  // 1 or 2
   int E, R, C;
-  const uint16_t* a;  // bf16 [max_rows][C]
+  const uint16_t* a;     // bf16 [max_rows][C]
+  const uint16_t* a_lo;  // optional bf16 [max_rows][C]: low parts, the operand is a + a_lo
   const int32_t* counts;
   const int32_t* basep;
   const int32_t* rows;

@@ -218,12 +218,24 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(const int32_t* _
 
 // ---------------------------------------------------------------------------
 // Gather token rows into bucket order as bf16 (the grouped GEMM's B operand),
-// zero pad rows, and optionally zero y. One warp per bucket row.
+// zero pad rows, and optionally zero y. One warp per bucket row. With xg_lo,
+// each value is also split: hi = bf16(x), lo = bf16(x - hi), so hi + lo keeps
+// 16 significant bits of x.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float bf16_lo_as_float(uint32_t packed, int half) {
+  return __uint_as_float(half ? (packed & 0xFFFF0000u) : (packed << 16));
+}
+
 __global__ void __launch_bounds__(256) gather_bf16_kernel(const float* __restrict__ x, int T, int D,
                                                           int k, const int32_t* __restrict__ rows,
                                                           const int32_t* __restrict__ basep, int E,
                                                           uint16_t* __restrict__ xg,
+                                                          uint16_t* __restrict__ xg_lo,
                                                           float* __restrict__ y_zero) {
   pdl_launch_dependents();
   pdl_wait();
@@ -235,19 +247,27 @@ __global__ void __launch_bounds__(256) gather_bf16_kernel(const float* __restric
   for (int p = warp_global; p < mpad; p += nwarps) {
     const int a = rows[p];
     uint2* dst = reinterpret_cast<uint2*>(xg + (size_t)p * D);
+    uint2* dst_lo = xg_lo ? reinterpret_cast<uint2*>(xg_lo + (size_t)p * D) : nullptr;
     if (a >= 0) {
       const float4* src = reinterpret_cast<const float4*>(x + (size_t)(a / k) * D);
       for (int i = lane; i < n4; i += 32) {
         const float4 v = src[i];
-        __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
-        __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
         uint2 o;
-        o.x = *reinterpret_cast<uint32_t*>(&lo);
-        o.y = *reinterpret_cast<uint32_t*>(&hi);
+        o.x = pack_bf16x2(v.x, v.y);
+        o.y = pack_bf16x2(v.z, v.w);
         dst[i] = o;
+        if (dst_lo) {
+          uint2 r;
+          r.x = pack_bf16x2(v.x - bf16_lo_as_float(o.x, 0), v.y - bf16_lo_as_float(o.x, 1));
+          r.y = pack_bf16x2(v.z - bf16_lo_as_float(o.y, 0), v.w - bf16_lo_as_float(o.y, 1));
+          dst_lo[i] = r;
+        }
       }
     } else {
-      for (int i = lane; i < n4; i += 32) dst[i] = make_uint2(0u, 0u);
+      for (int i = lane; i < n4; i += 32) {
+        dst[i] = make_uint2(0u, 0u);
+        if (dst_lo) dst_lo[i] = make_uint2(0u, 0u);
+      }
     }
   }
   if (y_zero) {
@@ -296,13 +316,13 @@ cudaError_t launch_bucket(const int32_t* ids, int T, int k, int E, int tile, int
 
 cudaError_t launch_gather_bf16(const float* x, int T, int D, int k, const int32_t* rows,
                                const int32_t* basep, int E, int max_rows, uint16_t* xg,
-                               float* y_zero, Launch L) {
+                               uint16_t* xg_lo, float* y_zero, Launch L) {
   int blocks = (max_rows + 7) / 8;
   const int cap = device_sm_count() * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   return launch_kernel(gather_bf16_kernel, dim3(blocks), dim3(256), 0, L, x, T, D, k, rows, basep,
-                       E, xg, y_zero);
+                       E, xg, xg_lo, y_zero);
 }
 
 }  // namespace moe

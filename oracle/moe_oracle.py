@@ -228,17 +228,26 @@ def expert_ffn(x_rows: np.ndarray, Wg: np.ndarray, bg, Wu: np.ndarray, bu, Wd: n
     """One expert on a batch of token rows, with dequantised float64 weights.
 
     g = Wg x + bg, u = Wu x + bu, h = swiglu_oai(g, u), o = Wd h + bd.
-    With operands="bf16" the token rows and h are rounded to bfloat16 before
-    their projections (the prefill rail's MMA operand precision); the weights
-    are exact in bfloat16 already.
+    operands selects the precision of the projections' activation operands
+    (the weights are exact in bfloat16 already):
+      "f64"        float64 throughout (the layer's definition);
+      "bf16"       x and h rounded to bfloat16 (bf16 tensor-core operands);
+      "bf16_split" x carried as two bfloat16 parts, hi = bf16(x) and
+                   lo = bf16(x - hi), so the gate/up operand is hi + lo;
+                   h rounded to bfloat16.
     """
     x = np.asarray(x_rows, np.float64)
     if operands == "bf16":
         x = round_bf16(x)
+    elif operands == "bf16_split":
+        hi = round_bf16(x)
+        x = hi + round_bf16(np.asarray(x, np.float64) - hi)
+    elif operands != "f64":
+        raise ValueError(operands)
     g = x @ Wg.T + (0.0 if bg is None else np.asarray(bg, np.float64))
     u = x @ Wu.T + (0.0 if bu is None else np.asarray(bu, np.float64))
     h = swiglu_oai(g, u)
-    if operands == "bf16":
+    if operands in ("bf16", "bf16_split"):
         h = round_bf16(h)
     return h @ Wd.T + (0.0 if bd is None else np.asarray(bd, np.float64))
 

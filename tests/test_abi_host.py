@@ -90,7 +90,7 @@ def test_swiglu_rejects_bad_dtype(moe):
 def test_grouped_mm_rejects_bad_arguments(moe):
     EINVAL, EUNS = moe.MOE_EINVAL, moe.MOE_EUNSUPPORTED
     base = dict(w_qs=FAKE, w_sc=FAKE, bias=None, w2_qs=None, w2_sc=None, bias2=None, E=4, R=64, C=64,
-                a=FAKE, counts=FAKE, basep=FAKE, rows=FAKE, max_rows=512, k=2, weights=None,
+                a=FAKE, a_lo=None, counts=FAKE, basep=FAKE, rows=FAKE, max_rows=512, k=2, weights=None,
                 epilogue=moe.MOE_EPI_STORE_BF16, alpha=1.702, limit=7.0, out=FAKE, out_ld=64)
     call = lambda **kw: moe.moe_mxfp4_grouped_mm(*dict(base, **kw).values(), stream=0)  # noqa: E731
     assert call(epilogue=9) == EINVAL
@@ -102,6 +102,7 @@ def test_grouped_mm_rejects_bad_arguments(moe):
     assert call(epilogue=moe.MOE_EPI_SWIGLU_BF16) == EINVAL          # second matrix missing
     assert call(epilogue=moe.MOE_EPI_SCATTER_WEIGHTED) == EINVAL     # weights missing
     assert call(a=FAKE + 8) == EINVAL
+    assert call(a_lo=FAKE + 8) == EINVAL
 
 
 def test_ffn_layer_rejects_bad_arguments(moe):

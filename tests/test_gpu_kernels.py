@@ -245,14 +245,18 @@ def test_gather_rows_bf16(moe):
     counts, basep, rows, inv, mr = _bucket_on_gpu(moe, ids, E)
     xg = torch.full((mr, D), -1, dtype=torch.int16, device="cuda")
     y = torch.full((T, D), 3.0, device="cuda")
-    assert moe.moe_gather_rows_bf16(dev(x), T, D, k, rows, basep, E, mr, xg, y) == 0
+    xlo = torch.full((mr, D), -1, dtype=torch.int16, device="cuda")
+    assert moe.moe_gather_rows_bf16(dev(x), T, D, k, rows, basep, E, mr, xg, xlo, y) == 0
     ref = O.bucket_csr(ids, E, 128)
     got = bf16_bits_to_f64(xg)
+    got_lo = bf16_bits_to_f64(xlo)
     mpad = ref["basep"][E]
     for p in range(mpad):
         a = ref["rows"][p]
-        exp = O.round_bf16(x[a // k]) if a >= 0 else np.zeros(D)
-        assert np.array_equal(got[p], exp), p
+        hi = O.round_bf16(x[a // k]) if a >= 0 else np.zeros(D)
+        lo = O.round_bf16(x[a // k].astype(np.float64) - hi) if a >= 0 else np.zeros(D)
+        assert np.array_equal(got[p], hi), p
+        assert np.array_equal(got_lo[p], lo), p
     assert torch.all(y == 0)
 
 
@@ -278,25 +282,31 @@ MM_CASES = [
 ]
 
 
+def split_operand(x):
+    hi = O.round_bf16(x)
+    return hi + O.round_bf16(np.asarray(x, np.float64) - hi)
+
+
 @pytest.mark.parametrize("E,R,C,cnt", MM_CASES)
-@pytest.mark.parametrize("with_bias", [True, False])
-def test_grouped_mm_store_parity(moe, E, R, C, cnt, with_bias):
+@pytest.mark.parametrize("with_bias,split", [(True, False), (False, False), (True, True)])
+def test_grouped_mm_store_parity(moe, E, R, C, cnt, with_bias, split):
     rng = np.random.default_rng(R + C + E)
     ids, qs, sc, x, bias = _mm_case(rng, E, R, C, cnt)
     T = ids.shape[0]
     counts, basep, rows, inv, mr = _bucket_on_gpu(moe, ids, E)
     xg = empty((mr, C), torch.int16)
-    assert moe.moe_gather_rows_bf16(dev(x), T, C, 1, rows, basep, E, mr, xg, None) == 0
+    xlo = empty((mr, C), torch.int16)
+    assert moe.moe_gather_rows_bf16(dev(x), T, C, 1, rows, basep, E, mr, xg, xlo if split else None) == 0
     out = torch.full((mr, R), 0, dtype=torch.int16, device="cuda")
     rc = moe.moe_mxfp4_grouped_mm(dev(qs), dev(sc), dev(bias) if with_bias else None, None, None, None,
-                                  E, R, C, xg, counts, basep, rows, mr, 1, None, moe.MOE_EPI_STORE_BF16,
-                                  1.702, 7.0, out, R)
+                                  E, R, C, xg, xlo if split else None, counts, basep, rows, mr, 1, None,
+                                  moe.MOE_EPI_STORE_BF16, 1.702, 7.0, out, R)
     assert rc == 0
     torch.cuda.synchronize()
     assert status(moe) == 0
     ref_b = O.bucket_csr(ids, E, 128)
     got = bf16_bits_to_f64(out)
-    xb = O.round_bf16(x)
+    xb = split_operand(x) if split else O.round_bf16(x)
     for e in range(E):
         if cnt[e] == 0:
             continue
@@ -307,8 +317,9 @@ def test_grouped_mm_store_parity(moe, E, R, C, cnt, with_bias):
         assert np.max(O.rownorm_rel_err(got[p0:p0 + cnt[e]], O.round_bf16(acc))) <= 8e-3, e
 
 
-@pytest.mark.parametrize("E,R,C,cnt", MM_CASES[:3])
-def test_grouped_mm_swiglu_parity(moe, E, R, C, cnt):
+@pytest.mark.parametrize("E,R,C,cnt", MM_CASES)
+@pytest.mark.parametrize("split", [False, True])
+def test_grouped_mm_swiglu_parity(moe, E, R, C, cnt, split):
     rng = np.random.default_rng(7 * R + C)
     ids, qs, sc, x, bias = _mm_case(rng, E, R, C, cnt)
     qs2 = rng.integers(0, 256, size=qs.shape, dtype=np.uint8)
@@ -317,16 +328,17 @@ def test_grouped_mm_swiglu_parity(moe, E, R, C, cnt):
     T = ids.shape[0]
     counts, basep, rows, inv, mr = _bucket_on_gpu(moe, ids, E)
     xg = empty((mr, C), torch.int16)
-    assert moe.moe_gather_rows_bf16(dev(x), T, C, 1, rows, basep, E, mr, xg, None) == 0
+    xlo = empty((mr, C), torch.int16)
+    assert moe.moe_gather_rows_bf16(dev(x), T, C, 1, rows, basep, E, mr, xg, xlo if split else None) == 0
     out = empty((mr, R), torch.int16)
     rc = moe.moe_mxfp4_grouped_mm(dev(qs), dev(sc), dev(bias), dev(qs2), dev(sc2), dev(bias2), E, R, C,
-                                  xg, counts, basep, rows, mr, 1, None, moe.MOE_EPI_SWIGLU_BF16,
-                                  1.702, 7.0, out, R)
+                                  xg, xlo if split else None, counts, basep, rows, mr, 1, None,
+                                  moe.MOE_EPI_SWIGLU_BF16, 1.702, 7.0, out, R)
     assert rc == 0
     assert status(moe) == 0
     ref_b = O.bucket_csr(ids, E, 128)
     got = bf16_bits_to_f64(out)
-    xb = O.round_bf16(x)
+    xb = split_operand(x) if split else O.round_bf16(x)
     for e in range(E):
         if cnt[e] == 0:
             continue
@@ -358,8 +370,9 @@ def test_grouped_mm_scatter_parity(moe, E, R, C, cnt, k):
     a[live] = h[ref_b["rows"][live]]
     a_bits = torch.from_numpy(a).to(torch.bfloat16).view(torch.int16).to("cuda")
     y = torch.zeros((T, R), dtype=torch.float32, device="cuda")
-    rc = moe.moe_mxfp4_grouped_mm(dev(qs), dev(sc), dev(bias), None, None, None, E, R, C, a_bits, counts,
-                                  basep, rows, mr, k, dev(w), moe.MOE_EPI_SCATTER_WEIGHTED, 1.702, 7.0, y, R)
+    rc = moe.moe_mxfp4_grouped_mm(dev(qs), dev(sc), dev(bias), None, None, None, E, R, C, a_bits, None,
+                                  counts, basep, rows, mr, k, dev(w), moe.MOE_EPI_SCATTER_WEIGHTED, 1.702, 7.0,
+                                  y, R)
     assert rc == 0
     assert status(moe) == 0
     hb = O.round_bf16(h)

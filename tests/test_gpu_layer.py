@@ -39,6 +39,8 @@ def run_layer(moe, layer, x_np, rail, k):
 
 def check_layer(moe, cfg, T, rail, sample=None, seed=None):
     spec, L, layer, cache = layer_for(moe, cfg)
+    if rail == moe.MOE_RAIL_AUTO:
+        rail = moe.MOE_RAIL_GEMV if T <= moe.MOE_GEMV_MAX_T else moe.MOE_RAIL_GROUPED_MM
     x = make_tokens(spec, T=T, seed=seed)
     y, ids, w = run_layer(moe, layer, x, rail, spec.k)
     logits = O.router_logits(x, L["w_router"], L["b_router"])
@@ -57,7 +59,7 @@ def check_layer(moe, cfg, T, rail, sample=None, seed=None):
         assert err.max() <= DECODE_TOL, err.max()
     else:
         ybf, _, _, _ = O.moe_layer(L, x, spec.k, token_idx=toks, ids=ids, weights=w_ref, cache=cache,
-                                   operands="bf16")
+                                   operands="bf16_split")
         err_bf = O.rownorm_rel_err(y[toks], ybf)
         err64 = O.rownorm_rel_err(y[toks], y64)
         assert err_bf.max() <= PREFILL_BF16_TOL, err_bf.max()
@@ -183,7 +185,7 @@ def test_layer_without_biases(moe):
     L0 = dict(L, b_router=np.zeros(spec.E, np.float32), bg=np.zeros((spec.E, spec.F), np.float32),
               bu=np.zeros((spec.E, spec.F), np.float32), bd=np.zeros((spec.E, spec.D), np.float32))
     y64, ids64, _, _ = O.moe_layer(L0, x, spec.k)
-    ybf, _, _, _ = O.moe_layer(L0, x, spec.k, operands="bf16")
+    ybf, _, _, _ = O.moe_layer(L0, x, spec.k, operands="bf16_split")
     for rail, ref, tol in ((moe.MOE_RAIL_GEMV, y64, DECODE_TOL), (moe.MOE_RAIL_GROUPED_MM, ybf, PREFILL_BF16_TOL)):
         y, ids, _ = run_layer(moe, layer, x, rail, spec.k)
         assert np.array_equal(ids, ids64)

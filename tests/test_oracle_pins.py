@@ -370,3 +370,32 @@ def test_bf16_operand_variant_stays_close():
     ybf, _, _, _ = O.moe_layer(L, L["x"], spec.k, operands="bf16")
     err = O.rownorm_rel_err(ybf, y64)
     assert np.all(err < 2e-2) and np.all(err > 0)
+
+
+def test_bf16_split_operand_closed_form():
+    # hi + lo reproduces x to 16 significant bits: exact for x with <= 16 bits,
+    # and otherwise within 2^-16 relative.
+    x = np.array([1.0 + 2.0 ** -12, -3.0 - 2.0 ** -15, 0.1, 12345.678], np.float32)
+    hi = O.round_bf16(x)
+    lo = O.round_bf16(x.astype(np.float64) - hi)
+    assert hi[0] == 1.0 and lo[0] == 2.0 ** -12
+    assert hi[1] + lo[1] == -3.0 - 2.0 ** -15
+    rel = np.abs((hi + lo) - x.astype(np.float64)) / np.abs(x.astype(np.float64))
+    assert np.all(rel <= 2.0 ** -16)
+
+
+def test_bf16_operand_sensitivity_at_full_scale():
+    """At the gpt-oss-shaped scale (E8M0 up to 135, D = 2880) |g| and |u| reach ~1e4,
+    so rounding x alone to bf16 moves a few g, u across the swiglu clamp knees and
+    the layer output by several percent; the split (hi + lo) operand stays far
+    inside the 2e-2 prefill tolerance. Oracle against oracle, two tokens."""
+    spec = spec_for(2)
+    L = make_layer(spec, with_tokens=False)
+    from synthetic import make_tokens
+    x = make_tokens(spec, T=2, seed=3)
+    cache = O.ExpertCache(L)
+    y64, ids, w, _ = O.moe_layer(L, x, spec.k, cache=cache)
+    ysplit, _, _, _ = O.moe_layer(L, x, spec.k, cache=cache, operands="bf16_split")
+    ybf, _, _, _ = O.moe_layer(L, x, spec.k, cache=cache, operands="bf16")
+    assert O.rownorm_rel_err(ysplit, y64).max() < 2e-3
+    assert O.rownorm_rel_err(ybf, y64).max() > 2e-2
