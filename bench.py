@@ -52,6 +52,8 @@ def parse_args():
     ap.add_argument("--layers", type=int, default=8, help="distinct decode layer weight sets rotated per step")
     ap.add_argument("--prefill-steps", type=int, default=20)
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--skip-decode", action="store_true",
+                    help="measure only the prefill step (profiling aid; the headline needs decode)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=2)
     return ap.parse_args()
@@ -236,6 +238,9 @@ def run_ours(args, dist: Dist):
     torch.cuda.set_device(dist.local_rank)
     dev = torch.device("cuda", dist.local_rank)
     hbm_peak, bf16_peak, bf16_sus, peak_src = load_peaks()
+    if args.skip_decode:
+        stream = torch.cuda.Stream(device=dev)
+        return {"prefill_t512": run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src)}
     K, W, NL = args.steps, args.warmup, args.layers
     spec = spec_for(1)
 
