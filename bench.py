@@ -55,7 +55,8 @@ def parse_args():
     ap.add_argument("--skip-decode", action="store_true",
                     help="measure only the prefill step (profiling aid; the headline needs decode)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-sample-tokens", type=int, default=2)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="minimum CPU time of the oracle sample (whole decode tokens)")
     return ap.parse_args()
 
 
@@ -209,18 +210,21 @@ def ncu_traffic(kernel_key: str):
 # ---------------------------------------------------------------------------
 # CPU oracle baseline (bounded sample)
 # ---------------------------------------------------------------------------
-def cpu_oracle_rate(n_tokens: int):
+def cpu_oracle_rate(min_seconds: float = 10.0, max_tokens: int = 64):
+    """Decode tokens through the float64 oracle until at least min_seconds of CPU work."""
     from oracle import moe_oracle as O
     from synthetic import make_layer, make_tokens, spec_for
 
     spec = spec_for(1)
     L = make_layer(spec, with_tokens=False)
-    x = make_tokens(spec, T=n_tokens, seed=12345)
+    x = make_tokens(spec, T=max_tokens, seed=12345)
     t0 = time.perf_counter()
-    for t in range(n_tokens):  # a fresh expert cache per token: each decode token dequantises its experts
-        O.moe_layer(L, x[t:t + 1], spec.k)
+    n = 0
+    while n < max_tokens and (n == 0 or time.perf_counter() - t0 < min_seconds):
+        O.moe_layer(L, x[n:n + 1], spec.k)  # a fresh expert cache per token: each dequantises its experts
+        n += 1
     dt = time.perf_counter() - t0
-    return n_tokens / dt, dt
+    return n / dt, dt, n
 
 
 # ---------------------------------------------------------------------------
@@ -265,15 +269,17 @@ def run_ours(args, dist: Dist):
             j = W + i
             layers[j % NL](xs[j:j + 1], rail=moe.MOE_RAIL_GEMV, out=ys[j:j + 1], ids_out=ids[j:j + 1])
     launches_per_step = (moe.moe_kernel_launches() - n0) / K
-    graph.replay()  # first replay uploads the graph; untimed
+    with torch.cuda.stream(stream):
+        graph.replay()  # first replay uploads the graph; untimed
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dist.local_rank) as clk:
         dist.barrier()
         torch.cuda.synchronize()
-        ev0.record(stream)
-        graph.replay()
-        ev1.record(stream)
+        with torch.cuda.stream(stream):  # replay on the stream the events are recorded on
+            ev0.record(stream)
+            graph.replay()
+            ev1.record(stream)
         torch.cuda.synchronize()
         dist.barrier()
     secs = ev0.elapsed_time(ev1) / 1e3
@@ -311,12 +317,14 @@ def run_ours(args, dist: Dist):
             moe.check(moe.moe_expert_gateup_swiglu(w["g_qs"], w["g_sc"], w["bg"], w["u_qs"], w["u_sc"], w["bu"],
                                                    E, F, D, 1, K_TOP, x1, cnt, bp, rows, 1.702, 7.0, h, stream),
                       "gateup")
-    kgraph.replay()
+    with torch.cuda.stream(stream):
+        kgraph.replay()
     torch.cuda.synchronize()
     k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    k0.record(stream)
-    kgraph.replay()
-    k1.record(stream)
+    with torch.cuda.stream(stream):
+        k0.record(stream)
+        kgraph.replay()
+        k1.record(stream)
     torch.cuda.synchronize()
     kern_s = k0.elapsed_time(k1) / 1e3 / Kk
     gateup_bytes = K_TOP * 2 * MAT_BYTES + K_TOP * 2 * F * 4 + D * 4 + K_TOP * F * 4
@@ -398,14 +406,17 @@ def run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src):
         for i in range(K):
             layers[i % NL](xs[i % NL], rail=moe.MOE_RAIL_GROUPED_MM, out=ys[i % NL])
     per_step = (moe.moe_kernel_launches() - n0) / K
-    graph.replay()
+    with torch.cuda.stream(stream):
+        graph.replay()
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     dist.barrier()
-    ev0.record(stream)
-    graph.replay()
-    ev1.record(stream)
-    torch.cuda.synchronize()
+    with ClockSampler(dist.local_rank) as clk:
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            graph.replay()
+            ev1.record(stream)
+        torch.cuda.synchronize()
     dist.barrier()
     secs = ev0.elapsed_time(ev1) / 1e3
     rate, secs_max = whole_job_rate(K * T, secs, dist)
@@ -421,7 +432,7 @@ def run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src):
             "roofline_frac": round(t_roof / (ms / 1e3), 4),
             "roofline_bound": "hbm" if alg_bytes / (hbm_peak * 1e9) >= flops / (bf16_peak * 1e12) else "tensor",
             "algorithmic_bytes": alg_bytes, "algorithmic_flops": flops, "kernels_per_step": per_step,
-            "peak_source": peak_src}
+            "peak_source": peak_src, "clocks": clk.summary()}
 
 
 def main():
@@ -429,8 +440,7 @@ def main():
     dist = Dist()
     if args.impl == "reference":
         if dist.rank == 0:
-            n = max(1, args.cpu_sample_tokens)
-            rate, dt = cpu_oracle_rate(n)
+            rate, dt, n = cpu_oracle_rate(args.cpu_seconds)
             cores = os.cpu_count()
             print(json.dumps({
                 "impl": "reference", "metric": METRIC, "value": round(rate, 4), "unit": "tokens/s",
@@ -448,11 +458,11 @@ def main():
     res = run_ours(args, dist)
     if dist.rank == 0:
         if not args.no_cpu_baseline:
-            rate, dt = cpu_oracle_rate(max(1, args.cpu_sample_tokens))
+            rate, dt, n = cpu_oracle_rate(args.cpu_seconds)
             res["cpu_baseline"] = {"value": round(rate, 4), "unit": "tokens/s", "cores": os.cpu_count(),
                                    "kind": "oracle",
-                                   "sample": f"{args.cpu_sample_tokens} decode tokens through the float64 numpy "
-                                             f"oracle ({dt:.1f} s; BLAS may use every core, elementwise work one)"}
+                                   "sample": f"{n} decode tokens through the float64 numpy oracle "
+                                             f"({dt:.1f} s; BLAS may use every core, elementwise work one)"}
         print(json.dumps(res), flush=True)
     dist.close()
 
