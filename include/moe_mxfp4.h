@@ -55,6 +55,7 @@ extern "C" {
 #define MOE_EINVAL (-1)
 #define MOE_ECUDA (-2)
 #define MOE_EUNSUPPORTED (-3)
+#define MOE_ESCRATCH (-4) /* the shape needs more scratch than MOE_DECODE_SCRATCH_BYTES */
 
 /* ---- device status bits (moe_get_status) ---- */
 #define MOE_STATUS_BAD_EXPERT_ID 0x1 /* an id outside [0, E) reached a kernel */
@@ -258,6 +259,38 @@ int moe_ffn_layer(const float* x, int T, int D, int F, int E, int k, const float
                   const uint8_t* d_sc, const float* bd, int rail, void* workspace,
                   size_t workspace_bytes, float* y, int32_t* ids_out, float* weights_out,
                   cudaStream_t stream);
+
+/* Size of the library's static decode scratch (moe_ffn_layer_decode_static). */
+#define MOE_DECODE_SCRATCH_BYTES (512 * 1024)
+
+/*
+ * moe_ffn_layer_decode_static -- moe_ffn_layer on the GEMV rail for callers
+ * that cannot allocate device memory where they run the layer: a serving loop
+ * that must stay allocation-free after start-up (cudaMalloc/cudaFree can
+ * synchronise the device), a plugin that is handed only a stream and tensors,
+ * or work recorded during a CUDA graph capture that forbids allocations. The
+ * pages have no counterpart; it is a deployment convenience.
+ * Arguments, results and limits are those of moe_ffn_layer with
+ * rail = MOE_RAIL_GEMV (1 <= T <= MOE_GEMV_MAX_T); there is no workspace
+ * argument: the scratch is one file-scope device array of
+ * MOE_DECODE_SCRATCH_BYTES bytes that every GPU which loads the library holds
+ * until the process exits. Shapes whose moe_ffn_workspace_bytes(T, D, F, E,
+ * k, MOE_RAIL_GEMV) exceeds that size are rejected with MOE_ESCRATCH before
+ * anything is enqueued (T = 8, k = 4, D = F = 2880 needs about 370 KB).
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture. All
+ * calls on a device share the array and it keeps the last call's contents;
+ * nothing in it needs to start at zero (every byte a call reads it first
+ * writes). Calls whose executions overlap on the GPU (different streams, or
+ * concurrent host threads) race on the array: serialise them.
+ * Calls no cudaMalloc, cudaFree or allocating library routine.
+ */
+int moe_ffn_layer_decode_static(const float* x, int T, int D, int F, int E, int k,
+                                const float* w_router, const float* b_router, const uint8_t* g_qs,
+                                const uint8_t* g_sc, const float* bg, const uint8_t* u_qs,
+                                const uint8_t* u_sc, const float* bu, const uint8_t* d_qs,
+                                const uint8_t* d_sc, const float* bd, float* y, int32_t* ids_out,
+                                float* weights_out, cudaStream_t stream);
 
 /*
  * moe_get_status -- waits for `stream`, then reads and clears the calling

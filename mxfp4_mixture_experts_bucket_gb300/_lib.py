@@ -28,6 +28,8 @@ MOE_OK = 0
 MOE_EINVAL = -1
 MOE_ECUDA = -2
 MOE_EUNSUPPORTED = -3
+MOE_ESCRATCH = -4
+MOE_DECODE_SCRATCH_BYTES = 512 * 1024
 MOE_STATUS_BAD_EXPERT_ID = 0x1
 MOE_STATUS_WAIT_TIMEOUT = 0x2
 MOE_DTYPE_F32 = 0
@@ -59,6 +61,7 @@ _SIGS = {
     "moe_expert_gateup_swiglu": (I, [P, P, P, P, P, P, I, I, I, I, I, P, P, P, P, F, F, P, P]),
     "moe_expert_down_combine": (I, [P, P, P, I, I, I, I, I, P, P, P, P, P, P, P, P]),
     "moe_ffn_layer": (I, [P, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, I, P, SZ, P, P, P, P]),
+    "moe_ffn_layer_decode_static": (I, [P, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P]),
     "moe_get_status": (I, [P, ctypes.POINTER(ctypes.c_int)]),
     "moe_last_cuda_error": (I, []),
     "moe_kernel_launches": (ctypes.c_uint64, []),
@@ -172,6 +175,14 @@ def moe_ffn_layer(x, T, D, F, E, k, w_router, b_router, g_qs, g_sc, bg, u_qs, u_
                               _ptr(g_sc), _ptr(bg), _ptr(u_qs), _ptr(u_sc), _ptr(bu), _ptr(d_qs),
                               _ptr(d_sc), _ptr(bd), rail, _ptr(workspace), workspace_bytes, _ptr(y),
                               _ptr(ids_out), _ptr(weights_out), _stream(stream))
+
+
+def moe_ffn_layer_decode_static(x, T, D, F, E, k, w_router, b_router, g_qs, g_sc, bg, u_qs, u_sc, bu,
+                                d_qs, d_sc, bd, y, ids_out=None, weights_out=None, stream=None):
+    return _lib.moe_ffn_layer_decode_static(_ptr(x), T, D, F, E, k, _ptr(w_router), _ptr(b_router),
+                                            _ptr(g_qs), _ptr(g_sc), _ptr(bg), _ptr(u_qs), _ptr(u_sc),
+                                            _ptr(bu), _ptr(d_qs), _ptr(d_sc), _ptr(bd), _ptr(y),
+                                            _ptr(ids_out), _ptr(weights_out), _stream(stream))
 
 
 def moe_get_status(stream=None):
