@@ -199,23 +199,23 @@ int moe_mxfp4_grouped_mm(const uint8_t* w_qs, const uint8_t* w_sc, const float* 
 /*
  * moe_expert_gateup_swiglu -- stage 0 of the fused decode expert chain ("dasLLAMA
  * gpt-oss arc", fused MoE expert chain commit: gate+up rows + bias + activation
- * per expert row span), the GEMV rail's first expert kernel. For every expert e
- * with counts[e] > 0 and every assignment a = rows[p], p in [basep[e],
- * basep[e] + counts[e]), with t = a / k:
+ * per expert row span), the GEMV rail's first expert kernel (the routed-expert
+ * GEMV MetalMoeGemvMx4 takes the router's expert ids the same way). For every
+ * assignment a = t*k + j with e = ids[a] in [0, E):
  *   h[a] = swiglu_oai(Wg[e] x_t + bg[e], Wu[e] x_t + bu[e]; alpha, limit)
- * Each weight row is streamed once for all of the expert's tokens. x: float
- * [T][D]; gate/up planes [E][F][D/2], [E][F][D/32]; bg, bu [E][F] or NULL;
- * counts/basep/rows: moe_bucket output (any tile); h: float [T*k][F] in the
- * block-pair order read by moe_expert_down_combine (within each 32-float group
- * of a row, values are interleaved as the MXFP4 nibble pairs (i, i+16) and the
- * group's 16-byte quads are permuted by the group index); treat it as opaque.
+ * Each weight row is streamed from HBM once for all of the tokens routed to
+ * its expert. x: float [T][D]; ids: int32 [T][k]; gate/up planes [E][F][D/2],
+ * [E][F][D/32]; bg, bu [E][F] or NULL; h: float [T*k][F] in the block-pair
+ * order read by moe_expert_down_combine (within each 32-float group of a row,
+ * values are interleaved as the MXFP4 nibble pairs (i, i+16) and the group's
+ * 16-byte quads are permuted by the group index); treat it as opaque. Ids
+ * outside [0, E) are skipped and set MOE_STATUS_BAD_EXPERT_ID.
  * Requires 1 <= T <= MOE_GEMV_MAX_T, k <= 8, D and F multiples of 64, <= 4096.
  */
 int moe_expert_gateup_swiglu(const uint8_t* g_qs, const uint8_t* g_sc, const float* bg,
                              const uint8_t* u_qs, const uint8_t* u_sc, const float* bu, int E,
-                             int F, int D, int T, int k, const float* x, const int32_t* counts,
-                             const int32_t* basep, const int32_t* rows, float alpha, float limit,
-                             float* h, cudaStream_t stream);
+                             int F, int D, int T, int k, const float* x, const int32_t* ids,
+                             float alpha, float limit, float* h, cudaStream_t stream);
 
 /*
  * moe_expert_down_combine -- stage 1 of the fused decode expert chain: every
@@ -223,14 +223,13 @@ int moe_expert_gateup_swiglu(const uint8_t* g_qs, const uint8_t* g_sc, const flo
  * output row span:
  *   y[t][c] = sum_{j=0..k-1} weights[t][j] * (Wd[ids[t][j]][c] . h[t*k+j] + bd[ids[t][j]][c])
  * summed for j = 0, 1, ..., k-1 in that order (deterministic). h: output of
- * moe_expert_gateup_swiglu; ids, weights: float/int32 [T][k]; down planes
- * [E][D][F/2], [E][D][F/32]; bd [E][D] or NULL; y: float [T][D], overwritten.
- * Same limits as moe_expert_gateup_swiglu.
+ * moe_expert_gateup_swiglu; ids int32 [T][k], weights float [T][k]; down
+ * planes [E][D][F/2], [E][D][F/32]; bd [E][D] or NULL; y: float [T][D],
+ * overwritten. Same limits as moe_expert_gateup_swiglu.
  */
 int moe_expert_down_combine(const uint8_t* d_qs, const uint8_t* d_sc, const float* bd, int E, int D,
                             int F, int T, int k, const float* h, const int32_t* ids,
-                            const float* weights, const int32_t* counts, const int32_t* basep,
-                            const int32_t* rows, float* y, cudaStream_t stream);
+                            const float* weights, float* y, cudaStream_t stream);
 
 /*
  * moe_ffn_layer -- the whole routed-expert chain for T tokens:
@@ -241,7 +240,8 @@ int moe_expert_down_combine(const uint8_t* d_qs, const uint8_t* d_sc, const floa
  *   h_j  = swiglu_oai(Wg[e] x_t + bg[e], Wu[e] x_t + bu[e])  (alpha 1.702, limit 7)
  * Rails: MOE_RAIL_GEMV (T <= MOE_GEMV_MAX_T) streams the touched experts'
  * weights through fp32 CUDA-core GEMVs (gate/up + swiglu fused, down + bias +
- * slot-order combine fused; deterministic). MOE_RAIL_GROUPED_MM runs the
+ * slot-order combine fused; deterministic); its two expert kernels take the
+ * top-k of the router logits themselves, so a decode step is three kernels. MOE_RAIL_GROUPED_MM runs the
  * tcgen05 grouped GEMM with bf16 MMAs (x enters gate/up split into bf16 high
  * and low parts, h enters down rounded to bf16), the swiglu fused into the
  * gate/up epilogue and the weighted scatter fused into the down epilogue. MOE_RAIL_AUTO picks GEMV for T <= MOE_GEMV_MAX_T.

@@ -58,8 +58,8 @@ _SIGS = {
     "moe_swiglu_oai": (I, [P, P, P, I64, I, F, F, P]),
     "moe_gather_rows_bf16": (I, [P, I, I, I, P, P, I, I, P, P, P, P]),
     "moe_mxfp4_grouped_mm": (I, [P, P, P, P, P, P, I, I, I, P, P, P, P, P, I, I, P, I, F, F, P, I64, P]),
-    "moe_expert_gateup_swiglu": (I, [P, P, P, P, P, P, I, I, I, I, I, P, P, P, P, F, F, P, P]),
-    "moe_expert_down_combine": (I, [P, P, P, I, I, I, I, I, P, P, P, P, P, P, P, P]),
+    "moe_expert_gateup_swiglu": (I, [P, P, P, P, P, P, I, I, I, I, I, P, P, F, F, P, P]),
+    "moe_expert_down_combine": (I, [P, P, P, I, I, I, I, I, P, P, P, P, P]),
     "moe_ffn_layer": (I, [P, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, I, P, SZ, P, P, P, P]),
     "moe_ffn_layer_decode_static": (I, [P, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P]),
     "moe_get_status": (I, [P, ctypes.POINTER(ctypes.c_int)]),
@@ -154,18 +154,16 @@ def moe_mxfp4_grouped_mm(w_qs, w_sc, bias, w2_qs, w2_sc, bias2, E, R, C, a, a_lo
                                      _ptr(out), out_ld, _stream(stream))
 
 
-def moe_expert_gateup_swiglu(g_qs, g_sc, bg, u_qs, u_sc, bu, E, F, D, T, k, x, counts, basep, rows,
-                             alpha, limit, h, stream=None):
+def moe_expert_gateup_swiglu(g_qs, g_sc, bg, u_qs, u_sc, bu, E, F, D, T, k, x, ids, alpha, limit, h,
+                             stream=None):
     return _lib.moe_expert_gateup_swiglu(_ptr(g_qs), _ptr(g_sc), _ptr(bg), _ptr(u_qs), _ptr(u_sc),
-                                         _ptr(bu), E, F, D, T, k, _ptr(x), _ptr(counts), _ptr(basep),
-                                         _ptr(rows), alpha, limit, _ptr(h), _stream(stream))
+                                         _ptr(bu), E, F, D, T, k, _ptr(x), _ptr(ids), alpha, limit,
+                                         _ptr(h), _stream(stream))
 
 
-def moe_expert_down_combine(d_qs, d_sc, bd, E, D, F, T, k, h, ids, weights, counts, basep, rows, y,
-                            stream=None):
+def moe_expert_down_combine(d_qs, d_sc, bd, E, D, F, T, k, h, ids, weights, y, stream=None):
     return _lib.moe_expert_down_combine(_ptr(d_qs), _ptr(d_sc), _ptr(bd), E, D, F, T, k, _ptr(h),
-                                        _ptr(ids), _ptr(weights), _ptr(counts), _ptr(basep),
-                                        _ptr(rows), _ptr(y), _stream(stream))
+                                        _ptr(ids), _ptr(weights), _ptr(y), _stream(stream))
 
 
 def moe_ffn_layer(x, T, D, F, E, k, w_router, b_router, g_qs, g_sc, bg, u_qs, u_sc, bu, d_qs, d_sc,

@@ -323,39 +323,37 @@ int moe_mxfp4_grouped_mm(const uint8_t* w_qs, const uint8_t* w_sc, const float* 
 
 int moe_expert_gateup_swiglu(const uint8_t* g_qs, const uint8_t* g_sc, const float* bg,
                              const uint8_t* u_qs, const uint8_t* u_sc, const float* bu, int E,
-                             int F, int D, int T, int k, const float* x, const int32_t* counts,
-                             const int32_t* basep, const int32_t* rows, float alpha, float limit,
-                             float* h, cudaStream_t stream) {
+                             int F, int D, int T, int k, const float* x, const int32_t* ids,
+                             float alpha, float limit, float* h, cudaStream_t stream) {
   MOE_REQUIRE(T >= 0 && T <= MOE_GEMV_MAX_T && k >= 1 && k <= 8 && E >= 1 && E <= 256);
   MOE_REQUIRE(D >= 64 && F >= 64 && D % 64 == 0 && F % 64 == 0);
   if (D > 4096 || F > 4096) return MOE_EUNSUPPORTED;
   if (T == 0) return MOE_OK;
-  MOE_REQUIRE(g_qs && g_sc && u_qs && u_sc && x && counts && basep && rows && h);
+  MOE_REQUIRE(g_qs && g_sc && u_qs && u_sc && x && ids && h);
   MOE_REQUIRE(aligned(g_qs, 16) && aligned(u_qs, 16) && aligned(x, 16) && aligned(h, 16));
   DeviceInfo* d = nullptr;
   int rc = current_device(&d);
   if (rc != MOE_OK) return rc;
   Launch L{stream, false};
-  return cuda_status(launch_gemv_gateup_swiglu(g_qs, g_sc, bg, u_qs, u_sc, bu, E, F, D, T, k, x,
-                                               counts, basep, rows, alpha, limit, h, L));
+  return cuda_status(launch_gemv_gateup(g_qs, g_sc, bg, u_qs, u_sc, bu, E, F, D, T, k, x, nullptr,
+                                        ids, nullptr, nullptr, alpha, limit, h, d->status, L));
 }
 
 int moe_expert_down_combine(const uint8_t* d_qs, const uint8_t* d_sc, const float* bd, int E, int D,
                             int F, int T, int k, const float* h, const int32_t* ids,
-                            const float* weights, const int32_t* counts, const int32_t* basep,
-                            const int32_t* rows, float* y, cudaStream_t stream) {
+                            const float* weights, float* y, cudaStream_t stream) {
   MOE_REQUIRE(T >= 0 && T <= MOE_GEMV_MAX_T && k >= 1 && k <= 8 && E >= 1 && E <= 256);
   MOE_REQUIRE(D >= 64 && F >= 64 && D % 64 == 0 && F % 64 == 0);
   if (D > 4096 || F > 4096) return MOE_EUNSUPPORTED;
   if (T == 0) return MOE_OK;
-  MOE_REQUIRE(d_qs && d_sc && h && ids && weights && counts && basep && rows && y);
+  MOE_REQUIRE(d_qs && d_sc && h && ids && weights && y);
   MOE_REQUIRE(aligned(d_qs, 16) && aligned(h, 16));
   DeviceInfo* d = nullptr;
   int rc = current_device(&d);
   if (rc != MOE_OK) return rc;
   Launch L{stream, false};
-  return cuda_status(launch_gemv_down_combine(d_qs, d_sc, bd, E, D, F, T, k, h, ids, weights, counts,
-                                              basep, rows, y, L));
+  return cuda_status(launch_gemv_down(d_qs, d_sc, bd, E, D, F, T, k, h, nullptr, ids, weights, y,
+                                      d->status, L));
 }
 
 int moe_ffn_layer(const float* x, int T, int D, int F, int E, int k, const float* w_router,
@@ -394,19 +392,20 @@ int moe_ffn_layer(const float* x, int T, int D, int F, int E, int k, const float
   rc = cuda_status(launch_router_logits(x, T, D, w_router, b_router, E, ws.logits, L));
   if (rc != MOE_OK) return rc;
   L.pdl = true;
+  if (rail == MOE_RAIL_GEMV) {
+    // decode: the two expert kernels take the top-k of the logits themselves
+    rc = cuda_status(launch_gemv_gateup(g_qs, g_sc, bg, u_qs, u_sc, bu, E, F, D, T, k, x, ws.logits,
+                                        nullptr, ids_out, weights_out, alpha, limit, ws.h, d->status,
+                                        L));
+    if (rc != MOE_OK) return rc;
+    return cuda_status(launch_gemv_down(d_qs, d_sc, bd, E, D, F, T, k, ws.h, ws.logits, nullptr,
+                                        nullptr, y, d->status, L));
+  }
   rc = cuda_status(launch_topk_softmax(ws.logits, T, E, k, ids, wts, L));
   if (rc != MOE_OK) return rc;
-  const int tile = (rail == MOE_RAIL_GEMV) ? 1 : MOE_MM_TILE;
-  rc = cuda_status(launch_bucket(ids, T, k, E, tile, (int)ws.max_rows, ws.counts, ws.basep, ws.rows,
-                                 ws.inv, d->status, L));
+  rc = cuda_status(launch_bucket(ids, T, k, E, MOE_MM_TILE, (int)ws.max_rows, ws.counts, ws.basep,
+                                 ws.rows, ws.inv, d->status, L));
   if (rc != MOE_OK) return rc;
-  if (rail == MOE_RAIL_GEMV) {
-    rc = cuda_status(launch_gemv_gateup_swiglu(g_qs, g_sc, bg, u_qs, u_sc, bu, E, F, D, T, k, x,
-                                               ws.counts, ws.basep, ws.rows, alpha, limit, ws.h, L));
-    if (rc != MOE_OK) return rc;
-    return cuda_status(launch_gemv_down_combine(d_qs, d_sc, bd, E, D, F, T, k, ws.h, ids, wts,
-                                                ws.counts, ws.basep, ws.rows, y, L));
-  }
   rc = cuda_status(launch_gather_bf16(x, T, D, k, ws.rows, ws.basep, E, (int)ws.max_rows, ws.xg,
                                       ws.xg_lo, y, L));
   if (rc != MOE_OK) return rc;

@@ -10,13 +10,16 @@
 // bucket's padded end exit early (fusion commit, second bullet).
 //
 // GB300 mapping (one CTA per 128 weight rows x one 128-row bucket tile):
-//   warp 0      TMA producer: MXFP4 nibble tiles (3D map [E][R][C/2]), the
-//               tile's E8M0 rows (one bulk copy), bf16 activation tiles (2D
-//               map, 128-byte swizzle, only the live 32-row chunks)
+//   warp 0      TMA producer of the MXFP4 nibble tiles (3D map [E][R][C/2])
+//               into a raw ring as deep as shared memory allows (HBM latency
+//               is hidden here), plus the tile's E8M0 rows (one bulk copy)
 //   warp 1      TMEM owner and single-thread tcgen05.mma issuer
-//   warps 2-9   dequantise MXFP4 -> bf16 into the UMMA 128B-swizzled K-major
-//               layout; seed the accumulator with the bias (tcgen05.st); run
-//               the epilogue from TMEM (tcgen05.ld)
+//   warp 2      TMA producer of the bf16 activation tiles (2D map, 128-byte
+//               swizzle, only the live 32-row chunks) into its own ring, whose
+//               depth grows as the tile's live rows shrink
+//   warps 3-10  dequantise MXFP4 -> bf16 into the UMMA 128B-swizzled K-major
+//               layout (two-stage hand-off ring); seed the accumulator with
+//               the bias (tcgen05.st); run the epilogue from TMEM (tcgen05.ld)
 // The MMA is "swap-AB": weight rows fill M = 128 and the bucket rows fill N,
 // rounded up to 16, so rows past counts[e] cost no tensor work.
 #include <cuda.h>
@@ -29,13 +32,17 @@ namespace mm {
 constexpr int BM = 128;  // weight rows per tile (MMA M)
 constexpr int BN = 128;  // bucket rows per tile (CSR tile height, MMA N <= BN)
 constexpr int BK = 64;   // reduction columns per stage (one 128-byte bf16 row)
-constexpr int MAX_OS = 3;  // operand stages (A tiles + B tiles); 2 for gate/up with split activations
-constexpr int RS = 4;      // raw MXFP4 stages
-constexpr int kThreads = 320;
-constexpr int kDqThreads = 256;  // warps 2..9
-constexpr int kATile = BM * BK * 2;  // 16 KB
-constexpr int kBTile = BN * BK * 2;  // 16 KB
+constexpr int OSA = 2;   // dequantised A stages (dequant -> MMA hand-off)
+constexpr int MAX_RS = 16;   // raw MXFP4 stages (HBM latency is hidden here)
+constexpr int MAX_BS = 8;    // activation (B) stages
+constexpr int kThreads = 352;    // 11 warps
+constexpr int kDqWarp0 = 3;      // warps 3..10 dequantise and run the epilogue
+constexpr int kDqThreads = 256;
+constexpr int kATile = BM * BK * 2;      // 16 KB
+constexpr int kBChunk = 32 * BK * 2;     // 4 KB: 32 activation rows
+constexpr int kBPool = 64 * 1024;        // activation ring, carved per tile
 constexpr int kRawTile = BM * (BK / 2);  // 4 KB of nibbles
+constexpr uint32_t kSmemLimit = 232448;  // 227 KB opt-in per block
 
 struct Params {
   const uint8_t* w_sc[2];
@@ -53,54 +60,49 @@ struct Params {
   int box_rows;  // rows of one weight TMA box: min(BM, R)
 };
 
-// Operand stages: three, except gate+up with split (hi+lo) activations, whose
-// two A tiles and two B tiles per stage only fit shared memory twice.
-template <int NMAT, bool SPLIT>
-struct StageCfg {
-  static constexpr int OS = (NMAT == 2 && SPLIT) ? 2 : 3;
-  static constexpr int NB = SPLIT ? 2 : 1;  // B tiles per stage (activation hi, lo)
-};
-
+// Shared-memory plan (identical on host and device): A ring, activation pool,
+// raw ring as deep as the remaining space allows, the tile's E8M0 rows,
+// barriers, small per-tile tables.
 struct Layout {
   uint32_t a, b, raw, sc, bars, misc, total;
   uint32_t sc_stride;  // bytes per matrix
+  int rs;              // raw stages
 };
 
-__host__ __device__ inline Layout make_layout(int nmat, int C, int os, int nb) {
+__host__ __device__ inline Layout make_layout(int nmat, int C) {
   Layout L;
-  uint32_t off = 0;
-  L.a = off;
-  off += os * nmat * kATile;
-  L.b = off;
-  off += os * nb * kBTile;
-  L.raw = off;
-  off += RS * nmat * kRawTile;
-  L.sc = off;
+  L.a = 0;
+  L.b = OSA * nmat * kATile;
+  L.raw = L.b + kBPool;
   L.sc_stride = (uint32_t)((BM * (C / 32) + 15) & ~15);
-  off += nmat * L.sc_stride;
-  L.bars = (off + 7) & ~7u;
-  off = L.bars + 32 * 8;
-  L.misc = off;
-  off += BN * 4 * 2 + 64;  // s_rows, s_w, tmem slot, abort flag, tile info
-  L.total = off + 1024;    // slack for 1024-byte alignment of the dynamic base
+  const uint32_t sc_size = nmat * L.sc_stride;
+  const uint32_t tail = 64 * 8 + (BN * 8 + 64) + 1024;  // barriers, tables, alignment slack
+  const uint32_t budget = kSmemLimit - L.raw - sc_size - tail;
+  int rs = (int)(budget / (uint32_t)(nmat * kRawTile));
+  L.rs = rs > MAX_RS ? MAX_RS : rs;
+  L.sc = L.raw + L.rs * nmat * kRawTile;
+  L.bars = (L.sc + sc_size + 7) & ~7u;
+  L.misc = L.bars + 64 * 8;
+  L.total = L.misc + BN * 8 + 64 + 1024;
   return L;
 }
 
 // barrier indices
 constexpr int kRawFull = 0;
-constexpr int kRawEmpty = kRawFull + RS;
-constexpr int kAFull = kRawEmpty + RS;
-constexpr int kBFull = kAFull + MAX_OS;
-constexpr int kOpEmpty = kBFull + MAX_OS;
-constexpr int kAccFull = kOpEmpty + MAX_OS;
+constexpr int kRawEmpty = kRawFull + MAX_RS;
+constexpr int kAFull = kRawEmpty + MAX_RS;
+constexpr int kAEmpty = kAFull + OSA;
+constexpr int kBFull = kAEmpty + OSA;
+constexpr int kBEmpty = kBFull + MAX_BS;
+constexpr int kAccFull = kBEmpty + MAX_BS;
 constexpr int kScFull = kAccFull + 1;
 constexpr int kBiasReady = kScFull + 1;
 constexpr int kNumBars = kBiasReady + 1;
-static_assert(kNumBars <= 32, "barrier space");
+static_assert(kNumBars <= 64, "barrier space");
 
 // f16x2 (unscaled E2M1 pair) * 2^(s-127) -> bf16x2, exact whenever representable.
 __device__ __forceinline__ uint32_t scale_to_bf16x2(uint32_t h2, float scale) {
-  float2 f = f16x2_to_float2(h2);
+  const float2 f = f16x2_to_float2(h2);
   __nv_bfloat162 b = __floats2bfloat162_rn(f.x * scale, f.y * scale);
   return *reinterpret_cast<uint32_t*>(&b);
 }
@@ -129,8 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     grouped_mm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
                       const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_alo,
                       const Params p) {
-  constexpr int OS = StageCfg<NMAT, SPLIT>::OS;
-  constexpr int NB = StageCfg<NMAT, SPLIT>::NB;
+  constexpr int NB = SPLIT ? 2 : 1;  // activation tiles per stage (hi, lo)
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -159,7 +160,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int rows_here = min(BM, p.R - m0);
   const bool seeded = (p.bias[0] != nullptr) || (NMAT == 2 && p.bias[1] != nullptr);
 
-  const Layout L = make_layout(NMAT, p.C, OS, NB);
+  const Layout L = make_layout(NMAT, p.C);
+  const int RS = L.rs;
+  const uint32_t b_stage = (uint32_t)(NB * nchunk * kBChunk);
+  const int NBS = min(MAX_BS, (int)(kBPool / b_stage));
   const uint32_t sbase = tc::smem_u32(smem);
   const uint32_t sA = sbase + L.a, sB = sbase + L.b, sRaw = sbase + L.raw;
   const uint8_t* scs = smem + L.sc;
@@ -175,10 +179,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(bar(kRawFull + i), 1);
       tc::mbar_init(bar(kRawEmpty + i), kDqThreads);
     }
-    for (int i = 0; i < OS; ++i) {
+    for (int i = 0; i < OSA; ++i) {
       tc::mbar_init(bar(kAFull + i), kDqThreads);
+      tc::mbar_init(bar(kAEmpty + i), 1);
+    }
+    for (int i = 0; i < NBS; ++i) {
       tc::mbar_init(bar(kBFull + i), 1);
-      tc::mbar_init(bar(kOpEmpty + i), 1);
+      tc::mbar_init(bar(kBEmpty + i), 1);
     }
     tc::mbar_init(bar(kAccFull), 1);
     tc::mbar_init(bar(kScFull), 1);
@@ -205,20 +212,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------ raw MXFP4 producer
     if (lane == 0) {
       tc::prefetch_tmap(&tm_w0);
       if (NMAT == 2) tc::prefetch_tmap(&tm_w1);
-      tc::prefetch_tmap(&tm_a);
-      if (SPLIT) tc::prefetch_tmap(&tm_alo);
       const uint32_t sc_bytes = (uint32_t)(rows_here * nbc);
       tc::mbar_expect_tx(bar(kScFull), NMAT * sc_bytes);
       for (int mat = 0; mat < NMAT; ++mat)
         tc::bulk_load(sbase + L.sc + mat * L.sc_stride,
                       p.w_sc[mat] + ((size_t)e * p.R + m0) * nbc, sc_bytes, bar(kScFull));
       const uint32_t raw_bytes = (uint32_t)(NMAT * p.box_rows * (BK / 2));
-      const uint32_t b_bytes = (uint32_t)(NB * nchunk * 32 * BK * 2);
-      int raw_issued = 0, b_issued = 0;
+      int issued = 0;
       for (int ks = 0; ks < nk; ++ks) {
         const int rs = ks % RS, rn = ks / RS;
         if (rn > 0 && !tc::mbar_wait(bar(kRawEmpty + rs), (rn - 1) & 1, s_abort)) { fail(); break; }
@@ -228,71 +232,84 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (NMAT == 2)
           tc::tma_load_3d(sRaw + (rs * NMAT + 1) * kRawTile, &tm_w1, ks * (BK / 2), m0, e,
                           bar(kRawFull + rs));
-        raw_issued = ks + 1;
-        const int os = ks % OS, on = ks / OS;
-        if (on > 0 && !tc::mbar_wait(bar(kOpEmpty + os), (on - 1) & 1, s_abort)) { fail(); break; }
-        tc::mbar_expect_tx(bar(kBFull + os), b_bytes);
-        for (int c = 0; c < nchunk; ++c) {
-          tc::tma_load_2d(sB + (os * NB) * kBTile + c * (32 * BK * 2), &tm_a, ks * BK,
-                          tile_row0 + 32 * c, bar(kBFull + os));
-          if (SPLIT)
-            tc::tma_load_2d(sB + (os * NB + 1) * kBTile + c * (32 * BK * 2), &tm_alo, ks * BK,
-                            tile_row0 + 32 * c, bar(kBFull + os));
-        }
-        b_issued = ks + 1;
+        issued = ks + 1;
       }
-      if (*s_abort) {
-        // let every copy already issued land before the CTA's shared memory goes away
+      if (*s_abort) {  // let every copy already issued land before shared memory goes away
         for (int s = 0; s < RS; ++s) {
-          const int n = (raw_issued > s) ? (raw_issued - 1 - s) / RS + 1 : 0;
+          const int n = (issued > s) ? (issued - 1 - s) / RS + 1 : 0;
           if (n > 0) tc::mbar_wait(bar(kRawFull + s), (n - 1) & 1, nullptr);
-        }
-        for (int s = 0; s < OS; ++s) {
-          const int n = (b_issued > s) ? (b_issued - 1 - s) / OS + 1 : 0;
-          if (n > 0) tc::mbar_wait(bar(kBFull + s), (n - 1) & 1, nullptr);
         }
         tc::mbar_wait(bar(kScFull), 0, nullptr);
       }
     }
+  } else if (warp == 2) {
+    // ------------------------------------------------ activation producer
+    if (lane == 0) {
+      tc::prefetch_tmap(&tm_a);
+      if (SPLIT) tc::prefetch_tmap(&tm_alo);
+      int issued = 0;
+      for (int ks = 0; ks < nk; ++ks) {
+        const int bs = ks % NBS, bn = ks / NBS;
+        if (bn > 0 && !tc::mbar_wait(bar(kBEmpty + bs), (bn - 1) & 1, s_abort)) { fail(); break; }
+        tc::mbar_expect_tx(bar(kBFull + bs), b_stage);
+        const uint32_t dst = sB + bs * b_stage;
+        for (int c = 0; c < nchunk; ++c) {
+          tc::tma_load_2d(dst + c * kBChunk, &tm_a, ks * BK, tile_row0 + 32 * c, bar(kBFull + bs));
+          if (SPLIT)
+            tc::tma_load_2d(dst + (nchunk + c) * kBChunk, &tm_alo, ks * BK, tile_row0 + 32 * c,
+                            bar(kBFull + bs));
+        }
+        issued = ks + 1;
+      }
+      if (*s_abort) {
+        for (int s = 0; s < NBS; ++s) {
+          const int n = (issued > s) ? (issued - 1 - s) / NBS + 1 : 0;
+          if (n > 0) tc::mbar_wait(bar(kBFull + s), (n - 1) & 1, nullptr);
+        }
+      }
+    }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc = tc::idesc_bf16_f32(BM, n_mma);
       bool ok = true;
       if (seeded && !tc::mbar_wait(bar(kBiasReady), 0, s_abort)) { fail(); ok = false; }
       tc::fence_after_sync();
       for (int ks = 0; ok && ks < nk; ++ks) {
-        const int os = ks % OS, on = ks / OS;
-        if (!tc::mbar_wait(bar(kAFull + os), on & 1, s_abort) ||
-            !tc::mbar_wait(bar(kBFull + os), on & 1, s_abort)) {
+        const int as = ks % OSA, an = ks / OSA;
+        const int bs = ks % NBS, bn = ks / NBS;
+        if (!tc::mbar_wait(bar(kAFull + as), an & 1, s_abort) ||
+            !tc::mbar_wait(bar(kBFull + bs), bn & 1, s_abort)) {
           fail();
           break;
         }
         tc::fence_after_sync();
+        const uint32_t bbase = sB + bs * b_stage;
 #pragma unroll
         for (int mat = 0; mat < NMAT; ++mat) {
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = tc::sw128_kmajor_desc(sA + (os * NMAT + mat) * kATile + kk * 32);
+            const uint64_t ad = tc::sw128_kmajor_desc(sA + (as * NMAT + mat) * kATile + kk * 32);
 #pragma unroll
             for (int hl = 0; hl < NB; ++hl) {  // activation hi part, then its lo part
-              const uint64_t bd = tc::sw128_kmajor_desc(sB + (os * NB + hl) * kBTile + kk * 32);
+              const uint64_t bd = tc::sw128_kmajor_desc(bbase + hl * nchunk * kBChunk + kk * 32);
               tc::mma_bf16(tmem + mat * 128, ad, bd, idesc,
                            (ks > 0 || kk > 0 || hl > 0 || seeded) ? 1u : 0u);
             }
           }
         }
-        tc::mma_commit(bar(kOpEmpty + os));
+        tc::mma_commit(bar(kAEmpty + as));
+        tc::mma_commit(bar(kBEmpty + bs));
       }
       // completes once every MMA issued above has finished
       tc::mma_commit(bar(kAccFull));
     }
   } else {
-    // ------------------------------------------------------------ dequant + epilogue
-    const int dt = threadIdx.x - 64;  // 0..255
-    const int q = warp & 3;           // TMEM lane quarter this warp may access
-    const int colhalf = (warp - 2) >> 2;
-    const int trow = 32 * q + lane;   // TMEM lane = weight row within the tile
+    // ------------------------------------------------ dequant + epilogue
+    const int dt = threadIdx.x - kDqWarp0 * 32;  // 0..255
+    const int q = warp & 3;                      // TMEM lane quarter this warp may access
+    const int colhalf = (warp - kDqWarp0) >> 2;
+    const int trow = 32 * q + lane;              // TMEM lane = weight row within the tile
     const int f = m0 + trow;
     if (seeded) {
       for (int mat = 0; mat < NMAT; ++mat) {
@@ -309,9 +326,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) fail();
     for (int ks = 0; ok && ks < nk; ++ks) {
       const int rs = ks % RS, rn = ks / RS;
-      const int os = ks % OS, on = ks / OS;
+      const int as = ks % OSA, an = ks / OSA;
       if (!tc::mbar_wait(bar(kRawFull + rs), rn & 1, s_abort) ||
-          (on > 0 && !tc::mbar_wait(bar(kOpEmpty + os), (on - 1) & 1, s_abort))) {
+          (an > 0 && !tc::mbar_wait(bar(kAEmpty + as), (an - 1) & 1, s_abort))) {
         fail();
         break;
       }
@@ -322,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float scale = e8m0_to_f32(scs[mat * L.sc_stride + r * nbc + 2 * ks + kb]);
         uint32_t o[16];
         dequant_block_bf16(qv, scale, o);
-        uint8_t* arow = smem + L.a + (os * NMAT + mat) * kATile + r * 128;
+        uint8_t* arow = smem + L.a + (as * NMAT + mat) * kATile + r * 128;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const int chunk = kb * 4 + c;
@@ -332,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(bar(kRawEmpty + rs));
-      tc::mbar_arrive(bar(kAFull + os));
+      tc::mbar_arrive(bar(kAFull + as));
     }
     // epilogue: TMEM -> registers -> global (warp-uniform decision: tcgen05.ld is warp-wide)
     __syncwarp();
@@ -432,8 +449,8 @@ template <int NMAT, int EPI, bool SPLIT>
 static cudaError_t launch_mm(const GroupedMMArgs& g, const CUtensorMap& t0, const CUtensorMap& t1,
                              const CUtensorMap& ta, const CUtensorMap& talo, const mm::Params& prm,
                              Launch L) {
-  using C = mm::StageCfg<NMAT, SPLIT>;
-  const mm::Layout lay = mm::make_layout(NMAT, g.C, C::OS, C::NB);
+  const mm::Layout lay = mm::make_layout(NMAT, g.C);
+  if (lay.rs < 2 || lay.total > mm::kSmemLimit) return cudaErrorInvalidValue;
   cudaError_t err = ensure_smem_limit(mm::grouped_mm_kernel<NMAT, EPI, SPLIT>, lay.total);
   if (err != cudaSuccess) return err;
   dim3 grid((g.R + mm::BM - 1) / mm::BM, g.max_rows / mm::BN);

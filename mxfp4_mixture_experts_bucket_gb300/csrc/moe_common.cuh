@@ -71,16 +71,13 @@ __device__ __forceinline__ float2 f16x2_to_float2(uint32_t h) {
   return __half22float2(v);
 }
 
-// Packed fp32 FMA on two lanes (Blackwell f32x2 datapath).
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  uint64_t ra, rb, rc, rd;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(rc) : "f"(c.x), "f"(c.y));
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
-  float2 d;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
-  return d;
+// Four bytes of E2M1 pairs -> four f16x2 (byte i -> h[i], low nibble -> low half).
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&h)[4]) {
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
 }
 
 // ---------------------------------------------------------------------------
@@ -110,25 +107,25 @@ __device__ __forceinline__ void load_pair_group(const float4* __restrict__ vec, 
 }
 
 // Dot of one MXFP4 block (16 nibble bytes, unscaled E2M1 values) with the
-// block's pairs of a vector (xv from load_pair_group). fp32 products and sums.
+// block's pairs of a vector (xv from load_pair_group). fp32 products and sums,
+// two lanes per instruction on the Blackwell f32x2 FMA path.
 __device__ __forceinline__ float mx_block_dot(uint4 q, const float4 (&xv)[8]) {
   const uint32_t w[4] = {q.x, q.y, q.z, q.w};
   float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
     // bytes 4m..4m+3 of the block are pairs 4m..4m+3 -> xv[2m], xv[2m+1]
+    uint32_t h[4];
+    e2m1x8_to_f16x2x4(w[m], h);
     const float4 xa = xv[2 * m];
     const float4 xb = xv[2 * m + 1];
-    const float2 v0 = f16x2_to_float2(e2m1x2_to_f16x2(w[m], 0));
-    const float2 v1 = f16x2_to_float2(e2m1x2_to_f16x2(w[m], 1));
-    const float2 v2 = f16x2_to_float2(e2m1x2_to_f16x2(w[m], 2));
-    const float2 v3 = f16x2_to_float2(e2m1x2_to_f16x2(w[m], 3));
-    acc0 = ffma2(v0, make_float2(xa.x, xa.y), acc0);
-    acc1 = ffma2(v1, make_float2(xa.z, xa.w), acc1);
-    acc0 = ffma2(v2, make_float2(xb.x, xb.y), acc0);
-    acc1 = ffma2(v3, make_float2(xb.z, xb.w), acc1);
+    acc0 = __ffma2_rn(f16x2_to_float2(h[0]), make_float2(xa.x, xa.y), acc0);
+    acc1 = __ffma2_rn(f16x2_to_float2(h[1]), make_float2(xa.z, xa.w), acc1);
+    acc0 = __ffma2_rn(f16x2_to_float2(h[2]), make_float2(xb.x, xb.y), acc0);
+    acc1 = __ffma2_rn(f16x2_to_float2(h[3]), make_float2(xb.z, xb.w), acc1);
   }
-  return (acc0.x + acc1.x) + (acc0.y + acc1.y);
+  const float2 acc = __fadd2_rn(acc0, acc1);
+  return acc.x + acc.y;
 }
 
 // ---------------------------------------------------------------------------
@@ -167,6 +164,62 @@ __device__ __forceinline__ uint32_t ldg_nc_u8(const uint8_t* p) {
   uint16_t r;
   asm volatile("ld.global.nc.u8 %0, [%1];" : "=h"(r) : "l"(p));
   return (uint32_t)r;
+}
+
+// ---------------------------------------------------------------------------
+// Router top-k then softmax over the k selected, one warp per token (E <= 256,
+// k <= 32). Order: descending logit, lower expert index first on equal
+// logits; NaN logits never win. Lane j < k gets slot j's expert and weight
+// exp(l_j - l_0) / sum_m exp(l_m - l_0).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ bool topk_better(float va, int ia, float vb, int ib) {
+  return (va > vb) || (va == vb && ia < ib);
+}
+
+__device__ __forceinline__ void warp_topk_softmax(const float* __restrict__ lt, int E, int k, int lane,
+                                                  int& my_id, float& my_w) {
+  constexpr int MAXPER = 8;
+  float v[MAXPER];
+#pragma unroll
+  for (int q = 0; q < MAXPER; ++q) {
+    const int e = lane + 32 * q;
+    float val = (e < E) ? lt[e] : -INFINITY;
+    if (val != val) val = -INFINITY;
+    v[q] = val;
+  }
+  uint32_t taken = 0;  // bit q: expert lane+32q already selected
+  float top0 = 0.f, sum = 0.f, my_ex = 0.f;
+  my_id = -1;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int q = 0; q < MAXPER; ++q) {
+      const int e = lane + 32 * q;
+      if (e < E && !((taken >> q) & 1u) && topk_better(v[q], e, bv, bi)) {
+        bv = v[q];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (topk_better(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (j == 0) top0 = bv;
+    const float ex = expf(bv - top0);
+    sum += ex;
+    if (lane == j) {
+      my_ex = ex;
+      my_id = bi;
+    }
+  }
+  my_w = my_ex / sum;
 }
 
 // ---------------------------------------------------------------------------

@@ -76,22 +76,21 @@ cudaError_t launch_mxfp4_gemv(const uint8_t* qs, const uint8_t* sc, int E, int R
                               const float* bias, float* out, int* status, Launch L);
 cudaError_t launch_swiglu(const float* g, const float* u, void* h, int64_t n, int h_dtype,
                           float alpha, float limit, Launch L);
-// Decode rail: gate/up projections + bias + swiglu for the bucketed assignments.
-// h is written pair-swizzled, one row of F floats per assignment t*k+j.
-cudaError_t launch_gemv_gateup_swiglu(const uint8_t* g_qs, const uint8_t* g_sc, const float* bg,
-                                      const uint8_t* u_qs, const uint8_t* u_sc, const float* bu,
-                                      int E, int F, int D, int T, int k, const float* x,
-                                      const int32_t* counts, const int32_t* basep,
-                                      const int32_t* rows, float alpha, float limit, float* h,
-                                      Launch L);
-// Decode rail: down projection + bias + router-weighted combine in slot order.
-cudaError_t launch_gemv_down_combine(const uint8_t* d_qs, const uint8_t* d_sc, const float* bd,
-                                     int E, int D, int F, int T, int k, const float* h,
-                                     const int32_t* ids, const float* w, const int32_t* counts,
-                                     const int32_t* basep, const int32_t* rows, float* y,
-                                     Launch L);
-size_t gemv_gateup_smem_bytes(int T, int D);
-size_t gemv_down_smem_bytes(int T, int k, int F);
+// Decode rail, stage 0: gate/up projections + bias + swiglu for every routed
+// assignment. Routing comes from `logits` (top-k + softmax inside the kernel)
+// when not NULL, else from `ids_in`; CTA 0 writes it to ids_out / w_out if not
+// NULL. h: [T*k][F] floats in block-pair order.
+cudaError_t launch_gemv_gateup(const uint8_t* g_qs, const uint8_t* g_sc, const float* bg,
+                               const uint8_t* u_qs, const uint8_t* u_sc, const float* bu, int E,
+                               int F, int D, int T, int k, const float* x, const float* logits,
+                               const int32_t* ids_in, int32_t* ids_out, float* w_out, float alpha,
+                               float limit, float* h, int* status, Launch L);
+// Decode rail, stage 1: down projection + bias + router-weighted combine in slot
+// order. Routing from `logits` when not NULL, else from ids_in / w_in.
+cudaError_t launch_gemv_down(const uint8_t* d_qs, const uint8_t* d_sc, const float* bd, int E,
+                             int D, int F, int T, int k, const float* h, const float* logits,
+                             const int32_t* ids_in, const float* w_in, float* y, int* status,
+                             Launch L);
 
 // ---- grouped_mm.cu ----
 struct GroupedMMArgs {

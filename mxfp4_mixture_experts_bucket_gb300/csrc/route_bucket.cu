@@ -71,12 +71,7 @@ __global__ void __launch_bounds__(128) router_logits_kernel(const float* __restr
 
 // ---------------------------------------------------------------------------
 // Top-k then softmax over the k selected; one warp per token.
-// Order: descending logit, lower expert index first on equal logits.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
-  return (va > vb) || (va == vb && ia < ib);
-}
-
 __global__ void __launch_bounds__(256) topk_softmax_kernel(const float* __restrict__ logits, int T,
                                                            int E, int k, int32_t* __restrict__ ids,
                                                            float* __restrict__ w) {
@@ -85,48 +80,13 @@ __global__ void __launch_bounds__(256) topk_softmax_kernel(const float* __restri
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= T) return;
-  constexpr int MAXPER = 8;  // E <= 256
-  float v[MAXPER];
-  const float* lt = logits + (size_t)t * E;
-#pragma unroll
-  for (int q = 0; q < MAXPER; ++q) {
-    const int e = lane + 32 * q;
-    float val = (e < E) ? lt[e] : -INFINITY;
-    if (val != val) val = -INFINITY;  // NaN never wins
-    v[q] = val;
+  int my_id;
+  float my_w;
+  warp_topk_softmax(logits + (size_t)t * E, E, k, lane, my_id, my_w);
+  if (lane < k) {
+    ids[(size_t)t * k + lane] = my_id;
+    w[(size_t)t * k + lane] = my_w;
   }
-  uint32_t taken = 0;  // bit q: expert lane+32q already selected
-  float top0 = 0.f, sum = 0.f, my_ex = 0.f;  // lane j keeps exp(l_j - l_0) of slot j (k <= 32)
-  for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-#pragma unroll
-    for (int q = 0; q < MAXPER; ++q) {
-      const int e = lane + 32 * q;
-      if (e < E && !((taken >> q) & 1u) && better(v[q], e, bv, bi)) {
-        bv = v[q];
-        bi = e;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (better(ov, oi, bv, bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    if (j == 0) top0 = bv;
-    const float ex = expf(bv - top0);
-    sum += ex;
-    if (lane == j) {
-      my_ex = ex;
-      ids[(size_t)t * k + j] = bi;
-    }
-  }
-  if (lane < k) w[(size_t)t * k + lane] = my_ex / sum;
 }
 
 // ---------------------------------------------------------------------------

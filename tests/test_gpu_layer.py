@@ -190,3 +190,28 @@ def test_layer_without_biases(moe):
         y, ids, _ = run_layer(moe, layer, x, rail, spec.k)
         assert np.array_equal(ids, ids64)
         assert O.rownorm_rel_err(y, ref).max() <= tol
+
+
+@pytest.mark.parametrize("T", [1, 3, 8])
+def test_decode_stage_entry_points_match_the_layer(moe, T):
+    """moe_route_topk -> moe_expert_gateup_swiglu -> moe_expert_down_combine (ids given)
+    equals the layer's GEMV rail (top-k taken inside the expert kernels), and the oracle."""
+    spec, L, layer, cache = layer_for(moe, 1)
+    E, k, D, F = spec.E, spec.k, spec.D, spec.F
+    x_np = make_tokens(spec, T=T, seed=60 + T)
+    y_layer, ids_l, w_l = run_layer(moe, layer, x_np, moe.MOE_RAIL_GEMV, k)
+    W = layer.w
+    x = dev(x_np)
+    logits, ids, w = empty((T, E), torch.float32), empty((T, k), torch.int32), empty((T, k), torch.float32)
+    assert moe.moe_route_topk(x, T, D, W["w_router"], W["b_router"], E, k, logits, ids, w) == 0
+    h = empty((T * k, F), torch.float32)
+    assert moe.moe_expert_gateup_swiglu(W["g_qs"], W["g_sc"], W["bg"], W["u_qs"], W["u_sc"], W["bu"], E, F, D,
+                                        T, k, x, ids, 1.702, 7.0, h) == 0
+    y = empty((T, D), torch.float32)
+    assert moe.moe_expert_down_combine(W["d_qs"], W["d_sc"], W["bd"], E, D, F, T, k, h, ids, w, y) == 0
+    torch.cuda.synchronize()
+    assert status(moe) == 0
+    assert np.array_equal(ids.cpu().numpy(), ids_l) and np.array_equal(w.cpu().numpy(), w_l)
+    assert torch.equal(y.cpu(), torch.from_numpy(y_layer))
+    y64, _, _, _ = O.moe_layer(L, x_np, k, ids=ids_l, weights=w_l.astype(np.float64), cache=cache)
+    assert O.rownorm_rel_err(y_layer, y64).max() <= DECODE_TOL
