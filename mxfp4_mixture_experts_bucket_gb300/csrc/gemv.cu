@@ -591,7 +591,7 @@ cudaError_t launch_swiglu(const float* g, const float* u, void* h, int64_t n, in
 // Shared memory of the decode kernels: the tokens (or h) plus a ring of weight
 // stages; 2 CTAs per SM when the tokens are few, one otherwise.
 static int gv_stages(size_t fixed_bytes, size_t stage_bytes) {
-  const size_t budget = (fixed_bytes + 16 * stage_bytes <= 100 * 1024) ? 100 * 1024 : 200 * 1024;
+  const size_t budget = (fixed_bytes + 12 * stage_bytes <= 100 * 1024) ? 100 * 1024 : 200 * 1024;
   size_t n = (budget > fixed_bytes) ? (budget - fixed_bytes) / stage_bytes : 0;
   if (n > (size_t)kGvMaxStages) n = kGvMaxStages;
   return (int)n;
