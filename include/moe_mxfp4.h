@@ -299,6 +299,16 @@ int moe_ffn_layer_decode_static(const float* x, int T, int D, int F, int E, int 
  */
 int moe_get_status(cudaStream_t stream, int* status);
 
+/*
+ * moe_get_timeout_site -- waits for `stream`, then reads and clears the site of
+ * the first pipeline wait that gave up on the calling device since the last
+ * read (0: none): kernel << 24 | role << 20 | stage << 12 | sequence index,
+ * kernel 1 = decode gate/up, 2 = decode down, 3 = grouped GEMM; role 0 = a
+ * producer waiting for a free stage, 1 = a consumer waiting for data (grouped
+ * GEMM: the warp index of the waiting role, 3 = dequant). For diagnosis only.
+ */
+int moe_get_timeout_site(cudaStream_t stream, int* site);
+
 /* moe_last_cuda_error -- the cudaError_t of the last MOE_ECUDA in this thread. */
 int moe_last_cuda_error(void);
 

@@ -63,6 +63,7 @@ _SIGS = {
     "moe_ffn_layer": (I, [P, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, I, P, SZ, P, P, P, P]),
     "moe_ffn_layer_decode_static": (I, [P, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P]),
     "moe_get_status": (I, [P, ctypes.POINTER(ctypes.c_int)]),
+    "moe_get_timeout_site": (I, [P, ctypes.POINTER(ctypes.c_int)]),
     "moe_last_cuda_error": (I, []),
     "moe_kernel_launches": (ctypes.c_uint64, []),
 }
@@ -186,6 +187,12 @@ def moe_ffn_layer_decode_static(x, T, D, F, E, k, w_router, b_router, g_qs, g_sc
 def moe_get_status(stream=None):
     v = ctypes.c_int(0)
     rc = _lib.moe_get_status(_stream(stream), ctypes.byref(v))
+    return rc, v.value
+
+
+def moe_get_timeout_site(stream=None):
+    v = ctypes.c_int(0)
+    rc = _lib.moe_get_timeout_site(_stream(stream), ctypes.byref(v))
     return rc, v.value
 
 

@@ -14,7 +14,8 @@
 
 namespace moe {
 
-__device__ int g_status_word;  // MOE_STATUS_* bits, one per device
+// Per device: [0] MOE_STATUS_* bits, [1] the first timeout site (moe_get_timeout_site).
+__device__ int g_status_word[2];
 
 static std::atomic<uint64_t> g_launches{0};
 static thread_local int t_last_cuda_error = 0;
@@ -468,6 +469,23 @@ int moe_get_status(cudaStream_t stream, int* status) {
   if ((err = cudaMemcpy(d->status, &zero, sizeof(int), cudaMemcpyHostToDevice)) != cudaSuccess)
     return cuda_status(err);
   *status = v;
+  return MOE_OK;
+}
+
+int moe_get_timeout_site(cudaStream_t stream, int* site) {
+  MOE_REQUIRE(site != nullptr);
+  DeviceInfo* d = nullptr;
+  int rc = current_device(&d);
+  if (rc != MOE_OK) return rc;
+  cudaError_t err = cudaStreamSynchronize(stream);
+  if (err != cudaSuccess) return cuda_status(err);
+  int v = 0;
+  if ((err = cudaMemcpy(&v, d->status + 1, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_status(err);
+  const int zero = 0;
+  if ((err = cudaMemcpy(d->status + 1, &zero, sizeof(int), cudaMemcpyHostToDevice)) != cudaSuccess)
+    return cuda_status(err);
+  *site = v;
   return MOE_OK;
 }
 

@@ -238,6 +238,7 @@ __global__ void __launch_bounds__(kGvThreads) gemv_gateup_kernel(
   const int ntask = nact * half;
   const int G = gridDim.x;
   const uint32_t stage_bytes = (uint32_t)(2 * D);
+  const int spc = nstages / kGvConsumers;  // stages owned by each consumer warp
   const volatile int* abort_flag = &s_abort;
 
   if (warp == 0) {
@@ -249,10 +250,11 @@ __global__ void __launch_bounds__(kGvThreads) gemv_gateup_kernel(
         const int ai = i / half;
         const int f0 = (i - ai * half) * 2;
         const int e = R.act_e[ai];
-        const int s = m % nstages, n = m / nstages;
+        const int j = m / kGvConsumers;  // the consumer's own task counter
+        const int s = (m % kGvConsumers) * spc + j % spc, n = j / spc;
         if (n > 0 && !tc::mbar_wait(tc::smem_u32(&empty_bar[s]), (n - 1) & 1, abort_flag)) {
           s_abort = 1;
-          set_status(status, 0x2);
+          report_timeout(status, 1, 0, s, m);
           break;
         }
         const uint32_t fb = tc::smem_u32(&full_bar[s]);
@@ -262,10 +264,10 @@ __global__ void __launch_bounds__(kGvThreads) gemv_gateup_kernel(
         tc::bulk_load(dst + D, u_qs + ((size_t)e * F + f0) * (D / 2), (uint32_t)D, fb);
         issued = m + 1;
       }
-      if (s_abort)
-        for (int s = 0; s < nstages; ++s) {
-          const int n = (issued > s) ? (issued - 1 - s) / nstages + 1 : 0;
-          if (n > 0) tc::mbar_wait(tc::smem_u32(&full_bar[s]), (n - 1) & 1, nullptr);
+      if (s_abort)  // let every copy already issued land before shared memory goes away
+        for (int m = (issued > 2 * nstages ? issued - 2 * nstages : 0); m < issued; ++m) {
+          const int j = m / kGvConsumers;
+          tc::mbar_wait(tc::smem_u32(&full_bar[(m % kGvConsumers) * spc + j % spc]), (j / spc) & 1, nullptr);
         }
     }
   } else {
@@ -297,10 +299,11 @@ __global__ void __launch_bounds__(kGvThreads) gemv_gateup_kernel(
       const int ai = i / half;
       const int f0 = (i - ai * half) * 2;
       const int e = R.act_e[ai];
-      const int s = m % nstages, n = m / nstages;
+      const int j = m / kGvConsumers;
+      const int s = cw * spc + j % spc, n = j / spc;
       if (!tc::mbar_wait(tc::smem_u32(&full_bar[s]), n & 1, abort_flag)) {
         s_abort = 1;
-        set_status(status, 0x2);
+        report_timeout(status, 1, 1, s, m);
         break;
       }
       const uint8_t* st = ring + (size_t)s * stage_bytes;
@@ -359,10 +362,10 @@ __global__ void __launch_bounds__(kGvThreads) gemv_gateup_kernel(
 // Fused down + bias + router-weighted combine in slot order (stage 1).
 // A CTA owns row pairs (c0, c0+1) = 2 * (blockIdx.x + G*m); for each it needs
 // the two down rows of every active expert (F bytes, contiguous). Warp 0
-// streams them into the shared-memory ring in (row pair, expert) order;
-// consumer warp m % 8 handles row pair m: dots each expert's rows with the h
-// rows of that expert's assignments, then lanes t < T sum the k slots of
-// token t in slot order.
+// streams them in (row pair, expert) order into stages owned by the consumer
+// of that row pair (warp m % 8), which dots each expert's rows with the h rows
+// of that expert's assignments, then lets lanes t < T sum the k slots of token
+// t in slot order.
 // ---------------------------------------------------------------------------
 template <int NBL>
 __global__ void __launch_bounds__(kGvThreads) gemv_down_kernel(
@@ -411,6 +414,7 @@ __global__ void __launch_bounds__(kGvThreads) gemv_down_kernel(
   const int G = gridDim.x;
   const int nmine = blockIdx.x < npairs ? (npairs - 1 - blockIdx.x) / G + 1 : 0;
   const uint32_t stage_bytes = (uint32_t)F;
+  const int spc = nstages / kGvConsumers;  // stages owned by each consumer warp
   const volatile int* abort_flag = &s_abort;
 
   if (warp == 0) {
@@ -420,10 +424,11 @@ __global__ void __launch_bounds__(kGvThreads) gemv_down_kernel(
         const int m = u / nact, ai = u - m * nact;
         const int c0 = 2 * (blockIdx.x + G * m);
         const int e = R.act_e[ai];
-        const int s = u % nstages, n = u / nstages;
+        const int j = (m / kGvConsumers) * nact + ai;  // the consumer's own step counter
+        const int s = (m % kGvConsumers) * spc + j % spc, n = j / spc;
         if (n > 0 && !tc::mbar_wait(tc::smem_u32(&empty_bar[s]), (n - 1) & 1, abort_flag)) {
           s_abort = 1;
-          set_status(status, 0x2);
+          report_timeout(status, 2, 0, s, u);
           break;
         }
         const uint32_t fb = tc::smem_u32(&full_bar[s]);
@@ -432,10 +437,11 @@ __global__ void __launch_bounds__(kGvThreads) gemv_down_kernel(
                       stage_bytes, fb);
         issued = u + 1;
       }
-      if (s_abort)
-        for (int s = 0; s < nstages; ++s) {
-          const int n = (issued > s) ? (issued - 1 - s) / nstages + 1 : 0;
-          if (n > 0) tc::mbar_wait(tc::smem_u32(&full_bar[s]), (n - 1) & 1, nullptr);
+      if (s_abort)  // let every copy already issued land before shared memory goes away
+        for (int u = (issued > 2 * nstages ? issued - 2 * nstages : 0); u < issued; ++u) {
+          const int m = u / nact, ai = u - m * nact;
+          const int j = (m / kGvConsumers) * nact + ai;
+          tc::mbar_wait(tc::smem_u32(&full_bar[(m % kGvConsumers) * spc + j % spc]), (j / spc) & 1, nullptr);
         }
     }
   } else {
@@ -463,10 +469,11 @@ __global__ void __launch_bounds__(kGvThreads) gemv_down_kernel(
           for (int j = 0; j < NBL; ++j) sc[r][j] = sc_nxt[r][j];
         if (ai + 1 < nact) load_scales(ai + 1, sc_nxt);
         const int u = m * nact + ai;
-        const int s = u % nstages, n = u / nstages;
+        const int j = (m / kGvConsumers) * nact + ai;
+        const int s = cw * spc + j % spc, n = j / spc;
         if (!tc::mbar_wait(tc::smem_u32(&full_bar[s]), n & 1, abort_flag)) {
           s_abort = 1;
-          set_status(status, 0x2);
+          report_timeout(status, 2, 1, s, u);
           ok = false;
           break;
         }
@@ -588,13 +595,13 @@ cudaError_t launch_swiglu(const float* g, const float* u, void* h, int64_t n, in
                        alpha, limit);
 }
 
-// Shared memory of the decode kernels: the tokens (or h) plus a ring of weight
-// stages; 2 CTAs per SM when the tokens are few, one otherwise.
+// Shared memory of the decode kernels: the tokens (or h) plus weight stages,
+// an equal number owned by each consumer warp (at most four each).
 static int gv_stages(size_t fixed_bytes, size_t stage_bytes) {
-  const size_t budget = (fixed_bytes + 12 * stage_bytes <= 100 * 1024) ? 100 * 1024 : 200 * 1024;
-  size_t n = (budget > fixed_bytes) ? (budget - fixed_bytes) / stage_bytes : 0;
-  if (n > (size_t)kGvMaxStages) n = kGvMaxStages;
-  return (int)n;
+  const size_t budget = 200 * 1024;
+  size_t per = (budget > fixed_bytes) ? (budget - fixed_bytes) / (stage_bytes * kGvConsumers) : 0;
+  if (per > 4) per = 4;
+  return (int)per * kGvConsumers;
 }
 
 cudaError_t launch_gemv_gateup(const uint8_t* g_qs, const uint8_t* g_sc, const float* bg,
@@ -605,7 +612,7 @@ cudaError_t launch_gemv_gateup(const uint8_t* g_qs, const uint8_t* g_sc, const f
   if (T <= 0) return cudaSuccess;
   const size_t xbytes = (size_t)T * D * 4;
   const int nstages = gv_stages(xbytes, (size_t)2 * D);
-  if (nstages < 2) return cudaErrorInvalidValue;
+  if (nstages < kGvConsumers) return cudaErrorInvalidValue;
   const size_t smem = xbytes + (size_t)nstages * 2 * D;
   const int sms = device_sm_count();
   const int nbl = ((D >> 5) + 31) / 32;
@@ -641,7 +648,7 @@ cudaError_t launch_gemv_down(const uint8_t* d_qs, const uint8_t* d_sc, const flo
     h_in_smem = 0;
   }
   const int nstages = gv_stages(hbytes, (size_t)F);
-  if (nstages < 2) return cudaErrorInvalidValue;
+  if (nstages < kGvConsumers) return cudaErrorInvalidValue;
   const size_t smem = hbytes + (size_t)nstages * F;
   const int sms = device_sm_count();
   const int nbl = ((F >> 5) + 31) / 32;

@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   auto fail = [&]() {
     *s_abort = 1;
-    set_status(p.status, 0x2);
+    report_timeout(p.status, 3, warp < kDqWarp0 ? warp : 3, 0, blockIdx.y);
   };
 
   if (warp == 0) {

@@ -25,6 +25,16 @@ __device__ __forceinline__ void set_status(int* status, int bits) {
   if (status) atomicOr(status, bits);
 }
 
+// A bounded wait gave up: set the timeout bit and keep the first site that did
+// (status[1], see moe_get_timeout_site): kernel << 24 | role << 20 |
+// (stage & 0xff) << 12 | (sequence index & 0xfff).
+__device__ __forceinline__ void report_timeout(int* status, int kernel, int role, int stage, int seq) {
+  if (!status) return;
+  atomicOr(status, 0x2);
+  const int site = (kernel << 24) | ((role & 0xf) << 20) | ((stage & 0xff) << 12) | (seq & 0xfff);
+  atomicCAS(status + 1, 0, site);
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));

@@ -26,6 +26,10 @@ def empty(shape, dtype):
 def status(moe):
     rc, st = moe.moe_get_status()
     assert rc == 0, rc
+    if st & moe.MOE_STATUS_WAIT_TIMEOUT:
+        _, site = moe.moe_get_timeout_site()
+        print(f"timeout site 0x{site:08x}: kernel {site >> 24} role {(site >> 20) & 15} "
+              f"stage {(site >> 12) & 255} seq {site & 4095}")
     return st
 
 
