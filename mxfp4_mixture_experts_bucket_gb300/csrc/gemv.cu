@@ -192,12 +192,12 @@ __device__ __forceinline__ void routing_inputs(DecodeRouting& R, int T, int k, i
 // them to every token routed to the expert. The E8M0 bytes are loaded by the
 // consumer lanes one task ahead. h[a] is written block-pair ordered.
 // ---------------------------------------------------------------------------
-constexpr int kGvConsumers = 8;
+constexpr int kGvConsumers = 12;
 constexpr int kGvThreads = (kGvConsumers + 1) * 32;
-constexpr int kGvMaxStages = 32;
+constexpr int kGvMaxStages = 48;
 
 template <int NBL>
-__global__ void __launch_bounds__(kGvThreads) gemv_gateup_kernel(
+__global__ void __launch_bounds__(kGvThreads, 1) gemv_gateup_kernel(
     const uint8_t* __restrict__ g_qs, const uint8_t* __restrict__ g_sc, const float* __restrict__ bg,
     const uint8_t* __restrict__ u_qs, const uint8_t* __restrict__ u_sc, const float* __restrict__ bu,
     int E, int F, int D, int T, int k, const float* __restrict__ x, const float* __restrict__ logits,
@@ -360,12 +360,12 @@ __global__ void __launch_bounds__(kGvThreads) gemv_gateup_kernel(
 
 // ---------------------------------------------------------------------------
 // Fused down + bias + router-weighted combine in slot order (stage 1).
-// A CTA owns row pairs (c0, c0+1) = 2 * (blockIdx.x + G*m); for each it needs
-// the two down rows of every active expert (F bytes, contiguous). Warp 0
-// streams them in (row pair, expert) order into stages owned by the consumer
-// of that row pair (warp m % 8), which dots each expert's rows with the h rows
-// of that expert's assignments, then lets lanes t < T sum the k slots of token
-// t in slot order.
+// A CTA owns output rows c = blockIdx.x + G*m; for each it needs row c of
+// every active expert's down matrix (F/2 nibble bytes each). Warp 0 streams
+// them in (row, expert) order into stages owned by the consumer of that row
+// (warp m % kGvConsumers), which dots each expert's row with the h rows of that
+// expert's assignments, then lets lanes t < T sum the k slots of token t in
+// slot order.
 // ---------------------------------------------------------------------------
 template <int NBL>
 __global__ void __launch_bounds__(kGvThreads) gemv_down_kernel(
@@ -376,11 +376,11 @@ __global__ void __launch_bounds__(kGvThreads) gemv_down_kernel(
   extern __shared__ float4 smem_f4[];
   const int TK = T * k;
   const size_t h_bytes = h_in_smem ? (size_t)TK * F * 4 : 0;
-  uint8_t* ring = reinterpret_cast<uint8_t*>(smem_f4) + h_bytes;  // nstages x F bytes
+  uint8_t* ring = reinterpret_cast<uint8_t*>(smem_f4) + h_bytes;  // nstages x F/2 bytes
   __shared__ DecodeRouting R;
   __shared__ __align__(8) uint64_t full_bar[kGvMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kGvMaxStages];
-  __shared__ float s_o[kGvConsumers][kMaxAssign][2];
+  __shared__ float s_o[kGvConsumers][kMaxAssign];
   __shared__ int s_abort;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   pdl_launch_dependents();
@@ -410,10 +410,9 @@ __global__ void __launch_bounds__(kGvThreads) gemv_down_kernel(
   const int nact = R.nact;
   if (nact == 0) return;
   const int nb = F >> 5;
-  const int npairs = D >> 1;
   const int G = gridDim.x;
-  const int nmine = blockIdx.x < npairs ? (npairs - 1 - blockIdx.x) / G + 1 : 0;
-  const uint32_t stage_bytes = (uint32_t)F;
+  const int nmine = blockIdx.x < D ? (D - 1 - blockIdx.x) / G + 1 : 0;  // rows of this CTA
+  const uint32_t stage_bytes = (uint32_t)(F / 2);
   const int spc = nstages / kGvConsumers;  // stages owned by each consumer warp
   const volatile int* abort_flag = &s_abort;
 
@@ -422,7 +421,7 @@ __global__ void __launch_bounds__(kGvThreads) gemv_down_kernel(
       int issued = 0;
       for (int u = 0; u < nmine * nact; ++u) {
         const int m = u / nact, ai = u - m * nact;
-        const int c0 = 2 * (blockIdx.x + G * m);
+        const int c = blockIdx.x + G * m;
         const int e = R.act_e[ai];
         const int j = (m / kGvConsumers) * nact + ai;  // the consumer's own step counter
         const int s = (m % kGvConsumers) * spc + j % spc, n = j / spc;
@@ -433,7 +432,7 @@ __global__ void __launch_bounds__(kGvThreads) gemv_down_kernel(
         }
         const uint32_t fb = tc::smem_u32(&full_bar[s]);
         tc::mbar_expect_tx(fb, stage_bytes);
-        tc::bulk_load(tc::smem_u32(ring + (size_t)s * stage_bytes), d_qs + ((size_t)e * D + c0) * (F / 2),
+        tc::bulk_load(tc::smem_u32(ring + (size_t)s * stage_bytes), d_qs + ((size_t)e * D + c) * (F / 2),
                       stage_bytes, fb);
         issued = u + 1;
       }
@@ -447,26 +446,22 @@ __global__ void __launch_bounds__(kGvThreads) gemv_down_kernel(
   } else {
     const int cw = warp - 1;
     for (int m = cw; m < nmine; m += kGvConsumers) {
-      const int c0 = 2 * (blockIdx.x + G * m);
+      const int c = blockIdx.x + G * m;
       bool ok = true;
-      uint32_t sc_nxt[2][NBL];
-      auto load_scales = [&](int ai, uint32_t (&sc)[2][NBL]) {
+      uint32_t sc_nxt[NBL];
+      auto load_scales = [&](int ai, uint32_t (&scl)[NBL]) {
         const int e = R.act_e[ai];
 #pragma unroll
-        for (int r = 0; r < 2; ++r)
-#pragma unroll
-          for (int j = 0; j < NBL; ++j) {
-            const int b = lane + 32 * j;
-            if (b < nb) sc[r][j] = ldg_nc_u8(d_sc + ((size_t)e * D + c0 + r) * nb + b);
-          }
+        for (int jb = 0; jb < NBL; ++jb) {
+          const int b = lane + 32 * jb;
+          if (b < nb) scl[jb] = ldg_nc_u8(d_sc + ((size_t)e * D + c) * nb + b);
+        }
       };
       load_scales(0, sc_nxt);
       for (int ai = 0; ai < nact; ++ai) {
-        uint32_t sc[2][NBL];
+        uint32_t scl[NBL];
 #pragma unroll
-        for (int r = 0; r < 2; ++r)
-#pragma unroll
-          for (int j = 0; j < NBL; ++j) sc[r][j] = sc_nxt[r][j];
+        for (int jb = 0; jb < NBL; ++jb) scl[jb] = sc_nxt[jb];
         if (ai + 1 < nact) load_scales(ai + 1, sc_nxt);
         const int u = m * nact + ai;
         const int j = (m / kGvConsumers) * nact + ai;
@@ -478,55 +473,43 @@ __global__ void __launch_bounds__(kGvThreads) gemv_down_kernel(
           break;
         }
         const uint8_t* st = ring + (size_t)s * stage_bytes;
-        uint4 q[2][NBL];
+        uint4 q[NBL];
 #pragma unroll
-        for (int r = 0; r < 2; ++r)
-#pragma unroll
-          for (int j = 0; j < NBL; ++j) {
-            const int b = lane + 32 * j;
-            if (b < nb) q[r][j] = *reinterpret_cast<const uint4*>(st + r * (F / 2) + b * 16);
-          }
+        for (int jb = 0; jb < NBL; ++jb) {
+          const int b = lane + 32 * jb;
+          if (b < nb) q[jb] = *reinterpret_cast<const uint4*>(st + b * 16);
+        }
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(tc::smem_u32(&empty_bar[s]));
         for (int li = R.act_off[ai]; li < R.act_off[ai + 1]; ++li) {
           const int a = R.lst[li];
           const float4* ha = hv4 + (size_t)a * (F >> 2);
-          float acc0 = 0.f, acc1 = 0.f;
+          float acc = 0.f;
 #pragma unroll
-          for (int j = 0; j < NBL; ++j) {
-            const int b = lane + 32 * j;
+          for (int jb = 0; jb < NBL; ++jb) {
+            const int b = lane + 32 * jb;
             if (b < nb) {
               float4 xv[8];
               load_pair_group(ha, b, xv);
-              acc0 = fmaf(mx_block_dot(q[0][j], xv), e8m0_to_f32(sc[0][j]), acc0);
-              acc1 = fmaf(mx_block_dot(q[1][j], xv), e8m0_to_f32(sc[1][j]), acc1);
+              acc = fmaf(mx_block_dot(q[jb], xv), e8m0_to_f32(scl[jb]), acc);
             }
           }
-          acc0 = warp_sum(acc0);
-          acc1 = warp_sum(acc1);
-          if (lane == 0) {
-            s_o[cw][a][0] = acc0;
-            s_o[cw][a][1] = acc1;
-          }
+          acc = warp_sum(acc);
+          if (lane == 0) s_o[cw][a] = acc;
         }
       }
       if (!ok) break;
       __syncwarp();
       if (lane < T) {
         const int t = lane;
-        float y0 = 0.f, y1 = 0.f;
-        for (int j = 0; j < k; ++j) {  // slot order
-          const int a = t * k + j;
+        float yv = 0.f;
+        for (int jj = 0; jj < k; ++jj) {  // slot order
+          const int a = t * k + jj;
           const int ej = R.ids[a];
           if (ej < 0 || ej >= E) continue;
-          const float wt = R.w[a];
-          const float b0 = bd ? bd[(size_t)ej * D + c0] : 0.f;
-          const float b1 = bd ? bd[(size_t)ej * D + c0 + 1] : 0.f;
-          y0 = fmaf(wt, s_o[cw][a][0] + b0, y0);
-          y1 = fmaf(wt, s_o[cw][a][1] + b1, y1);
+          yv = fmaf(R.w[a], s_o[cw][a] + (bd ? bd[(size_t)ej * D + c] : 0.f), yv);
         }
-        y[(size_t)t * D + c0] = y0;
-        y[(size_t)t * D + c0 + 1] = y1;
+        y[(size_t)t * D + c] = yv;
       }
       __syncwarp();
     }
@@ -598,7 +581,7 @@ cudaError_t launch_swiglu(const float* g, const float* u, void* h, int64_t n, in
 // Shared memory of the decode kernels: the tokens (or h) plus weight stages,
 // an equal number owned by each consumer warp (at most four each).
 static int gv_stages(size_t fixed_bytes, size_t stage_bytes) {
-  const size_t budget = 200 * 1024;
+  const size_t budget = 210 * 1024;
   size_t per = (budget > fixed_bytes) ? (budget - fixed_bytes) / (stage_bytes * kGvConsumers) : 0;
   if (per > 4) per = 4;
   return (int)per * kGvConsumers;
@@ -647,9 +630,9 @@ cudaError_t launch_gemv_down(const uint8_t* d_qs, const uint8_t* d_sc, const flo
     hbytes = 0;
     h_in_smem = 0;
   }
-  const int nstages = gv_stages(hbytes, (size_t)F);
+  const int nstages = gv_stages(hbytes, (size_t)F / 2);
   if (nstages < kGvConsumers) return cudaErrorInvalidValue;
-  const size_t smem = hbytes + (size_t)nstages * F;
+  const size_t smem = hbytes + (size_t)nstages * (F / 2);
   const int sms = device_sm_count();
   const int nbl = ((F >> 5) + 31) / 32;
   cudaError_t err;
