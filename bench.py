@@ -325,8 +325,8 @@ def run_ours(args, dist: Dist):
     gateup_bytes = K_TOP * 2 * MAT_BYTES + K_TOP * 2 * F * 4 + D * 4 + K_TOP * F * 4
     achieved = gateup_bytes / kern_s / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-                "frac": round(achieved / hbm_peak, 4), "traffic": ncu_traffic("gemv_gateup_kernel"),
-                "kernel": "gemv_gateup_kernel", "algorithmic_bytes_per_launch": gateup_bytes,
+                "frac": round(achieved / hbm_peak, 4), "traffic": ncu_traffic("decode_expert_kernel<0>"),
+                "kernel": "decode_expert_kernel<0>", "algorithmic_bytes_per_launch": gateup_bytes,
                 "launch_us": round(kern_s * 1e6, 3), "peak_source": f"{peak_src} hbm_gbs (burst copy)"}
 
     # ---- end to end through the public API, host buffers, no graph ----

@@ -205,11 +205,10 @@ int moe_mxfp4_grouped_mm(const uint8_t* w_qs, const uint8_t* w_sc, const float* 
  *   h[a] = swiglu_oai(Wg[e] x_t + bg[e], Wu[e] x_t + bu[e]; alpha, limit)
  * Each weight row is streamed from HBM once for all of the tokens routed to
  * its expert. x: float [T][D]; ids: int32 [T][k]; gate/up planes [E][F][D/2],
- * [E][F][D/32]; bg, bu [E][F] or NULL; h: float [T*k][F] in the block-pair
- * order read by moe_expert_down_combine (within each 32-float group of a row,
- * values are interleaved as the MXFP4 nibble pairs (i, i+16) and the group's
- * 16-byte quads are permuted by the group index); treat it as opaque. Ids
- * outside [0, E) are skipped and set MOE_STATUS_BAD_EXPERT_ID.
+ * [E][F][D/32]; bg, bu [E][F] or NULL; h: float [T*k][F], row a = h[a] (rows
+ * of assignments with an invalid id are left as they were). x and h must be
+ * 16-byte aligned. Ids outside [0, E) are skipped and set
+ * MOE_STATUS_BAD_EXPERT_ID.
  * Requires 1 <= T <= MOE_GEMV_MAX_T, k <= 8, D and F multiples of 64, <= 4096.
  */
 int moe_expert_gateup_swiglu(const uint8_t* g_qs, const uint8_t* g_sc, const float* bg,

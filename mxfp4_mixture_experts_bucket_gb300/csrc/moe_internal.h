@@ -76,10 +76,12 @@ cudaError_t launch_mxfp4_gemv(const uint8_t* qs, const uint8_t* sc, int E, int R
                               const float* bias, float* out, int* status, Launch L);
 cudaError_t launch_swiglu(const float* g, const float* u, void* h, int64_t n, int h_dtype,
                           float alpha, float limit, Launch L);
+
+// ---- decode.cu ----
 // Decode rail, stage 0: gate/up projections + bias + swiglu for every routed
 // assignment. Routing comes from `logits` (top-k + softmax inside the kernel)
 // when not NULL, else from `ids_in`; CTA 0 writes it to ids_out / w_out if not
-// NULL. h: [T*k][F] floats in block-pair order.
+// NULL. h: [T*k][F] floats, row per assignment.
 cudaError_t launch_gemv_gateup(const uint8_t* g_qs, const uint8_t* g_sc, const float* bg,
                                const uint8_t* u_qs, const uint8_t* u_sc, const float* bu, int E,
                                int F, int D, int T, int k, const float* x, const float* logits,
