@@ -332,6 +332,7 @@ int moe_expert_gateup_swiglu(const uint8_t* g_qs, const uint8_t* g_sc, const flo
   if (T == 0) return MOE_OK;
   MOE_REQUIRE(g_qs && g_sc && u_qs && u_sc && x && ids && h);
   MOE_REQUIRE(aligned(g_qs, 16) && aligned(u_qs, 16) && aligned(x, 16) && aligned(h, 16));
+  MOE_REQUIRE(aligned(g_sc, 16) && aligned(u_sc, 16));
   DeviceInfo* d = nullptr;
   int rc = current_device(&d);
   if (rc != MOE_OK) return rc;
@@ -348,7 +349,7 @@ int moe_expert_down_combine(const uint8_t* d_qs, const uint8_t* d_sc, const floa
   if (D > 4096 || F > 4096) return MOE_EUNSUPPORTED;
   if (T == 0) return MOE_OK;
   MOE_REQUIRE(d_qs && d_sc && h && ids && weights && y);
-  MOE_REQUIRE(aligned(d_qs, 16) && aligned(h, 16));
+  MOE_REQUIRE(aligned(d_qs, 16) && aligned(d_sc, 16) && aligned(h, 16));
   DeviceInfo* d = nullptr;
   int rc = current_device(&d);
   if (rc != MOE_OK) return rc;

@@ -32,12 +32,13 @@ namespace mm {
 constexpr int BM = 128;  // weight rows per tile (MMA M)
 constexpr int BN = 128;  // bucket rows per tile (CSR tile height, MMA N <= BN)
 constexpr int BK = 64;   // reduction columns per stage (one 128-byte bf16 row)
-constexpr int OSA = 2;   // dequantised A stages (dequant -> MMA hand-off)
+constexpr int OSA = 3;   // dequantised A stages (dequant -> MMA hand-off)
 constexpr int MAX_RS = 16;   // raw MXFP4 stages (HBM latency is hidden here)
 constexpr int MAX_BS = 8;    // activation (B) stages
 constexpr int kThreads = 352;    // 11 warps
 constexpr int kDqWarp0 = 3;      // warps 3..10 dequantise and run the epilogue
 constexpr int kDqThreads = 256;
+constexpr int kDqWarps = kDqThreads / 32;  // hand-off barriers count one arrival per warp
 constexpr int kATile = BM * BK * 2;      // 16 KB
 constexpr int kBChunk = 32 * BK * 2;     // 4 KB: 32 activation rows
 constexpr int kBPool = 64 * 1024;        // activation ring, carved per tile
@@ -177,10 +178,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < RS; ++i) {
       tc::mbar_init(bar(kRawFull + i), 1);
-      tc::mbar_init(bar(kRawEmpty + i), kDqThreads);
+      tc::mbar_init(bar(kRawEmpty + i), kDqWarps);
     }
     for (int i = 0; i < OSA; ++i) {
-      tc::mbar_init(bar(kAFull + i), kDqThreads);
+      tc::mbar_init(bar(kAFull + i), kDqWarps);
       tc::mbar_init(bar(kAEmpty + i), 1);
     }
     for (int i = 0; i < NBS; ++i) {
@@ -189,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc::mbar_init(bar(kAccFull), 1);
     tc::mbar_init(bar(kScFull), 1);
-    tc::mbar_init(bar(kBiasReady), kDqThreads);
+    tc::mbar_init(bar(kBiasReady), kDqWarps);
     *s_abort = 0;
     tc::fence_mbar_init();
   }
@@ -319,17 +320,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::tmem_wait_st();
       tc::fence_before_sync();
-      tc::mbar_arrive(bar(kBiasReady));
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(bar(kBiasReady));
     }
     const int r = dt >> 1, kb = dt & 1;
-    bool ok = tc::mbar_wait(bar(kScFull), 0, s_abort);
-    if (!ok) fail();
+    const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(kScFull), 0, s_abort));
+    if (!ok && lane == 0) fail();
     for (int ks = 0; ok && ks < nk; ++ks) {
       const int rs = ks % RS, rn = ks / RS;
       const int as = ks % OSA, an = ks / OSA;
-      if (!tc::mbar_wait(bar(kRawFull + rs), rn & 1, s_abort) ||
-          (an > 0 && !tc::mbar_wait(bar(kAEmpty + as), (an - 1) & 1, s_abort))) {
-        fail();
+      // every lane waits (each then sees the stage's data); the warp leaves
+      // together if any lane's wait gave up, so the __syncwarp below stays uniform
+      const bool w_ok = tc::mbar_wait(bar(kRawFull + rs), rn & 1, s_abort) &&
+                        (an == 0 || tc::mbar_wait(bar(kAEmpty + as), (an - 1) & 1, s_abort));
+      if (!__all_sync(0xffffffffu, w_ok)) {
+        if (lane == 0) fail();
         break;
       }
 #pragma unroll
@@ -347,9 +352,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
         }
       }
+      // every thread's stores become visible to the tensor core's async proxy,
+      // then one lane per warp hands the stage on
       tc::fence_proxy_async_smem();
-      tc::mbar_arrive(bar(kRawEmpty + rs));
-      tc::mbar_arrive(bar(kAFull + as));
+      __syncwarp();
+      if (lane == 0) {
+        tc::mbar_arrive(bar(kRawEmpty + rs));
+        tc::mbar_arrive(bar(kAFull + as));
+      }
     }
     // epilogue: TMEM -> registers -> global (warp-uniform decision: tcgen05.ld is warp-wide)
     __syncwarp();
