@@ -133,6 +133,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_alo,
                       const Params p) {
   constexpr int NB = SPLIT ? 2 : 1;  // activation tiles per stage (hi, lo)
+  // TMEM columns per matrix. With split activations one MMA covers the hi and
+  // the lo rows of the stage (N = 2 * 32 * nchunk <= 256): the hi products land
+  // in columns [0, HN), the lo products in [HN, 2 HN), and the epilogue adds
+  // the two halves.
+  constexpr uint32_t AW = SPLIT ? 256 : 128;
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -156,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (live <= 0) return;
   const int n_mma = (live + 15) & ~15;
   const int nchunk = (live + 31) >> 5;
+  const int hn = 32 * nchunk;  // split: first TMEM column of the lo products
   const int nk = p.C / BK;
   const int nbc = p.C / 32;
   const int rows_here = min(BM, p.R - m0);
@@ -194,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *s_abort = 0;
     tc::fence_mbar_init();
   }
-  if (warp == 1) tc::tmem_alloc(tc::smem_u32(s_tmem), NMAT * 128);
+  if (warp == 1) tc::tmem_alloc(tc::smem_u32(s_tmem), NMAT * AW);
   if (EPI == MOE_EPI_SCATTER_WEIGHTED_ID) {
     for (int i = threadIdx.x; i < BN; i += kThreads) {
       const int a = (i < live) ? p.rows[tile_row0 + i] : -1;
@@ -272,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = tc::idesc_bf16_f32(BM, n_mma);
+      const uint32_t idesc = tc::idesc_bf16_f32(BM, SPLIT ? 2 * hn : n_mma);
       bool ok = true;
       if (seeded && !tc::mbar_wait(bar(kBiasReady), 0, s_abort)) { fail(); ok = false; }
       tc::fence_after_sync();
@@ -291,12 +297,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t ad = tc::sw128_kmajor_desc(sA + (as * NMAT + mat) * kATile + kk * 32);
-#pragma unroll
-            for (int hl = 0; hl < NB; ++hl) {  // activation hi part, then its lo part
-              const uint64_t bd = tc::sw128_kmajor_desc(bbase + hl * nchunk * kBChunk + kk * 32);
-              tc::mma_bf16(tmem + mat * 128, ad, bd, idesc,
-                           (ks > 0 || kk > 0 || hl > 0 || seeded) ? 1u : 0u);
-            }
+            // B rows: the live chunks, then (split) their lo parts right behind them
+            const uint64_t bd = tc::sw128_kmajor_desc(bbase + kk * 32);
+            tc::mma_bf16(tmem + mat * AW, ad, bd, idesc, (ks > 0 || kk > 0 || seeded) ? 1u : 0u);
           }
         }
         tc::mma_commit(bar(kAEmpty + as));
@@ -315,8 +318,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (seeded) {
       for (int mat = 0; mat < NMAT; ++mat) {
         const float bv = (p.bias[mat] != nullptr && f < p.R) ? p.bias[mat][(size_t)e * p.R + f] : 0.f;
-        for (int c = colhalf; c < n_mma / 16; c += 2)
-          tc::tmem_st16(tmem + ((uint32_t)(32 * q) << 16) + mat * 128 + 16 * c, __float_as_uint(bv));
+        const int ncols = SPLIT ? 2 * hn : n_mma;
+        for (int c = colhalf; c < ncols / 16; c += 2)
+          tc::tmem_st16(tmem + ((uint32_t)(32 * q) << 16) + mat * AW + 16 * c,
+                        __float_as_uint(16 * c < (SPLIT ? hn : ncols) ? bv : 0.f));
       }
       tc::tmem_wait_st();
       tc::fence_before_sync();
@@ -371,9 +376,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = colhalf; c < n_mma / 16; c += 2) {
         uint32_t v0[16], v1[16];
         if (NMAT == 2) {
-          tc::tmem_ld16x2_wait(tbase + 16 * c, tbase + 128 + 16 * c, v0, v1);
+          tc::tmem_ld16x2_wait(tbase + 16 * c, tbase + AW + 16 * c, v0, v1);
+          if (SPLIT) {  // add the lo products
+            uint32_t l0[16], l1[16];
+            tc::tmem_ld16x2_wait(tbase + hn + 16 * c, tbase + AW + hn + 16 * c, l0, l1);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              v0[i] = __float_as_uint(__uint_as_float(v0[i]) + __uint_as_float(l0[i]));
+              v1[i] = __float_as_uint(__uint_as_float(v1[i]) + __uint_as_float(l1[i]));
+            }
+          }
         } else {
           tc::tmem_ld16_wait(tbase + 16 * c, v0);
+          if (SPLIT) {  // add the lo products
+            uint32_t l0[16];
+            tc::tmem_ld16_wait(tbase + hn + 16 * c, l0);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v0[i] = __float_as_uint(__uint_as_float(v0[i]) + __uint_as_float(l0[i]));
+          }
         }
         if (f < p.R) {
 #pragma unroll
@@ -402,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, NMAT * 128);
+    tc::tmem_dealloc(tmem, NMAT * AW);
   }
 }
 
