@@ -17,9 +17,11 @@
 //   warp 2      TMA producer of the bf16 activation tiles (2D map, 128-byte
 //               swizzle, only the live 32-row chunks) into its own ring, whose
 //               depth grows as the tile's live rows shrink
-//   warps 3-10  dequantise MXFP4 -> bf16 into the UMMA 128B-swizzled K-major
-//               layout (two-stage hand-off ring); seed the accumulator with
-//               the bias (tcgen05.st); run the epilogue from TMEM (tcgen05.ld)
+//   warps 3-18  two groups of eight dequantise MXFP4 -> bf16 into the UMMA
+//               128B-swizzled K-major layout, alternate k-steps each, so two
+//               dequant chains are in flight (three-stage hand-off ring); the
+//               first group seeds the accumulator with the bias (tcgen05.st);
+//               all sixteen run the epilogue from TMEM (tcgen05.ld)
 // The MMA is "swap-AB": weight rows fill M = 128 and the bucket rows fill N,
 // rounded up to 16, so rows past counts[e] cost no tensor work.
 #include <cuda.h>
@@ -35,9 +37,10 @@ constexpr int BK = 64;   // reduction columns per stage (one 128-byte bf16 row)
 constexpr int OSA = 3;   // dequantised A stages (dequant -> MMA hand-off)
 constexpr int MAX_RS = 16;   // raw MXFP4 stages (HBM latency is hidden here)
 constexpr int MAX_BS = 8;    // activation (B) stages
-constexpr int kThreads = 352;    // 11 warps
-constexpr int kDqWarp0 = 3;      // warps 3..10 dequantise and run the epilogue
-constexpr int kDqThreads = 256;
+constexpr int kDqGroups = 2;     // dequant groups, taking alternate k-steps
+constexpr int kThreads = (3 + 8 * kDqGroups) * 32;  // 19 warps
+constexpr int kDqWarp0 = 3;      // warps 3..18 dequantise (group g: warps 3+8g..10+8g) and run the epilogue
+constexpr int kDqThreads = 256;  // per group
 constexpr int kDqWarps = kDqThreads / 32;  // hand-off barriers count one arrival per warp
 constexpr int kATile = BM * BK * 2;      // 16 KB
 constexpr int kBChunk = 32 * BK * 2;     // 4 KB: 32 activation rows
@@ -310,12 +313,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------ dequant + epilogue
-    const int dt = threadIdx.x - kDqWarp0 * 32;  // 0..255
+    const int group = (warp - kDqWarp0) >> 3;
+    const int dt = threadIdx.x - kDqWarp0 * 32 - kDqThreads * group;  // 0..255 within the group
     const int q = warp & 3;                      // TMEM lane quarter this warp may access
-    const int colhalf = (warp - kDqWarp0) >> 2;
+    const int colhalf = ((warp - kDqWarp0) >> 2) & 1;  // bias seeding (group 0)
+    const int colquarter = (warp - kDqWarp0) >> 2;      // epilogue: 0..3
     const int trow = 32 * q + lane;              // TMEM lane = weight row within the tile
     const int f = m0 + trow;
-    if (seeded) {
+    if (seeded && group == 0) {
       for (int mat = 0; mat < NMAT; ++mat) {
         const float bv = (p.bias[mat] != nullptr && f < p.R) ? p.bias[mat][(size_t)e * p.R + f] : 0.f;
         const int ncols = SPLIT ? 2 * hn : n_mma;
@@ -331,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = dt >> 1, kb = dt & 1;
     const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(kScFull), 0, s_abort));
     if (!ok && lane == 0) fail();
-    for (int ks = 0; ok && ks < nk; ++ks) {
+    for (int ks = group; ok && ks < nk; ks += kDqGroups) {
       const int rs = ks % RS, rn = ks / RS;
       const int as = ks % OSA, an = ks / OSA;
       // every lane waits (each then sees the stage's data); the warp leaves
@@ -373,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (go) {
       tc::fence_after_sync();
       const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16);
-      for (int c = colhalf; c < n_mma / 16; c += 2) {
+      for (int c = colquarter; c < n_mma / 16; c += 4) {
         uint32_t v0[16], v1[16];
         if (NMAT == 2) {
           tc::tmem_ld16x2_wait(tbase + 16 * c, tbase + AW + 16 * c, v0, v1);
