@@ -250,10 +250,10 @@ cudaError_t launch_router_logits(const float* x, int T, int D, const float* wr, 
     return launch_kernel(router_logits_kernel<1, 1>, grid, dim3(128), 0, L, x, T, D, wr, br, E,
                          logits);
   }
-  // 4 tokens x 4 experts per block, 8 threads per dot: enough blocks to keep
-  // every SM's loads in flight at prefill sizes too
-  dim3 grid((T + 3) / 4, (E + 3) / 4);
-  return launch_kernel(router_logits_kernel<4, 4>, grid, dim3(128), 0, L, x, T, D, wr, br, E,
+  // 2 tokens x 2 experts per block, a warp per dot: coalesced loads and enough
+  // blocks to keep every SM's loads in flight at prefill sizes too
+  dim3 grid((T + 1) / 2, (E + 1) / 2);
+  return launch_kernel(router_logits_kernel<2, 2>, grid, dim3(128), 0, L, x, T, D, wr, br, E,
                        logits);
 }
 
