@@ -288,20 +288,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ks = 0; ok && ks < nk; ++ks) {
         const int as = ks % OSA, an = ks / OSA;
         const int bs = ks % NBS, bn = ks / NBS;
-        if (!tc::mbar_wait(bar(kAFull + as), an & 1, s_abort) ||
-            !tc::mbar_wait(bar(kBFull + bs), bn & 1, s_abort)) {
+        if (!tc::mbar_wait2(bar(kAFull + as), an & 1, bar(kBFull + bs), bn & 1, s_abort)) {
           fail();
           break;
         }
         tc::fence_after_sync();
-        const uint32_t bbase = sB + bs * b_stage;
+        // Descriptors once per k-step; a K slice of 16 bf16 is 32 bytes further,
+        // i.e. +2 in the 16-byte start-address field (tiles stay below 256 KB).
+        const uint64_t a_desc = tc::sw128_kmajor_desc(sA + as * NMAT * kATile);
+        // B rows: the live chunks, then (split) their lo parts right behind them
+        const uint64_t b_desc = tc::sw128_kmajor_desc(sB + bs * b_stage);
 #pragma unroll
         for (int mat = 0; mat < NMAT; ++mat) {
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = tc::sw128_kmajor_desc(sA + (as * NMAT + mat) * kATile + kk * 32);
-            // B rows: the live chunks, then (split) their lo parts right behind them
-            const uint64_t bd = tc::sw128_kmajor_desc(bbase + kk * 32);
+            const uint64_t ad = a_desc + (uint64_t)((mat * kATile + kk * 32) >> 4);
+            const uint64_t bd = b_desc + (uint64_t)(kk * 2);
             tc::mma_bf16(tmem + mat * AW, ad, bd, idesc, (ks > 0 || kk > 0 || seeded) ? 1u : 0u);
           }
         }

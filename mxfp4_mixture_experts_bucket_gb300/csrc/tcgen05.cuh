@@ -60,6 +60,28 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   }
 }
 
+// Bounded wait for two phases at once (both probed each round, so their
+// latencies overlap). Returns false if it gave up, like mbar_wait.
+__device__ __forceinline__ bool mbar_wait2(uint32_t bar_a, uint32_t parity_a, uint32_t bar_b,
+                                           uint32_t parity_b, const volatile int* abort_flag) {
+  bool da = false, db = false;
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    if (!da) da = mbar_test(bar_a, parity_a);
+    if (!db) db = mbar_test(bar_b, parity_b);
+    if (da && db) return true;
+    if ((it & 31u) == 31u) {
+      if (abort_flag && *abort_flag) return false;
+      const uint64_t now = globaltimer_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > kWaitTimeoutNs) {
+        return false;
+      }
+    }
+  }
+}
+
 // ---- TMA ----
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int c0, int c1,
                                             uint32_t bar) {
