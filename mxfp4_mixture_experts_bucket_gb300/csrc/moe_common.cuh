@@ -188,6 +188,39 @@ __device__ __forceinline__ bool topk_better(float va, int ia, float vb, int ib) 
 
 __device__ __forceinline__ void warp_topk_softmax(const float* __restrict__ lt, int E, int k, int lane,
                                                   int& my_id, float& my_w) {
+  if (E <= 32) {
+    // One expert per lane: its slot is its rank, the number of experts ahead
+    // of it in the order above (32 independent broadcasts, no argmax chain).
+    float v = (lane < E) ? lt[lane] : -INFINITY;
+    if (v != v) v = -INFINITY;
+    const int me = (lane < E) ? lane : 0x7fffffff;
+    int rank = 0;
+#pragma unroll
+    for (int o = 0; o < 32; ++o) {
+      const float ov = __shfl_sync(0xffffffffu, v, o);
+      rank += (o < E) && topk_better(ov, o, v, me);
+    }
+    const bool sel = (lane < E) && rank < k;
+    // the lane holding slot j, for j = 0..k-1 (k <= E <= 32 lanes are ranked 0..E-1)
+    const float top0 = __shfl_sync(0xffffffffu, v, __ffs(__ballot_sync(0xffffffffu, sel && rank == 0)) - 1);
+    const float ex = expf(v - top0);
+    float sum = 0.f;
+    for (int j = 0; j < k; ++j)  // slot order, as below
+      sum += __shfl_sync(0xffffffffu, ex, __ffs(__ballot_sync(0xffffffffu, sel && rank == j)) - 1);
+    // hand slot j to lane j
+    my_id = -1;
+    float my_ex = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const int src = __ffs(__ballot_sync(0xffffffffu, sel && rank == j)) - 1;
+      const float exj = __shfl_sync(0xffffffffu, ex, src);
+      if (lane == j) {
+        my_id = src;
+        my_ex = exj;
+      }
+    }
+    my_w = my_ex / sum;
+    return;
+  }
   constexpr int MAXPER = 8;
   float v[MAXPER];
 #pragma unroll
