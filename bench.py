@@ -330,24 +330,20 @@ def run_ours(args, dist: Dist):
                 "launch_us": round(kern_s * 1e6, 3), "peak_source": f"{peak_src} hbm_gbs (burst copy)"}
 
     # ---- end to end through the public API, host buffers, no graph ----
+    # MoeLayer.forward_host: one C call per step copies the step's pinned host x
+    # in, runs the layer and copies y back to pinned host memory.
     x_host = torch.randn((K, D), generator=torch.Generator().manual_seed(99)).pin_memory()
     y_host = torch.empty((K, D)).pin_memory()
-    xd = torch.empty((1, D), device=dev)
-    yd = torch.empty((1, D), device=dev)
     with torch.cuda.stream(stream):
         for i in range(3):
-            xd.copy_(x_host[i:i + 1], non_blocking=True)
-            layers[i % NL](xd, out=yd)
-            y_host[i:i + 1].copy_(yd, non_blocking=True)
+            layers[i % NL].forward_host(x_host[i:i + 1], y_host[i:i + 1], stream=stream)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     dist.barrier()
     with torch.cuda.stream(stream):
         e0.record(stream)
         for i in range(K):
-            xd.copy_(x_host[i:i + 1], non_blocking=True)
-            layers[i % NL](xd, out=yd)
-            y_host[i:i + 1].copy_(yd, non_blocking=True)
+            layers[i % NL].forward_host(x_host[i:i + 1], y_host[i:i + 1], stream=stream)
         e1.record(stream)
     torch.cuda.synchronize()
     dist.barrier()
@@ -366,7 +362,7 @@ def run_ours(args, dist: Dist):
         "layer_roofline_frac": round((step_bytes / (hbm_peak * 1e9)) / (secs_max / K), 4),
         "roofline": roofline,
         "e2e": {"value": round(e2e_rate, 1), "unit": "tokens/s", "h2d_bytes_per_step": D * 4, "d2h_bytes_per_step": D * 4,
-                "path": "MoeLayer.forward -> moe_ffn_layer per step, pinned host x in, host y out, no graph"},
+                "path": "MoeLayer.forward_host -> moe_ffn_layer_hostio per step: pinned host x in, layer, pinned host y out, no graph"},
         "clocks": clocks,
         "gpu_launches": int(round(launches_per_step * K)),
         "kernels_per_step": launches_per_step,

@@ -259,6 +259,24 @@ int moe_ffn_layer(const float* x, int T, int D, int F, int E, int k, const float
                   size_t workspace_bytes, float* y, int32_t* ids_out, float* weights_out,
                   cudaStream_t stream);
 
+/*
+ * moe_ffn_layer_hostio -- moe_ffn_layer for tokens that live in host memory:
+ * on `stream` it copies x_host [T][D] to x_dev, runs moe_ffn_layer (same
+ * definition, rails, limits and workspace contract), and copies y_dev [T][D]
+ * back to y_host, all enqueued from C so that a serving loop pays one call per
+ * step. x_host and y_host should be pinned (page-locked) for the copies to be
+ * asynchronous; x_dev and y_dev are caller-owned device buffers of T*D floats,
+ * 16-byte aligned. The call returns once the work is enqueued: y_host holds the
+ * result after the stream has been synchronised. Errors as moe_ffn_layer; a
+ * failed copy returns MOE_ECUDA.
+ */
+int moe_ffn_layer_hostio(const float* x_host, float* y_host, float* x_dev, float* y_dev, int T, int D,
+                         int F, int E, int k, const float* w_router, const float* b_router,
+                         const uint8_t* g_qs, const uint8_t* g_sc, const float* bg,
+                         const uint8_t* u_qs, const uint8_t* u_sc, const float* bu,
+                         const uint8_t* d_qs, const uint8_t* d_sc, const float* bd, int rail,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Size of the library's static decode scratch (moe_ffn_layer_decode_static). */
 #define MOE_DECODE_SCRATCH_BYTES (512 * 1024)
 

@@ -61,6 +61,7 @@ _SIGS = {
     "moe_expert_gateup_swiglu": (I, [P, P, P, P, P, P, I, I, I, I, I, P, P, F, F, P, P]),
     "moe_expert_down_combine": (I, [P, P, P, I, I, I, I, I, P, P, P, P, P]),
     "moe_ffn_layer": (I, [P, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, I, P, SZ, P, P, P, P]),
+    "moe_ffn_layer_hostio": (I, [P, P, P, P, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, I, P, SZ, P]),
     "moe_ffn_layer_decode_static": (I, [P, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P]),
     "moe_get_status": (I, [P, ctypes.POINTER(ctypes.c_int)]),
     "moe_get_timeout_site": (I, [P, ctypes.POINTER(ctypes.c_int)]),
@@ -174,6 +175,15 @@ def moe_ffn_layer(x, T, D, F, E, k, w_router, b_router, g_qs, g_sc, bg, u_qs, u_
                               _ptr(g_sc), _ptr(bg), _ptr(u_qs), _ptr(u_sc), _ptr(bu), _ptr(d_qs),
                               _ptr(d_sc), _ptr(bd), rail, _ptr(workspace), workspace_bytes, _ptr(y),
                               _ptr(ids_out), _ptr(weights_out), _stream(stream))
+
+
+def moe_ffn_layer_hostio(x_host, y_host, x_dev, y_dev, T, D, F, E, k, w_router, b_router, g_qs, g_sc,
+                         bg, u_qs, u_sc, bu, d_qs, d_sc, bd, rail, workspace, workspace_bytes,
+                         stream=None):
+    return _lib.moe_ffn_layer_hostio(_ptr(x_host), _ptr(y_host), _ptr(x_dev), _ptr(y_dev), T, D, F, E, k,
+                                     _ptr(w_router), _ptr(b_router), _ptr(g_qs), _ptr(g_sc), _ptr(bg),
+                                     _ptr(u_qs), _ptr(u_sc), _ptr(bu), _ptr(d_qs), _ptr(d_sc), _ptr(bd),
+                                     rail, _ptr(workspace), workspace_bytes, _stream(stream))
 
 
 def moe_ffn_layer_decode_static(x, T, D, F, E, k, w_router, b_router, g_qs, g_sc, bg, u_qs, u_sc, bu,

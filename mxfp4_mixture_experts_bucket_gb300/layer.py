@@ -39,6 +39,7 @@ class MoeLayer:
         self.F = self.w["g_qs"].shape[1]
         self.k = k
         self._ws: Dict[int, torch.Tensor] = {}
+        self._io: Dict[int, tuple] = {}
 
     def workspace(self, T: int, rail: int) -> torch.Tensor:
         n = _lib.moe_ffn_workspace_bytes(T, self.D, self.F, self.E, self.k, rail)
@@ -65,5 +66,34 @@ class MoeLayer:
                                 weights_out, stream)
         _lib.check(rc, "moe_ffn_layer")
         return out
+
+    def forward_host(self, x_host: torch.Tensor, y_host: Optional[torch.Tensor] = None,
+                     rail: int = _lib.MOE_RAIL_AUTO, stream=None) -> torch.Tensor:
+        """The layer for tokens in host memory, one C call per step (moe_ffn_layer_hostio).
+
+        x_host: [T, D] float32 CPU tensor, ideally pinned; y_host (allocated pinned
+        if None): [T, D] float32 CPU tensor. The copies and the layer are only
+        enqueued on the stream: synchronise it before reading y_host.
+        """
+        T = x_host.shape[0]
+        if x_host.device.type != "cpu" or x_host.dtype != torch.float32 or not x_host.is_contiguous():
+            raise ValueError("x_host must be a contiguous float32 CPU tensor")
+        if y_host is None:
+            y_host = torch.empty((T, self.D), dtype=torch.float32, pin_memory=True)
+        if y_host.device.type != "cpu" or y_host.dtype != torch.float32 or not y_host.is_contiguous():
+            raise ValueError("y_host must be a contiguous float32 CPU tensor")
+        io = self._io.get(T)
+        if io is None:
+            io = (torch.empty((T, self.D), dtype=torch.float32, device=self.device),
+                  torch.empty((T, self.D), dtype=torch.float32, device=self.device))
+            self._io[T] = io
+        ws = self.workspace(T, rail)
+        w = self.w
+        rc = _lib.moe_ffn_layer_hostio(x_host, y_host, io[0], io[1], T, self.D, self.F, self.E, self.k,
+                                       w["w_router"], w["b_router"], w["g_qs"], w["g_sc"], w["bg"],
+                                       w["u_qs"], w["u_sc"], w["bu"], w["d_qs"], w["d_sc"], w["bd"], rail,
+                                       ws, ws.numel(), stream)
+        _lib.check(rc, "moe_ffn_layer_hostio")
+        return y_host
 
     __call__ = forward

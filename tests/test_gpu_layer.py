@@ -215,3 +215,19 @@ def test_decode_stage_entry_points_match_the_layer(moe, T):
     assert torch.equal(y.cpu(), torch.from_numpy(y_layer))
     y64, _, _, _ = O.moe_layer(L, x_np, k, ids=ids_l, weights=w_l.astype(np.float64), cache=cache)
     assert O.rownorm_rel_err(y_layer, y64).max() <= DECODE_TOL
+
+
+@pytest.mark.parametrize("cfg,T,rail", [(1, 1, "GEMV"), (1, 3, "GEMV"), (0, 8, "GEMV"), (0, 8, "GROUPED_MM")])
+def test_forward_host_matches_forward(moe, cfg, T, rail):
+    """moe_ffn_layer_hostio (host x in, host y out, one call) gives the same bits as
+    moe_ffn_layer on device buffers, for two calls in a row on one stream."""
+    spec, L, layer, _ = layer_for(moe, cfg)
+    r = getattr(moe, f"MOE_RAIL_{rail}")
+    for rep in range(2):
+        x_np = make_tokens(spec, T=T, seed=300 + 10 * cfg + T + rep)
+        y_dev = layer(dev(x_np), rail=r)
+        x_host = torch.from_numpy(x_np).pin_memory()
+        y_host = layer.forward_host(x_host, rail=r)
+        torch.cuda.synchronize()
+        assert status(moe) == 0
+        assert torch.equal(y_host, y_dev.cpu())
