@@ -260,22 +260,43 @@ int moe_ffn_layer(const float* x, int T, int D, int F, int E, int k, const float
                   cudaStream_t stream);
 
 /*
- * moe_ffn_layer_hostio -- moe_ffn_layer for tokens that live in host memory:
- * on `stream` it copies x_host [T][D] to x_dev, runs moe_ffn_layer (same
- * definition, rails, limits and workspace contract), and copies y_dev [T][D]
- * back to y_host, all enqueued from C so that a serving loop pays one call per
- * step. x_host and y_host should be pinned (page-locked) for the copies to be
- * asynchronous; x_dev and y_dev are caller-owned device buffers of T*D floats,
- * 16-byte aligned. The call returns once the work is enqueued: y_host holds the
- * result after the stream has been synchronised. Errors as moe_ffn_layer; a
- * failed copy returns MOE_ECUDA.
+ * moe_ffn_args_t -- every argument of moe_ffn_layer that stays fixed from one
+ * step to the next, plus two device staging buffers x_dev and y_dev of T*D
+ * floats (16-byte aligned). Filled once by the caller; the library neither
+ * keeps nor frees anything it points to.
  */
-int moe_ffn_layer_hostio(const float* x_host, float* y_host, float* x_dev, float* y_dev, int T, int D,
-                         int F, int E, int k, const float* w_router, const float* b_router,
-                         const uint8_t* g_qs, const uint8_t* g_sc, const float* bg,
-                         const uint8_t* u_qs, const uint8_t* u_sc, const float* bu,
-                         const uint8_t* d_qs, const uint8_t* d_sc, const float* bd, int rail,
-                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
+typedef struct {
+  int T, D, F, E, k, rail;
+  const float* w_router;
+  const float* b_router;
+  const uint8_t* g_qs;
+  const uint8_t* g_sc;
+  const float* bg;
+  const uint8_t* u_qs;
+  const uint8_t* u_sc;
+  const float* bu;
+  const uint8_t* d_qs;
+  const uint8_t* d_sc;
+  const float* bd;
+  void* workspace;
+  size_t workspace_bytes;
+  float* x_dev;
+  float* y_dev;
+} moe_ffn_args_t;
+
+/*
+ * moe_ffn_layer_hostio -- moe_ffn_layer for tokens that live in host memory:
+ * on `stream` it copies x_host [T][D] to args->x_dev, runs moe_ffn_layer with
+ * the fixed arguments in *args (same definition, rails, limits and workspace
+ * contract), and copies args->y_dev back to y_host [T][D], all enqueued from C
+ * so that a serving loop passes four arguments per step. x_host and y_host
+ * should be pinned (page-locked) for the copies to be asynchronous. The call
+ * returns once the work is enqueued: y_host holds the result after the stream
+ * has been synchronised. Errors as moe_ffn_layer; a failed copy returns
+ * MOE_ECUDA.
+ */
+int moe_ffn_layer_hostio(const moe_ffn_args_t* args, const float* x_host, float* y_host,
+                         cudaStream_t stream);
 
 /* Size of the library's static decode scratch (moe_ffn_layer_decode_static). */
 #define MOE_DECODE_SCRATCH_BYTES (512 * 1024)

@@ -61,7 +61,7 @@ _SIGS = {
     "moe_expert_gateup_swiglu": (I, [P, P, P, P, P, P, I, I, I, I, I, P, P, F, F, P, P]),
     "moe_expert_down_combine": (I, [P, P, P, I, I, I, I, I, P, P, P, P, P]),
     "moe_ffn_layer": (I, [P, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, I, P, SZ, P, P, P, P]),
-    "moe_ffn_layer_hostio": (I, [P, P, P, P, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, I, P, SZ, P]),
+    "moe_ffn_layer_hostio": (I, [P, P, P, P]),
     "moe_ffn_layer_decode_static": (I, [P, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P]),
     "moe_get_status": (I, [P, ctypes.POINTER(ctypes.c_int)]),
     "moe_get_timeout_site": (I, [P, ctypes.POINTER(ctypes.c_int)]),
@@ -177,13 +177,24 @@ def moe_ffn_layer(x, T, D, F, E, k, w_router, b_router, g_qs, g_sc, bg, u_qs, u_
                               _ptr(ids_out), _ptr(weights_out), _stream(stream))
 
 
-def moe_ffn_layer_hostio(x_host, y_host, x_dev, y_dev, T, D, F, E, k, w_router, b_router, g_qs, g_sc,
-                         bg, u_qs, u_sc, bu, d_qs, d_sc, bd, rail, workspace, workspace_bytes,
-                         stream=None):
-    return _lib.moe_ffn_layer_hostio(_ptr(x_host), _ptr(y_host), _ptr(x_dev), _ptr(y_dev), T, D, F, E, k,
-                                     _ptr(w_router), _ptr(b_router), _ptr(g_qs), _ptr(g_sc), _ptr(bg),
-                                     _ptr(u_qs), _ptr(u_sc), _ptr(bu), _ptr(d_qs), _ptr(d_sc), _ptr(bd),
-                                     rail, _ptr(workspace), workspace_bytes, _stream(stream))
+class MoeFfnArgs(ctypes.Structure):
+    """moe_ffn_args_t of the header: the fixed arguments of moe_ffn_layer_hostio."""
+    _fields_ = [("T", I), ("D", I), ("F", I), ("E", I), ("k", I), ("rail", I),
+                ("w_router", P), ("b_router", P), ("g_qs", P), ("g_sc", P), ("bg", P),
+                ("u_qs", P), ("u_sc", P), ("bu", P), ("d_qs", P), ("d_sc", P), ("bd", P),
+                ("workspace", P), ("workspace_bytes", SZ), ("x_dev", P), ("y_dev", P)]
+
+
+def make_ffn_args(T, D, F, E, k, rail, w_router, b_router, g_qs, g_sc, bg, u_qs, u_sc, bu, d_qs, d_sc,
+                  bd, workspace, workspace_bytes, x_dev, y_dev) -> MoeFfnArgs:
+    return MoeFfnArgs(T, D, F, E, k, rail, _ptr(w_router), _ptr(b_router), _ptr(g_qs), _ptr(g_sc),
+                      _ptr(bg), _ptr(u_qs), _ptr(u_sc), _ptr(bu), _ptr(d_qs), _ptr(d_sc), _ptr(bd),
+                      _ptr(workspace), workspace_bytes, _ptr(x_dev), _ptr(y_dev))
+
+
+def moe_ffn_layer_hostio(args, x_host, y_host, stream=None):
+    return _lib.moe_ffn_layer_hostio(None if args is None else ctypes.byref(args), _ptr(x_host),
+                                     _ptr(y_host), _stream(stream))
 
 
 def moe_ffn_layer_decode_static(x, T, D, F, E, k, w_router, b_router, g_qs, g_sc, bg, u_qs, u_sc, bu,

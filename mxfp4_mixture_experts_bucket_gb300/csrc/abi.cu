@@ -456,23 +456,21 @@ int moe_ffn_layer(const float* x, int T, int D, int F, int E, int k, const float
   return cuda_status(launch_grouped_mm(gd, L));
 }
 
-int moe_ffn_layer_hostio(const float* x_host, float* y_host, float* x_dev, float* y_dev, int T, int D,
-                         int F, int E, int k, const float* w_router, const float* b_router,
-                         const uint8_t* g_qs, const uint8_t* g_sc, const float* bg,
-                         const uint8_t* u_qs, const uint8_t* u_sc, const float* bu,
-                         const uint8_t* d_qs, const uint8_t* d_sc, const float* bd, int rail,
-                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-  MOE_REQUIRE(T >= 0 && D >= 64);
-  if (T == 0) return MOE_OK;
-  MOE_REQUIRE(x_host && y_host && x_dev && y_dev);
-  const size_t bytes = (size_t)T * D * sizeof(float);
-  cudaError_t err = cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, stream);
+int moe_ffn_layer_hostio(const moe_ffn_args_t* args, const float* x_host, float* y_host,
+                         cudaStream_t stream) {
+  MOE_REQUIRE(args != nullptr);
+  const moe_ffn_args_t& a = *args;
+  MOE_REQUIRE(a.T >= 0 && a.D >= 64);
+  if (a.T == 0) return MOE_OK;
+  MOE_REQUIRE(x_host && y_host && a.x_dev && a.y_dev);
+  const size_t bytes = (size_t)a.T * a.D * sizeof(float);
+  cudaError_t err = cudaMemcpyAsync(a.x_dev, x_host, bytes, cudaMemcpyHostToDevice, stream);
   if (err != cudaSuccess) return cuda_status(err);
-  const int rc = moe_ffn_layer(x_dev, T, D, F, E, k, w_router, b_router, g_qs, g_sc, bg, u_qs, u_sc, bu,
-                               d_qs, d_sc, bd, rail, workspace, workspace_bytes, y_dev, nullptr, nullptr,
-                               stream);
+  const int rc = moe_ffn_layer(a.x_dev, a.T, a.D, a.F, a.E, a.k, a.w_router, a.b_router, a.g_qs, a.g_sc,
+                               a.bg, a.u_qs, a.u_sc, a.bu, a.d_qs, a.d_sc, a.bd, a.rail, a.workspace,
+                               a.workspace_bytes, a.y_dev, nullptr, nullptr, stream);
   if (rc != MOE_OK) return rc;
-  return cuda_status(cudaMemcpyAsync(y_host, y_dev, bytes, cudaMemcpyDeviceToHost, stream));
+  return cuda_status(cudaMemcpyAsync(y_host, a.y_dev, bytes, cudaMemcpyDeviceToHost, stream));
 }
 
 int moe_get_status(cudaStream_t stream, int* status) {

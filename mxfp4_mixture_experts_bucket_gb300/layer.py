@@ -39,7 +39,7 @@ class MoeLayer:
         self.F = self.w["g_qs"].shape[1]
         self.k = k
         self._ws: Dict[int, torch.Tensor] = {}
-        self._io: Dict[int, tuple] = {}
+        self._io: Dict[tuple, tuple] = {}
 
     def workspace(self, T: int, rail: int) -> torch.Tensor:
         n = _lib.moe_ffn_workspace_bytes(T, self.D, self.F, self.E, self.k, rail)
@@ -82,17 +82,19 @@ class MoeLayer:
             y_host = torch.empty((T, self.D), dtype=torch.float32, pin_memory=True)
         if y_host.device.type != "cpu" or y_host.dtype != torch.float32 or not y_host.is_contiguous():
             raise ValueError("y_host must be a contiguous float32 CPU tensor")
-        io = self._io.get(T)
-        if io is None:
-            io = (torch.empty((T, self.D), dtype=torch.float32, device=self.device),
-                  torch.empty((T, self.D), dtype=torch.float32, device=self.device))
-            self._io[T] = io
-        ws = self.workspace(T, rail)
-        w = self.w
-        rc = _lib.moe_ffn_layer_hostio(x_host, y_host, io[0], io[1], T, self.D, self.F, self.E, self.k,
-                                       w["w_router"], w["b_router"], w["g_qs"], w["g_sc"], w["bg"],
-                                       w["u_qs"], w["u_sc"], w["bu"], w["d_qs"], w["d_sc"], w["bd"], rail,
-                                       ws, ws.numel(), stream)
+        key = (T, rail)
+        io = self._io.get(key)
+        if io is None:  # staging buffers and the fixed arguments, once per (T, rail)
+            xd = torch.empty((T, self.D), dtype=torch.float32, device=self.device)
+            yd = torch.empty((T, self.D), dtype=torch.float32, device=self.device)
+            ws = self.workspace(T, rail)
+            w = self.w
+            args = _lib.make_ffn_args(T, self.D, self.F, self.E, self.k, rail, w["w_router"], w["b_router"],
+                                      w["g_qs"], w["g_sc"], w["bg"], w["u_qs"], w["u_sc"], w["bu"],
+                                      w["d_qs"], w["d_sc"], w["bd"], ws, ws.numel(), xd, yd)
+            io = (xd, yd, args)
+            self._io[key] = io
+        rc = _lib.moe_ffn_layer_hostio(io[2], x_host, y_host, stream)
         _lib.check(rc, "moe_ffn_layer_hostio")
         return y_host
 

@@ -137,3 +137,12 @@ def test_valid_call_without_a_gpu_reports_a_cuda_error(moe):
         pytest.skip("a GPU is present")
     rc, _ = moe.moe_get_status(stream=0)
     assert rc in (moe.MOE_ECUDA, moe.MOE_EUNSUPPORTED)
+
+
+def test_hostio_rejects_missing_arguments(moe):
+    """moe_ffn_layer_hostio checks its argument block on the host before enqueueing anything."""
+    assert moe.moe_ffn_layer_hostio(None, 0, 0, 0) == moe.MOE_EINVAL
+    args = moe.MoeFfnArgs(1, 64, 64, 4, 2, moe.MOE_RAIL_GEMV)
+    assert moe.moe_ffn_layer_hostio(args, 0, 0, 0) == moe.MOE_EINVAL  # no host or staging buffers
+    args.T = 0
+    assert moe.moe_ffn_layer_hostio(args, 0, 0, 0) == moe.MOE_OK      # nothing to do
