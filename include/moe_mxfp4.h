@@ -74,6 +74,7 @@ extern "C" {
 #define MOE_RAIL_AUTO 0       /* GEMV rail when T <= MOE_GEMV_MAX_T, grouped GEMM otherwise */
 #define MOE_RAIL_GEMV 1
 #define MOE_RAIL_GROUPED_MM 2
+#define MOE_RAIL_GROUPED_MX 3 /* grouped GEMM on the block-scaled (MXFP4 x E4M3) tensor cores */
 #define MOE_GEMV_MAX_T 8
 
 /* Bucket tile height of the grouped-GEMM rail (rows per tensor-core tile). */
@@ -243,7 +244,14 @@ int moe_expert_down_combine(const uint8_t* d_qs, const uint8_t* d_sc, const floa
  * top-k of the router logits themselves, so a decode step is three kernels. MOE_RAIL_GROUPED_MM runs the
  * tcgen05 grouped GEMM with bf16 MMAs (x enters gate/up split into bf16 high
  * and low parts, h enters down rounded to bf16), the swiglu fused into the
- * gate/up epilogue and the weighted scatter fused into the down epilogue. MOE_RAIL_AUTO picks GEMV for T <= MOE_GEMV_MAX_T.
+ * gate/up epilogue and the weighted scatter fused into the down epilogue.
+ * MOE_RAIL_GROUPED_MX has the same structure on the block-scaled tensor cores:
+ * the MXFP4 weights enter the MMA as stored (no dequantisation); x enters as
+ * a sum of three E4M3 blocks and h as two (each block of 32 on its own E8M0
+ * scale, each term carrying the rounding residual of the ones before: about
+ * 12 and 8 significant bits). Both grouped rails accumulate in fp32 and
+ * scatter with float atomics (order not deterministic).
+ * MOE_RAIL_AUTO picks GEMV for T <= MOE_GEMV_MAX_T.
  * x: float [T][D]; w_router [E][D]; b_router [E] or NULL; gate/up planes
  * [E][F][D/2], [E][F][D/32]; down planes [E][D][F/2], [E][D][F/32]; biases
  * bg, bu [E][F], bd [E][D] (each may be NULL); y: float [T][D], overwritten.

@@ -40,6 +40,7 @@ MOE_EPI_SCATTER_WEIGHTED = 2
 MOE_RAIL_AUTO = 0
 MOE_RAIL_GEMV = 1
 MOE_RAIL_GROUPED_MM = 2
+MOE_RAIL_GROUPED_MX = 3
 MOE_GEMV_MAX_T = 8
 MOE_MM_TILE = 128
 

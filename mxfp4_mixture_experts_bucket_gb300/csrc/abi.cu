@@ -102,6 +102,11 @@ struct Workspace {
   uint16_t* xg;    // grouped rail: [max_rows][D] bf16, high parts of x
   uint16_t* xg_lo; // grouped rail: [max_rows][D] bf16, low parts of x
   uint16_t* hg;    // grouped rail: [max_rows][F] bf16
+  // block-scaled rail: E4M3 operand terms in bucket order and their scale words
+  uint8_t* xq;       // [kMxXTerms][max_rows][D]
+  uint32_t* xs;      // [kMxXTerms][D/128 rounded up][max_rows]
+  uint8_t* hq;       // [kMxHTerms][max_rows][F]
+  uint32_t* hs;      // [kMxHTerms][F/128 rounded up][max_rows]
   size_t max_rows;
 };
 
@@ -125,6 +130,12 @@ size_t layout_workspace(int T, int D, int F, int E, int k, int rail, char* base,
   w.inv = reinterpret_cast<int32_t*>(take((size_t)T * k * 4));
   if (rail == MOE_RAIL_GEMV) {
     w.h = reinterpret_cast<float*>(take((size_t)T * k * F * 4));
+  } else if (rail == MOE_RAIL_GROUPED_MX) {
+    const size_t nd = (size_t)(D / 32 + 3) / 4, nf = (size_t)(F / 32 + 3) / 4;
+    w.xq = reinterpret_cast<uint8_t*>(take(kMxXTerms * mr * D));
+    w.xs = reinterpret_cast<uint32_t*>(take(kMxXTerms * nd * mr * 4));
+    w.hq = reinterpret_cast<uint8_t*>(take(kMxHTerms * mr * F));
+    w.hs = reinterpret_cast<uint32_t*>(take(kMxHTerms * nf * mr * 4));
   } else {
     w.xg = reinterpret_cast<uint16_t*>(take(mr * D * 2));
     w.xg_lo = reinterpret_cast<uint16_t*>(take(mr * D * 2));
@@ -195,7 +206,7 @@ size_t moe_bucket_max_rows(int T, int k, int E, int tile) {
 size_t moe_ffn_workspace_bytes(int T, int D, int F, int E, int k, int rail) {
   if (T < 0 || D < 1 || F < 1 || E < 1 || k < 1 || k > E) return 0;
   rail = resolve_rail(T, rail);
-  if (rail != MOE_RAIL_GEMV && rail != MOE_RAIL_GROUPED_MM) return 0;
+  if (rail != MOE_RAIL_GEMV && rail != MOE_RAIL_GROUPED_MM && rail != MOE_RAIL_GROUPED_MX) return 0;
   return layout_workspace(T, D, F, E, k, rail, nullptr, nullptr);
 }
 
@@ -367,7 +378,7 @@ int moe_ffn_layer(const float* x, int T, int D, int F, int E, int k, const float
   MOE_REQUIRE(T >= 0 && D >= 64 && F >= 64 && D % 64 == 0 && F % 64 == 0);
   MOE_REQUIRE(E >= 1 && E <= 256 && k >= 1 && k <= E && k <= 32);
   rail = resolve_rail(T, rail);
-  MOE_REQUIRE(rail == MOE_RAIL_GEMV || rail == MOE_RAIL_GROUPED_MM);
+  MOE_REQUIRE(rail == MOE_RAIL_GEMV || rail == MOE_RAIL_GROUPED_MM || rail == MOE_RAIL_GROUPED_MX);
   if (rail == MOE_RAIL_GEMV) {
     MOE_REQUIRE(T <= MOE_GEMV_MAX_T && k <= 8);
     if (D > 4096 || F > 4096) return MOE_EUNSUPPORTED;
@@ -408,6 +419,53 @@ int moe_ffn_layer(const float* x, int T, int D, int F, int E, int k, const float
   rc = cuda_status(launch_bucket(ids, T, k, E, MOE_MM_TILE, (int)ws.max_rows, ws.counts, ws.basep,
                                  ws.rows, ws.inv, d->status, L));
   if (rc != MOE_OK) return rc;
+  if (rail == MOE_RAIL_GROUPED_MX) {
+    rc = cuda_status(launch_quant_rows_mx(x, T, D, k, ws.rows, ws.basep, E, (int)ws.max_rows, ws.xq, ws.xs, y,
+                                          L));
+    if (rc != MOE_OK) return rc;
+    GroupedMXArgs g{};
+    g.w_qs[0] = g_qs;
+    g.w_sc[0] = g_sc;
+    g.bias[0] = bg;
+    g.w_qs[1] = u_qs;
+    g.w_sc[1] = u_sc;
+    g.bias[1] = bu;
+    g.nmat = 2;
+    g.E = E;
+    g.R = F;
+    g.C = D;
+    g.a_terms = ws.xq;
+    g.a_sc = ws.xs;
+    g.counts = ws.counts;
+    g.basep = ws.basep;
+    g.rows = ws.rows;
+    g.max_rows = (int)ws.max_rows;
+    g.k = k;
+    g.weights = wts;
+    g.alpha = alpha;
+    g.limit = limit;
+    g.h_terms = ws.hq;
+    g.h_sc = ws.hs;
+    g.status = d->status;
+    rc = cuda_status(launch_grouped_mx(g, L));
+    if (rc != MOE_OK) return rc;
+    GroupedMXArgs gd = g;
+    gd.w_qs[0] = d_qs;
+    gd.w_sc[0] = d_sc;
+    gd.bias[0] = bd;
+    gd.w_qs[1] = nullptr;
+    gd.w_sc[1] = nullptr;
+    gd.bias[1] = nullptr;
+    gd.nmat = 1;
+    gd.R = D;
+    gd.C = F;
+    gd.a_terms = ws.hq;
+    gd.a_sc = ws.hs;
+    gd.h_terms = nullptr;
+    gd.h_sc = nullptr;
+    gd.y = y;
+    return cuda_status(launch_grouped_mx(gd, L));
+  }
   rc = cuda_status(launch_gather_bf16(x, T, D, k, ws.rows, ws.basep, E, (int)ws.max_rows, ws.xg,
                                       ws.xg_lo, y, L));
   if (rc != MOE_OK) return rc;

@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace moe {
@@ -117,5 +118,43 @@ struct GroupedMMArgs {
 };
 // Returns cudaErrorInvalidValue for unsupported shapes (checked by the caller first).
 cudaError_t launch_grouped_mm(const GroupedMMArgs& args, Launch L);
+// Tiled tensor map through the driver's encoder (no fill for out-of-range
+// elements, 256-byte L2 promotion); false if the encoder is missing or refuses.
+bool encode_tiled_map(CUtensorMap* tm, CUtensorMapDataType dtype, int rank, const void* base,
+                      const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                      CUtensorMapSwizzle swizzle);
+
+// ---- grouped_mx.cu ----
+// Gate/up (nmat 2) or down (nmat 1) on the block-scaled tensor cores. The
+// activation operand is a sum of E4M3 terms (gate/up: 3, down: 2), each
+// [max_rows][C] in the MMA's per-block K order, terms back to back, with scale
+// words [terms][C/128 rounded up][max_rows].
+struct GroupedMXArgs {
+  const uint8_t* w_qs[2];
+  const uint8_t* w_sc[2];
+  const float* bias[2];
+  int nmat;
+  int E, R, C;
+  const uint8_t* a_terms;
+  const uint32_t* a_sc;
+  const int32_t* counts;
+  const int32_t* basep;
+  const int32_t* rows;
+  int max_rows;
+  int k;
+  const float* weights;
+  float alpha, limit;
+  uint8_t* h_terms;  // nmat 2: swiglu output in the down operand's format, [2][max_rows][R]
+  uint32_t* h_sc;    // nmat 2: [2][R/128 rounded up][max_rows]
+  float* y;          // nmat 1: [T][R], accumulated into (zeroed beforehand)
+  int* status;
+};
+constexpr int kMxXTerms = 3;
+constexpr int kMxHTerms = 2;
+cudaError_t launch_grouped_mx(const GroupedMXArgs& args, Launch L);
+// x rows in bucket order -> kMxXTerms E4M3 terms + scale words; zeroes y_zero [T][D] if given.
+cudaError_t launch_quant_rows_mx(const float* x, int T, int D, int k, const int32_t* rows, const int32_t* basep,
+                                 int E, int max_rows, uint8_t* q_terms, uint32_t* sc_terms, float* y_zero,
+                                 Launch L);
 
 }  // namespace moe

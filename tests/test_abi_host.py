@@ -41,6 +41,9 @@ def test_workspace_bytes(moe):
     assert moe.moe_ffn_workspace_bytes(512, 2880, 2880, 32, 4, moe.MOE_RAIL_AUTO) == mm
     assert moe.moe_ffn_workspace_bytes(1, 2880, 2880, 4, 8, moe.MOE_RAIL_AUTO) == 0  # k > E
     assert moe.moe_ffn_workspace_bytes(1, 2880, 2880, 32, 4, 7) == 0  # unknown rail
+    mx = moe.moe_ffn_workspace_bytes(512, 2880, 2880, 32, 4, moe.MOE_RAIL_GROUPED_MX)
+    # three E4M3 terms of x and two of h, plus one scale word per 4 blocks of each term
+    assert mx >= mr * 2880 * 5 + 5 * 23 * mr * 4 and mx % 256 == 0
 
 
 def test_route_topk_rejects_bad_arguments(moe):

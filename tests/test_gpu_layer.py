@@ -57,6 +57,10 @@ def check_layer(moe, cfg, T, rail, sample=None, seed=None):
     if rail == moe.MOE_RAIL_GEMV:
         err = O.rownorm_rel_err(y[toks], y64)
         assert err.max() <= DECODE_TOL, err.max()
+    elif rail == moe.MOE_RAIL_GROUPED_MX:
+        err64 = O.rownorm_rel_err(y[toks], y64)
+        print(f"mx rail cfg {cfg} T {T}: rownorm err vs float64 {err64.max():.3e}")
+        assert err64.max() <= PREFILL_TOL, err64.max()
     else:
         ybf, _, _, _ = O.moe_layer(L, x, spec.k, token_idx=toks, ids=ids, weights=w_ref, cache=cache,
                                    operands="bf16_split")
@@ -67,7 +71,7 @@ def check_layer(moe, cfg, T, rail, sample=None, seed=None):
     return y, ids
 
 
-@pytest.mark.parametrize("rail_name", ["GEMV", "GROUPED_MM"])
+@pytest.mark.parametrize("rail_name", ["GEMV", "GROUPED_MM", "GROUPED_MX"])
 def test_tiny_layer_both_rails(moe, rail_name):
     check_layer(moe, 0, 8, getattr(moe, "MOE_RAIL_" + rail_name))
 
@@ -77,9 +81,10 @@ def test_tiny_layer_gemv_token_counts(moe, T):
     check_layer(moe, 0, T, moe.MOE_RAIL_GEMV, seed=40 + T)
 
 
+@pytest.mark.parametrize("rail_name", ["GROUPED_MM", "GROUPED_MX"])
 @pytest.mark.parametrize("T", [1, 9, 40, 131])
-def test_tiny_layer_grouped_token_counts(moe, T):
-    check_layer(moe, 0, T, moe.MOE_RAIL_GROUPED_MM, seed=50 + T)
+def test_tiny_layer_grouped_token_counts(moe, T, rail_name):
+    check_layer(moe, 0, T, getattr(moe, "MOE_RAIL_" + rail_name), seed=50 + T)
 
 
 def test_decode_T1_full_size(moe):
@@ -97,9 +102,14 @@ def test_prefill_T512_full_size_sampled(moe):
     check_layer(moe, 2, 512, moe.MOE_RAIL_AUTO, sample=np.array([0, 1, 255, 511]))
 
 
-def test_skew_T4096_full_size_sampled(moe):
+def test_prefill_T512_full_size_sampled_mx(moe):
+    check_layer(moe, 2, 512, moe.MOE_RAIL_GROUPED_MX, sample=np.array([0, 1, 100, 255, 511]))
+
+
+@pytest.mark.parametrize("rail_name", ["GROUPED_MM", "GROUPED_MX"])
+def test_skew_T4096_full_size_sampled(moe, rail_name):
     spec, L, layer, cache = layer_for(moe, 4)
-    y, ids = check_layer(moe, 4, 4096, moe.MOE_RAIL_GROUPED_MM, sample=np.array([0, 777, 4095]))
+    y, ids = check_layer(moe, 4, 4096, getattr(moe, "MOE_RAIL_" + rail_name), sample=np.array([0, 777, 4095]))
     counts = np.bincount(ids.reshape(-1), minlength=spec.E)
     # the stated shape of the skewed workload: about half of the assignments on the
     # two hot experts, several experts nearly empty
@@ -186,7 +196,8 @@ def test_layer_without_biases(moe):
               bu=np.zeros((spec.E, spec.F), np.float32), bd=np.zeros((spec.E, spec.D), np.float32))
     y64, ids64, _, _ = O.moe_layer(L0, x, spec.k)
     ybf, _, _, _ = O.moe_layer(L0, x, spec.k, operands="bf16_split")
-    for rail, ref, tol in ((moe.MOE_RAIL_GEMV, y64, DECODE_TOL), (moe.MOE_RAIL_GROUPED_MM, ybf, PREFILL_BF16_TOL)):
+    for rail, ref, tol in ((moe.MOE_RAIL_GEMV, y64, DECODE_TOL), (moe.MOE_RAIL_GROUPED_MM, ybf, PREFILL_BF16_TOL),
+                           (moe.MOE_RAIL_GROUPED_MX, y64, PREFILL_TOL)):
         y, ids, _ = run_layer(moe, layer, x, rail, spec.k)
         assert np.array_equal(ids, ids64)
         assert O.rownorm_rel_err(y, ref).max() <= tol
@@ -217,7 +228,8 @@ def test_decode_stage_entry_points_match_the_layer(moe, T):
     assert O.rownorm_rel_err(y_layer, y64).max() <= DECODE_TOL
 
 
-@pytest.mark.parametrize("cfg,T,rail", [(1, 1, "GEMV"), (1, 3, "GEMV"), (0, 8, "GEMV"), (0, 8, "GROUPED_MM")])
+@pytest.mark.parametrize("cfg,T,rail", [(1, 1, "GEMV"), (1, 3, "GEMV"), (0, 8, "GEMV"), (0, 8, "GROUPED_MM"),
+                                        (0, 8, "GROUPED_MX")])
 def test_forward_host_matches_forward(moe, cfg, T, rail):
     """moe_ffn_layer_hostio (host x in, host y out, one call) gives the same bits as
     moe_ffn_layer on device buffers, for two calls in a row on one stream."""
