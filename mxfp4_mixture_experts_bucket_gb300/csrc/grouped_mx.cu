@@ -456,8 +456,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int r = xr0 + 16 * i;
-          const uint2 v = *reinterpret_cast<const uint2*>(raw + r * (BK / 2) + xc * 8);
-          *reinterpret_cast<uint4*>(at + r * 128 + ((xc ^ (r & 7)) << 4)) = make_uint4(v.x, v.y, 0u, 0u);
+          // the MMA ignores the chunk's second 8 bytes: only the nibbles are written
+          *reinterpret_cast<uint2*>(at + r * 128 + ((xc ^ (r & 7)) << 4)) =
+              *reinterpret_cast<const uint2*>(raw + r * (BK / 2) + xc * 8);
         }
       }
       const uint32_t slot = tmem + sc0 + (uint32_t)as * kScCols;
