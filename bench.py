@@ -6,7 +6,8 @@ shaped decode step (E=32 experts, top-4, D=F=2880, MXFP4 weights, T=1), the
 weight GB/s it streams, the dominant kernel's roofline fraction, the same
 metric end to end through the public API with host buffers, and the CPU
 oracle as a baseline. The prefill step (T=512) is measured in the same run
-and reported under "prefill_t512".
+and reported under "prefill_t512" (bf16 grouped GEMM) and "prefill_t512_mx"
+(block-scaled MXFP4 grouped GEMM).
 
 Timing: CUDA events on the launching stream around exactly --steps steps,
 captured in one CUDA graph, after --warmup eager steps; every step uses the
@@ -244,7 +245,9 @@ def run_ours(args, dist: Dist):
     hbm_peak, bf16_peak, bf16_sus, peak_src = load_peaks()
     if args.skip_decode:
         stream = torch.cuda.Stream(device=dev)
-        return {"prefill_t512": run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src)}
+        return {"prefill_t512": run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src),
+                "prefill_t512_mx": run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src,
+                                               rail=moe.MOE_RAIL_GROUPED_MX)}
     K, W, NL = args.steps, args.warmup, args.layers
     spec = spec_for(1)
 
@@ -372,15 +375,19 @@ def run_ours(args, dist: Dist):
 
     if not args.no_prefill:
         result["prefill_t512"] = run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src)
+        result["prefill_t512_mx"] = run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src,
+                                                rail=moe.MOE_RAIL_GROUPED_MX)
     return result
 
 
-def run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src):
+def run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src, rail=None):
     import torch
     from synthetic import make_layer_torch, spec_for
 
     spec = spec_for(2)
     T, K = 512, args.prefill_steps
+    if rail is None:
+        rail = moe.MOE_RAIL_GROUPED_MM
     NL = 2
     layers = [moe.MoeLayer(make_layer_torch(spec, li + 31 * dist.rank, dev), k=K_TOP, device=dev) for li in range(NL)]
     g = torch.Generator(device=dev)
@@ -389,13 +396,13 @@ def run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src):
     ys = [torch.empty((T, D), device=dev) for _ in range(NL)]
     with torch.cuda.stream(stream):
         for i in range(3):
-            layers[i % NL](xs[i % NL], rail=moe.MOE_RAIL_GROUPED_MM, out=ys[i % NL])
+            layers[i % NL](xs[i % NL], rail=rail, out=ys[i % NL])
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     n0 = moe.moe_kernel_launches()
     with torch.cuda.graph(graph, stream=stream):
         for i in range(K):
-            layers[i % NL](xs[i % NL], rail=moe.MOE_RAIL_GROUPED_MM, out=ys[i % NL])
+            layers[i % NL](xs[i % NL], rail=rail, out=ys[i % NL])
     per_step = (moe.moe_kernel_launches() - n0) / K
     with torch.cuda.stream(stream):
         graph.replay()
@@ -419,7 +426,10 @@ def run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src):
     flops = T * K_TOP * 3 * 2 * D * F
     t_roof = max(alg_bytes / (hbm_peak * 1e9), flops / (bf16_peak * 1e12))
     return {"tokens_per_s": round(rate, 1), "ms_per_step": round(ms, 4), "steps": K, "workload": WORKLOAD_PREFILL,
-            "weight_gbs": round(weight_bytes / (ms / 1e3) / 1e9, 1), "dtype": "bf16 MMA, fp32 accumulate",
+            "weight_gbs": round(weight_bytes / (ms / 1e3) / 1e9, 1),
+            "dtype": ("bf16 MMA, fp32 accumulate" if rail == moe.MOE_RAIL_GROUPED_MM else
+                      "MXFP4 x E4M3-term block-scaled MMA (x: 3 terms, h: 2), fp32 accumulate"),
+            "rail": "grouped_mm" if rail == moe.MOE_RAIL_GROUPED_MM else "grouped_mx",
             "roofline_frac": round(t_roof / (ms / 1e3), 4),
             "roofline_bound": "hbm" if alg_bytes / (hbm_peak * 1e9) >= flops / (bf16_peak * 1e12) else "tensor",
             "algorithmic_bytes": alg_bytes, "algorithmic_flops": flops, "kernels_per_step": per_step,

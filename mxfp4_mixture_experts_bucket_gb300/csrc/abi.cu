@@ -279,7 +279,7 @@ int moe_gather_rows_bf16(const float* x, int T, int D, int k, const int32_t* row
   int rc = current_device(&d);
   if (rc != MOE_OK) return rc;
   Launch L{stream, false};
-  return cuda_status(launch_gather_bf16(x, T, D, k, rows, basep, E, max_rows, xg, xg_lo, y_zero, L));
+  return cuda_status(launch_gather_bf16(x, T, D, k, rows, basep, E, max_rows, xg, xg_lo, y_zero, true, L));
 }
 
 int moe_mxfp4_grouped_mm(const uint8_t* w_qs, const uint8_t* w_sc, const float* bias,
@@ -467,7 +467,7 @@ int moe_ffn_layer(const float* x, int T, int D, int F, int E, int k, const float
     return cuda_status(launch_grouped_mx(gd, L));
   }
   rc = cuda_status(launch_gather_bf16(x, T, D, k, ws.rows, ws.basep, E, (int)ws.max_rows, ws.xg,
-                                      ws.xg_lo, y, L));
+                                      ws.xg_lo, y, false, L));
   if (rc != MOE_OK) return rc;
   GroupedMMArgs g{};
   g.w_qs[0] = g_qs;

@@ -69,7 +69,7 @@ cudaError_t launch_bucket(const int32_t* ids, int T, int k, int E, int tile, int
                           int* status, Launch L);
 cudaError_t launch_gather_bf16(const float* x, int T, int D, int k, const int32_t* rows,
                                const int32_t* basep, int E, int max_rows, uint16_t* xg,
-                               uint16_t* xg_lo, float* y_zero, Launch L);
+                               uint16_t* xg_lo, float* y_zero, bool zero_pads, Launch L);
 
 // ---- gemv.cu ----
 cudaError_t launch_mxfp4_gemv(const uint8_t* qs, const uint8_t* sc, int E, int R, int C,

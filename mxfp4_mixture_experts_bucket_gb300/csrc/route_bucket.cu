@@ -69,6 +69,87 @@ __global__ void __launch_bounds__(128) router_logits_kernel(const float* __restr
   }
 }
 
+// Prefill sizes (T > 8): a block takes 4 tokens x 32 experts; the 4 token rows
+// sit in shared memory and each warp computes 4 tokens x 4 experts = 16 dots,
+// its lanes splitting K (float4 steps), so every router row is read once per
+// 4 tokens instead of once per dot. Partial sums: one per lane, then a warp
+// xor-reduction per dot.
+constexpr int kRouterTileT = 4;
+__global__ void __launch_bounds__(256) router_logits_tile_kernel(const float* __restrict__ x, int T, int D,
+                                                                 const float* __restrict__ wr,
+                                                                 const float* __restrict__ br, int E,
+                                                                 float* __restrict__ logits) {
+  pdl_launch_dependents();
+  pdl_wait();
+  extern __shared__ float4 xs4[];  // [kRouterTileT][D/4]
+  const int n4 = D >> 2;
+  const int t0 = blockIdx.x * kRouterTileT;
+  constexpr int U = 12;  // loads in flight per thread while the tile is staged
+  for (int i0 = threadIdx.x; i0 < kRouterTileT * n4; i0 += U * 256) {
+    float4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = i0 + u * 256;
+      const int tt = i / n4, c = i - tt * n4;
+      v[u] = (i < kRouterTileT * n4 && t0 + tt < T) ? __ldg(reinterpret_cast<const float4*>(x + (size_t)(t0 + tt) * D) + c)
+                                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (i0 + u * 256 < kRouterTileT * n4) xs4[i0 + u * 256] = v[u];
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e0 = blockIdx.y * 32 + 4 * warp;
+  const float4* wrow[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) wrow[j] = reinterpret_cast<const float4*>(wr + (size_t)min(e0 + j, E - 1) * D);
+  float acc[kRouterTileT][4];
+#pragma unroll
+  for (int tt = 0; tt < kRouterTileT; ++tt)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[tt][j] = 0.f;
+  auto step = [&](const float4 (&wv)[4], int i) {
+#pragma unroll
+    for (int tt = 0; tt < kRouterTileT; ++tt) {
+      const float4 xv = xs4[tt * n4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float a = acc[tt][j];
+        a = fmaf(xv.x, wv[j].x, a);
+        a = fmaf(xv.y, wv[j].y, a);
+        a = fmaf(xv.z, wv[j].z, a);
+        a = fmaf(xv.w, wv[j].w, a);
+        acc[tt][j] = a;
+      }
+    }
+  };
+  int i = lane;
+  for (; i + 96 < n4; i += 128) {  // four steps' router loads in flight before any use
+    float4 wv[4][4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) wv[u][j] = __ldg(wrow[j] + i + 32 * u);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) step(wv[u], i + 32 * u);
+  }
+  for (; i < n4; i += 32) {
+    float4 wv[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) wv[j] = __ldg(wrow[j] + i);
+    step(wv, i);
+  }
+#pragma unroll
+  for (int tt = 0; tt < kRouterTileT; ++tt)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float v = warp_sum(acc[tt][j]);
+      const int t = t0 + tt, e = e0 + j;
+      if (lane == 0 && t < T && e < E) logits[(size_t)t * E + e] = v + (br ? br[e] : 0.f);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Top-k then softmax over the k selected; one warp per token.
 // ---------------------------------------------------------------------------
@@ -196,7 +277,7 @@ __global__ void __launch_bounds__(256) gather_bf16_kernel(const float* __restric
                                                           const int32_t* __restrict__ basep, int E,
                                                           uint16_t* __restrict__ xg,
                                                           uint16_t* __restrict__ xg_lo,
-                                                          float* __restrict__ y_zero) {
+                                                          float* __restrict__ y_zero, int zero_pads) {
   pdl_launch_dependents();
   pdl_wait();
   const int lane = threadIdx.x & 31;
@@ -223,12 +304,12 @@ __global__ void __launch_bounds__(256) gather_bf16_kernel(const float* __restric
           dst_lo[i] = r;
         }
       }
-    } else {
+    } else if (zero_pads) {
       for (int i = lane; i < n4; i += 32) {
         dst[i] = make_uint2(0u, 0u);
         if (dst_lo) dst_lo[i] = make_uint2(0u, 0u);
       }
-    }
+    }  // otherwise pad rows are left as they are (the layer never stores their MMA columns)
   }
   if (y_zero) {
     float4* y4 = reinterpret_cast<float4*>(y_zero);
@@ -250,11 +331,18 @@ cudaError_t launch_router_logits(const float* x, int T, int D, const float* wr, 
     return launch_kernel(router_logits_kernel<1, 1>, grid, dim3(128), 0, L, x, T, D, wr, br, E,
                          logits);
   }
-  // 2 tokens x 2 experts per block, a warp per dot: coalesced loads and enough
-  // blocks to keep every SM's loads in flight at prefill sizes too
-  dim3 grid((T + 1) / 2, (E + 1) / 2);
-  return launch_kernel(router_logits_kernel<2, 2>, grid, dim3(128), 0, L, x, T, D, wr, br, E,
-                       logits);
+  if (T <= 8) {
+    // 2 tokens x 2 experts per block, a warp per dot: coalesced loads and enough
+    // blocks to keep every SM's loads in flight
+    dim3 grid((T + 1) / 2, (E + 1) / 2);
+    return launch_kernel(router_logits_kernel<2, 2>, grid, dim3(128), 0, L, x, T, D, wr, br, E,
+                         logits);
+  }
+  const size_t smem = (size_t)kRouterTileT * D * sizeof(float);
+  cudaError_t err = ensure_smem_limit(router_logits_tile_kernel, smem);
+  if (err != cudaSuccess) return err;
+  dim3 grid((T + kRouterTileT - 1) / kRouterTileT, (E + 31) / 32);
+  return launch_kernel(router_logits_tile_kernel, grid, dim3(256), smem, L, x, T, D, wr, br, E, logits);
 }
 
 cudaError_t launch_topk_softmax(const float* logits, int T, int E, int k, int32_t* ids, float* w,
@@ -273,13 +361,13 @@ cudaError_t launch_bucket(const int32_t* ids, int T, int k, int E, int tile, int
 
 cudaError_t launch_gather_bf16(const float* x, int T, int D, int k, const int32_t* rows,
                                const int32_t* basep, int E, int max_rows, uint16_t* xg,
-                               uint16_t* xg_lo, float* y_zero, Launch L) {
+                               uint16_t* xg_lo, float* y_zero, bool zero_pads, Launch L) {
   int blocks = (max_rows + 7) / 8;
   const int cap = device_sm_count() * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   return launch_kernel(gather_bf16_kernel, dim3(blocks), dim3(256), 0, L, x, T, D, k, rows, basep,
-                       E, xg, xg_lo, y_zero);
+                       E, xg, xg_lo, y_zero, zero_pads ? 1 : 0);
 }
 
 }  // namespace moe
