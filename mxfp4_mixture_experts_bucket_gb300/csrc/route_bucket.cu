@@ -69,38 +69,32 @@ __global__ void __launch_bounds__(128) router_logits_kernel(const float* __restr
   }
 }
 
-// Prefill sizes (T > 8): a block takes 4 tokens x 32 experts; the 4 token rows
-// sit in shared memory and each warp computes 4 tokens x 4 experts = 16 dots,
-// its lanes splitting K (float4 steps), so every router row is read once per
-// 4 tokens instead of once per dot. Partial sums: one per lane, then a warp
-// xor-reduction per dot.
+// Prefill sizes (T > 8): a block takes 4 tokens x 16 experts with 16 warps:
+// warp w computes 4 tokens x 4 experts (experts 4 (w % 4) ..) over one quarter
+// of the dot length (w / 4), its lanes splitting that quarter in float4 steps;
+// x rows come through L1 (every row is read by the block's four expert
+// groups). The four partial sums of a dot are added in quarter order through
+// shared memory, so the result does not depend on scheduling.
 constexpr int kRouterTileT = 4;
-__global__ void __launch_bounds__(256) router_logits_tile_kernel(const float* __restrict__ x, int T, int D,
+constexpr int kRouterTileE = 16;
+__global__ void __launch_bounds__(512) router_logits_tile_kernel(const float* __restrict__ x, int T, int D,
                                                                  const float* __restrict__ wr,
                                                                  const float* __restrict__ br, int E,
                                                                  float* __restrict__ logits) {
   pdl_launch_dependents();
   pdl_wait();
-  extern __shared__ float4 xs4[];  // [kRouterTileT][D/4]
-  const int n4 = D >> 2;
-  const int t0 = blockIdx.x * kRouterTileT;
-  constexpr int U = 12;  // loads in flight per thread while the tile is staged
-  for (int i0 = threadIdx.x; i0 < kRouterTileT * n4; i0 += U * 256) {
-    float4 v[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int i = i0 + u * 256;
-      const int tt = i / n4, c = i - tt * n4;
-      v[u] = (i < kRouterTileT * n4 && t0 + tt < T) ? __ldg(reinterpret_cast<const float4*>(x + (size_t)(t0 + tt) * D) + c)
-                                                    : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (i0 + u * 256 < kRouterTileT * n4) xs4[i0 + u * 256] = v[u];
-  }
-  __syncthreads();
+  __shared__ float part[4][kRouterTileT * kRouterTileE];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e0 = blockIdx.y * 32 + 4 * warp;
+  const int eg = warp & 3, kq = warp >> 2;
+  const int n4 = D >> 2;
+  const int q4 = (n4 + 3) >> 2;
+  const int i0 = kq * q4, i1 = min(n4, i0 + q4);
+  const int t0 = blockIdx.x * kRouterTileT;
+  const int e0 = blockIdx.y * kRouterTileE + 4 * eg;
+  const float4* xrow[kRouterTileT];
+#pragma unroll
+  for (int tt = 0; tt < kRouterTileT; ++tt)
+    xrow[tt] = reinterpret_cast<const float4*>(x + (size_t)min(t0 + tt, T - 1) * D);
   const float4* wrow[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) wrow[j] = reinterpret_cast<const float4*>(wr + (size_t)min(e0 + j, E - 1) * D);
@@ -109,45 +103,57 @@ __global__ void __launch_bounds__(256) router_logits_tile_kernel(const float* __
   for (int tt = 0; tt < kRouterTileT; ++tt)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[tt][j] = 0.f;
-  auto step = [&](const float4 (&wv)[4], int i) {
+  auto step = [&](const float4 (&xv)[kRouterTileT], const float4 (&wv)[4]) {
 #pragma unroll
-    for (int tt = 0; tt < kRouterTileT; ++tt) {
-      const float4 xv = xs4[tt * n4 + i];
+    for (int tt = 0; tt < kRouterTileT; ++tt)
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         float a = acc[tt][j];
-        a = fmaf(xv.x, wv[j].x, a);
-        a = fmaf(xv.y, wv[j].y, a);
-        a = fmaf(xv.z, wv[j].z, a);
-        a = fmaf(xv.w, wv[j].w, a);
+        a = fmaf(xv[tt].x, wv[j].x, a);
+        a = fmaf(xv[tt].y, wv[j].y, a);
+        a = fmaf(xv[tt].z, wv[j].z, a);
+        a = fmaf(xv[tt].w, wv[j].w, a);
         acc[tt][j] = a;
       }
-    }
   };
-  int i = lane;
-  for (; i + 96 < n4; i += 128) {  // four steps' router loads in flight before any use
-    float4 wv[4][4];
+  int i = i0 + lane;
+  for (; i + 32 < i1; i += 64) {  // two steps' loads in flight before any use
+    float4 xa[kRouterTileT], wa[4], xb[kRouterTileT], wb[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
+    for (int tt = 0; tt < kRouterTileT; ++tt) {
+      xa[tt] = __ldg(xrow[tt] + i);
+      xb[tt] = __ldg(xrow[tt] + i + 32);
+    }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) wv[u][j] = __ldg(wrow[j] + i + 32 * u);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) step(wv[u], i + 32 * u);
+    for (int j = 0; j < 4; ++j) {
+      wa[j] = __ldg(wrow[j] + i);
+      wb[j] = __ldg(wrow[j] + i + 32);
+    }
+    step(xa, wa);
+    step(xb, wb);
   }
-  for (; i < n4; i += 32) {
-    float4 wv[4];
+  if (i < i1) {
+    float4 xa[kRouterTileT], wa[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) wv[j] = __ldg(wrow[j] + i);
-    step(wv, i);
+    for (int tt = 0; tt < kRouterTileT; ++tt) xa[tt] = __ldg(xrow[tt] + i);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) wa[j] = __ldg(wrow[j] + i);
+    step(xa, wa);
   }
 #pragma unroll
   for (int tt = 0; tt < kRouterTileT; ++tt)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const float v = warp_sum(acc[tt][j]);
-      const int t = t0 + tt, e = e0 + j;
-      if (lane == 0 && t < T && e < E) logits[(size_t)t * E + e] = v + (br ? br[e] : 0.f);
+      if (lane == 0) part[kq][tt * kRouterTileE + 4 * eg + j] = v;
     }
+  __syncthreads();
+  if (threadIdx.x < kRouterTileT * kRouterTileE) {
+    const int tt = threadIdx.x / kRouterTileE, el = threadIdx.x % kRouterTileE;
+    const int t = t0 + tt, e = blockIdx.y * kRouterTileE + el;
+    const float v = ((part[0][threadIdx.x] + part[1][threadIdx.x]) + part[2][threadIdx.x]) + part[3][threadIdx.x];
+    if (t < T && e < E) logits[(size_t)t * E + e] = v + (br ? br[e] : 0.f);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -338,11 +344,8 @@ cudaError_t launch_router_logits(const float* x, int T, int D, const float* wr, 
     return launch_kernel(router_logits_kernel<2, 2>, grid, dim3(128), 0, L, x, T, D, wr, br, E,
                          logits);
   }
-  const size_t smem = (size_t)kRouterTileT * D * sizeof(float);
-  cudaError_t err = ensure_smem_limit(router_logits_tile_kernel, smem);
-  if (err != cudaSuccess) return err;
-  dim3 grid((T + kRouterTileT - 1) / kRouterTileT, (E + 31) / 32);
-  return launch_kernel(router_logits_tile_kernel, grid, dim3(256), smem, L, x, T, D, wr, br, E, logits);
+  dim3 grid((T + kRouterTileT - 1) / kRouterTileT, (E + kRouterTileE - 1) / kRouterTileE);
+  return launch_kernel(router_logits_tile_kernel, grid, dim3(512), 0, L, x, T, D, wr, br, E, logits);
 }
 
 cudaError_t launch_topk_softmax(const float* logits, int T, int E, int k, int32_t* ids, float* w,
