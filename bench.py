@@ -365,7 +365,8 @@ def run_ours(args, dist: Dist):
         "layer_roofline_frac": round((step_bytes / (hbm_peak * 1e9)) / (secs_max / K), 4),
         "roofline": roofline,
         "e2e": {"value": round(e2e_rate, 1), "unit": "tokens/s", "h2d_bytes_per_step": D * 4, "d2h_bytes_per_step": D * 4,
-                "path": "MoeLayer.forward_host -> moe_ffn_layer_hostio per step: pinned host x in, layer, pinned host y out, no graph"},
+                "path": "MoeLayer.forward_host -> moe_ffn_layer_hostio per step: x read from and y written to pinned host "
+                        "memory by the kernels themselves (no copy-engine transfers), no graph"},
         "clocks": clocks,
         "gpu_launches": int(round(launches_per_step * K)),
         "kernels_per_step": launches_per_step,

@@ -221,7 +221,7 @@ int moe_route_topk(const float* x, int T, int D, const float* w_router, const fl
   int rc = current_device(&d);
   if (rc != MOE_OK) return rc;
   Launch L{stream, false};
-  rc = cuda_status(launch_router_logits(x, T, D, w_router, b_router, E, logits, L));
+  rc = cuda_status(launch_router_logits(x, T, D, w_router, b_router, E, logits, nullptr, L));
   if (rc != MOE_OK) return rc;
   L.pdl = true;
   return cuda_status(launch_topk_softmax(logits, T, E, k, ids, weights, L));
@@ -349,7 +349,7 @@ int moe_expert_gateup_swiglu(const uint8_t* g_qs, const uint8_t* g_sc, const flo
   if (rc != MOE_OK) return rc;
   Launch L{stream, false};
   return cuda_status(launch_gemv_gateup(g_qs, g_sc, bg, u_qs, u_sc, bu, E, F, D, T, k, x, nullptr,
-                                        ids, nullptr, nullptr, alpha, limit, h, d->status, L));
+                                        ids, nullptr, nullptr, alpha, limit, h, d->status, false, L));
 }
 
 int moe_expert_down_combine(const uint8_t* d_qs, const uint8_t* d_sc, const float* bd, int E, int D,
@@ -369,7 +369,12 @@ int moe_expert_down_combine(const uint8_t* d_qs, const uint8_t* d_sc, const floa
                                       d->status, L));
 }
 
-int moe_ffn_layer(const float* x, int T, int D, int F, int E, int k, const float* w_router,
+}  // extern "C"
+
+namespace {
+// moe_ffn_layer with an optional device copy of x made by the router on the
+// GEMV rail (x may then live in mapped host memory: it is read once).
+int ffn_layer_impl(const float* x, float* x_copy, int T, int D, int F, int E, int k, const float* w_router,
                   const float* b_router, const uint8_t* g_qs, const uint8_t* g_sc, const float* bg,
                   const uint8_t* u_qs, const uint8_t* u_sc, const float* bu, const uint8_t* d_qs,
                   const uint8_t* d_sc, const float* bd, int rail, void* workspace,
@@ -402,14 +407,16 @@ int moe_ffn_layer(const float* x, int T, int D, int F, int E, int k, const float
   const float alpha = 1.702f, limit = 7.0f;
 
   Launch L{stream, false};
-  rc = cuda_status(launch_router_logits(x, T, D, w_router, b_router, E, ws.logits, L));
+  if (rail != MOE_RAIL_GEMV) x_copy = nullptr;  // prefill sizes read x from device memory
+  MOE_REQUIRE(x_copy == nullptr || aligned(x_copy, 16));
+  rc = cuda_status(launch_router_logits(x, T, D, w_router, b_router, E, ws.logits, x_copy, L));
   if (rc != MOE_OK) return rc;
   L.pdl = true;
   if (rail == MOE_RAIL_GEMV) {
     // decode: the two expert kernels take the top-k of the logits themselves
-    rc = cuda_status(launch_gemv_gateup(g_qs, g_sc, bg, u_qs, u_sc, bu, E, F, D, T, k, x, ws.logits,
-                                        nullptr, ids_out, weights_out, alpha, limit, ws.h, d->status,
-                                        L));
+    rc = cuda_status(launch_gemv_gateup(g_qs, g_sc, bg, u_qs, u_sc, bu, E, F, D, T, k, x_copy ? x_copy : x,
+                                        ws.logits, nullptr, ids_out, weights_out, alpha, limit, ws.h, d->status,
+                                        x_copy != nullptr, L));
     if (rc != MOE_OK) return rc;
     return cuda_status(launch_gemv_down(d_qs, d_sc, bd, E, D, F, T, k, ws.h, ws.logits, nullptr,
                                         nullptr, y, d->status, L));
@@ -514,6 +521,37 @@ int moe_ffn_layer(const float* x, int T, int D, int F, int E, int k, const float
   return cuda_status(launch_grouped_mm(gd, L));
 }
 
+}  // namespace
+
+extern "C" {
+
+int moe_ffn_layer(const float* x, int T, int D, int F, int E, int k, const float* w_router,
+                  const float* b_router, const uint8_t* g_qs, const uint8_t* g_sc, const float* bg,
+                  const uint8_t* u_qs, const uint8_t* u_sc, const float* bu, const uint8_t* d_qs,
+                  const uint8_t* d_sc, const float* bd, int rail, void* workspace,
+                  size_t workspace_bytes, float* y, int32_t* ids_out, float* weights_out,
+                  cudaStream_t stream) {
+  return ffn_layer_impl(x, nullptr, T, D, F, E, k, w_router, b_router, g_qs, g_sc, bg, u_qs, u_sc, bu, d_qs, d_sc,
+                        bd, rail, workspace, workspace_bytes, y, ids_out, weights_out, stream);
+}
+
+}  // extern "C"
+
+namespace {
+// Device address of pinned (page-locked, mapped) host memory, or nullptr for
+// pageable memory.
+const void* mapped_host(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+}  // namespace
+
+extern "C" {
+
 int moe_ffn_layer_hostio(const moe_ffn_args_t* args, const float* x_host, float* y_host,
                          cudaStream_t stream) {
   MOE_REQUIRE(args != nullptr);
@@ -521,6 +559,18 @@ int moe_ffn_layer_hostio(const moe_ffn_args_t* args, const float* x_host, float*
   MOE_REQUIRE(a.T >= 0 && a.D >= 64);
   if (a.T == 0) return MOE_OK;
   MOE_REQUIRE(x_host && y_host && a.x_dev && a.y_dev);
+  if (resolve_rail(a.T, a.rail) == MOE_RAIL_GEMV) {
+    // Decode rail with pinned buffers: no copies. The router reads x once from
+    // host memory (over the CPU-GPU link) and leaves a copy in x_dev for the
+    // gate/up kernel; the down kernel stores each element of y once, straight
+    // into host memory.
+    const float* dx = static_cast<const float*>(mapped_host(x_host));
+    float* dy = static_cast<float*>(const_cast<void*>(mapped_host(y_host)));
+    if (dx && dy)
+      return ffn_layer_impl(dx, a.x_dev, a.T, a.D, a.F, a.E, a.k, a.w_router, a.b_router, a.g_qs, a.g_sc, a.bg,
+                            a.u_qs, a.u_sc, a.bu, a.d_qs, a.d_sc, a.bd, a.rail, a.workspace, a.workspace_bytes,
+                            dy, nullptr, nullptr, stream);
+  }
   const size_t bytes = (size_t)a.T * a.D * sizeof(float);
   cudaError_t err = cudaMemcpyAsync(a.x_dev, x_host, bytes, cudaMemcpyHostToDevice, stream);
   if (err != cudaSuccess) return cuda_status(err);

@@ -342,6 +342,7 @@ struct DecodeArgs {
   int tw;      // warps per team
   int spt;     // stages per team
   int staged;  // vectors split into shared memory once per CTA
+  int vec_wait;  // gate/up: x is written by the previous kernel (read it after the wait)
   uint32_t stage_bytes;
   int* status;
 };
@@ -462,8 +463,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_expert_kernel(const Dec
         if (A.w_out) A.w_out[a] = Rt.w[a];
       }
   } else {
-    // x is the layer's input; h (down) comes from the previous kernel
-    if (KIND == 1) pdl_wait();
+    // x is the layer's input (unless the router copies it there); h (down) comes
+    // from the previous kernel
+    if (KIND == 1 || A.vec_wait) pdl_wait();
     if (A.staged) stage_split_vectors(A.vec, nvec, C, vwords, vfac, threadIdx.x - 32, kDecThreads - 32);
   }
   __syncthreads();
@@ -689,10 +691,11 @@ cudaError_t launch_gemv_gateup(const uint8_t* g_qs, const uint8_t* g_sc, const f
                                const uint8_t* u_qs, const uint8_t* u_sc, const float* bu, int E,
                                int F, int D, int T, int k, const float* x, const float* logits,
                                const int32_t* ids_in, int32_t* ids_out, float* w_out, float alpha,
-                               float limit, float* h, int* status, Launch L) {
+                               float limit, float* h, int* status, bool x_from_prev, Launch L) {
   if (T <= 0) return cudaSuccess;
   if (T * k > kMaxAssign) return cudaErrorInvalidValue;
   DecodeArgs A = {};
+  A.vec_wait = x_from_prev ? 1 : 0;
   A.qs[0] = g_qs;
   A.qs[1] = u_qs;
   A.sc[0] = g_sc;

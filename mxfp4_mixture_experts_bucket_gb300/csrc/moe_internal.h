@@ -60,8 +60,9 @@ int resident_blocks_per_sm(K kern, int threads, size_t smem) {
 }
 
 // ---- route_bucket.cu ----
+// x_copy (T <= 8 only, may be null): receives a copy of x [T][D] written by the kernel.
 cudaError_t launch_router_logits(const float* x, int T, int D, const float* wr, const float* br,
-                                 int E, float* logits, Launch L);
+                                 int E, float* logits, float* x_copy, Launch L);
 cudaError_t launch_topk_softmax(const float* logits, int T, int E, int k, int32_t* ids, float* w,
                                 Launch L);
 cudaError_t launch_bucket(const int32_t* ids, int T, int k, int E, int tile, int max_rows,
@@ -83,11 +84,12 @@ cudaError_t launch_swiglu(const float* g, const float* u, void* h, int64_t n, in
 // assignment. Routing comes from `logits` (top-k + softmax inside the kernel)
 // when not NULL, else from `ids_in`; CTA 0 writes it to ids_out / w_out if not
 // NULL. h: [T*k][F] floats, row per assignment.
+// x_from_prev: x is written by the previous kernel in the stream (wait before reading it).
 cudaError_t launch_gemv_gateup(const uint8_t* g_qs, const uint8_t* g_sc, const float* bg,
                                const uint8_t* u_qs, const uint8_t* u_sc, const float* bu, int E,
                                int F, int D, int T, int k, const float* x, const float* logits,
                                const int32_t* ids_in, int32_t* ids_out, float* w_out, float alpha,
-                               float limit, float* h, int* status, Launch L);
+                               float limit, float* h, int* status, bool x_from_prev, Launch L);
 // Decode rail, stage 1: down projection + bias + router-weighted combine in slot
 // order. Routing from `logits` when not NULL, else from ids_in / w_in.
 cudaError_t launch_gemv_down(const uint8_t* d_qs, const uint8_t* d_sc, const float* bd, int E,

@@ -18,7 +18,8 @@ template <int TT, int EG>
 __global__ void __launch_bounds__(128) router_logits_kernel(const float* __restrict__ x, int T, int D,
                                                             const float* __restrict__ wr,
                                                             const float* __restrict__ br, int E,
-                                                            float* __restrict__ logits) {
+                                                            float* __restrict__ logits,
+                                                            float* __restrict__ x_copy) {
   pdl_launch_dependents();
   pdl_wait();
   constexpr int NDOT = TT * EG;
@@ -35,20 +36,49 @@ __global__ void __launch_bounds__(128) router_logits_kernel(const float* __restr
     const float4* xr = reinterpret_cast<const float4*>(x + (size_t)t * D);
     const float4* wrr = reinterpret_cast<const float4*>(wr + (size_t)e * D);
     const int n4 = D >> 2;
+    // the copy of x (if asked for) comes from the expert-0 dots of the first block column
+    float4* xc = (x_copy && blockIdx.y == 0 && d % EG == 0) ? reinterpret_cast<float4*>(x_copy + (size_t)t * D)
+                                                            : nullptr;
     float a0 = 0.f, a1 = 0.f;
-    int i = gi;
-    for (; i + G < n4; i += 2 * G) {
-      const float4 xa = xr[i], wa = wrr[i];
-      const float4 xb = xr[i + G], wb = wrr[i + G];
-      a0 = fmaf(xa.x, wa.x, a0); a0 = fmaf(xa.y, wa.y, a0);
-      a0 = fmaf(xa.z, wa.z, a0); a0 = fmaf(xa.w, wa.w, a0);
-      a1 = fmaf(xb.x, wb.x, a1); a1 = fmaf(xb.y, wb.y, a1);
-      a1 = fmaf(xb.z, wb.z, a1); a1 = fmaf(xb.w, wb.w, a1);
-    }
-    for (; i < n4; i += G) {
-      const float4 xa = xr[i], wa = wrr[i];
-      a0 = fmaf(xa.x, wa.x, a0); a0 = fmaf(xa.y, wa.y, a0);
-      a0 = fmaf(xa.z, wa.z, a0); a0 = fmaf(xa.w, wa.w, a0);
+    if constexpr (NDOT == 1) {
+      // one dot per block (T = 1): all of the thread's loads in flight at once,
+      // summed in the same order as the loop below (even steps a0, odd steps a1)
+      constexpr int MAXJ = 8;  // D <= 4096
+      float4 xv[MAXJ], wv[MAXJ];
+#pragma unroll
+      for (int j = 0; j < MAXJ; ++j)
+        if (gi + G * j < n4) {
+          xv[j] = xr[gi + G * j];
+          wv[j] = wrr[gi + G * j];
+        }
+#pragma unroll
+      for (int j = 0; j < MAXJ; ++j)
+        if (gi + G * j < n4) {
+          float& a = (j & 1) ? a1 : a0;
+          a = fmaf(xv[j].x, wv[j].x, a); a = fmaf(xv[j].y, wv[j].y, a);
+          a = fmaf(xv[j].z, wv[j].z, a); a = fmaf(xv[j].w, wv[j].w, a);
+          if (xc) xc[gi + G * j] = xv[j];
+        }
+    } else {
+      int i = gi;
+      for (; i + G < n4; i += 2 * G) {
+        const float4 xa = xr[i], wa = wrr[i];
+        const float4 xb = xr[i + G], wb = wrr[i + G];
+        a0 = fmaf(xa.x, wa.x, a0); a0 = fmaf(xa.y, wa.y, a0);
+        a0 = fmaf(xa.z, wa.z, a0); a0 = fmaf(xa.w, wa.w, a0);
+        a1 = fmaf(xb.x, wb.x, a1); a1 = fmaf(xb.y, wb.y, a1);
+        a1 = fmaf(xb.z, wb.z, a1); a1 = fmaf(xb.w, wb.w, a1);
+        if (xc) {
+          xc[i] = xa;
+          xc[i + G] = xb;
+        }
+      }
+      for (; i < n4; i += G) {
+        const float4 xa = xr[i], wa = wrr[i];
+        a0 = fmaf(xa.x, wa.x, a0); a0 = fmaf(xa.y, wa.y, a0);
+        a0 = fmaf(xa.z, wa.z, a0); a0 = fmaf(xa.w, wa.w, a0);
+        if (xc) xc[i] = xa;
+      }
     }
     acc = a0 + a1;
   }
@@ -330,20 +360,21 @@ __global__ void __launch_bounds__(256) gather_bf16_kernel(const float* __restric
 // launchers
 // ---------------------------------------------------------------------------
 cudaError_t launch_router_logits(const float* x, int T, int D, const float* wr, const float* br,
-                                 int E, float* logits, Launch L) {
+                                 int E, float* logits, float* x_copy, Launch L) {
   if (T <= 0) return cudaSuccess;
   if (T == 1) {
     dim3 grid(1, E);
     return launch_kernel(router_logits_kernel<1, 1>, grid, dim3(128), 0, L, x, T, D, wr, br, E,
-                         logits);
+                         logits, x_copy);
   }
   if (T <= 8) {
     // 2 tokens x 2 experts per block, a warp per dot: coalesced loads and enough
     // blocks to keep every SM's loads in flight
     dim3 grid((T + 1) / 2, (E + 1) / 2);
     return launch_kernel(router_logits_kernel<2, 2>, grid, dim3(128), 0, L, x, T, D, wr, br, E,
-                         logits);
+                         logits, x_copy);
   }
+  if (x_copy) return cudaErrorInvalidValue;  // prefill sizes take x from device memory
   dim3 grid((T + kRouterTileT - 1) / kRouterTileT, (E + kRouterTileE - 1) / kRouterTileE);
   return launch_kernel(router_logits_tile_kernel, grid, dim3(512), 0, L, x, T, D, wr, br, E, logits);
 }

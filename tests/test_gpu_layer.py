@@ -243,3 +243,22 @@ def test_forward_host_matches_forward(moe, cfg, T, rail):
         torch.cuda.synchronize()
         assert status(moe) == 0
         assert torch.equal(y_host, y_dev.cpu())
+
+
+def test_forward_host_pinned_and_pageable(moe):
+    """Host-I/O decode with pinned buffers (the kernels read x and write y in host
+    memory, no copies) and with pageable ones (copied through the staging
+    buffers): every result equals the device-buffer call bit for bit."""
+    spec, L, layer, _ = layer_for(moe, 1)
+    rail = moe.MOE_RAIL_GEMV
+    xs = [torch.from_numpy(make_tokens(spec, T=1, seed=400 + i)).pin_memory() for i in range(3)]
+    ys = [torch.full((1, spec.D), float("nan")).pin_memory() for _ in range(3)]
+    for x, y in zip(xs, ys):
+        layer.forward_host(x, y, rail=rail)
+    xp = torch.from_numpy(make_tokens(spec, T=1, seed=403))
+    yp = torch.full((1, spec.D), float("nan"))
+    layer.forward_host(xp, yp, rail=rail)
+    torch.cuda.synchronize()
+    assert status(moe) == 0
+    for x, y in zip(xs + [xp], ys + [yp]):
+        assert torch.equal(y, layer(dev(x.numpy()), rail=rail).cpu())
