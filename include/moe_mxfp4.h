@@ -302,10 +302,11 @@ typedef struct {
  * returns once the work is enqueued: y_host holds the result after the stream
  * has been synchronised. Errors as moe_ffn_layer; a failed copy returns
  * MOE_ECUDA.
- * On the GEMV rail with pinned x_host and y_host nothing is copied: the
- * kernels read x and write y in host memory directly through the pinned
- * mapping (x_dev and y_dev are then not touched). Other rails, and pageable
- * buffers, copy through x_dev and y_dev as described.
+ * On the GEMV rail with pinned x_host and y_host no copy is enqueued: the
+ * router kernel reads x from host memory through the pinned mapping and
+ * writes the device copy into x_dev (the expert kernels read that), and the
+ * down kernel writes y straight into y_host (y_dev is not touched). Other
+ * rails, and pageable buffers, copy through x_dev and y_dev as described.
  */
 int moe_ffn_layer_hostio(const moe_ffn_args_t* args, const float* x_host, float* y_host,
                          cudaStream_t stream);
