@@ -33,9 +33,12 @@
 //     chosen per MMA by the scale-factor id.
 //
 // CTA = 128 weight rows x one 128-row bucket tile (swap-AB: weight rows are
-// M, bucket rows N <= 128). Warps:
+// M, bucket rows N <= 128). The activation terms are stacked along N (term t
+// at B rows t*hn, hn = 32 * live chunks) so that one MMA can take several
+// terms while reading its A slice from shared memory once; the terms land in
+// separate accumulator column blocks that the epilogue adds. Warps:
 //   0       TMA producer: packed nibble tiles [E][R][C/2] (64 B x 128 rows per
-//           matrix per stage) into a raw ring; the tile's E8M0 rows (one bulk copy)
+//           matrix per stage) into a raw ring
 //   1       TMEM owner, single-thread MMA issuer
 //   2       activation producer: the E4M3 term tiles (live 32-row chunks) and
 //           their scale words
