@@ -210,6 +210,53 @@ def round_bf16(a: np.ndarray) -> np.ndarray:
     return out
 
 
+E4M3_MAX = 448.0
+
+
+def round_e4m3(a: np.ndarray) -> np.ndarray:
+    """Round to the nearest E4M3 value, ties to the even mantissa, saturating at +-448.
+
+    E4M3 (OCP 8-bit float): sign, 4 exponent bits with bias 7, 3 mantissa bits.
+    Normal values are (1 + m/8) * 2^(e-7) for e = 1..15 (e = 15, m = 7 is NaN, so
+    the largest finite value is 448); subnormals are (m/8) * 2^-6. So a magnitude
+    in [2^k, 2^(k+1)) (k >= -6) is rounded to a multiple of 2^(k-3), and anything
+    below 2^-6 to a multiple of 2^-9.
+    """
+    a = np.asarray(a, np.float64)
+    mag = np.abs(a)
+    k = np.floor(np.log2(np.where(mag > 0, mag, 1.0)))
+    quantum = 2.0 ** (np.maximum(k, -6.0) - 3.0)
+    r = np.minimum(np.round(mag / quantum) * quantum, E4M3_MAX)  # np.round: half to even
+    return np.copysign(r, a)
+
+
+def split_e4m3_terms(v: np.ndarray, nterms: int) -> np.ndarray:
+    """The operand the block-scaled prefill rail multiplies instead of v.
+
+    A reading of the prefill operand precision for the block-scaled rail (the
+    pages fix no 8-bit activation operand): along the last axis every block of
+    32 values is carried as a sum of nterms E4M3 blocks. Term t takes the
+    residual r of the terms before it (r = v for the first), gets the power of
+    two 2^s with s = floor(log2 max|r|) - 7 (bounded below by E8M0's -127), so
+    that the block's largest |r| / 2^s lies in [128, 256), and is
+    2^s * round_e4m3(r / 2^s). The values are taken as float32 first (the
+    layer's activations are float32). Returns the sum of the terms.
+    """
+    v = np.asarray(v, np.float32).astype(np.float64)
+    shape = v.shape
+    assert shape[-1] % 32 == 0
+    r = v.reshape(shape[:-1] + (shape[-1] // 32, 32))
+    total = np.zeros_like(r)
+    for _ in range(nterms):
+        amax = np.max(np.abs(r), axis=-1, keepdims=True)
+        s = np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 7.0
+        s = np.maximum(s, -127.0)
+        term = round_e4m3(r / 2.0 ** s) * 2.0 ** s
+        total = total + term
+        r = r - term
+    return total.reshape(shape)
+
+
 # ----------------------------------------------------------------------------
 # Projections and the expert FFN
 # ----------------------------------------------------------------------------
@@ -234,7 +281,9 @@ def expert_ffn(x_rows: np.ndarray, Wg: np.ndarray, bg, Wu: np.ndarray, bu, Wd: n
       "bf16"       x and h rounded to bfloat16 (bf16 tensor-core operands);
       "bf16_split" x carried as two bfloat16 parts, hi = bf16(x) and
                    lo = bf16(x - hi), so the gate/up operand is hi + lo;
-                   h rounded to bfloat16.
+                   h rounded to bfloat16;
+      "e4m3_terms" the block-scaled rail's operands: x as three E4M3 terms
+                   and h as two (split_e4m3_terms).
     """
     x = np.asarray(x_rows, np.float64)
     if operands == "bf16":
@@ -242,6 +291,8 @@ def expert_ffn(x_rows: np.ndarray, Wg: np.ndarray, bg, Wu: np.ndarray, bu, Wd: n
     elif operands == "bf16_split":
         hi = round_bf16(x)
         x = hi + round_bf16(np.asarray(x, np.float64) - hi)
+    elif operands == "e4m3_terms":
+        x = split_e4m3_terms(x, 3)
     elif operands != "f64":
         raise ValueError(operands)
     g = x @ Wg.T + (0.0 if bg is None else np.asarray(bg, np.float64))
@@ -249,6 +300,8 @@ def expert_ffn(x_rows: np.ndarray, Wg: np.ndarray, bg, Wu: np.ndarray, bu, Wd: n
     h = swiglu_oai(g, u)
     if operands in ("bf16", "bf16_split"):
         h = round_bf16(h)
+    elif operands == "e4m3_terms":
+        h = split_e4m3_terms(h, 2)
     return h @ Wd.T + (0.0 if bd is None else np.asarray(bd, np.float64))
 
 

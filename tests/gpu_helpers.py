@@ -10,6 +10,7 @@ DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
 DECODE_TOL = 1e-4   # fp32 decode rail, row-normwise
 PREFILL_TOL = 2e-2  # bf16-MMA prefill rail vs the float64 layer, row-normwise (1e-3 floor)
 PREFILL_BF16_TOL = 5e-3  # prefill rail vs the oracle evaluated with the same bf16 operands
+PREFILL_MX_TOL = 1e-3    # block-scaled rail vs the oracle evaluated with the same E4M3-term operands
 
 
 def dev(a, dtype=None):

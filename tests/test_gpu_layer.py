@@ -11,7 +11,7 @@ import torch
 
 from oracle import moe_oracle as O
 from synthetic import make_layer, make_tokens, spec_for
-from tests.gpu_helpers import (DECODE_TOL, PREFILL_BF16_TOL, PREFILL_TOL, dev, empty,
+from tests.gpu_helpers import (DECODE_TOL, PREFILL_BF16_TOL, PREFILL_MX_TOL, PREFILL_TOL, dev, empty,
                                status)
 
 pytestmark = pytest.mark.gpu
@@ -59,8 +59,13 @@ def check_layer(moe, cfg, T, rail, sample=None, seed=None):
         assert err.max() <= DECODE_TOL, err.max()
     elif rail == moe.MOE_RAIL_GROUPED_MX:
         err64 = O.rownorm_rel_err(y[toks], y64)
-        print(f"mx rail cfg {cfg} T {T}: rownorm err vs float64 {err64.max():.3e}")
+        ye4, _, _, _ = O.moe_layer(L, x, spec.k, token_idx=toks, ids=ids, weights=w_ref, cache=cache,
+                                   operands="e4m3_terms")
+        err_e4 = O.rownorm_rel_err(y[toks], ye4)
+        print(f"mx rail cfg {cfg} T {T}: rownorm err vs float64 {err64.max():.3e}, "
+              f"vs the same E4M3-term operands {err_e4.max():.3e}")
         assert err64.max() <= PREFILL_TOL, err64.max()
+        assert err_e4.max() <= PREFILL_MX_TOL, err_e4.max()
     else:
         ybf, _, _, _ = O.moe_layer(L, x, spec.k, token_idx=toks, ids=ids, weights=w_ref, cache=cache,
                                    operands="bf16_split")

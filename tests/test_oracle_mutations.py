@@ -13,6 +13,8 @@ from tests.test_oracle_pins import (
     check_dequant_vs_brute,
     check_e2m1,
     check_layer_vs_brute,
+    check_round_e4m3,
+    check_split_vs_brute,
     check_swiglu_points,
     check_topk_vs_brute,
 )
@@ -24,6 +26,8 @@ def test_pins_pass_on_the_real_oracle():
     assert check_topk_vs_brute(O.topk_softmax)
     assert check_bucket_vs_brute(O.bucket_csr)
     assert check_swiglu_points(O.swiglu_oai)
+    assert check_round_e4m3(O.round_e4m3)
+    assert check_split_vs_brute(O.split_e4m3_terms)
 
 
 def test_e2m1_subnormal_mistake_is_caught():
@@ -149,3 +153,47 @@ def test_unweighted_combine_is_caught():
         y2, _, _, _ = O.moe_layer(layer, x, k, ids=ids, weights=np.ones_like(w))
         return y2, ids, w, logits
     assert not check_layer_vs_brute(bad)
+
+
+def test_e4m3_truncation_is_caught():
+    def bad(a):  # rounds toward zero instead of to nearest
+        a = np.asarray(a, np.float64)
+        mag = np.abs(a)
+        k = np.floor(np.log2(np.where(mag > 0, mag, 1.0)))
+        q = 2.0 ** (np.maximum(k, -6.0) - 3.0)
+        return np.copysign(np.minimum(np.floor(mag / q) * q, O.E4M3_MAX), a)
+    assert not check_round_e4m3(bad)
+
+
+def test_e4m3_ties_away_from_zero_are_caught():
+    def bad(a):
+        a = np.asarray(a, np.float64)
+        mag = np.abs(a)
+        k = np.floor(np.log2(np.where(mag > 0, mag, 1.0)))
+        q = 2.0 ** (np.maximum(k, -6.0) - 3.0)
+        return np.copysign(np.minimum(np.floor(mag / q + 0.5) * q, O.E4M3_MAX), a)
+    assert not check_round_e4m3(bad)
+
+
+def test_e4m3_term_scale_off_by_one_is_caught():
+    # scale exponent floor(log2 max) - 8: the largest values saturate at 448
+    def bad(v, nterms):
+        v = np.asarray(v, np.float32).astype(np.float64)
+        shape = v.shape
+        r = v.reshape(shape[:-1] + (shape[-1] // 32, 32))
+        total = np.zeros_like(r)
+        for _ in range(nterms):
+            amax = np.max(np.abs(r), axis=-1, keepdims=True)
+            s = np.maximum(np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 8.0, -127.0)
+            term = O.round_e4m3(r / 2.0 ** s) * 2.0 ** s
+            total, r = total + term, r - term
+        return total.reshape(shape)
+    assert not check_split_vs_brute(bad)
+
+
+def test_e4m3_terms_without_residual_are_caught():
+    # every term re-encodes v instead of the residual of the terms before it
+    def bad(v, nterms):
+        one = O.split_e4m3_terms(v, 1)
+        return one * nterms
+    assert not check_split_vs_brute(bad)

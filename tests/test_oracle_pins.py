@@ -399,3 +399,119 @@ def test_bf16_operand_sensitivity_at_full_scale():
     ybf, _, _, _ = O.moe_layer(L, x, spec.k, cache=cache, operands="bf16")
     assert O.rownorm_rel_err(ysplit, y64).max() < 2e-3
     assert O.rownorm_rel_err(ybf, y64).max() > 2e-2
+
+
+# ----------------------------------------------------------------------------
+# E4M3 rounding and the E4M3-term operand of the block-scaled rail
+# ----------------------------------------------------------------------------
+
+def e4m3_code_values():
+    """Every E4M3 code's value from the bit fields (NaN for the two NaN codes)."""
+    vals = []
+    for c in range(256):
+        sign = -1.0 if c & 0x80 else 1.0
+        e, m = (c >> 3) & 15, c & 7
+        if e == 15 and m == 7:
+            vals.append(float("nan"))
+        elif e == 0:
+            vals.append(sign * (m / 8.0) * 2.0 ** -6)
+        else:
+            vals.append(sign * (1 + m / 8.0) * 2.0 ** (e - 7))
+    return vals
+
+
+def brute_round_e4m3(v):
+    """Nearest finite E4M3 value by exhaustive search; ties to the even code."""
+    best, best_d, best_c = None, None, None
+    for c, cv in enumerate(e4m3_code_values()):
+        if cv != cv:
+            continue
+        if math.copysign(1.0, cv) != math.copysign(1.0, v) and cv == 0.0:
+            continue  # keep the sign of zero
+        d = abs(cv - v)
+        if best is None or d < best_d or (d == best_d and (c & 1) == 0 and (best_c & 1) == 1):
+            best, best_d, best_c = cv, d, c
+    return best
+
+
+def e4m3_probe_values():
+    rng = np.random.default_rng(5)
+    v = list(rng.normal(0, 3, 300)) + list(rng.normal(0, 200, 100)) + list(rng.normal(0, 0.01, 100))
+    v += [0.0, -0.0, 448.0, 460.0, 464.0, 470.0, 1e9, -1e9, 1.0625, 1.1875, -2.5 * 2.0 ** -9,
+          2.0 ** -10, 3 * 2.0 ** -10, 15 * 2.0 ** -10, 2.0 ** -6 - 2.0 ** -10, 240.0, 232.0]
+    return [float(np.float32(x)) for x in v]
+
+
+def check_round_e4m3(round_e4m3):
+    vals = e4m3_probe_values()
+    got = round_e4m3(np.array(vals))
+    return all(g == brute_round_e4m3(v) and math.copysign(1, g) == math.copysign(1, brute_round_e4m3(v))
+               for g, v in zip(got, vals))
+
+
+def brute_split_e4m3_terms(block, nterms):
+    """One block of 32 values, pure Python: per term the scale exponent from
+    frexp (|max| / 2^s in [128, 256)), elements by exhaustive E4M3 search."""
+    r = [float(np.float32(x)) for x in block]
+    total = [0.0] * len(r)
+    for _ in range(nterms):
+        amax = max(abs(x) for x in r)
+        if amax == 0.0:
+            s = -127
+        else:
+            _, e = math.frexp(amax)  # amax = m * 2^e, m in [0.5, 1)
+            s = max(e - 8, -127)
+        for i in range(len(r)):
+            t = brute_round_e4m3(r[i] / 2.0 ** s) * 2.0 ** s
+            total[i] += t
+            r[i] -= t
+    return total
+
+
+def check_split_vs_brute(split_e4m3_terms, seed=6):
+    rng = np.random.default_rng(seed)
+    for scale in (1.0, 1e-30, 3e4, 2.0 ** -120):
+        blocks = (rng.normal(0, scale, (3, 32)) * rng.choice([1.0, 0.01, 1e-4], (3, 32))).astype(np.float32)
+        blocks[2, 5:] = 0.0
+        for n in (1, 2, 3):
+            got = split_e4m3_terms(blocks, n)
+            for b in range(3):
+                if list(got[b]) != brute_split_e4m3_terms(blocks[b], n):
+                    return False
+    return True
+
+
+def test_round_e4m3_matches_exhaustive_search():
+    assert check_round_e4m3(O.round_e4m3)
+
+
+def test_split_e4m3_terms_matches_brute_force():
+    assert check_split_vs_brute(O.split_e4m3_terms)
+
+
+def test_split_e4m3_terms_error_bound():
+    # each term leaves at most 2^-4 of the block's largest residual: n terms
+    # reproduce every block within 2^(-4n) of its largest magnitude
+    rng = np.random.default_rng(8)
+    x = (rng.normal(0, 1, (64, 64)) * np.exp(rng.normal(0, 3, (64, 1)))).astype(np.float32)
+    blocks = x.astype(np.float64).reshape(64, 2, 32)
+    amax = np.abs(blocks).max(axis=-1, keepdims=True)
+    for n in (1, 2, 3, 4):
+        err = np.abs(O.split_e4m3_terms(x, n).reshape(64, 2, 32) - blocks)
+        assert np.all(err <= amax * 2.0 ** (-4 * n)), n
+    assert np.array_equal(O.split_e4m3_terms(np.zeros((2, 32), np.float32), 3), np.zeros((2, 32)))
+
+
+def test_e4m3_term_operands_at_full_scale():
+    """The block-scaled rail's operands (x in three E4M3 terms, h in two) keep the
+    gpt-oss-shaped layer well inside the 2e-2 prefill tolerance. Oracle against
+    oracle, two tokens."""
+    spec = spec_for(2)
+    L = make_layer(spec, with_tokens=False)
+    from synthetic import make_tokens
+    x = make_tokens(spec, T=2, seed=3)
+    cache = O.ExpertCache(L)
+    y64, _, _, _ = O.moe_layer(L, x, spec.k, cache=cache)
+    ye4, _, _, _ = O.moe_layer(L, x, spec.k, cache=cache, operands="e4m3_terms")
+    err = O.rownorm_rel_err(ye4, y64)
+    assert np.all(err < 1e-2) and np.all(err > 0)
