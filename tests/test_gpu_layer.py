@@ -267,3 +267,57 @@ def test_forward_host_pinned_and_pageable(moe):
     assert status(moe) == 0
     for x, y in zip(xs + [xp], ys + [yp]):
         assert torch.equal(y, layer(dev(x.numpy()), rail=rail).cpu())
+
+
+def _e4m3_values():
+    vals = np.empty(256)
+    for c in range(256):
+        s = -1.0 if c & 0x80 else 1.0
+        e, m = (c >> 3) & 15, c & 7
+        vals[c] = np.nan if (e == 15 and m == 7) else (s * (m / 8.0) * 2.0 ** -6 if e == 0 else
+                                                       s * (1 + m / 8.0) * 2.0 ** (e - 7))
+    return vals
+
+
+@pytest.mark.parametrize("cfg,T", [(0, 40), (2, 48)])
+def test_mx_activation_terms_are_exact(moe, cfg, T):
+    """The block-scaled rail's x operand, read back from the layer workspace (three
+    E4M3 terms per bucket row in the MMA's per-block column order, E8M0 words per
+    stage of four blocks), equals the oracle's split_e4m3_terms(x, 3) bit for bit."""
+    spec, L, layer, _ = layer_for(moe, cfg)
+    E, k, D = spec.E, spec.k, spec.D
+    rail = moe.MOE_RAIL_GROUPED_MX
+    x = make_tokens(spec, T=T, seed=500 + cfg)
+    layer(dev(x), rail=rail)
+    torch.cuda.synchronize()
+    assert status(moe) == 0
+    ws = layer.workspace(T, rail).cpu().numpy()
+    ru = lambda v, a: (v + a - 1) // a * a
+    mr = ru(T * k + E * 127, 128)
+    nd = (D // 32 + 3) // 4
+    off, parts = 0, {}
+    for name, nbytes in (("logits", T * E * 4), ("ids", T * k * 4), ("w", T * k * 4), ("counts", E * 4),
+                         ("basep", (E + 1) * 4), ("rows", mr * 4), ("inv", T * k * 4),
+                         ("xq", 3 * mr * D), ("xs", 3 * nd * mr * 4)):
+        parts[name] = ws[off:off + nbytes]
+        off = ru(off + nbytes, 256)
+    basep = parts["basep"].view(np.int32)
+    rows = parts["rows"].view(np.int32)
+    xq = parts["xq"].reshape(3, mr, D)
+    xs = parts["xs"].view(np.uint32).reshape(3, nd, mr)
+    vals = _e4m3_values()
+    pos = np.array([2 * (c % 16) + c // 16 for c in range(32)])
+    ref = O.split_e4m3_terms(x, 3)
+    checked = 0
+    for p in range(int(basep[E])):
+        a = int(rows[p])
+        if a < 0:
+            continue
+        got = np.zeros(D)
+        for t in range(3):
+            for b in range(D // 32):
+                code = (int(xs[t, b // 4, p]) >> (8 * (b % 4))) & 0xFF
+                got[32 * b:32 * b + 32] += vals[xq[t, p, 32 * b + pos]] * 2.0 ** (code - 127)
+        assert np.array_equal(got, ref[a // k]), (p, a)
+        checked += 1
+    assert checked == T * k
