@@ -321,3 +321,35 @@ def test_mx_activation_terms_are_exact(moe, cfg, T):
         assert np.array_equal(got, ref[a // k]), (p, a)
         checked += 1
     assert checked == T * k
+
+
+@pytest.mark.parametrize("T,rail_name", [(8, "GEMV"), (50, "GROUPED_MM"), (50, "GROUPED_MX"),
+                                         (300, "GROUPED_MM"), (300, "GROUPED_MX")])
+def test_rectangular_layer(moe, T, rail_name):
+    """D != F and neither a multiple of 128 (D = 192, F = 320): ragged last K stages
+    on both projections and ragged weight-row tiles; T = 300 fills whole 128-row
+    bucket tiles."""
+    spec = spec_for(0, name="rectangular", E=6, k=2, D=192, F=320, seed=4242)
+    L = make_layer(spec, with_tokens=False)
+    layer = moe.MoeLayer(L, k=spec.k)
+    rail = getattr(moe, "MOE_RAIL_" + rail_name)
+    x = make_tokens(spec, T=T, seed=77)
+    y, ids, _ = run_layer(moe, layer, x, rail, spec.k)
+    logits = O.router_logits(x, L["w_router"], L["b_router"])
+    ids_ref, _ = O.topk_softmax(logits, spec.k)
+    clear = O.routing_margins(logits, spec.k) > 1e-4 * np.abs(logits).max()
+    assert np.array_equal(ids[clear], ids_ref[clear])
+    w_ref = np.take_along_axis(logits, ids.astype(np.int64), 1)
+    w_ref = np.exp(w_ref - w_ref[:, :1])
+    w_ref /= w_ref.sum(1, keepdims=True)
+    y64, _, _, _ = O.moe_layer(L, x, spec.k, ids=ids, weights=w_ref)
+    err64 = O.rownorm_rel_err(y, y64).max()
+    if rail == moe.MOE_RAIL_GEMV:
+        assert err64 <= DECODE_TOL, err64
+        return
+    assert err64 <= PREFILL_TOL, err64
+    operands, tol = (("bf16_split", PREFILL_BF16_TOL) if rail == moe.MOE_RAIL_GROUPED_MM
+                     else ("e4m3_terms", PREFILL_MX_TOL))
+    ymod, _, _, _ = O.moe_layer(L, x, spec.k, ids=ids, weights=w_ref, operands=operands)
+    err = O.rownorm_rel_err(y, ymod).max()
+    assert err <= tol, (operands, err)
