@@ -190,6 +190,12 @@ def load_peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+def decode_config(global_batch: int, parallelism: str, l2: str, timing: str) -> dict:
+    """The decode workload's config object, shared by both arms (same keys)."""
+    return {"workload": WORKLOAD_DECODE, "T": 1, "E": E, "k": K_TOP, "dim": D, "nfe": F,
+            "global_batch": global_batch, "parallelism": parallelism, "l2": l2, "timing": timing}
+
+
 def ncu_traffic(kernel_key: str):
     """Per-launch DRAM bytes from the committed ncu summary, if the kernel source is unchanged since."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
@@ -356,11 +362,10 @@ def run_ours(args, dist: Dist):
         "metric": METRIC, "value": round(rate, 1), "unit": "tokens/s", "n_gpus": dist.world, "steps": K,
         "warmup": W, "ms_per_step": round(secs_max / K * 1e3, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD_DECODE, "T": 1, "E": E, "k": K_TOP, "dim": D, "nfe": F,
-                   "global_batch": dist.world, "parallelism": f"replicas x{dist.world}",
-                   "l2": f"inputs larger than L2: {NL} distinct layer weight sets "
-                         f"({NL * E * EXPERT_BYTES / 1e9:.1f} GB) rotated every step",
-                   "timing": "one CUDA graph of the timed steps, CUDA events on its stream"},
+        "config": decode_config(dist.world, f"replicas x{dist.world}",
+                                f"inputs larger than L2: {NL} distinct layer weight sets "
+                                f"({NL * E * EXPERT_BYTES / 1e9:.1f} GB) rotated every step",
+                                "one CUDA graph of the timed steps, CUDA events on its stream"),
         "weight_gbs": round(weight_bytes_step * K / secs_max * dist.world / 1e9, 1),
         "layer_roofline_frac": round((step_bytes / (hbm_peak * 1e9)) / (secs_max / K), 4),
         "roofline": roofline,
@@ -449,7 +454,9 @@ def main():
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": round(dt / n * 1e3, 2), "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": WORKLOAD_DECODE, "T": 1, "E": E, "k": K_TOP, "dim": D, "nfe": F},
+                "config": decode_config(1, "float64 oracle on the host cores (rank 0)",
+                                        "not applicable: host memory, every token dequantises its 4 experts",
+                                        "wall clock over the sampled tokens"),
                 "cpu_baseline": {"value": round(rate, 4), "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                  "sample": f"{n} decode tokens through the float64 numpy oracle "
                                            "(each dequantises its 4 experts)"},

@@ -55,3 +55,26 @@ def test_single_process_is_its_own_world():
     d = bench.Dist()
     assert d.world == 1 and d.pg is None
     assert bench.whole_job_rate(10.0, 2.0, d) == (5.0, 2.0)
+
+
+def test_reference_arm_prints_the_contract_line():
+    """bench.py --impl reference times the float64 oracle on the host (no GPU
+    needed) and prints one JSON line with the same metric, unit, direction and
+    config keys as the GPU arm."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--steps", "2",
+                          "--warmup", "1", "--cpu-seconds", "1"], capture_output=True, text=True, timeout=600,
+                         cwd=root)
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["unit"] == "tokens/s" and line["higher_is_better"] is True
+    assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["value"] == line["value"]
+    assert set(line["config"]) == {"workload", "T", "E", "k", "dim", "nfe", "global_batch", "parallelism", "l2",
+                                   "timing"}
