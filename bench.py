@@ -217,6 +217,15 @@ def ncu_traffic(kernel_key: str):
 # ---------------------------------------------------------------------------
 # CPU oracle baseline (bounded sample)
 # ---------------------------------------------------------------------------
+def host_cores():
+    """Cores this process may run on (affinity / cgroup aware where the OS says), and the machine's count."""
+    try:
+        usable = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        usable = os.cpu_count() or 1
+    return usable, os.cpu_count()
+
+
 def cpu_oracle_rate(min_seconds: float = 10.0, max_tokens: int = 64):
     """Decode tokens through the float64 oracle until at least min_seconds of CPU work."""
     from oracle import moe_oracle as O
@@ -448,7 +457,7 @@ def main():
     if args.impl == "reference":
         if dist.rank == 0:
             rate, dt, n = cpu_oracle_rate(args.cpu_seconds)
-            cores = os.cpu_count()
+            cores, machine_cores = host_cores()
             print(json.dumps({
                 "impl": "reference", "metric": METRIC, "value": round(rate, 4), "unit": "tokens/s",
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -457,7 +466,8 @@ def main():
                 "config": decode_config(1, "float64 oracle on the host cores (rank 0)",
                                         "not applicable: host memory, every token dequantises its 4 experts",
                                         "wall clock over the sampled tokens"),
-                "cpu_baseline": {"value": round(rate, 4), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                "cpu_baseline": {"value": round(rate, 4), "unit": "tokens/s", "cores": cores,
+                                 "machine_cores": machine_cores, "kind": "oracle",
                                  "sample": f"{n} decode tokens through the float64 numpy oracle "
                                            "(each dequantises its 4 experts)"},
                 "e2e": {"value": round(rate, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -468,7 +478,9 @@ def main():
     if dist.rank == 0:
         if not args.no_cpu_baseline:
             rate, dt, n = cpu_oracle_rate(args.cpu_seconds)
-            res["cpu_baseline"] = {"value": round(rate, 4), "unit": "tokens/s", "cores": os.cpu_count(),
+            cores, machine_cores = host_cores()
+            res["cpu_baseline"] = {"value": round(rate, 4), "unit": "tokens/s", "cores": cores,
+                                   "machine_cores": machine_cores,
                                    "kind": "oracle",
                                    "sample": f"{n} decode tokens through the float64 numpy oracle "
                                              f"({dt:.1f} s; BLAS may use every core, elementwise work one)"}

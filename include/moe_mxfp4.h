@@ -148,6 +148,11 @@ int moe_mxfp4_gemv(const uint8_t* w_qs, const uint8_t* w_sc, int E, int R, int C
  * elementwise over n floats (gpt-oss uses alpha = 1.702, limit = 7). h is
  * float (h_dtype MOE_DTYPE_F32) or bfloat16 (MOE_DTYPE_BF16, rounded to
  * nearest even). The sigmoid is evaluated without overflow for any g.
+ * The pages name this activation as the MetalSwigluOaiPf kernel of the prefill
+ * chain ("dasLLAMA gpt-oss arc", Metal fusion lane commit, second bullet: the
+ * swiglu rows past each bucket's live end exit early) and as the activation of
+ * stage 0 of the fused MoE expert chain commit; its constants and the one-sided
+ * gate clamp are those of gpt-oss.
  */
 int moe_swiglu_oai(const float* g, const float* u, void* h, int64_t n, int h_dtype, float alpha,
                    float limit, cudaStream_t stream);
@@ -236,6 +241,13 @@ int moe_expert_down_combine(const uint8_t* d_qs, const uint8_t* d_sc, const floa
  *   route (moe_route_topk) -> bucket -> gate/up projections with bias and
  *   swiglu_oai -> down projection with bias -> router-weighted combine in
  *   slot order.
+ * This is the chain of "dasLLAMA gpt-oss arc": the Metal fusion lane commit
+ * for prefill (MetalMoeBucket with the prefix folded in, bias-seeded
+ * MetalMoeMulMmMx4 for gate/up and down, MetalSwigluOaiPf between them, ghost
+ * rows exiting early) and the fused MoE expert chain commit for decode (stage 0:
+ * gate+up rows, bias, activation; stage 1: down rows, bias and the weighted sum
+ * in slot order), with the routed-expert GEMV of "dasLLAMA: dig the last two
+ * board reds green", section "gpt-oss: mx4 kernels to the lab-winning shape".
  *   y[t] = sum_j weights[t][j] * (Wd[e] h_j + bd[e]),  e = ids[t][j],
  *   h_j  = swiglu_oai(Wg[e] x_t + bg[e], Wu[e] x_t + bu[e])  (alpha 1.702, limit 7)
  * Rails: MOE_RAIL_GEMV (T <= MOE_GEMV_MAX_T) streams the touched experts'
@@ -318,22 +330,23 @@ int moe_ffn_layer_hostio(const moe_ffn_args_t* args, const float* x_host, float*
  * moe_ffn_layer_decode_static -- moe_ffn_layer on the GEMV rail for callers
  * that cannot allocate device memory where they run the layer: a serving loop
  * that must stay allocation-free after start-up (cudaMalloc/cudaFree can
- * synchronise the device), a plugin that is handed only a stream and tensors,
- * or work recorded during a CUDA graph capture that forbids allocations. The
- * pages have no counterpart; it is a deployment convenience.
+ * synchronise the device), or a plugin that is handed only a stream and
+ * tensors. The pages have no counterpart; it is a deployment convenience.
  * Arguments, results and limits are those of moe_ffn_layer with
- * rail = MOE_RAIL_GEMV (1 <= T <= MOE_GEMV_MAX_T); there is no workspace
- * argument: the scratch is one file-scope device array of
- * MOE_DECODE_SCRATCH_BYTES bytes that every GPU which loads the library holds
- * until the process exits. Shapes whose moe_ffn_workspace_bytes(T, D, F, E,
- * k, MOE_RAIL_GEMV) exceeds that size are rejected with MOE_ESCRATCH before
- * anything is enqueued (T = 8, k = 4, D = F = 2880 needs about 370 KB).
+ * rail = MOE_RAIL_GEMV (1 <= T <= MOE_GEMV_MAX_T; T = 0 returns MOE_OK and
+ * enqueues nothing); there is no workspace argument: the scratch is one
+ * file-scope device array of MOE_DECODE_SCRATCH_BYTES bytes that every GPU
+ * which loads the library holds until the process exits. Shapes whose
+ * moe_ffn_workspace_bytes(T, D, F, E, k, MOE_RAIL_GEMV) exceeds that size are
+ * rejected with MOE_ESCRATCH before anything is enqueued (T = 8, k = 4,
+ * D = F = 2880 needs about 370 KB; T = 8, k = 8 at that width does not fit).
  * The first call on each device looks up the array's device address (with
- * that device current); make that first call before any stream capture. All
- * calls on a device share the array and it keeps the last call's contents;
- * nothing in it needs to start at zero (every byte a call reads it first
- * writes). Calls whose executions overlap on the GPU (different streams, or
- * concurrent host threads) race on the array: serialise them.
+ * that device current) and keeps it for the life of the process; make that
+ * first call before any stream capture, and do not use the library across
+ * cudaDeviceReset. All calls on a device share the array and it keeps the last
+ * call's contents; nothing in it needs to start at zero (every byte a call
+ * reads it first writes). Calls whose executions overlap on the GPU (different
+ * streams, or concurrent host threads) race on the array: serialise them.
  * Calls no cudaMalloc, cudaFree or allocating library routine.
  */
 int moe_ffn_layer_decode_static(const float* x, int T, int D, int F, int E, int k,

@@ -21,6 +21,7 @@ static std::atomic<uint64_t> g_launches{0};
 static thread_local int t_last_cuda_error = 0;
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+void set_last_cuda_error(int err) { t_last_cuda_error = err; }
 
 namespace {
 

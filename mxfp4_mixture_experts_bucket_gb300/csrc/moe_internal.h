@@ -20,6 +20,8 @@ struct Launch {
 
 // Counts every kernel the library enqueues (defined in abi.cu).
 void count_launch();
+// Records a cudaError_t for moe_last_cuda_error in the calling thread (abi.cu).
+void set_last_cuda_error(int err);
 int device_sm_count();
 
 template <typename... KArgs, typename... Args>

@@ -4,16 +4,16 @@
 // Who needs it: callers that cannot call cudaMalloc at the point where they run
 // the layer, for example a serving loop that must stay allocation-free after
 // start-up (cudaMalloc and cudaFree can synchronise the device and stall other
-// streams), a plugin inside a host framework that hands over only a stream and
-// its tensors, or code that records work while a CUDA graph is being captured
-// in a mode that forbids allocations. They pass inputs and outputs as usual;
-// everything else the decode rail needs comes from this file's array.
+// streams), or a plugin inside a host framework that hands over only a stream
+// and its tensors. They pass inputs and outputs as usual; everything else the
+// decode rail needs comes from this file's array.
 #include <cstdint>
 #include <mutex>
 
 #include <cuda_runtime.h>
 
 #include "../../include/moe_mxfp4.h"
+#include "moe_internal.h"
 
 namespace {
 
@@ -26,15 +26,24 @@ std::mutex g_scratch_mu;
 void* g_scratch_ptr[kMaxDevices] = {nullptr};
 
 // Device address of g_decode_scratch on the current device, looked up once per
-// device with that device current.
+// device with that device current (and kept for the life of the process: the
+// library is not meant to be used across cudaDeviceReset).
 int scratch_for_current_device(void** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ECUDA;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) {
+    moe::set_last_cuda_error((int)err);
+    return MOE_ECUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return MOE_EUNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
   if (g_scratch_ptr[dev] == nullptr) {
     void* p = nullptr;
-    const cudaError_t err = cudaGetSymbolAddress(&p, g_decode_scratch);
-    if (err != cudaSuccess || p == nullptr) return MOE_ECUDA;
+    err = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (err != cudaSuccess || p == nullptr) {
+      moe::set_last_cuda_error((int)(err != cudaSuccess ? err : cudaErrorInvalidSymbol));
+      return MOE_ECUDA;
+    }
     g_scratch_ptr[dev] = p;
   }
   *out = g_scratch_ptr[dev];

@@ -25,8 +25,8 @@ What it computes, and where each step is defined:
   ("dasLLAMA gpt-oss arc", fused MoE expert chain commit: stage 1 sums the
   experts' down rows "in slot order").
 
-Readings where the pages are silent are listed in the design doc; the ones that
-change arithmetic are noted beside the function that takes them.
+Where the pages are silent the oracle takes the plainest reading; the readings
+that change arithmetic are noted beside the function that takes them.
 
 Every function here is pinned by a test in tests/test_oracle_pins.py against
 something other than itself (the printed E2M1 table, math.ldexp, brute force

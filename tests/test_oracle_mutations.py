@@ -9,11 +9,14 @@ import numpy as np
 from oracle import moe_oracle as O
 from tests.test_oracle_pins import (
     check_bias_linearity,
+    check_bucket_max_rows,
     check_bucket_vs_brute,
     check_dequant_vs_brute,
     check_e2m1,
     check_layer_vs_brute,
     check_round_e4m3,
+    check_routing_margins,
+    check_rownorm_rel_err,
     check_split_vs_brute,
     check_swiglu_points,
     check_topk_vs_brute,
@@ -28,6 +31,9 @@ def test_pins_pass_on_the_real_oracle():
     assert check_swiglu_points(O.swiglu_oai)
     assert check_round_e4m3(O.round_e4m3)
     assert check_split_vs_brute(O.split_e4m3_terms)
+    assert check_routing_margins(O.routing_margins)
+    assert check_rownorm_rel_err(O.rownorm_rel_err)
+    assert check_bucket_max_rows(O.bucket_max_rows)
 
 
 def test_e2m1_subnormal_mistake_is_caught():
@@ -197,3 +203,86 @@ def test_e4m3_terms_without_residual_are_caught():
         one = O.split_e4m3_terms(v, 1)
         return one * nterms
     assert not check_split_vs_brute(bad)
+
+
+def test_margin_of_the_boundary_gap_only_is_caught():
+    # only the k-th / (k+1)-th gap, not the gaps between the selected slots
+    def bad(logits, k):
+        s = -np.sort(-np.asarray(logits, np.float64), axis=1)
+        if k >= s.shape[1]:
+            return np.full(s.shape[0], np.inf)
+        return s[:, k - 1] - s[:, k]
+    assert not check_routing_margins(bad)
+
+
+def test_margin_without_the_boundary_gap_is_caught():
+    # gaps among the k selected only (the k / k+1 boundary forgotten)
+    def bad(logits, k):
+        s = -np.sort(-np.asarray(logits, np.float64), axis=1)
+        gaps = s[:, :k - 1] - s[:, 1:k]
+        return gaps.min(axis=1) if gaps.shape[1] else np.full(s.shape[0], np.inf)
+    assert not check_routing_margins(bad)
+
+
+def test_margin_over_the_wrong_axis_is_caught():
+    def bad(logits, k):
+        s = -np.sort(-np.asarray(logits, np.float64), axis=0)  # sorts across tokens
+        kk = min(k + 1, s.shape[1])
+        gaps = s[:, :kk - 1] - s[:, 1:kk]
+        return np.abs(gaps).min(axis=1) if gaps.shape[1] else np.full(s.shape[0], np.inf)
+    assert not check_routing_margins(bad)
+
+
+def test_margin_of_the_smallest_logits_is_caught():
+    def bad(logits, k):
+        s = np.sort(np.asarray(logits, np.float64), axis=1)  # ascending: the bottom k+1
+        kk = min(k + 1, s.shape[1])
+        gaps = s[:, 1:kk] - s[:, :kk - 1]
+        return gaps.min(axis=1) if gaps.shape[1] else np.full(s.shape[0], np.inf)
+    assert not check_routing_margins(bad)
+
+
+def test_error_relative_to_the_result_is_caught():
+    def bad(y, y_ref, floor=1e-3):
+        num = np.abs(np.asarray(y) - np.asarray(y_ref)).max(axis=-1)
+        return num / np.maximum(np.abs(np.asarray(y)).max(axis=-1), floor)
+    assert not check_rownorm_rel_err(bad)
+
+
+def test_error_with_one_scale_for_all_rows_is_caught():
+    def bad(y, y_ref, floor=1e-3):
+        num = np.abs(np.asarray(y) - np.asarray(y_ref)).max(axis=-1)
+        return num / max(np.abs(np.asarray(y_ref)).max(), floor)
+    assert not check_rownorm_rel_err(bad)
+
+
+def test_mean_error_is_caught():
+    def bad(y, y_ref, floor=1e-3):
+        num = np.abs(np.asarray(y) - np.asarray(y_ref)).mean(axis=-1)
+        return num / np.maximum(np.abs(np.asarray(y_ref)).max(axis=-1), floor)
+    assert not check_rownorm_rel_err(bad)
+
+
+def test_error_with_a_fixed_floor_is_caught():
+    def bad(y, y_ref, floor=1e-3):
+        return O.rownorm_rel_err(y, y_ref, floor=1e-3)
+    assert not check_rownorm_rel_err(bad)
+
+
+def test_max_rows_without_the_round_up_is_caught():
+    def bad(T, k, E, tile):
+        return T * k + E * (tile - 1)
+    assert not check_bucket_max_rows(bad)
+
+
+def test_max_rows_with_a_full_tile_per_expert_is_caught():
+    def bad(T, k, E, tile):
+        n = T * k + E * tile
+        return -(-n // tile) * tile
+    assert not check_bucket_max_rows(bad)
+
+
+def test_max_rows_without_the_expert_padding_is_caught():
+    def bad(T, k, E, tile):
+        return -(-(T * k) // tile) * tile
+    assert not check_bucket_max_rows(bad)

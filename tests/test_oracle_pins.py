@@ -138,6 +138,74 @@ def check_bias_linearity(moe_layer):
     return bool(np.allclose(y1 - y0, expect, rtol=1e-9, atol=1e-12 * np.abs(y1).max()))
 
 
+
+def check_routing_margins(routing_margins):
+    """Hand-written logits whose smallest top-(k+1) gap is known."""
+    cases = [
+        # (logits [T, E], k, expected per-token margin)
+        ([[5.0, 3.0, 2.5, 1.0, 0.0]], 2, [0.5]),          # the k / k+1 gap (3 vs 2.5) is the smallest
+        ([[4.0, 3.9, 1.0, 0.0]], 2, [0.1]),               # a gap between selected slots is smaller
+        ([[1.0, 2.0, 2.0, 0.0]], 1, [0.0]),               # exact tie at the k / k+1 boundary
+        ([[1.0, 3.0, 2.0]], 3, [1.0]),                    # k = E: only the gaps between the k selected
+        ([[7.0]], 1, [math.inf]),                         # k = E = 1: nothing to separate
+        ([[0.0, -2.0, 9.0, -1.0, 4.0],                    # tokens are rows: 9, 4, 0 -> 4;
+          [0.0, 1.0, 2.0, 3.0, 10.0]], 2, [4.0, 1.0]),     # 10, 3, 2 -> 1
+        ([[-3.0, -1.0, -6.0, -1.25]], 2, [0.25]),         # negative logits, unsorted input
+        ([[2.0, 8.0, 5.0, 7.5, 6.0]], 3, [0.5]),          # 8, 7.5, 6, 5: gaps 0.5, 1.5, 1
+    ]
+    for logits, k, exp in cases:
+        got = np.asarray(routing_margins(np.array(logits, dtype=np.float64), k), np.float64)
+        if got.shape != (len(exp),) or not np.allclose(got, exp, rtol=0, atol=1e-12):
+            return False
+    return True
+
+
+def check_rownorm_rel_err(rownorm_rel_err):
+    """Per-row max abs error over the reference row's max magnitude, floored."""
+    cases = [
+        # (y, y_ref, floor, expected per-row error)
+        ([[1.5, -4.0, 2.0]], [[1.0, -4.0, 2.0]], 1e-3, [0.125]),   # 0.5 / 4
+        ([[4.0]], [[2.0]], 1e-3, [1.0]),                           # relative to the reference, not to y
+        ([[1.0, 1.0, 1.0, 1.4]], [[1.0, 1.0, 1.0, 1.0]], 1e-3, [0.4]),  # the max error, not the mean
+        ([[101.0, 0.0], [1.0, 0.5]], [[100.0, 0.0], [1.0, 0.0]], 1e-3, [0.01, 0.5]),  # rows scaled separately
+        ([[1e-4, 0.0]], [[0.0, 0.0]], 1e-3, [0.1]),                # the floor replaces a zero row's scale
+        ([[2e-4, 0.0]], [[5e-4, 0.0]], 1e-3, [0.3]),               # ... and a row smaller than the floor
+        ([[2e-4, 0.0]], [[5e-4, 0.0]], 1e-6, [0.6]),               # the floor argument is used
+    ]
+    for y, y_ref, floor, exp in cases:
+        got = np.asarray(rownorm_rel_err(np.array(y), np.array(y_ref), floor=floor), np.float64)
+        if got.shape != (len(exp),) or not np.allclose(got, exp, rtol=1e-12, atol=0):
+            return False
+    return True
+
+
+def check_bucket_max_rows(bucket_max_rows):
+    """Hand values of T*k + E*(tile-1) rounded up to a whole tile, and the bound over every routing."""
+    cases = [
+        ((1, 4, 32, 1), 4),          # tile 1: no padding at all
+        ((512, 4, 32, 128), 6144),   # 2048 + 32*127 = 6112 -> 48 tiles
+        ((8, 2, 4, 16), 80),         # 16 + 60 = 76 -> 5 tiles
+        ((0, 4, 32, 128), 4096),     # no tokens: every expert could still own a padded tile
+        ((3, 1, 2, 4), 12),          # 3 + 6 = 9 -> 3 tiles
+        ((4096, 4, 32, 128), 20480), # 16384 + 4064 = 20448 -> 160 tiles
+    ]
+    for args, exp in cases:
+        if int(bucket_max_rows(*args)) != exp:
+            return False
+    # every assignment of ids in tiny cases fits under the bound; with k = 1 the
+    # worst one (one token per expert) reaches it exactly
+    import itertools
+    for T, k, E, tile, tight in [(3, 1, 3, 2, True), (3, 2, 3, 2, False), (2, 2, 2, 3, False)]:
+        bound = int(bucket_max_rows(T, k, E, tile))
+        worst = 0
+        for choice in itertools.product(range(E), repeat=T * k):
+            counts = np.bincount(np.array(choice), minlength=E)
+            worst = max(worst, int(sum(-(-c // tile) * tile for c in counts)))
+        if worst > bound or (tight and worst != bound):
+            return False
+    return True
+
+
 # ---------------------------------------------------------------------------
 # tests
 # ---------------------------------------------------------------------------
@@ -515,3 +583,15 @@ def test_e4m3_term_operands_at_full_scale():
     ye4, _, _, _ = O.moe_layer(L, x, spec.k, cache=cache, operands="e4m3_terms")
     err = O.rownorm_rel_err(ye4, y64)
     assert np.all(err < 1e-2) and np.all(err > 0)
+
+
+def test_routing_margins_closed_form():
+    assert check_routing_margins(O.routing_margins)
+
+
+def test_rownorm_rel_err_closed_form():
+    assert check_rownorm_rel_err(O.rownorm_rel_err)
+
+
+def test_bucket_max_rows_hand_values_and_bound():
+    assert check_bucket_max_rows(O.bucket_max_rows)

@@ -1,8 +1,8 @@
 """The allocation-free decode entry point (moe_ffn_layer_decode_static).
 
 It exists for callers that cannot allocate device memory where they run the
-layer (allocation-free serving loops, plugins handed only a stream and tensors,
-capture-time code); its scratch is a static device array inside the library.
+layer (allocation-free serving loops, plugins handed only a stream and
+tensors); its scratch is a static device array inside the library.
 This file is collected last so that a failure here leaves every other test
 already run.
 """
@@ -55,3 +55,14 @@ def test_static_scratch_rejects_shapes_beyond_its_size(moe):
     # beyond the GEMV rail's token limit
     rc = moe.moe_ffn_layer_decode_static(FAKE, 9, 64, 64, 4, 2, *([FAKE] * 11), FAKE, None, None, stream=0)
     assert rc == moe.MOE_EINVAL
+    # the gpt-oss width with eight tokens of eight experts: h alone is 8*8*2880*4 B > 512 KiB
+    assert moe.moe_ffn_workspace_bytes(8, 2880, 2880, 32, 8, moe.MOE_RAIL_GEMV) > moe.MOE_DECODE_SCRATCH_BYTES
+    rc = moe.moe_ffn_layer_decode_static(FAKE, 8, 2880, 2880, 32, 8, *([FAKE] * 11), FAKE, None, None, stream=0)
+    assert rc == moe.MOE_ESCRATCH
+
+
+def test_static_scratch_zero_tokens_is_a_no_op(moe):
+    n0 = moe.moe_kernel_launches()
+    rc = moe.moe_ffn_layer_decode_static(FAKE, 0, 2880, 2880, 32, 4, *([FAKE] * 11), FAKE, None, None, stream=0)
+    assert rc == moe.MOE_OK
+    assert moe.moe_kernel_launches() == n0
