@@ -266,8 +266,8 @@ def run_ours(args, dist: Dist):
     K, W, NL = args.steps, args.warmup, args.layers
     spec = spec_for(1)
 
-    # ---- decode: NL distinct layers resident (NL x 423 MB), one token per step ----
-    layers = [moe.MoeLayer(make_layer_torch(spec, li + 17 * dist.rank, dev), k=K_TOP, device=dev)
+    # ---- decode: NL distinct layers resident, prepacked for the block-scaled decode rail ----
+    layers = [moe.MoeLayer(make_layer_torch(spec, li + 17 * dist.rank, dev), k=K_TOP, device=dev, packed=True)
               for li in range(NL)]
     g = torch.Generator(device=dev)
     g.manual_seed(4242 + dist.rank)
@@ -275,17 +275,18 @@ def run_ours(args, dist: Dist):
     ys = torch.empty((K + W, D), device=dev)
     ids = torch.empty((K + W, K_TOP), dtype=torch.int32, device=dev)
     stream = torch.cuda.Stream(device=dev)
+    decode_rail = moe.MOE_RAIL_AUTO  # prepacked layer, T = 1: MOE_RAIL_DECODE_MX
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         for i in range(W):  # eager warm-up steps
-            layers[i % NL](xs[i:i + 1], rail=moe.MOE_RAIL_GEMV, out=ys[i:i + 1], ids_out=ids[i:i + 1])
+            layers[i % NL](xs[i:i + 1], rail=decode_rail, out=ys[i:i + 1], ids_out=ids[i:i + 1])
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     n0 = moe.moe_kernel_launches()
     with torch.cuda.graph(graph, stream=stream):
         for i in range(K):
             j = W + i
-            layers[j % NL](xs[j:j + 1], rail=moe.MOE_RAIL_GEMV, out=ys[j:j + 1], ids_out=ids[j:j + 1])
+            layers[j % NL](xs[j:j + 1], rail=decode_rail, out=ys[j:j + 1], ids_out=ids[j:j + 1])
     launches_per_step = (moe.moe_kernel_launches() - n0) / K
     with torch.cuda.stream(stream):
         graph.replay()  # first replay uploads the graph; untimed
@@ -310,26 +311,24 @@ def run_ours(args, dist: Dist):
     step_bytes = touched * EXPERT_BYTES + K_TOP * (2 * F + D) * 4 + E * D * 4 + 2 * D * 4
     weight_bytes_step = touched * EXPERT_BYTES
 
-    # ---- dominant kernel alone: fused gate/up + swiglu GEMV, cold weights ----
+    # ---- dominant kernel alone: the gate/up stage (decode_mx_kernel<0>), cold weights ----
+    # Each launch runs on another layer's weights with its own workspace, prepared
+    # by that token's prologue stage before the graph; the launches follow one
+    # another as programmatic dependents, as inside the layer.
     Kk = min(K, 120)
-    routes = []
+    stage_ws = []
     for i in range(Kk):
         lay = layers[i % NL]
-        w = lay.w
-        logits = torch.empty((1, E), device=dev)
-        rid = torch.empty((1, K_TOP), dtype=torch.int32, device=dev)
-        rw = torch.empty((1, K_TOP), device=dev)
-        x1 = xs[i:i + 1]
-        moe.check(moe.moe_route_topk(x1, 1, D, w["w_router"], w["b_router"], E, K_TOP, logits, rid, rw, stream), "route")
-        routes.append((lay, x1, rid, torch.empty((K_TOP, F), device=dev)))
+        wsb = torch.empty(lay.workspace(1, moe.MOE_RAIL_DECODE_MX).numel(), dtype=torch.uint8, device=dev)
+        moe.check(moe.moe_ffn_layer_packed_stage(lay.packed_struct, xs[i:i + 1], 1, wsb, wsb.numel(),
+                                                 moe.MOE_STAGE_PROLOGUE, stream=stream), "prologue")
+        stage_ws.append((lay, wsb))
     torch.cuda.synchronize()
     kgraph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(kgraph, stream=stream):
-        for lay, x1, rid, h in routes:
-            w = lay.w
-            moe.check(moe.moe_expert_gateup_swiglu(w["g_qs"], w["g_sc"], w["bg"], w["u_qs"], w["u_sc"], w["bu"],
-                                                   E, F, D, 1, K_TOP, x1, rid, 1.702, 7.0, h, stream),
-                      "gateup")
+        for lay, wsb in stage_ws:
+            moe.check(moe.moe_ffn_layer_packed_stage(lay.packed_struct, None, 1, wsb, wsb.numel(),
+                                                     moe.MOE_STAGE_GATEUP, stream=stream), "gateup")
     with torch.cuda.stream(stream):
         kgraph.replay()
     torch.cuda.synchronize()
@@ -343,49 +342,90 @@ def run_ours(args, dist: Dist):
     gateup_bytes = K_TOP * 2 * MAT_BYTES + K_TOP * 2 * F * 4 + D * 4 + K_TOP * F * 4
     achieved = gateup_bytes / kern_s / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-                "frac": round(achieved / hbm_peak, 4), "traffic": ncu_traffic("decode_expert_kernel<0>"),
-                "kernel": "decode_expert_kernel<0>", "algorithmic_bytes_per_launch": gateup_bytes,
+                "frac": round(achieved / hbm_peak, 4), "traffic": ncu_traffic("decode_mx_kernel<0>"),
+                "kernel": "decode_mx_kernel<0>", "algorithmic_bytes_per_launch": gateup_bytes,
                 "launch_us": round(kern_s * 1e6, 3), "peak_source": f"{peak_src} hbm_gbs (burst copy)"}
+    del stage_ws
 
-    # ---- end to end through the public API, host buffers, no graph ----
-    # MoeLayer.forward_host: one C call per step copies the step's pinned host x
-    # in, runs the layer and copies y back to pinned host memory.
+    # ---- end to end through the public API, host buffers ----
+    # A serving step: MoeLayer.forward_host (one C call: the kernels read the
+    # pinned x and write y into pinned host memory), then the host waits for y,
+    # since the next token depends on it. Wall clock over K steps.
     x_host = torch.randn((K, D), generator=torch.Generator().manual_seed(99)).pin_memory()
     y_host = torch.empty((K, D)).pin_memory()
     with torch.cuda.stream(stream):
         for i in range(3):
             layers[i % NL].forward_host(x_host[i:i + 1], y_host[i:i + 1], stream=stream)
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     dist.barrier()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            layers[i % NL].forward_host(x_host[i:i + 1], y_host[i:i + 1], stream=stream)
+            stream.synchronize()
+    e2e_secs = time.perf_counter() - t0
+    dist.barrier()
+    e2e_rate, _ = whole_job_rate(K, e2e_secs, dist)
+    # the same calls back to back without the per-step wait (launches overlap)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         e0.record(stream)
         for i in range(K):
             layers[i % NL].forward_host(x_host[i:i + 1], y_host[i:i + 1], stream=stream)
         e1.record(stream)
     torch.cuda.synchronize()
-    dist.barrier()
-    e2e_rate, _ = whole_job_rate(K, e0.elapsed_time(e1) / 1e3, dist)
+    pipe_rate, _ = whole_job_rate(K, e0.elapsed_time(e1) / 1e3, dist)
+    rc, st = moe.moe_get_status(stream)
+    assert rc == 0 and st == 0, f"device status {st}"
+
+    # ---- the CUDA-core GEMV rail on the same layers (canonical planes), for comparison ----
+    gemv_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            layers[i % NL](xs[i:i + 1], rail=moe.MOE_RAIL_GEMV, out=ys[i:i + 1])
+    torch.cuda.synchronize()
+    with torch.cuda.graph(gemv_graph, stream=stream):
+        for i in range(K):
+            j = W + i
+            layers[j % NL](xs[j:j + 1], rail=moe.MOE_RAIL_GEMV, out=ys[j:j + 1])
+    with torch.cuda.stream(stream):
+        gemv_graph.replay()
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g0.record(stream)
+        gemv_graph.replay()
+        g1.record(stream)
+    torch.cuda.synchronize()
+    gemv_rate, gemv_secs = whole_job_rate(K, g0.elapsed_time(g1) / 1e3, dist)
+    del gemv_graph
 
     result = {
         "metric": METRIC, "value": round(rate, 1), "unit": "tokens/s", "n_gpus": dist.world, "steps": K,
         "warmup": W, "ms_per_step": round(secs_max / K * 1e3, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "vs_baseline": None,
+        "dtype": "f32 accumulate; MXFP4 weights x MXFP4 activations (8 E2M1 terms per value, ~1e-7 of the block max)",
+        "data": "synthetic",
         "config": decode_config(dist.world, f"replicas x{dist.world}",
                                 f"inputs larger than L2: {NL} distinct layer weight sets "
                                 f"({NL * E * EXPERT_BYTES / 1e9:.1f} GB) rotated every step",
                                 "one CUDA graph of the timed steps, CUDA events on its stream"),
+        "rail": "decode_mx (block-scaled tensor cores, prepacked weights)",
         "weight_gbs": round(weight_bytes_step * K / secs_max * dist.world / 1e9, 1),
         "layer_roofline_frac": round((step_bytes / (hbm_peak * 1e9)) / (secs_max / K), 4),
         "roofline": roofline,
         "e2e": {"value": round(e2e_rate, 1), "unit": "tokens/s", "h2d_bytes_per_step": D * 4, "d2h_bytes_per_step": D * 4,
-                "path": "MoeLayer.forward_host -> moe_ffn_layer_hostio per step: x read from and y written to pinned host "
-                        "memory by the kernels themselves (no copy-engine transfers), no graph"},
+                "path": "MoeLayer.forward_host -> moe_ffn_layer_packed_hostio, then the host waits for y every step "
+                        "(wall clock); x and y move through the pinned mapping, no copy-engine transfers"},
+        "e2e_pipelined": {"value": round(pipe_rate, 1), "unit": "tokens/s",
+                          "path": "the same calls back to back without the per-step wait (CUDA events)"},
+        "decode_t1_cuda_core": {"tokens_per_s": round(gemv_rate, 1), "ms_per_step": round(gemv_secs / K * 1e3, 5),
+                                "rail": "gemv (CUDA cores, canonical planes, f16 hi/lo activations, fp32 sums)"},
         "clocks": clocks,
         "gpu_launches": int(round(launches_per_step * K)),
         "kernels_per_step": launches_per_step,
     }
-    del layers, routes
+    del layers
     torch.cuda.empty_cache()
 
     if not args.no_prefill:

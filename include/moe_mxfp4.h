@@ -75,6 +75,7 @@ extern "C" {
 #define MOE_RAIL_GEMV 1
 #define MOE_RAIL_GROUPED_MM 2
 #define MOE_RAIL_GROUPED_MX 3 /* grouped GEMM on the block-scaled (MXFP4 x E4M3) tensor cores */
+#define MOE_RAIL_DECODE_MX 4  /* T <= MOE_GEMV_MAX_T on the block-scaled tensor cores (prepacked weights) */
 #define MOE_GEMV_MAX_T 8
 
 /* Bucket tile height of the grouped-GEMM rail (rows per tensor-core tile). */
@@ -323,6 +324,120 @@ typedef struct {
 int moe_ffn_layer_hostio(const moe_ffn_args_t* args, const float* x_host, float* y_host,
                          cudaStream_t stream);
 
+/*
+ * ---- Prepacked weights for the block-scaled tensor-core rails ----
+ *
+ * The same MXFP4 values (E2M1 codes and E8M0 exponents, nothing decoded or
+ * rounded), placed so that one contiguous copy brings a 128-row weight tile
+ * into shared memory in the operand order of tcgen05.mma kind::mxf4:
+ *   qs_p: tile by tile, NK = ceil(C/128) chunks of 64 bytes per row. Expert e,
+ *        128-row tile t (rows_t = 128, or R - 128t for the last tile) starts at
+ *        byte (e*R + 128t) * NK*64; inside it the 128-column chunk j starts at
+ *        rows_t*64*j and is the 64-byte-swizzled image of its rows: block kb of
+ *        tile row m at m*64 + 16*(kb ^ ((m >> 1) & 3)) (its 16 bytes as stored;
+ *        blocks past C/32 are zero). moe_mxfp4_packed_qs_bytes(E, R, C) =
+ *        E*R*NK*64.
+ *   sf_p [E][ceil(R/128)][NK][512] bytes, NK = ceil(C/128): byte
+ *        16*(m%32) + 4*(m/32) + kb of an atom is the exponent of tile row m,
+ *        block 4j+kb (127 where the row or block does not exist).
+ *        moe_mxfp4_packed_sf_bytes(E, R, C).
+ */
+size_t moe_mxfp4_packed_qs_bytes(int E, int R, int C);
+size_t moe_mxfp4_packed_sf_bytes(int E, int R, int C);
+
+/*
+ * moe_mxfp4_prepack -- canonical planes qs [E][R][C/2], sc [E][R][C/32] ->
+ * prepacked planes qs_p, sf_p (layout above). Run once per weight matrix
+ * stack, e.g. at load time. Requires R a multiple of 64 and C a multiple of
+ * 32; qs, sc, sf_p 16-byte aligned, qs_p 32-byte aligned. The layer kernels
+ * further require C a multiple of 64.
+ */
+int moe_mxfp4_prepack(const uint8_t* qs, const uint8_t* sc, int E, int R, int C, uint8_t* qs_p,
+                      uint8_t* sf_p, cudaStream_t stream);
+
+/*
+ * moe_packed_layer_t -- one layer's device weights with the three expert
+ * matrix stacks prepacked (gate/up [E][F][D], down [E][D][F]); biases and the
+ * router as in moe_ffn_layer (b_router, bg, bu, bd may be NULL).
+ */
+typedef struct {
+  int D, F, E, k;
+  const float* w_router;
+  const float* b_router;
+  const uint8_t* g_qs;
+  const uint8_t* g_sf;
+  const float* bg;
+  const uint8_t* u_qs;
+  const uint8_t* u_sf;
+  const float* bu;
+  const uint8_t* d_qs;
+  const uint8_t* d_sf;
+  const float* bd;
+} moe_packed_layer_t;
+
+/*
+ * moe_ffn_packed_workspace_bytes -- device workspace of moe_ffn_layer_packed
+ * (MOE_RAIL_AUTO resolves as there). Returns 0 for invalid arguments or a
+ * rail the packed layer does not run. Host only.
+ */
+size_t moe_ffn_packed_workspace_bytes(int T, int D, int F, int E, int k, int rail);
+
+/*
+ * moe_ffn_layer_packed -- moe_ffn_layer (same definition of y, routing and
+ * combine) on prepacked weights. Rails: MOE_RAIL_DECODE_MX (MOE_RAIL_AUTO for
+ * T <= MOE_GEMV_MAX_T) runs the decode step as three kernels: a prologue
+ * (router logits; x as a sum of eight MXFP4 terms per value, each block of 32
+ * E2M1 codes on its own E8M0 scale, the residual left ~1e-7 of the block's
+ * largest value), gate/up + bias + swiglu on the block-scaled tensor cores
+ * (tcgen05.mma kind::mxf4) with the MXFP4 weights as stored, and down on the
+ * same tensor cores with the router weights folded into the operand (w*h as
+ * eight MXFP4 terms) so that all k experts of a token accumulate in one fp32
+ * accumulator, plus sum_j w_j bd[e_j] in slot order. Every SM streams an
+ * equal share of the routed experts' weight tiles; tiles shared by several
+ * CTAs are summed in a fixed order, so results are deterministic.
+ * h_out (may be NULL): receives the swiglu outputs h[t*k+j][F] of the
+ * assignments (decode rail only). Other arguments and limits as in
+ * moe_ffn_layer; D and F multiples of 64; k*T <= 64. Returns
+ * MOE_EUNSUPPORTED for T > MOE_GEMV_MAX_T.
+ */
+int moe_ffn_layer_packed(const moe_packed_layer_t* layer, const float* x, int T, int rail, void* workspace,
+                         size_t workspace_bytes, float* y, int32_t* ids_out, float* weights_out, float* h_out,
+                         cudaStream_t stream);
+
+/* Stages of the block-scaled decode rail (moe_ffn_layer_packed_stage, a bit mask). */
+#define MOE_STAGE_PROLOGUE 1 /* router logits, x as E4M3 operand terms, counters zeroed */
+#define MOE_STAGE_GATEUP 2   /* gate/up + bias + swiglu, the down operand written to the workspace */
+#define MOE_STAGE_DOWN 4     /* down + bias + router-weighted combine into y */
+
+/*
+ * moe_ffn_layer_packed_stage -- the stages of moe_ffn_layer_packed on the
+ * decode rail (T <= MOE_GEMV_MAX_T), selected by the bit mask `stages`, on the
+ * same workspace: a stage reads what the earlier stages of the same workspace
+ * left there (the prologue's logits, operand and zeroed counters; the gate/up
+ * stage's down operand), so running them one call at a time in order equals
+ * one moe_ffn_layer_packed call. The pages gate their fused chain against the
+ * per-op composition ("dasLLAMA gpt-oss arc", fused MoE expert chain commit);
+ * this is the per-stage view for tests and profiling. The gate/up and down
+ * stages are launched as programmatic dependents of the work before them in
+ * the stream. y is written by the down stage only; ids_out, weights_out and
+ * h_out (each may be NULL) by the gate/up stage.
+ */
+int moe_ffn_layer_packed_stage(const moe_packed_layer_t* layer, const float* x, int T, void* workspace,
+                               size_t workspace_bytes, int stages, float* y, int32_t* ids_out,
+                               float* weights_out, float* h_out, cudaStream_t stream);
+
+/*
+ * moe_ffn_layer_packed_hostio -- moe_ffn_layer_packed for tokens in host
+ * memory: x_host [T][D] in, y_host [T][D] out, one call per step. With pinned
+ * (page-locked) buffers on the decode rail nothing is copied by the copy
+ * engines: the prologue reads x through the pinned mapping and the down
+ * kernel stores y into it; pageable buffers are staged through the workspace
+ * with cudaMemcpyAsync. The call only enqueues: synchronise the stream before
+ * reading y_host.
+ */
+int moe_ffn_layer_packed_hostio(const moe_packed_layer_t* layer, int T, int rail, void* workspace,
+                                size_t workspace_bytes, const float* x_host, float* y_host, cudaStream_t stream);
+
 /* Size of the library's static decode scratch (moe_ffn_layer_decode_static). */
 #define MOE_DECODE_SCRATCH_BYTES (512 * 1024)
 
@@ -367,9 +482,12 @@ int moe_get_status(cudaStream_t stream, int* status);
  * moe_get_timeout_site -- waits for `stream`, then reads and clears the site of
  * the first pipeline wait that gave up on the calling device since the last
  * read (0: none): kernel << 24 | role << 20 | stage << 12 | sequence index,
- * kernel 1 = decode gate/up, 2 = decode down, 3 = grouped GEMM; role 0 = a
- * producer waiting for a free stage, 1 = a consumer waiting for data (grouped
- * GEMM: the warp index of the waiting role, 3 = dequant). For diagnosis only.
+ * kernel 1 = decode gate/up, 2 = decode down (CUDA-core GEMV rail), 3 = grouped
+ * GEMM (bf16), 4 = grouped GEMM (block-scaled), 5 = decode gate/up, 6 = decode
+ * down (block-scaled decode rail); role 0 = a producer waiting for a free
+ * stage, 1 = a consumer waiting for data, 2 = an epilogue waiting for its
+ * accumulator (grouped GEMMs: the warp index of the waiting role, 3 or 4 = the
+ * dequantising or expanding warps). For diagnosis only.
  */
 int moe_get_timeout_site(cudaStream_t stream, int* site);
 

@@ -41,6 +41,10 @@ MOE_RAIL_AUTO = 0
 MOE_RAIL_GEMV = 1
 MOE_RAIL_GROUPED_MM = 2
 MOE_RAIL_GROUPED_MX = 3
+MOE_RAIL_DECODE_MX = 4
+MOE_STAGE_PROLOGUE = 1
+MOE_STAGE_GATEUP = 2
+MOE_STAGE_DOWN = 4
 MOE_GEMV_MAX_T = 8
 MOE_MM_TILE = 128
 
@@ -64,6 +68,13 @@ _SIGS = {
     "moe_ffn_layer": (I, [P, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, I, P, SZ, P, P, P, P]),
     "moe_ffn_layer_hostio": (I, [P, P, P, P]),
     "moe_ffn_layer_decode_static": (I, [P, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P]),
+    "moe_mxfp4_packed_qs_bytes": (SZ, [I, I, I]),
+    "moe_mxfp4_packed_sf_bytes": (SZ, [I, I, I]),
+    "moe_mxfp4_prepack": (I, [P, P, I, I, I, P, P, P]),
+    "moe_ffn_packed_workspace_bytes": (SZ, [I, I, I, I, I, I]),
+    "moe_ffn_layer_packed": (I, [P, P, I, I, P, SZ, P, P, P, P, P]),
+    "moe_ffn_layer_packed_hostio": (I, [P, I, I, P, SZ, P, P, P]),
+    "moe_ffn_layer_packed_stage": (I, [P, P, I, P, SZ, I, P, P, P, P, P]),
     "moe_get_status": (I, [P, ctypes.POINTER(ctypes.c_int)]),
     "moe_get_timeout_site": (I, [P, ctypes.POINTER(ctypes.c_int)]),
     "moe_last_cuda_error": (I, []),
@@ -204,6 +215,55 @@ def moe_ffn_layer_decode_static(x, T, D, F, E, k, w_router, b_router, g_qs, g_sc
                                             _ptr(g_qs), _ptr(g_sc), _ptr(bg), _ptr(u_qs), _ptr(u_sc),
                                             _ptr(bu), _ptr(d_qs), _ptr(d_sc), _ptr(bd), _ptr(y),
                                             _ptr(ids_out), _ptr(weights_out), _stream(stream))
+
+
+def moe_mxfp4_packed_qs_bytes(E, R, C):
+    return _lib.moe_mxfp4_packed_qs_bytes(E, R, C)
+
+
+def moe_mxfp4_packed_sf_bytes(E, R, C):
+    return _lib.moe_mxfp4_packed_sf_bytes(E, R, C)
+
+
+def moe_mxfp4_prepack(qs, sc, E, R, C, qs_p, sf_p, stream=None):
+    return _lib.moe_mxfp4_prepack(_ptr(qs), _ptr(sc), E, R, C, _ptr(qs_p), _ptr(sf_p), _stream(stream))
+
+
+class MoePackedLayer(ctypes.Structure):
+    """moe_packed_layer_t of the header: one layer's weights with prepacked expert planes."""
+    _fields_ = [("D", I), ("F", I), ("E", I), ("k", I), ("w_router", P), ("b_router", P),
+                ("g_qs", P), ("g_sf", P), ("bg", P), ("u_qs", P), ("u_sf", P), ("bu", P),
+                ("d_qs", P), ("d_sf", P), ("bd", P)]
+
+
+def make_packed_layer(D, F, E, k, w_router, b_router, g_qs, g_sf, bg, u_qs, u_sf, bu, d_qs, d_sf,
+                      bd) -> MoePackedLayer:
+    return MoePackedLayer(D, F, E, k, _ptr(w_router), _ptr(b_router), _ptr(g_qs), _ptr(g_sf), _ptr(bg),
+                          _ptr(u_qs), _ptr(u_sf), _ptr(bu), _ptr(d_qs), _ptr(d_sf), _ptr(bd))
+
+
+def moe_ffn_packed_workspace_bytes(T, D, F, E, k, rail=MOE_RAIL_AUTO):
+    return _lib.moe_ffn_packed_workspace_bytes(T, D, F, E, k, rail)
+
+
+def moe_ffn_layer_packed(layer, x, T, rail, workspace, workspace_bytes, y, ids_out=None, weights_out=None,
+                         h_out=None, stream=None):
+    return _lib.moe_ffn_layer_packed(None if layer is None else ctypes.byref(layer), _ptr(x), T, rail,
+                                     _ptr(workspace), workspace_bytes, _ptr(y), _ptr(ids_out),
+                                     _ptr(weights_out), _ptr(h_out), _stream(stream))
+
+
+def moe_ffn_layer_packed_stage(layer, x, T, workspace, workspace_bytes, stages, y=None, ids_out=None,
+                               weights_out=None, h_out=None, stream=None):
+    return _lib.moe_ffn_layer_packed_stage(None if layer is None else ctypes.byref(layer), _ptr(x), T,
+                                           _ptr(workspace), workspace_bytes, stages, _ptr(y), _ptr(ids_out),
+                                           _ptr(weights_out), _ptr(h_out), _stream(stream))
+
+
+def moe_ffn_layer_packed_hostio(layer, T, rail, workspace, workspace_bytes, x_host, y_host, stream=None):
+    return _lib.moe_ffn_layer_packed_hostio(None if layer is None else ctypes.byref(layer), T, rail,
+                                            _ptr(workspace), workspace_bytes, _ptr(x_host), _ptr(y_host),
+                                            _stream(stream))
 
 
 def moe_get_status(stream=None):

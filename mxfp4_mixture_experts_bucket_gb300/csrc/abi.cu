@@ -10,6 +10,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/moe_mxfp4.h"
+#include "decode_mx.cuh"
 #include "moe_internal.h"
 
 namespace moe {
@@ -145,6 +146,50 @@ size_t layout_workspace(int T, int D, int F, int E, int k, int rail, char* base,
   w.max_rows = mr;
   if (ws) *ws = w;
   return off;
+}
+
+// Workspace of the block-scaled decode rail on prepacked weights.
+struct PackedWorkspace {
+  float* logits;  // [T][E]
+  uint8_t* xq;    // x operand chunks [NK_D][npad][64]
+  uint8_t* xsf;   // [NK_D][512]
+  uint8_t* hq;    // down operand chunks [T*k][NK_F][npad][64]
+  uint8_t* hsf;   // [T*k][NK_F][512]
+  float* part;    // partial sums [kDecodeMxMaxGrid][2][2][T][128]
+  int* cnt;       // arrival counters per unit and lane quarter: gate/up [T*k*NK_F][4], then down [NK_D][4]
+  int ncnt_gu, ncnt;
+  float* xs;      // host-I/O staging [T][D]
+  float* ys;      // [T][D]
+};
+
+size_t layout_packed_workspace(int T, int D, int F, int k, int E, char* base, PackedWorkspace* ws) {
+  const int npad = dmx::npad_for(T);
+  const size_t nkd = (size_t)(D + 127) / 128, nkf = (size_t)(F + 127) / 128;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    char* p = base ? base + off : nullptr;
+    off = round_up(off + bytes, 256);
+    return p;
+  };
+  PackedWorkspace w{};
+  w.logits = reinterpret_cast<float*>(take((size_t)T * E * 4));
+  w.xq = reinterpret_cast<uint8_t*>(take(nkd * npad * 64));
+  w.xsf = reinterpret_cast<uint8_t*>(take(nkd * 512));
+  w.hq = reinterpret_cast<uint8_t*>(take((size_t)T * k * nkf * npad * 64));
+  w.hsf = reinterpret_cast<uint8_t*>(take((size_t)T * k * nkf * 512));
+  w.part = reinterpret_cast<float*>(take((size_t)kDecodeMxMaxGrid * 2 * 2 * T * 128 * 4));
+  w.ncnt_gu = (int)(4 * (size_t)T * k * nkf);  // one counter per unit and lane quarter
+  w.ncnt = w.ncnt_gu + 4 * (int)nkd;
+  w.cnt = reinterpret_cast<int*>(take((size_t)w.ncnt * 4));
+  w.xs = reinterpret_cast<float*>(take((size_t)T * D * 4));
+  w.ys = reinterpret_cast<float*>(take((size_t)T * D * 4));
+  if (ws) *ws = w;
+  return off;
+}
+
+int resolve_packed_rail(int T, int rail) {
+  if (rail == MOE_RAIL_AUTO) return T <= MOE_GEMV_MAX_T ? MOE_RAIL_DECODE_MX : MOE_RAIL_GROUPED_MX;
+  return rail;
 }
 
 }  // namespace
@@ -580,6 +625,162 @@ int moe_ffn_layer_hostio(const moe_ffn_args_t* args, const float* x_host, float*
                                a.workspace_bytes, a.y_dev, nullptr, nullptr, stream);
   if (rc != MOE_OK) return rc;
   return cuda_status(cudaMemcpyAsync(y_host, a.y_dev, bytes, cudaMemcpyDeviceToHost, stream));
+}
+
+size_t moe_mxfp4_packed_qs_bytes(int E, int R, int C) {
+  if (E < 1 || R < 1 || C < 32 || R % 64 != 0 || C % 32 != 0) return 0;
+  return packed_qs_bytes(E, R, C);
+}
+
+size_t moe_mxfp4_packed_sf_bytes(int E, int R, int C) {
+  if (E < 1 || R < 1 || C < 32 || R % 64 != 0 || C % 32 != 0) return 0;
+  return packed_sf_bytes(E, R, C);
+}
+
+int moe_mxfp4_prepack(const uint8_t* qs, const uint8_t* sc, int E, int R, int C, uint8_t* qs_p,
+                      uint8_t* sf_p, cudaStream_t stream) {
+  MOE_REQUIRE(E >= 1 && R >= 64 && C >= 32 && R % 64 == 0 && C % 32 == 0);
+  MOE_REQUIRE(qs && sc && qs_p && sf_p);
+  MOE_REQUIRE(aligned(qs, 16) && aligned(sc, 16) && aligned(qs_p, 32) && aligned(sf_p, 16));
+  DeviceInfo* d = nullptr;
+  int rc = current_device(&d);
+  if (rc != MOE_OK) return rc;
+  Launch L{stream, false};
+  return cuda_status(launch_prepack(qs, sc, E, R, C, qs_p, sf_p, L));
+}
+
+size_t moe_ffn_packed_workspace_bytes(int T, int D, int F, int E, int k, int rail) {
+  if (T < 0 || D < 64 || F < 64 || D % 64 != 0 || F % 64 != 0 || E < 1 || k < 1 || k > E) return 0;
+  if (resolve_packed_rail(T, rail) != MOE_RAIL_DECODE_MX || T > MOE_GEMV_MAX_T) return 0;
+  return layout_packed_workspace(T, D, F, k, E, nullptr, nullptr);
+}
+
+}  // extern "C"
+
+namespace {
+int packed_layer_impl(const moe_packed_layer_t* Lp, const float* x, int T, int rail, void* workspace,
+                      size_t workspace_bytes, float* y, int32_t* ids_out, float* weights_out, float* h_out,
+                      cudaStream_t stream, int stages = MOE_STAGE_PROLOGUE | MOE_STAGE_GATEUP | MOE_STAGE_DOWN) {
+  MOE_REQUIRE(Lp != nullptr && T >= 0);
+  const moe_packed_layer_t& P = *Lp;
+  MOE_REQUIRE(P.D >= 64 && P.F >= 64 && P.D % 64 == 0 && P.F % 64 == 0);
+  MOE_REQUIRE(P.E >= 1 && P.E <= 256 && P.k >= 1 && P.k <= P.E && P.k <= 32);
+  rail = resolve_packed_rail(T, rail);
+  MOE_REQUIRE(rail == MOE_RAIL_DECODE_MX || rail == MOE_RAIL_GROUPED_MX);
+  if (rail != MOE_RAIL_DECODE_MX || T > MOE_GEMV_MAX_T) return MOE_EUNSUPPORTED;
+  MOE_REQUIRE(T * P.k <= 64);
+  if (P.D > 4096 || P.F > 4096) return MOE_EUNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  MOE_REQUIRE(stages >= 1 && stages <= 7);
+  MOE_REQUIRE(workspace && P.w_router && P.g_qs && P.g_sf && P.u_qs && P.u_sf && P.d_qs && P.d_sf);
+  MOE_REQUIRE(x || !(stages & MOE_STAGE_PROLOGUE));
+  MOE_REQUIRE(y || !(stages & MOE_STAGE_DOWN));
+  MOE_REQUIRE(aligned(x, 16) && aligned(P.w_router, 16) && aligned(workspace, 256));
+  MOE_REQUIRE(aligned(P.g_qs, 32) && aligned(P.u_qs, 32) && aligned(P.d_qs, 32));
+  MOE_REQUIRE(aligned(P.g_sf, 16) && aligned(P.u_sf, 16) && aligned(P.d_sf, 16));
+  const size_t need = layout_packed_workspace(T, P.D, P.F, P.k, P.E, nullptr, nullptr);
+  MOE_REQUIRE(workspace_bytes >= need);
+  DeviceInfo* d = nullptr;
+  int rc = current_device(&d);
+  if (rc != MOE_OK) return rc;
+  PackedWorkspace ws;
+  layout_packed_workspace(T, P.D, P.F, P.k, P.E, static_cast<char*>(workspace), &ws);
+  const int npad = dmx::npad_for(T);
+  Launch L{stream, false};
+  if (stages & MOE_STAGE_PROLOGUE) {
+    rc = cuda_status(launch_decode_prologue(x, T, P.D, P.w_router, P.b_router, P.E, ws.logits, ws.xq, ws.xsf,
+                                            npad, ws.cnt, ws.ncnt, L));
+    if (rc != MOE_OK) return rc;
+  }
+  L.pdl = true;
+  DecodeMXArgs g{};
+  g.kind = 0;
+  g.w_qs[0] = P.g_qs;
+  g.w_qs[1] = P.u_qs;
+  g.w_sf[0] = P.g_sf;
+  g.w_sf[1] = P.u_sf;
+  g.bias[0] = P.bg;
+  g.bias[1] = P.bu;
+  g.E = P.E;
+  g.R = P.F;
+  g.C = P.D;
+  g.T = T;
+  g.k = P.k;
+  g.b_q = ws.xq;
+  g.b_sf = ws.xsf;
+  g.logits = ws.logits;
+  g.ids_out = ids_out;
+  g.w_out = weights_out;
+  g.alpha = 1.702f;
+  g.limit = 7.0f;
+  g.hq = ws.hq;
+  g.hsf = ws.hsf;
+  g.h_out = h_out;
+  g.part = ws.part;
+  g.cnt = ws.cnt;
+  g.status = d->status;
+  if (stages & MOE_STAGE_GATEUP) {
+    rc = cuda_status(launch_decode_mx(g, L));
+    if (rc != MOE_OK) return rc;
+  }
+  if (!(stages & MOE_STAGE_DOWN)) return MOE_OK;
+  DecodeMXArgs dn{};
+  dn.kind = 1;
+  dn.w_qs[0] = dn.w_qs[1] = P.d_qs;
+  dn.w_sf[0] = dn.w_sf[1] = P.d_sf;
+  dn.bias[0] = P.bd;
+  dn.E = P.E;
+  dn.R = P.D;
+  dn.C = P.F;
+  dn.T = T;
+  dn.k = P.k;
+  dn.b_q = ws.hq;
+  dn.b_sf = ws.hsf;
+  dn.logits = ws.logits;
+  dn.y = y;
+  dn.part = ws.part;
+  dn.cnt = ws.cnt + ws.ncnt_gu;
+  dn.status = d->status;
+  return cuda_status(launch_decode_mx(dn, L));
+}
+}  // namespace
+
+extern "C" {
+
+int moe_ffn_layer_packed(const moe_packed_layer_t* layer, const float* x, int T, int rail, void* workspace,
+                         size_t workspace_bytes, float* y, int32_t* ids_out, float* weights_out, float* h_out,
+                         cudaStream_t stream) {
+  return packed_layer_impl(layer, x, T, rail, workspace, workspace_bytes, y, ids_out, weights_out, h_out, stream);
+}
+
+int moe_ffn_layer_packed_stage(const moe_packed_layer_t* layer, const float* x, int T, void* workspace,
+                               size_t workspace_bytes, int stages, float* y, int32_t* ids_out,
+                               float* weights_out, float* h_out, cudaStream_t stream) {
+  return packed_layer_impl(layer, x, T, MOE_RAIL_DECODE_MX, workspace, workspace_bytes, y, ids_out, weights_out,
+                           h_out, stream, stages);
+}
+
+int moe_ffn_layer_packed_hostio(const moe_packed_layer_t* layer, int T, int rail, void* workspace,
+                                size_t workspace_bytes, const float* x_host, float* y_host, cudaStream_t stream) {
+  MOE_REQUIRE(layer != nullptr && T >= 0);
+  if (T == 0) return MOE_OK;
+  MOE_REQUIRE(x_host && y_host && workspace && layer->D >= 64);
+  const float* dx = static_cast<const float*>(mapped_host(x_host));
+  float* dy = static_cast<float*>(const_cast<void*>(mapped_host(y_host)));
+  if (dx && dy && aligned(dx, 16))  // pinned: the kernels read x and write y through the mapping
+    return packed_layer_impl(layer, dx, T, rail, workspace, workspace_bytes, dy, nullptr, nullptr, nullptr, stream);
+  if (resolve_packed_rail(T, rail) != MOE_RAIL_DECODE_MX || T > MOE_GEMV_MAX_T) return MOE_EUNSUPPORTED;
+  MOE_REQUIRE(workspace_bytes >= layout_packed_workspace(T, layer->D, layer->F, layer->k, layer->E, nullptr, nullptr));
+  MOE_REQUIRE(aligned(workspace, 256));
+  PackedWorkspace ws;
+  layout_packed_workspace(T, layer->D, layer->F, layer->k, layer->E, static_cast<char*>(workspace), &ws);
+  const size_t bytes = (size_t)T * layer->D * sizeof(float);
+  cudaError_t err = cudaMemcpyAsync(ws.xs, x_host, bytes, cudaMemcpyHostToDevice, stream);
+  if (err != cudaSuccess) return cuda_status(err);
+  const int rc = packed_layer_impl(layer, ws.xs, T, rail, workspace, workspace_bytes, ws.ys, nullptr, nullptr,
+                                   nullptr, stream);
+  if (rc != MOE_OK) return rc;
+  return cuda_status(cudaMemcpyAsync(y_host, ws.ys, bytes, cudaMemcpyDeviceToHost, stream));
 }
 
 int moe_get_status(cudaStream_t stream, int* status) {

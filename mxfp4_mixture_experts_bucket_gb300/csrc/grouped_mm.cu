@@ -425,6 +425,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  // Lanes that ran a role alone (lane 0 of the producer and MMA warps) rejoin
+  // their warp first: the CTA barrier counts whole warps.
+  __syncwarp();
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 1) {

@@ -50,6 +50,7 @@
 //           seeds the accumulators with the bias; all eight run the epilogue.
 #include <cuda.h>
 
+#include "mx_terms.cuh"
 #include "tcgen05.cuh"
 
 namespace moe {
@@ -115,50 +116,6 @@ __device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b,
   asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b),
                "r"(c), "r"(d)
                : "memory");
-}
-
-// ---------------------------------------------------------------- E4M3 terms
-// Position of stored column c (0..31) of a block in the MMA's K order.
-__device__ __forceinline__ int mx_pos(int c) { return 2 * (c & 15) + (c >> 4); }
-
-// E8M0 code of a block whose largest magnitude has the bit pattern am: the
-// block divided by 2^(code-127) has its largest element in [128, 256), inside
-// E4M3's range (448), never saturating.
-__device__ __forceinline__ uint32_t block_code(uint32_t am) {
-  const int eb = (int)(am >> 23);
-  return (uint32_t)(eb > 7 ? eb - 7 : 0);
-}
-// 2^(127 - code) for code in [0, 248], a normal float
-__device__ __forceinline__ float inv_scale(uint32_t code) { return __uint_as_float((254u - code) << 23); }
-// 2^(code - 127) for code in [0, 254]
-__device__ __forceinline__ float fwd_scale(uint32_t code) {
-  return code ? __uint_as_float(code << 23) : __uint_as_float(0x00400000u);
-}
-__device__ __forceinline__ uint32_t f32_to_e4m3(float v) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.f), "f"(v));  // second operand -> low byte
-  return r & 0xFFu;
-}
-// Exact value of an E4M3 code (never the NaN code here): its seven magnitude
-// bits placed at the top of an fp32 exponent/mantissa give value * 2^-120.
-__device__ __forceinline__ float e4m3_to_f32(uint32_t q) {
-  const float s = __uint_as_float(((q & 0x80u) << 24) | ((q & 0x7Fu) << 20));
-  return __fmul_rn(s, __uint_as_float(0x7B800000u));  // * 2^120
-}
-
-// One block of 32 values, one per lane (all lanes of the warp take part):
-// v = sum_t E4M3(q[t]) * 2^(s[t]-127) + (rounding of the last term); each term
-// encodes the residual of the ones before it exactly, then rounds it.
-template <int NT>
-__device__ __forceinline__ void split_terms(float v, uint32_t (&q)[NT], uint32_t (&s)[NT]) {
-  float r = v;
-#pragma unroll
-  for (int t = 0; t < NT; ++t) {
-    const uint32_t am = __reduce_max_sync(0xffffffffu, __float_as_uint(r) & 0x7FFFFFFFu);
-    s[t] = block_code(am);
-    q[t] = f32_to_e4m3(__fmul_rn(r, inv_scale(s[t])));
-    if (t + 1 < NT) r = __fmaf_rn(-e4m3_to_f32(q[t]), fwd_scale(s[t]), r);  // exact residual
-  }
 }
 
 // Shared-memory plan, identical on host and device.
@@ -549,6 +506,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  // Lanes that ran a role alone (lane 0 of the producer and MMA warps) rejoin
+  // their warp first: the CTA barrier counts whole warps.
+  __syncwarp();
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 1) {

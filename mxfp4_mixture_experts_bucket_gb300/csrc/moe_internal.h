@@ -99,6 +99,44 @@ cudaError_t launch_gemv_down(const uint8_t* d_qs, const uint8_t* d_sc, const flo
                              const int32_t* ids_in, const float* w_in, float* y, int* status,
                              Launch L);
 
+// ---- prepack.cu ----
+// Prepacked MXFP4 planes of the block-scaled rails (layout in prepack.cu).
+size_t packed_qs_bytes(int E, int R, int C);
+size_t packed_sf_bytes(int E, int R, int C);
+cudaError_t launch_prepack(const uint8_t* qs, const uint8_t* sc, int E, int R, int C, uint8_t* qs_p,
+                           uint8_t* sf_p, Launch L);
+
+// ---- route_bucket.cu: prologue of the block-scaled decode rail ----
+// Router logits, x as E4M3 operand chunks xq [NK][npad][128] + atoms xsf [NK][512],
+// and zero[0 .. nzero) = 0.
+cudaError_t launch_decode_prologue(const float* x, int T, int D, const float* wr, const float* br, int E,
+                                   float* logits, uint8_t* xq, uint8_t* xsf, int npad, int* zero, int nzero,
+                                   Launch L);
+
+// ---- decode_mx.cu ----
+constexpr int kDecodeMxMaxGrid = 256;  // partial-sum slots are sized for this many CTAs
+struct DecodeMXArgs {
+  int kind;  // 0: gate/up + swiglu (two matrices), 1: down + combine
+  const uint8_t* w_qs[2];  // prepacked planes
+  const uint8_t* w_sf[2];
+  const float* bias[2];
+  int E, R, C, T, k;
+  const uint8_t* b_q;   // activation operand chunks
+  const uint8_t* b_sf;
+  const float* logits;
+  int32_t* ids_out;
+  float* w_out;
+  float alpha, limit;
+  uint8_t* hq;
+  uint8_t* hsf;
+  float* h_out;
+  float* y;
+  float* part;
+  int* cnt;
+  int* status;
+};
+cudaError_t launch_decode_mx(const DecodeMXArgs& a, Launch L);
+
 // ---- grouped_mm.cu ----
 struct GroupedMMArgs {
   const uint8_t* w_qs[2];

@@ -5,7 +5,9 @@
 // folded into the bucket kernel, each expert's block computing its own padded
 // base in-block and publishing basep[e]; the resulting CSR is bit-identical
 // to the two-pass one.
+#include "decode_mx.cuh"
 #include "moe_common.cuh"
+#include "mx_terms.cuh"
 
 namespace moe {
 
@@ -14,22 +16,21 @@ namespace moe {
 // Each block computes TT tokens x EG experts; every dot product is spread over
 // G = 128 / (TT*EG) consecutive threads (float4 loads, shuffle / smem reduce).
 // ---------------------------------------------------------------------------
+// One block's dots (block coordinates bx over tokens, by over experts); shared
+// with the decode prologue of the block-scaled rail.
 template <int TT, int EG>
-__global__ void __launch_bounds__(128) router_logits_kernel(const float* __restrict__ x, int T, int D,
-                                                            const float* __restrict__ wr,
-                                                            const float* __restrict__ br, int E,
-                                                            float* __restrict__ logits,
-                                                            float* __restrict__ x_copy) {
-  pdl_launch_dependents();
-  pdl_wait();
+__device__ __forceinline__ void router_logits_block(const float* __restrict__ x, int T, int D,
+                                                    const float* __restrict__ wr, const float* __restrict__ br,
+                                                    int E, float* __restrict__ logits, float* __restrict__ x_copy,
+                                                    int bx, int by) {
   constexpr int NDOT = TT * EG;
   constexpr int G = 128 / NDOT;
   static_assert(G * NDOT == 128, "threads per dot");
   const int tid = threadIdx.x;
   const int d = tid / G;   // which dot of this block
   const int gi = tid % G;  // thread within the dot's group
-  const int t = blockIdx.x * TT + d / EG;
-  const int e = blockIdx.y * EG + d % EG;
+  const int t = bx * TT + d / EG;
+  const int e = by * EG + d % EG;
   const bool live = (t < T) && (e < E);
   float acc = 0.f;
   if (live) {
@@ -37,7 +38,7 @@ __global__ void __launch_bounds__(128) router_logits_kernel(const float* __restr
     const float4* wrr = reinterpret_cast<const float4*>(wr + (size_t)e * D);
     const int n4 = D >> 2;
     // the copy of x (if asked for) comes from the expert-0 dots of the first block column
-    float4* xc = (x_copy && blockIdx.y == 0 && d % EG == 0) ? reinterpret_cast<float4*>(x_copy + (size_t)t * D)
+    float4* xc = (x_copy && by == 0 && d % EG == 0) ? reinterpret_cast<float4*>(x_copy + (size_t)t * D)
                                                             : nullptr;
     float a0 = 0.f, a1 = 0.f;
     if constexpr (NDOT == 1) {
@@ -97,6 +98,70 @@ __global__ void __launch_bounds__(128) router_logits_kernel(const float* __restr
       logits[(size_t)t * E + e] = s + (br ? br[e] : 0.f);
     }
   }
+}
+
+template <int TT, int EG>
+__global__ void __launch_bounds__(128) router_logits_kernel(const float* __restrict__ x, int T, int D,
+                                                            const float* __restrict__ wr,
+                                                            const float* __restrict__ br, int E,
+                                                            float* __restrict__ logits,
+                                                            float* __restrict__ x_copy) {
+  pdl_launch_dependents();
+  pdl_wait();
+  router_logits_block<TT, EG>(x, T, D, wr, br, E, logits, x_copy, blockIdx.x, blockIdx.y);
+}
+
+// ---------------------------------------------------------------------------
+// Decode prologue of the block-scaled decode rail (T <= 8): the router logits
+// (blocks [0, nlog), laid out as router_logits_kernel's grid), the x operand of
+// the gate/up MMAs as kDecTerms E2M1 terms per value in the operand-chunk
+// layout of decode_mx.cuh (the remaining blocks, a warp per (token, 32-block)),
+// and the zeroing of the expert kernels' arrival counters. x may live in
+// mapped host memory: every value is read once.
+// ---------------------------------------------------------------------------
+template <int TT, int EG>
+__global__ void __launch_bounds__(128) decode_prologue_kernel(const float* __restrict__ x, int T, int D,
+                                                              const float* __restrict__ wr,
+                                                              const float* __restrict__ br, int E,
+                                                              float* __restrict__ logits, int nlog_x, int nlog,
+                                                              uint8_t* __restrict__ xq, uint8_t* __restrict__ xsf,
+                                                              int npad, int* __restrict__ zero, int nzero) {
+  pdl_launch_dependents();
+  pdl_wait();
+  if ((int)blockIdx.x < nlog) {
+    router_logits_block<TT, EG>(x, T, D, wr, br, E, logits, nullptr, blockIdx.x % nlog_x, blockIdx.x / nlog_x);
+    return;
+  }
+  using namespace dmx;
+  const int qb = blockIdx.x - nlog, nqb = gridDim.x - nlog;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nb = D / 32, NK = (D + 127) / 128;
+  if (qb == 0)
+    for (int i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0;
+  const int gw = qb * 4 + warp, nw = nqb * 4;
+  for (int task = gw; task < T * nb; task += nw) {
+    const int t = task / nb, blk = task - t * nb;
+    const float v = x[(size_t)t * D + 32 * blk + lane];
+    uint32_t q[kDecTerms], sc[kDecTerms];
+    mx::split_terms_e2m1<kDecTerms>(v, q, sc);
+    const int j = blk >> 2, kb = blk & 3;
+    uint8_t* chunk = xq + (size_t)j * npad * 64;
+#pragma unroll
+    for (int term = 0; term < kDecTerms; ++term) {
+      const int n = t * kDecTerms + term;
+      const uint32_t byte = mx::pack_e2m1_block(q[term]);
+      if (lane < 16) chunk[chunk_off(n, kb, lane)] = (uint8_t)byte;
+      if (lane == 0) xsf[(size_t)j * 512 + atom_off(n, kb)] = (uint8_t)sc[term];
+    }
+  }
+  // rows past T * kDecTerms: zero codes on a scale of 1
+  const int npr = npad - T * kDecTerms;
+  for (int task = gw; task < NK * npr; task += nw) {
+    const int j = task / npr, n = T * kDecTerms + (task - j * npr);
+    if (lane < 16) reinterpret_cast<uint32_t*>(xq + (size_t)j * npad * 64 + chunk_off(n, lane >> 2, 4 * (lane & 3)))[0] = 0u;
+    if (lane < 4) xsf[(size_t)j * 512 + atom_off(n, lane)] = 127;
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");  // read next by the copy engine
 }
 
 // Prefill sizes (T > 8): a block takes 4 tokens x 16 experts with 16 warps:
@@ -377,6 +442,24 @@ cudaError_t launch_router_logits(const float* x, int T, int D, const float* wr, 
   if (x_copy) return cudaErrorInvalidValue;  // prefill sizes take x from device memory
   dim3 grid((T + kRouterTileT - 1) / kRouterTileT, (E + kRouterTileE - 1) / kRouterTileE);
   return launch_kernel(router_logits_tile_kernel, grid, dim3(512), 0, L, x, T, D, wr, br, E, logits);
+}
+
+cudaError_t launch_decode_prologue(const float* x, int T, int D, const float* wr, const float* br, int E,
+                                   float* logits, uint8_t* xq, uint8_t* xsf, int npad, int* zero, int nzero,
+                                   Launch L) {
+  if (T <= 0 || T > 8) return cudaErrorInvalidValue;
+  const int nb = D / 32;
+  int nq = (T * nb + 7) / 8;
+  if (nq < 1) nq = 1;
+  if (nq > 64) nq = 64;
+  if (T == 1) {
+    const int nlog = E;
+    return launch_kernel(decode_prologue_kernel<1, 1>, dim3(nlog + nq), dim3(128), 0, L, x, T, D, wr, br, E,
+                         logits, 1, nlog, xq, xsf, npad, zero, nzero);
+  }
+  const int nlx = (T + 1) / 2, nlog = nlx * ((E + 1) / 2);
+  return launch_kernel(decode_prologue_kernel<2, 2>, dim3(nlog + nq), dim3(128), 0, L, x, T, D, wr, br, E,
+                       logits, nlx, nlog, xq, xsf, npad, zero, nzero);
 }
 
 cudaError_t launch_topk_softmax(const float* logits, int T, int E, int k, int32_t* ids, float* w,

@@ -60,6 +60,27 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   }
 }
 
+// As mbar_wait, for waits whose latency does not matter (a role idling until
+// its turn): the thread sleeps between probes so that it leaves the issue slots
+// of its SM sub-partition to the warps that are working.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, const volatile int* abort_flag,
+                                                uint32_t sleep_ns) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_test(bar, parity)) return true;
+    __nanosleep(sleep_ns);
+    if ((it & 7u) == 7u) {
+      if (abort_flag && *abort_flag) return false;
+      const uint64_t now = globaltimer_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > kWaitTimeoutNs) {
+        return false;
+      }
+    }
+  }
+}
+
 // Bounded wait for two phases at once (both probed each round, so their
 // latencies overlap). Returns false if it gave up, like mbar_wait.
 __device__ __forceinline__ bool mbar_wait2(uint32_t bar_a, uint32_t parity_a, uint32_t bar_b,
@@ -97,6 +118,23 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm,
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* tm, int c0, int c1, int c2, int c3,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+// 5-D tiled load with an L2 cache policy (streamed weights).
+__device__ __forceinline__ void tma_load_5d_hint(uint32_t dst, const CUtensorMap* tm, int c0, int c1, int c2,
+                                                 int c3, int c4, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar), "l"(policy)
       : "memory");
 }
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
@@ -156,6 +194,53 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
   d |= (uint64_t)1 << 46;                    // descriptor version for tcgen05
   d |= (uint64_t)2 << 61;                    // 128-byte swizzle
   return d;
+}
+
+// The same for rows of 64 bytes with the 64-byte swizzle (8-row groups 512 B
+// apart); the tile base must be 512-byte aligned.
+__device__ __forceinline__ uint64_t sw64_kmajor_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address
+  d |= (uint64_t)1 << 16;                    // leading-dimension byte offset (unused for this layout)
+  d |= (uint64_t)(512 >> 4) << 32;           // stride-dimension byte offset
+  d |= (uint64_t)1 << 46;                    // descriptor version for tcgen05
+  d |= (uint64_t)4 << 61;                    // 64-byte swizzle
+  return d;
+}
+
+// Shared-memory descriptor of an unswizzled K-major operand built from core
+// matrices (8 rows x 16 bytes, 128 contiguous bytes): lbo = byte distance
+// between core matrices adjacent along K, sbo = along M (or N).
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version for tcgen05; no swizzle
+  return d;
+}
+
+// Shared-memory descriptor of an unswizzled block of 16-byte rows (8-row core
+// matrices 128 bytes apart), the source of tcgen05.cp's 32x128b shape.
+__device__ __forceinline__ uint64_t rows16_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address
+  d |= (uint64_t)(128 >> 4) << 16;           // leading-dimension byte offset
+  d |= (uint64_t)(128 >> 4) << 32;           // stride-dimension byte offset: next 8 rows
+  d |= (uint64_t)1 << 46;                    // descriptor version for tcgen05
+  return d;
+}
+
+// Copies 32 rows of 16 bytes from shared memory into tensor memory lanes 0..31,
+// columns taddr..taddr+3, replicated into all four lane quarters; ordered with
+// the MMAs issued after it by the same thread.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Named barrier over `threads` threads (barrier 0 is __syncthreads).
+__device__ __forceinline__ void named_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 // Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B (both
@@ -218,6 +303,12 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, uint32_t v) {
       "%1, %1, %1, %1, %1};" ::"r"(taddr),
       "r"(v)
       : "memory");
+}
+// 32 lanes x 4 consecutive 32-bit columns from registers.
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");

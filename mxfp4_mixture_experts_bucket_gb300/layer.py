@@ -25,7 +25,8 @@ class MoeLayer:
     Host (numpy or torch CPU) arrays are copied to `device` once.
     """
 
-    def __init__(self, weights: Dict[str, object], k: int, device="cuda"):
+    def __init__(self, weights: Dict[str, object], k: int, device="cuda", packed: bool = False,
+                 keep_canonical: bool = True):
         self.device = torch.device(device)
         self.w: Dict[str, Optional[torch.Tensor]] = {}
         for key in _WEIGHT_KEYS:
@@ -40,12 +41,44 @@ class MoeLayer:
         self.k = k
         self._ws: Dict[int, torch.Tensor] = {}
         self._io: Dict[tuple, tuple] = {}
+        self.packed = None
+        if packed:
+            self._prepack()
+            if not keep_canonical:
+                for key in ("g_qs", "g_sc", "u_qs", "u_sc", "d_qs", "d_sc"):
+                    self.w[key] = None
+
+    def _prepack(self):
+        """Prepacked copies of the three expert stacks (moe_mxfp4_prepack) and the layer struct."""
+        pk: Dict[str, torch.Tensor] = {}
+        for m, (R, C) in (("g", (self.F, self.D)), ("u", (self.F, self.D)), ("d", (self.D, self.F))):
+            nq = _lib.moe_mxfp4_packed_qs_bytes(self.E, R, C)
+            ns = _lib.moe_mxfp4_packed_sf_bytes(self.E, R, C)
+            if nq == 0 or ns == 0:
+                raise _lib.MoeError(f"shape ({self.E}, {R}, {C}) cannot be prepacked")
+            qs_p = torch.empty(nq, dtype=torch.uint8, device=self.device)
+            sf_p = torch.empty(ns, dtype=torch.uint8, device=self.device)
+            _lib.check(_lib.moe_mxfp4_prepack(self.w[m + "_qs"], self.w[m + "_sc"], self.E, R, C, qs_p, sf_p),
+                       "moe_mxfp4_prepack")
+            pk[m + "_qs"], pk[m + "_sf"] = qs_p, sf_p
+        self.packed = pk
+        w = self.w
+        self.packed_struct = _lib.make_packed_layer(self.D, self.F, self.E, self.k, w["w_router"], w["b_router"],
+                                                    pk["g_qs"], pk["g_sf"], w["bg"], pk["u_qs"], pk["u_sf"],
+                                                    w["bu"], pk["d_qs"], pk["d_sf"], w["bd"])
+
+    def _use_packed(self, T: int, rail: int) -> bool:
+        return self.packed is not None and (rail == _lib.MOE_RAIL_DECODE_MX or
+                                            (rail == _lib.MOE_RAIL_AUTO and T <= _lib.MOE_GEMV_MAX_T))
 
     def workspace(self, T: int, rail: int) -> torch.Tensor:
-        n = _lib.moe_ffn_workspace_bytes(T, self.D, self.F, self.E, self.k, rail)
+        if self._use_packed(T, rail):
+            n = _lib.moe_ffn_packed_workspace_bytes(T, self.D, self.F, self.E, self.k, rail)
+        else:
+            n = _lib.moe_ffn_workspace_bytes(T, self.D, self.F, self.E, self.k, rail)
         if n == 0 and T > 0:
-            raise _lib.MoeError("invalid shape for moe_ffn_workspace_bytes")
-        key = (n, rail)
+            raise _lib.MoeError("invalid shape for the layer's workspace")
+        key = (n, rail, self._use_packed(T, rail))
         buf = self._ws.get(key)
         if buf is None:
             buf = torch.empty(max(n, 256), dtype=torch.uint8, device=self.device)
@@ -54,11 +87,16 @@ class MoeLayer:
 
     def forward(self, x: torch.Tensor, rail: int = _lib.MOE_RAIL_AUTO, out: Optional[torch.Tensor] = None,
                 ids_out: Optional[torch.Tensor] = None, weights_out: Optional[torch.Tensor] = None,
-                stream=None) -> torch.Tensor:
+                stream=None, h_out: Optional[torch.Tensor] = None) -> torch.Tensor:
         T = x.shape[0]
         if out is None:
             out = torch.empty((T, self.D), dtype=torch.float32, device=self.device)
         ws = self.workspace(T, rail)
+        if self._use_packed(T, rail):
+            rc = _lib.moe_ffn_layer_packed(self.packed_struct, x, T, rail, ws, ws.numel(), out, ids_out,
+                                           weights_out, h_out, stream)
+            _lib.check(rc, "moe_ffn_layer_packed")
+            return out
         w = self.w
         rc = _lib.moe_ffn_layer(x, T, self.D, self.F, self.E, self.k, w["w_router"], w["b_router"],
                                 w["g_qs"], w["g_sc"], w["bg"], w["u_qs"], w["u_sc"], w["bu"],
@@ -82,6 +120,12 @@ class MoeLayer:
             y_host = torch.empty((T, self.D), dtype=torch.float32, pin_memory=True)
         if y_host.device.type != "cpu" or y_host.dtype != torch.float32 or not y_host.is_contiguous():
             raise ValueError("y_host must be a contiguous float32 CPU tensor")
+        if self._use_packed(T, rail):
+            ws = self.workspace(T, rail)
+            rc = _lib.moe_ffn_layer_packed_hostio(self.packed_struct, T, rail, ws, ws.numel(), x_host, y_host,
+                                                  stream)
+            _lib.check(rc, "moe_ffn_layer_packed_hostio")
+            return y_host
         key = (T, rail)
         io = self._io.get(key)
         if io is None:  # staging buffers and the fixed arguments, once per (T, rail)

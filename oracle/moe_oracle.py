@@ -257,6 +257,58 @@ def split_e4m3_terms(v: np.ndarray, nterms: int) -> np.ndarray:
     return total.reshape(shape)
 
 
+E2M1_MAX = 6.0
+
+
+def round_e2m1(a: np.ndarray) -> np.ndarray:
+    """Round to the nearest E2M1 value, ties to the even code (mantissa bit 0), saturating at +-6.
+
+    The E2M1 magnitudes are {0, 0.5, 1, 1.5, 2, 3, 4, 6} (the table of the
+    pages' MXFP4 format): a multiple of 0.5 below 2, of 1 in [2, 4) and of 2 in
+    [4, 6]. Codes with an even mantissa are 0, 1, 2, 4 (and 6 has an odd one),
+    so a tie between two neighbours goes to 0, 1, 2 or 4.
+    """
+    a = np.asarray(a, np.float64)
+    mag = np.abs(a)
+    q = np.where(mag < 2.0, 0.5, np.where(mag < 4.0, 1.0, 2.0))
+    lo = np.floor(mag / q) * q
+    hi = lo + q
+    frac = mag - lo
+    # lo's code is even when lo is 0, 1, 2 or 4 (0.5, 1.5, 3 and 6 are odd)
+    lo_even = np.isin(lo, (0.0, 1.0, 2.0, 4.0))
+    up = (frac > q / 2) | ((frac == q / 2) & ~lo_even)
+    r = np.minimum(np.where(up, hi, lo), E2M1_MAX)
+    return np.copysign(r, a)
+
+
+def split_e2m1_terms(v: np.ndarray, nterms: int) -> np.ndarray:
+    """The activation operand of the block-scaled decode rail: each block of 32
+    values along the last axis as a sum of nterms E2M1 blocks.
+
+    A reading of the decode precision for that rail (the pages' decode GEMV
+    multiplies float activations; an activation operand in the MXFP4 element
+    format is not on the pages). Term t takes the residual r of the terms
+    before it (r = v for the first), gets the power of two 2^e with the
+    smallest e such that the block's largest |r| / 2^e <= 6 (bounded to
+    E8M0's range [-127, 127]), and is 2^e * round_e2m1(r / 2^e). The values
+    are taken as float32 first. Returns the sum of the terms.
+    """
+    v = np.asarray(v, np.float32).astype(np.float64)
+    shape = v.shape
+    assert shape[-1] % 32 == 0
+    r = v.reshape(shape[:-1] + (shape[-1] // 32, 32))
+    total = np.zeros_like(r)
+    for _ in range(nterms):
+        amax = np.max(np.abs(r), axis=-1, keepdims=True)
+        e = np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 2.0
+        e = np.where(amax > E2M1_MAX * 2.0 ** e, e + 1.0, e)
+        e = np.clip(e, -127.0, 127.0)
+        term = round_e2m1(r / 2.0 ** e) * 2.0 ** e
+        total = total + term
+        r = r - term
+    return total.reshape(shape)
+
+
 # ----------------------------------------------------------------------------
 # Projections and the expert FFN
 # ----------------------------------------------------------------------------
@@ -348,6 +400,48 @@ def moe_layer(layer: Dict[str, np.ndarray], x: np.ndarray, k: int, token_idx=Non
                            operands=operands)[0]
             y[n] += float(weights[t, j]) * o
     return y, ids, weights, logits
+
+
+def moe_layer_decode_terms(layer: Dict[str, np.ndarray], x: np.ndarray, k: int, x_terms: int = 8,
+                           h_terms: int = 8, token_idx=None, cache: Optional[ExpertCache] = None,
+                           fmt: str = "e2m1"):
+    """The operands of the block-scaled decode rail, evaluated in float64.
+
+    A reading of the decode precision for that rail (the pages' decode GEMV
+    multiplies float activations; a low-precision tensor-core operand is not
+    on the pages): x enters gate/up as x_terms terms (fmt "e2m1":
+    split_e2m1_terms, the MXFP4 element format; "e4m3": split_e4m3_terms), and
+    the router weight is folded into the down operand, which is w_j * h_j
+    carried as h_terms terms of the same format, so that
+        y[t] = sum_j ( Wd[e_j] . split(w_j * h_j) + w_j * bd[e_j] )
+    with h_j = swiglu_oai(Wg[e_j] . split(x_t) + bg, Wu[e_j] . split(x_t) + bu).
+    Without the splitting this is the layer itself (the weight distributes over
+    the down projection). Returns (y [n, D], ids, weights, h [n, k, F]).
+    """
+    x = np.asarray(x, np.float32)
+    T = x.shape[0]
+    logits = router_logits(x, layer["w_router"], layer.get("b_router"))
+    ids, weights = topk_softmax(logits, k)
+    if token_idx is None:
+        token_idx = np.arange(T)
+    cache = cache or ExpertCache(layer)
+    D = layer["d_qs"].shape[1]
+    F = layer["g_qs"].shape[1]
+    y = np.zeros((len(token_idx), D), dtype=np.float64)
+    hs = np.zeros((len(token_idx), k, F), dtype=np.float64)
+    split = {"e2m1": split_e2m1_terms, "e4m3": split_e4m3_terms}[fmt]
+    for n, t in enumerate(token_idx):
+        xt = split(x[t:t + 1].astype(np.float64), x_terms)
+        for j in range(k):  # slot order
+            e = int(ids[t, j])
+            Wg, Wu, Wd = cache(e)
+            g = xt @ Wg.T + np.asarray(layer["bg"][e], np.float64)
+            u = xt @ Wu.T + np.asarray(layer["bu"][e], np.float64)
+            h = swiglu_oai(g, u)
+            hs[n, j] = h[0]
+            hw = split(float(weights[t, j]) * h, h_terms)
+            y[n] += (hw @ Wd.T)[0] + float(weights[t, j]) * np.asarray(layer["bd"][e], np.float64)
+    return y, ids, weights, hs
 
 
 # ----------------------------------------------------------------------------

@@ -14,7 +14,8 @@ FAKE = 1 << 20  # a non-null, 256-byte aligned pointer value that is never deref
 
 def test_library_exports_every_declared_symbol(moe):
     names = moe._lib.declared_functions()
-    assert len(names) == 17
+    assert len(names) == 24
+    assert set(names) <= set(moe._lib._SIGS), "every declared function has a binding"
     for n in names:
         assert hasattr(moe._lib._lib, n), n
 
@@ -149,3 +150,31 @@ def test_hostio_rejects_missing_arguments(moe):
     assert moe.moe_ffn_layer_hostio(args, 0, 0, 0) == moe.MOE_EINVAL  # no host or staging buffers
     args.T = 0
     assert moe.moe_ffn_layer_hostio(args, 0, 0, 0) == moe.MOE_OK      # nothing to do
+
+
+def test_packed_sizes(moe):
+    # qs_p: E * R * ceil(C/128) * 64 bytes; sf_p: one 512-byte atom per 128-row tile and 128-column chunk
+    assert moe.moe_mxfp4_packed_qs_bytes(32, 2880, 2880) == 32 * 2880 * 23 * 64  # rows padded to 128-column chunks
+    assert moe.moe_mxfp4_packed_sf_bytes(32, 2880, 2880) == 32 * 23 * 23 * 512
+    assert moe.moe_mxfp4_packed_qs_bytes(3, 192, 320) == 3 * 192 * 3 * 64
+    assert moe.moe_mxfp4_packed_sf_bytes(3, 192, 320) == 3 * 2 * 3 * 512
+    assert moe.moe_mxfp4_packed_qs_bytes(3, 100, 320) == 0
+    assert moe.moe_mxfp4_packed_sf_bytes(3, 192, 48) == 0
+    assert moe.moe_ffn_packed_workspace_bytes(1, 2880, 2880, 32, 4, moe.MOE_RAIL_AUTO) > 0
+    assert moe.moe_ffn_packed_workspace_bytes(1, 2880, 2880, 32, 4, moe.MOE_RAIL_DECODE_MX) % 256 == 0
+    assert moe.moe_ffn_packed_workspace_bytes(9, 2880, 2880, 32, 4, moe.MOE_RAIL_AUTO) == 0
+
+
+def test_packed_layer_rejects_on_the_host(moe):
+    L = moe.make_packed_layer(2880, 2880, 32, 4, FAKE, None, FAKE, FAKE, None, FAKE, FAKE, None, FAKE, FAKE, None)
+    n = moe.moe_ffn_packed_workspace_bytes(1, 2880, 2880, 32, 4, moe.MOE_RAIL_AUTO)
+    assert moe.moe_ffn_layer_packed(None, FAKE, 1, 0, FAKE, n, FAKE, stream=0) == moe.MOE_EINVAL
+    assert moe.moe_ffn_layer_packed(L, FAKE, 1, 0, FAKE, n - 256, FAKE, stream=0) == moe.MOE_EINVAL
+    assert moe.moe_ffn_layer_packed(L, FAKE + 8, 1, 0, FAKE, n, FAKE, stream=0) == moe.MOE_EINVAL
+    L.g_qs = FAKE + 16  # prepacked planes must be 32-byte aligned for the copy engine
+    assert moe.moe_ffn_layer_packed(L, FAKE, 1, 0, FAKE, n, FAKE, stream=0) == moe.MOE_EINVAL
+    L.g_qs = FAKE
+    L.D = 2880 + 32
+    assert moe.moe_ffn_layer_packed(L, FAKE, 1, 0, FAKE, n, FAKE, stream=0) == moe.MOE_EINVAL
+    L.D = 2880
+    assert moe.moe_ffn_layer_packed(L, FAKE, 0, 0, FAKE, n, FAKE, stream=0) == moe.MOE_OK

@@ -11,12 +11,15 @@ from tests.test_oracle_pins import (
     check_bias_linearity,
     check_bucket_max_rows,
     check_bucket_vs_brute,
+    check_decode_terms_layer,
     check_dequant_vs_brute,
     check_e2m1,
     check_layer_vs_brute,
+    check_round_e2m1,
     check_round_e4m3,
     check_routing_margins,
     check_rownorm_rel_err,
+    check_split_e2m1_vs_brute,
     check_split_vs_brute,
     check_swiglu_points,
     check_topk_vs_brute,
@@ -34,6 +37,8 @@ def test_pins_pass_on_the_real_oracle():
     assert check_routing_margins(O.routing_margins)
     assert check_rownorm_rel_err(O.rownorm_rel_err)
     assert check_bucket_max_rows(O.bucket_max_rows)
+    assert check_round_e2m1(O.round_e2m1)
+    assert check_split_e2m1_vs_brute(O.split_e2m1_terms)
 
 
 def test_e2m1_subnormal_mistake_is_caught():
@@ -286,3 +291,71 @@ def test_max_rows_without_the_expert_padding_is_caught():
     def bad(T, k, E, tile):
         return -(-(T * k) // tile) * tile
     assert not check_bucket_max_rows(bad)
+
+
+def test_decode_terms_with_the_weight_applied_twice_are_caught():
+    def bad(layer, x, k, x_terms=8, h_terms=8):
+        y, ids, w, h = O.moe_layer_decode_terms(layer, x, k, x_terms, h_terms)
+        # the combine multiplies by w again although the operand already carries it
+        y2 = np.zeros_like(y)
+        for t in range(x.shape[0]):
+            for j in range(k):
+                e = int(ids[t, j])
+                Wd = O.dequant_mxfp4(layer["d_qs"][e], layer["d_sc"][e])
+                hw = O.split_e2m1_terms(w[t, j] * h[t:t + 1, j], h_terms)
+                y2[t] += w[t, j] * ((hw @ Wd.T)[0] + layer["bd"][e])
+        return y2, ids, w, h
+    assert not check_decode_terms_layer(bad)
+
+
+def test_decode_terms_without_the_gate_bias_are_caught():
+    def bad(layer, x, k, x_terms=8, h_terms=8):
+        L = dict(layer)
+        L["bg"] = np.zeros_like(layer["bg"])
+        return O.moe_layer_decode_terms(L, x, k, x_terms, h_terms)
+    assert not check_decode_terms_layer(bad)
+
+
+def test_e2m1_ties_away_from_zero_are_caught():
+    def bad(a):
+        a = np.asarray(a, np.float64)
+        mag = np.abs(a)
+        q = np.where(mag < 2.0, 0.5, np.where(mag < 4.0, 1.0, 2.0))
+        return np.copysign(np.minimum(np.floor(mag / q + 0.5) * q, 6.0), a)
+    assert not check_round_e2m1(bad)
+
+
+def test_e2m1_without_saturation_is_caught():
+    def bad(a):
+        a = np.asarray(a, np.float64)
+        mag = np.abs(a)
+        q = np.where(mag < 2.0, 0.5, np.where(mag < 4.0, 1.0, 2.0))
+        lo = np.floor(mag / q) * q
+        frac = mag - lo
+        even = np.isin(lo, (0.0, 1.0, 2.0, 4.0))
+        up = (frac > q / 2) | ((frac == q / 2) & ~even)
+        return np.copysign(np.where(up, lo + q, lo), a)  # 7.0 stays 8.0
+    assert not check_round_e2m1(bad)
+
+
+def test_e2m1_term_scale_one_step_too_small_is_caught():
+    # 2^e with max|r| / 2^e in (6, 12]: the largest values saturate at 6
+    def bad(v, nterms):
+        v = np.asarray(v, np.float32).astype(np.float64)
+        shape = v.shape
+        r = v.reshape(shape[:-1] + (shape[-1] // 32, 32))
+        total = np.zeros_like(r)
+        for _ in range(nterms):
+            amax = np.max(np.abs(r), axis=-1, keepdims=True)
+            e = np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 2.0
+            e = np.clip(e - (amax <= 6.0 * 2.0 ** e), -127.0, 127.0)
+            term = O.round_e2m1(r / 2.0 ** e) * 2.0 ** e
+            total, r = total + term, r - term
+        return total.reshape(shape)
+    assert not check_split_e2m1_vs_brute(bad)
+
+
+def test_e2m1_terms_without_residual_are_caught():
+    def bad(v, nterms):
+        return O.split_e2m1_terms(v, 1) * nterms
+    assert not check_split_e2m1_vs_brute(bad)

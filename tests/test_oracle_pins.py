@@ -206,6 +206,94 @@ def check_bucket_max_rows(bucket_max_rows):
     return True
 
 
+
+def check_decode_terms_layer(layer_fn):
+    """With enough terms to hold every bit of the float32 operands the decode
+    rail's operand model is the layer itself (the router weight distributes over
+    the down projection); with five terms it stays within its 2^-20 bound."""
+    spec = spec_for(0)
+    L = make_layer(spec, layer=5)
+    y_ref, ids_ref, w_ref, _ = O.moe_layer(L, L["x"], spec.k)
+    y8, ids, w, h8 = layer_fn(L, L["x"], spec.k, x_terms=13, h_terms=13)  # 13 E2M1 terms hold a float32
+    if not np.array_equal(ids, ids_ref) or np.max(O.rownorm_rel_err(y8, y_ref, floor=1e-300)) > 1e-6:
+        return False
+    # h of each slot against the float64 expert (x in eight terms is x itself)
+    for t in range(L["x"].shape[0]):
+        for j in range(spec.k):
+            e = int(ids[t, j])
+            g = L["x"][t].astype(np.float64) @ O.dequant_mxfp4(L["g_qs"][e], L["g_sc"][e]).T + L["bg"][e]
+            u = L["x"][t].astype(np.float64) @ O.dequant_mxfp4(L["u_qs"][e], L["u_sc"][e]).T + L["bu"][e]
+            if np.max(np.abs(h8[t, j] - O.swiglu_oai(g, u))) > 1e-9 * max(1.0, np.abs(h8[t, j]).max()):
+                return False
+    y5, _, _, _ = layer_fn(L, L["x"], spec.k)
+    return bool(np.max(O.rownorm_rel_err(y5, y_ref)) < 1e-4)
+
+
+
+def e2m1_magnitudes():
+    """The 8 non-negative E2M1 magnitudes by code, from the printed table."""
+    gold = load_e2m1_golden()
+    return [gold[c] for c in range(8)]
+
+
+def brute_round_e2m1(v):
+    """Nearest E2M1 value by exhaustive search over the 16 codes, ties to the code with mantissa bit 0."""
+    gold = load_e2m1_golden()
+    best = None
+    for c in range(16):
+        val = gold[c]
+        if (val < 0) != (v < 0 or (v == 0 and math.copysign(1.0, v) < 0)) and val != 0:
+            continue
+        d = abs(v - val)
+        key = (d, c & 1)  # nearer first, then even mantissa
+        if best is None or key < best[0]:
+            best = (key, val)
+    mag = min(abs(best[1]), 6.0)
+    return math.copysign(mag, v)
+
+
+def e2m1_probe_values():
+    vals = [0.0, 0.1, 0.24, 0.25, 0.26, 0.5, 0.74, 0.75, 0.76, 1.0, 1.25, 1.3, 1.5, 1.75, 1.8, 2.0, 2.49,
+            2.5, 2.51, 3.0, 3.5, 3.9, 4.0, 4.9, 5.0, 5.1, 6.0, 6.9, 7.0, 100.0]
+    return np.array(vals + [-v for v in vals if v != 0.0])
+
+
+def check_round_e2m1(round_e2m1):
+    v = e2m1_probe_values()
+    got = np.asarray(round_e2m1(v), np.float64)
+    ref = np.array([brute_round_e2m1(float(a)) for a in v])
+    return bool(np.array_equal(got, ref))
+
+
+def brute_split_e2m1_terms(block, nterms):
+    """Pure-Python split of one block of 32 into E2M1 terms: the smallest power of two 2^e with
+    max|r| <= 6 * 2^e, found by counting, and the exhaustive nearest-value search above."""
+    r = [float(np.float32(b)) for b in block]
+    total = [0.0] * 32
+    for _ in range(nterms):
+        amax = max(abs(a) for a in r)
+        e = -127
+        while e < 127 and amax > 6.0 * 2.0 ** e:
+            e += 1
+        terms = [brute_round_e2m1(a / 2.0 ** e) * 2.0 ** e for a in r]
+        total = [t0 + t1 for t0, t1 in zip(total, terms)]
+        r = [a - t for a, t in zip(r, terms)]
+    return total
+
+
+def check_split_e2m1_vs_brute(split_e2m1_terms, seed=8):
+    rng = np.random.default_rng(seed)
+    for scale in (1e-30, 1e-3, 1.0, 37.0, 3e4):
+        blocks = (rng.standard_normal((3, 32)) * scale).astype(np.float32)
+        blocks[1, 5] = 0.0
+        for n in (1, 2, 4, 8):
+            got = split_e2m1_terms(blocks, n)
+            ref = np.array([brute_split_e2m1_terms(b, n) for b in blocks])
+            if not np.array_equal(got, ref):
+                return False
+    return True
+
+
 # ---------------------------------------------------------------------------
 # tests
 # ---------------------------------------------------------------------------
@@ -595,3 +683,38 @@ def test_rownorm_rel_err_closed_form():
 
 def test_bucket_max_rows_hand_values_and_bound():
     assert check_bucket_max_rows(O.bucket_max_rows)
+
+
+def test_decode_terms_layer_reduces_to_the_layer():
+    assert check_decode_terms_layer(O.moe_layer_decode_terms)
+
+
+def test_round_e2m1_matches_exhaustive_search():
+    assert check_round_e2m1(O.round_e2m1)
+    # every E2M1 value is a fixed point
+    vals = np.array(e2m1_magnitudes() + [-m for m in e2m1_magnitudes()[1:]])
+    assert np.array_equal(O.round_e2m1(vals), vals)
+
+
+def test_split_e2m1_terms_matches_brute_force():
+    assert check_split_e2m1_vs_brute(O.split_e2m1_terms)
+
+
+def test_split_e2m1_terms_converges():
+    # 13 terms hold every bit of a float32 block (each term takes >= 2 bits of the
+    # residual's leading value); fewer terms stay within their own residual bound
+    x = np.random.default_rng(3).standard_normal((16, 256)).astype(np.float32)
+    assert np.array_equal(O.split_e2m1_terms(x, 13), x.astype(np.float64))
+    for n in (2, 4, 8):
+        err = np.abs(O.split_e2m1_terms(x, n) - x).reshape(16, 8, 32).max(-1)
+        amax = np.abs(x).reshape(16, 8, 32).max(-1)
+        assert np.all(err <= amax * 3.0 ** -n), n
+
+
+def test_decode_terms_layer_in_both_formats():
+    spec = spec_for(0)
+    L = make_layer(spec, layer=6)
+    y_ref, _, _, _ = O.moe_layer(L, L["x"], spec.k)
+    for fmt, n in (("e2m1", 8), ("e4m3", 5)):
+        y, _, _, _ = O.moe_layer_decode_terms(L, L["x"], spec.k, x_terms=n, h_terms=n, fmt=fmt)
+        assert np.max(O.rownorm_rel_err(y, y_ref)) < 1e-5, fmt
