@@ -346,7 +346,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_expert_kernel(const Dec
   float* vfac = reinterpret_cast<float*>(vwords + (A.staged ? (size_t)nvec * nb * 32 : 0));
   float* s_o = vfac + (A.staged ? nvec * nb : 0);  // down: [team][TK][kDecRows]
 
-  pdl_launch_dependents();
+  // The down kernel releases its dependents at once; the gate/up kernel only
+  // after its wait for the router, so that a down kernel that starts early
+  // finds the router logits complete: it routes and streams its weights
+  // before its own wait (only the split vectors, h, come from gate/up).
+  if (KIND == 1) pdl_launch_dependents();
   if (warp == 0) {
     if (lane == 0) {
       for (int i = 0; i < nstages; ++i) {
@@ -362,7 +366,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_expert_kernel(const Dec
       s_abort = 0;
       tc::fence_mbar_init();
     }
-    pdl_wait();  // router logits come from the previous kernel
+    if (KIND == 0 || !A.logits) pdl_wait();  // gate/up: router logits come from the previous kernel
     routing_inputs(Rt, T, k, E, lane, A.logits, A.ids_in, A.w_in);
     build_routing(Rt, TK, E, lane, KIND == 0 ? A.status : nullptr);
     if (KIND == 0 && blockIdx.x == 0 && A.ids_out)
@@ -370,13 +374,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_expert_kernel(const Dec
         A.ids_out[a] = Rt.ids[a];
         if (A.w_out) A.w_out[a] = Rt.w[a];
       }
-  } else {
-    // x is the layer's input (unless the router copies it there); h (down) comes
-    // from the previous kernel
-    if (KIND == 1 || A.vec_wait) pdl_wait();
-    if (A.staged) stage_split_vectors(A.vec, nvec, C, vwords, vfac, threadIdx.x - 32, kDecThreads - 32);
   }
   __syncthreads();
+  if (KIND == 0) pdl_launch_dependents();
   const int nact = Rt.nact;
   if (nact == 0) {
     // No valid assignment: the down kernel still owes y = 0.
@@ -439,6 +439,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_expert_kernel(const Dec
   }
 
   // ---------------- consumers ----------------
+  // x is the layer's input (unless the router copies it there); h (down) comes
+  // from the previous kernel. The split vectors go to shared memory for all
+  // consumer warps (a named barrier over them: the producer is already streaming).
+  if (KIND == 1 || A.vec_wait) pdl_wait();
+  if (A.staged) {
+    stage_split_vectors(A.vec, nvec, C, vwords, vfac, threadIdx.x - 32, kDecThreads - 32);
+    tc::named_sync(1, kDecThreads - 32);
+  }
   const int cw = warp - 1;
   const int team = cw / tw, wt = cw - team * tw;
   if (team >= nteams) return;

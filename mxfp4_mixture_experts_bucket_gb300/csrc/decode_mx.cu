@@ -25,15 +25,15 @@
 // bumps the tile's counter, and the last one adds the partials in CTA order
 // (deterministic) and runs the epilogue. Nothing ever waits for another CTA.
 //   gate/up unit = (routed expert, 128-row tile of F); epilogue: bias, swiglu_oai,
-//     the router weight, and the down operand: w*h as E4M3 terms, written in
+//     the router weight, and the down operand: w*h as E2M1 terms, written in
 //     the operand-chunk layout of decode_mx.cuh (one chunk per tile).
 //   down unit = 128-row tile of D, steps over (routed expert, chunk of F): all
 //     experts of a token accumulate into the same columns (w is folded into the
 //     operand), epilogue: + sum_j w_j bd[e_j] in slot order, y stored.
 //
-// Warps: 0..5 = producers (warp 0 also builds the routing table), 6 = tensor-
-// memory owner and MMA issuer, 7..10 = scale loaders, then epilogue (one per
-// tensor-memory lane quarter). The scale atoms go from shared memory into
+// Warps: 0..5 = producers (warp 0 also builds the routing table), 6 = MMA
+// issuer, 7..10 = scale loaders and epilogue (one per tensor-memory lane
+// quarter; warp 7 also allocates and frees tensor memory). The scale atoms go from shared memory into
 // tensor memory through the epilogue warps' registers (tcgen05.st): a
 // tcgen05.cp would take ~80 tensor-pipe cycles per atom, and a step's six
 // atoms cost as much pipe time as its eight MMAs (measured). The copy engine serves the bulk copies one issuing thread makes in
@@ -55,9 +55,11 @@ namespace dmx {
 
 constexpr int kProd = 6;  // producer warps 0..5, one copy of each step apiece
 constexpr int kMmaWarp = 6;
+constexpr int kTmemWarp = 7;  // the first epilogue warp allocates and frees tensor memory
 constexpr int kThreads = 11 * 32;
 constexpr int kMaxStages = 6;
 constexpr int kMaxAccSlots = 4;
+constexpr int kScaleBatch = 4;  // steps whose scales one tensor-memory store wait covers (< stages)
 constexpr int kATile = 8192;    // one 128-row x 128-column tile of E2M1 codes (64 bytes a row)
 constexpr int kAtom = 512;
 constexpr uint32_t kTmemCols = 512;
@@ -182,6 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t accf_bar[kMaxAccSlots];
   __shared__ __align__(8) uint64_t acce_bar[kMaxAccSlots];
   __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ __align__(8) uint64_t tfree_bar;  // the epilogue warps and the MMA thread are done with tensor memory
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
 
@@ -190,7 +193,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int AS = p.acc_slots;
   const int T = p.T, k = p.k, E = p.E, R = p.R;
 
-  pdl_launch_dependents();
+  // The down kernel may start once every gate/up CTA has passed its wait for
+  // the prologue, so the routing inputs (prologue output) are complete by then
+  // and the down kernel routes, and streams its weights, before its own wait.
+  if (KIND == 1) pdl_launch_dependents();
   if (warp == 1 && lane == 0) {
     for (int i = 0; i < NS; ++i) {
       tc::mbar_init(tc::smem_u32(&full_bar[i]), kProd);
@@ -202,11 +208,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(tc::smem_u32(&acce_bar[i]), 4);
     }
     tc::mbar_init(tc::smem_u32(&drain_bar), 1);
+    tc::mbar_init(tc::smem_u32(&tfree_bar), 5);
     s_abort = 0;
     tc::fence_mbar_init();
   }
-  if (warp == kMmaWarp) tc::tmem_alloc(tc::smem_u32(&s_tmem), kTmemCols);
-  pdl_wait();  // logits, the activation operand and the zeroed counters come from earlier kernels
+  if (warp == kTmemWarp) tc::tmem_alloc(tc::smem_u32(&s_tmem), kTmemCols);
+  if (KIND == 0) {
+    pdl_wait();  // logits, the activation operand and the zeroed counters come from the prologue
+    pdl_launch_dependents();
+  }
   if (warp == 0) {
     routing_inputs(Rt, T, k, E, lane, p.logits, nullptr, nullptr);
     build_routing(Rt, T * k, E, lane, KIND == 0 ? p.status : nullptr);
@@ -235,7 +245,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sf_chunk = 4 * (NMAT + 1), sfw = (uint32_t)SC * sf_chunk;
 
   if (total == 0) {
-    // no valid assignment: y = 0 (the down kernel owes it)
+    // no valid assignment: y = 0 (the down kernel owes it, after the gate/up
+    // kernel, so that the grid still ends after its predecessor)
+    if (KIND == 1) pdl_wait();
     if (KIND == 1)
       for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < T * R; i += gridDim.x * blockDim.x) p.y[i] = 0.f;
   } else if (cta < G) {
@@ -253,6 +265,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       report_timeout(p.status, 5 + KIND, role, 0, seq);
     };
 
+    // Down kernel: the weight producers (warps 0 .. 1 + NMAT) stream before the
+    // gate/up kernel has finished; every other role reads its output (the
+    // activation operand) or follows those that do.
+    if (KIND == 1 && warp >= 2 + NMAT) pdl_wait();
     if (warp < kProd) {
       // ------------------------------------------------ producers
       if (lane == 0) {
@@ -351,38 +367,40 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int slot = lu % AS;
           const uint32_t sb = tc::smem_u32(smem) + (uint32_t)st * p.stage_bytes;
           const uint32_t sfs = tmem + sf0 + (uint32_t)st * sfw;
-          // Everything per MMA below is a compile-time offset from these: the issuing
-          // thread must keep up with one MMA every ~85 cycles.
-          // 64-byte-swizzled operands, rows of one chunk; a K half is 32 bytes on
+          // 64-byte-swizzled operands; a chunk's K halves are 32 bytes apart. The
+          // issue loop stays compact (one K half of every matrix per pass, the
+          // descriptors advanced by adding to their start-address field, which
+          // holds shared-memory address / 16 and cannot carry out of its 14
+          // bits below 256 KB).
           const int rows_t = min(128, R - 128 * tile);
-          const uint32_t bstride = (uint32_t)(p.npad * 64);
           const uint32_t dacc = tmem + (uint32_t)slot * acc_cols;
-          const int nkb_last = min(4, nbc - 4 * (j0 + nch - 1));
+          const int nkb_last = min(4, nbc - 4 * (j0 + nch - 1));  // even: widths are multiples of 64
+          const int nkh = 2 * (nch - 1) + nkb_last / 2;
+          const uint64_t adesc0 = tc::sw64_kmajor_desc(sb);
+          const uint64_t bdesc0 = tc::sw64_kmajor_desc(sb + p.off_b);
+          const uint32_t a_c16 = (uint32_t)(rows_t * 64) >> 4, b_c16 = (uint32_t)(p.npad * 64) >> 4;
+          constexpr uint32_t kAMat16 = (uint32_t)(SCMAX * kATile) >> 4;
+#pragma unroll 1
+          for (int x = 0; x < nkh; ++x) {
+            const uint32_t c = (uint32_t)x >> 1, kh = (uint32_t)x & 1u;
+            const uint64_t ad = adesc0 + (c * a_c16 + 2u * kh);
+            const uint64_t bd = bdesc0 + (c * b_c16 + 2u * kh);
+            const uint32_t id = idesc | (kh ? ((2u << 4) | (2u << 29)) : 0u);  // scale bytes 2kh, 2kh+1
+            const uint32_t sfc = sfs + c * sf_chunk;
+            const uint32_t acc = (first && x == 0) ? 0u : 1u;
 #pragma unroll
-          for (int c = 0; c < SCMAX; ++c)
-            if (c < nch) {
-              const int nkb = (c == nch - 1) ? nkb_last : 4;
-              const uint32_t a_chunk = (uint32_t)(rows_t * 64 * c);
-              const uint32_t b_chunk = sb + p.off_b + (uint32_t)c * bstride;
-#pragma unroll
-              for (int kh = 0; kh < 2; ++kh)
-                if (2 * kh < nkb) {  // blocks 2kh, 2kh+1 (the width is a multiple of 64)
-                  const uint32_t sfid = ((uint32_t)(2 * kh) << 4) | ((uint32_t)(2 * kh) << 29);
-                  const uint64_t bdesc = tc::sw64_kmajor_desc(b_chunk + 32 * kh);
-#pragma unroll
-                  for (int m = 0; m < NMAT; ++m)
-                    mma_mxf4(dacc + (uint32_t)(m * p.npad),
-                             tc::sw64_kmajor_desc(sb + (uint32_t)(m * SC * kATile) + a_chunk + 32 * kh), bdesc,
-                             idesc | sfid, sfs + c * sf_chunk + 4 * m, sfs + c * sf_chunk + 4 * NMAT,
-                             (first && c == 0 && kh == 0) ? 0u : 1u);
-                }
-            }
+            for (int m = 0; m < NMAT; ++m)
+              mma_mxf4(dacc + (uint32_t)(m * p.npad), ad + (uint64_t)(m * kAMat16), bd, id, sfc + 4 * m,
+                       sfc + 4 * NMAT, acc);
+          }
           tc::mma_commit(tc::smem_u32(&empty_bar[st]));
           if (last) tc::mma_commit(tc::smem_u32(&accf_bar[slot]));
         }
         // every MMA issued above completes before tensor memory is released
         tc::mma_commit(tc::smem_u32(&drain_bar));
         tc::mbar_wait(tc::smem_u32(&drain_bar), 0, nullptr);
+        tc::fence_before_sync();
+        tc::mbar_arrive(tc::smem_u32(&tfree_bar));
       }
     } else {
       // ------------------------------------------------ epilogue (warps 5..8)
@@ -402,36 +420,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       int i = 0, lu_steps = -1, ldone = 0;
       while (ldone < nunits_cta) {
         const bool step_left = i < nsteps;
-        const int next_lu = lu_steps + ((step_left && (i == 0 || sp.s == 0)) ? 1 : 0);
+        int next_lu = lu_steps + ((step_left && (i == 0 || sp.s == 0)) ? 1 : 0);
         if (step_left && next_lu < ldone + AS) {
-          // ---- the scales of step i
-          lu_steps = next_lu;
-          const int st = i % NS, n = i / NS;
-          bool ok = tc::mbar_wait(tc::smem_u32(&full_bar[st]), n & 1, abort_flag);
-          if (!__all_sync(0xffffffffu, ok)) {
-            if (lane == 0) fail(3, i);
-            break;
-          }
-          int ai, tile, j0, nch;
-          step_cover<KIND>(sp, NT, NK, nkc, SC, ai, tile, j0, nch);
-          const uint8_t* sbp = smem + (size_t)st * p.stage_bytes;
-          const uint32_t sfs = lane_base + sf0 + (uint32_t)st * sfw;
-#pragma unroll
-          for (int c = 0; c < SCMAX; ++c)
-            if (c < nch) {
-#pragma unroll
-              for (int m = 0; m <= NMAT; ++m) {  // weight atoms, then the activation atom
-                const uint8_t* atom = sbp + (m < NMAT ? p.off_sfa + (m * SC + c) * kAtom : p.off_sfb + c * kAtom);
-                const uint4 w = *reinterpret_cast<const uint4*>(atom + 16 * lane);
-                tc::tmem_st4(sfs + c * sf_chunk + 4 * m, w.x, w.y, w.z, w.w);
+          // ---- the scales of step i, and of the steps after it whose data has
+          // landed too (up to kScaleBatch, each allowed by the rule above): one
+          // wait for the tensor-memory stores per batch
+          uint32_t st_mask = 0;
+          bool failed = false;
+          for (int nbat = 0;;) {
+            lu_steps = next_lu;
+            const int st = i % NS, n = i / NS;
+            if (nbat == 0) {
+              bool ok = tc::mbar_wait(tc::smem_u32(&full_bar[st]), n & 1, abort_flag);
+              if (!__all_sync(0xffffffffu, ok)) {
+                if (lane == 0) fail(3, i);
+                failed = true;
+                break;
               }
             }
+            int ai, tile, j0, nch;
+            step_cover<KIND>(sp, NT, NK, nkc, SC, ai, tile, j0, nch);
+            const uint8_t* sbp = smem + (size_t)st * p.stage_bytes;
+            const uint32_t sfs = lane_base + sf0 + (uint32_t)st * sfw;
+#pragma unroll
+            for (int c = 0; c < SCMAX; ++c)
+              if (c < nch) {
+#pragma unroll
+                for (int m = 0; m <= NMAT; ++m) {  // weight atoms, then the activation atom
+                  const uint8_t* atom = sbp + (m < NMAT ? p.off_sfa + (m * SC + c) * kAtom : p.off_sfb + c * kAtom);
+                  const uint4 w = *reinterpret_cast<const uint4*>(atom + 16 * lane);
+                  tc::tmem_st4(sfs + c * sf_chunk + 4 * m, w.x, w.y, w.z, w.w);
+                }
+              }
+            st_mask |= 1u << st;
+            ++i;
+            advance(sp);
+            if (++nbat == kScaleBatch || i >= nsteps) break;
+            next_lu = lu_steps + (sp.s == 0 ? 1 : 0);
+            if (next_lu >= ldone + AS) break;
+            if (!__all_sync(0xffffffffu, tc::mbar_peek(tc::smem_u32(&full_bar[i % NS]), (i / NS) & 1))) break;
+          }
+          if (failed) break;
           tc::tmem_wait_st();
           tc::fence_before_sync();
           __syncwarp();
-          if (lane == 0) tc::mbar_arrive(tc::smem_u32(&sfr_bar[st]));
-          ++i;
-          advance(sp);
+          if (lane == 0)
+            for (int st = 0; st < NS; ++st)
+              if (st_mask >> st & 1u) tc::mbar_arrive(tc::smem_u32(&sfr_bar[st]));
           continue;
         }
         // ---- the epilogue of unit ldone
@@ -499,18 +534,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int m = 0; m < NMAT; ++m)
 #pragma unroll
             for (int t = 0; t < 8; ++t) v[m][t] = 0.f;
-          for (int cc = cf; cc <= cl; ++cc) {
-            const int pc = (u == (int)(range_lo(cc, total, G) / spu)) ? 0 : 1;
-            const float* src = p.part + (size_t)(cc * 2 + pc) * NMAT * T * 128;
-            float pv[NMAT][8];
+          // the partials of PB CTAs are loaded together, then added in CTA order
+          constexpr int PB = KIND == 0 ? 2 : 4;
+          for (int c0 = cf; c0 <= cl; c0 += PB) {
+            float pv[PB][NMAT][8];
 #pragma unroll
-            for (int m = 0; m < NMAT; ++m)
+            for (int b = 0; b < PB; ++b) {
+              const int cc = c0 + b;
+              const float* src = nullptr;
+              if (cc <= cl) {
+                const int pc = (u == (int)(range_lo(cc, total, G) / spu)) ? 0 : 1;
+                src = p.part + (size_t)(cc * 2 + pc) * NMAT * T * 128;
+              }
 #pragma unroll
-              for (int t = 0; t < 8; ++t) pv[m][t] = t < T ? __ldcg(src + (m * T + t) * 128 + row) : 0.f;
+              for (int m = 0; m < NMAT; ++m)
 #pragma unroll
-            for (int m = 0; m < NMAT; ++m)
+                for (int t = 0; t < 8; ++t) pv[b][m][t] = (src && t < T) ? __ldcg(src + (m * T + t) * 128 + row) : 0.f;
+            }
 #pragma unroll
-              for (int t = 0; t < 8; ++t) v[m][t] += pv[m][t];
+            for (int b = 0; b < PB; ++b)
+#pragma unroll
+              for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+                for (int t = 0; t < 8; ++t) v[m][t] += pv[b][m][t];
           }
         }
 
@@ -549,7 +595,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane < 4) reinterpret_cast<uint32_t*>(chunk + chunk_off(n, q, 0))[lane] = 0u;
             if (lane == 0) atom[atom_off(n, q)] = 127;
           }
-          asm volatile("fence.proxy.async.global;" ::: "memory");  // read next by the copy engine
         } else {
           // ---- down: + sum_j w_j bd[e_j] in slot order, y stored
           const int c = u * 128 + row;
@@ -560,15 +605,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      tc::fence_before_sync();  // this warp's tensor-memory reads are complete
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&tfree_bar));
+      // the down operand written above is read next by the copy engine
+      if (KIND == 0) asm volatile("fence.proxy.async.global;" ::: "memory");
     }
   }
 
-  // Lanes that ran a role alone (lane 0 of the producer and MMA warps) rejoin
-  // their warp first: the CTA barrier counts whole warps.
-  __syncwarp();
-  tc::fence_before_sync();
-  __syncthreads();
-  if (warp == kMmaWarp) {
+  // Tensor memory goes back when the epilogue warps and the MMA thread have
+  // arrived on an mbarrier, freed by warp kTmemWarp, whose code is warp-uniform
+  // throughout. (No CTA-wide barrier here: it would also count warps whose lane
+  // 0 is still in its role loop.) Shared memory lives until every thread has
+  // exited, and every copy issued has landed by then: each is consumed by the
+  // MMAs, or waited for by its producer on abort.
+  if (warp == kTmemWarp) {
+    if (total > 0 && cta < G) tc::mbar_wait_sleep(tc::smem_u32(&tfree_bar), 0, nullptr, 64);
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
   }

@@ -39,6 +39,20 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
+// Non-blocking test of the phase with the given parity (try_wait may suspend
+// the thread for a while before it reports an incomplete phase; test_wait
+// returns at once).
+__device__ __forceinline__ bool mbar_peek(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
 
 // Bounded wait for the phase with the given parity to complete. Returns false
