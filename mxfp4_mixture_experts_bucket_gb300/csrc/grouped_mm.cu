@@ -101,7 +101,8 @@ constexpr int kBEmpty = kBFull + MAX_BS;
 constexpr int kAccFull = kBEmpty + MAX_BS;
 constexpr int kScFull = kAccFull + 1;
 constexpr int kBiasReady = kScFull + 1;
-constexpr int kNumBars = kBiasReady + 1;
+constexpr int kTFree = kBiasReady + 1;  // the epilogue warps and the MMA thread are done with tensor memory
+constexpr int kNumBars = kTFree + 1;
 static_assert(kNumBars <= 64, "barrier space");
 
 // f16x2 (unscaled E2M1 pair) * 2^(s-127) -> bf16x2, exact whenever representable.
@@ -200,10 +201,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::mbar_init(bar(kAccFull), 1);
     tc::mbar_init(bar(kScFull), 1);
     tc::mbar_init(bar(kBiasReady), kDqWarps);
+    tc::mbar_init(bar(kTFree), 2 * kDqWarps + 1);
     *s_abort = 0;
     tc::fence_mbar_init();
   }
-  if (warp == 1) tc::tmem_alloc(tc::smem_u32(s_tmem), NMAT * AW);
+  if (warp == kDqWarp0) tc::tmem_alloc(tc::smem_u32(s_tmem), NMAT * AW);
   if (EPI == MOE_EPI_SCATTER_WEIGHTED_ID) {
     for (int i = threadIdx.x; i < BN; i += kThreads) {
       const int a = (i < live) ? p.rows[tile_row0 + i] : -1;
@@ -312,6 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // completes once every MMA issued above has finished
       tc::mma_commit(bar(kAccFull));
+      tc::mma_commit(bar(kTFree));  // on every path, once the MMAs issued have finished
     }
   } else {
     // ------------------------------------------------ dequant + epilogue
@@ -425,14 +428,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  // Lanes that ran a role alone (lane 0 of the producer and MMA warps) rejoin
-  // their warp first: the CTA barrier counts whole warps.
-  __syncwarp();
-  tc::fence_before_sync();
-  __syncthreads();
-  if (warp == 1) {
-    tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, NMAT * AW);
+  // Tensor memory goes back once every epilogue warp and the MMA thread have
+  // arrived on an mbarrier, freed by warp kDqWarp0, whose code is warp-uniform
+  // throughout. (No CTA-wide barrier: it would also count warps whose lane 0 is
+  // still in its role loop.) Shared memory lives until every thread has exited;
+  // the producers wait for their copies in flight before they leave on an abort.
+  if (warp >= kDqWarp0) {
+    tc::fence_before_sync();
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(bar(kTFree));
+    if (warp == kDqWarp0) {
+      tc::mbar_wait_sleep(bar(kTFree), 0, nullptr, 64);
+      tc::fence_after_sync();
+      tc::tmem_dealloc(tmem, NMAT * AW);
+    }
   }
 }
 
