@@ -71,12 +71,25 @@ extern "C" {
 #define MOE_EPI_SCATTER_WEIGHTED 2 /* out[t][r] += weights[a] * acc, a = rows[p]   */
 
 /* ---- layer rails ---- */
-#define MOE_RAIL_AUTO 0       /* GEMV rail when T <= MOE_GEMV_MAX_T, grouped GEMM otherwise */
+#define MOE_RAIL_AUTO 0       /* by T: see MOE_AUTO_GEMV_MAX_T and MOE_AUTO_MX_MAX_T */
 #define MOE_RAIL_GEMV 1
 #define MOE_RAIL_GROUPED_MM 2
 #define MOE_RAIL_GROUPED_MX 3 /* grouped GEMM on the block-scaled (MXFP4 x E4M3) tensor cores */
 #define MOE_RAIL_DECODE_MX 4  /* T <= MOE_GEMV_MAX_T on the block-scaled tensor cores (prepacked weights) */
 #define MOE_GEMV_MAX_T 8
+/*
+ * MOE_RAIL_AUTO on the canonical planes (moe_ffn_layer and friends) takes the
+ * rail measured fastest on GB300 for the gpt-oss shape (E=32, k=4,
+ * D=F=2880): the CUDA-core GEMV rail for T <= MOE_AUTO_GEMV_MAX_T, the
+ * block-scaled grouped GEMM for T <= MOE_AUTO_MX_MAX_T, the bf16 grouped GEMM
+ * beyond. The rails differ in precision: the GEMV rail is held to 1e-4 of a
+ * float64 reference (row-normwise), the grouped rails to 2e-2; a caller that
+ * needs the tighter bound names MOE_RAIL_GEMV. On prepacked planes
+ * (moe_ffn_layer_packed) MOE_RAIL_AUTO is MOE_RAIL_DECODE_MX for
+ * T <= MOE_GEMV_MAX_T.
+ */
+#define MOE_AUTO_GEMV_MAX_T 3
+#define MOE_AUTO_MX_MAX_T 320
 
 /* Bucket tile height of the grouped-GEMM rail (rows per tensor-core tile). */
 #define MOE_MM_TILE 128
@@ -157,6 +170,19 @@ int moe_mxfp4_gemv(const uint8_t* w_qs, const uint8_t* w_sc, int E, int R, int C
  */
 int moe_swiglu_oai(const float* g, const float* u, void* h, int64_t n, int h_dtype, float alpha,
                    float limit, cudaStream_t stream);
+
+/*
+ * moe_rms_renorm -- y[t][c] = x[t][c] / sqrt(mean over c of x[t][c]^2) for
+ * t < T, c < D (a row of zeros stays zero): the renormalisation between the
+ * layers of a stack of MoE layers, which keeps the hidden state of a deep
+ * stack bounded. It is not a step of the MoE layer: gpt-oss puts an RMSNorm
+ * before each MoE block (its learned gain is not modelled here). x, y: float
+ * [T][D] in device memory, owned by the caller; in place (y == x) is allowed.
+ * The sum of squares is added in a fixed order, so the result is
+ * deterministic. Returns MOE_EINVAL for T < 0, D < 1 or a NULL pointer with
+ * T > 0.
+ */
+int moe_rms_renorm(const float* x, int T, int D, float* y, cudaStream_t stream);
 
 /*
  * moe_gather_rows_bf16 -- activation rows of the grouped GEMM in bucket order:
@@ -264,7 +290,7 @@ int moe_expert_down_combine(const uint8_t* d_qs, const uint8_t* d_sc, const floa
  * scale, each term carrying the rounding residual of the ones before: about
  * 12 and 8 significant bits). Both grouped rails accumulate in fp32 and
  * scatter with float atomics (order not deterministic).
- * MOE_RAIL_AUTO picks GEMV for T <= MOE_GEMV_MAX_T.
+ * MOE_RAIL_AUTO picks by T (MOE_AUTO_GEMV_MAX_T, MOE_AUTO_MX_MAX_T above).
  * x: float [T][D]; w_router [E][D]; b_router [E] or NULL; gate/up planes
  * [E][F][D/2], [E][F][D/32]; down planes [E][D][F/2], [E][D][F/32]; biases
  * bg, bu [E][F], bd [E][D] (each may be NULL); y: float [T][D], overwritten.
@@ -490,6 +516,19 @@ int moe_get_status(cudaStream_t stream, int* status);
  * dequantising or expanding warps). For diagnosis only.
  */
 int moe_get_timeout_site(cudaStream_t stream, int* site);
+
+/*
+ * moe_selftest_wait_timeout -- exercises the failure path of the bounded
+ * pipeline waits without any fault: one CTA lands a 1 KB bulk copy from `src`
+ * (device memory, 16-byte aligned, at least 1024 bytes, only read), holds 32
+ * columns of tensor memory, and waits for an mbarrier that nothing arrives at.
+ * After the wait limit (about 2 s) the kernel sets MOE_STATUS_WAIT_TIMEOUT in
+ * the device status word with the site (15 << 24) | (2 << 20) (see
+ * moe_get_timeout_site), waits for its copy, frees tensor memory and returns;
+ * the context stays usable. Enqueued on `stream` only. Returns MOE_EINVAL for
+ * a NULL or unaligned `src`.
+ */
+int moe_selftest_wait_timeout(const void* src, cudaStream_t stream);
 
 /* moe_last_cuda_error -- the cudaError_t of the last MOE_ECUDA in this thread. */
 int moe_last_cuda_error(void);

@@ -46,6 +46,8 @@ MOE_STAGE_PROLOGUE = 1
 MOE_STAGE_GATEUP = 2
 MOE_STAGE_DOWN = 4
 MOE_GEMV_MAX_T = 8
+MOE_AUTO_GEMV_MAX_T = 3
+MOE_AUTO_MX_MAX_T = 320
 MOE_MM_TILE = 128
 
 P = ctypes.c_void_p
@@ -61,6 +63,8 @@ _SIGS = {
     "moe_bucket": (I, [P, I, I, I, I, P, P, P, P, P]),
     "moe_mxfp4_gemv": (I, [P, P, I, I, I, P, I, P, I64, P, P, P]),
     "moe_swiglu_oai": (I, [P, P, P, I64, I, F, F, P]),
+    "moe_rms_renorm": (I, [P, I, I, P, P]),
+    "moe_selftest_wait_timeout": (I, [P, P]),
     "moe_gather_rows_bf16": (I, [P, I, I, I, P, P, I, I, P, P, P, P]),
     "moe_mxfp4_grouped_mm": (I, [P, P, P, P, P, P, I, I, I, P, P, P, P, P, I, I, P, I, F, F, P, I64, P]),
     "moe_expert_gateup_swiglu": (I, [P, P, P, P, P, P, I, I, I, I, I, P, P, F, F, P, P]),
@@ -149,6 +153,14 @@ def moe_bucket(ids, T, k, E, tile, counts, basep, rows, inv, stream=None):
 def moe_mxfp4_gemv(w_qs, w_sc, E, R, C, experts, n, x, x_stride, bias, out, stream=None):
     return _lib.moe_mxfp4_gemv(_ptr(w_qs), _ptr(w_sc), E, R, C, _ptr(experts), n, _ptr(x), x_stride,
                                _ptr(bias), _ptr(out), _stream(stream))
+
+
+def moe_selftest_wait_timeout(src, stream=None):
+    return _lib.moe_selftest_wait_timeout(_ptr(src), _stream(stream))
+
+
+def moe_rms_renorm(x, T, D, y, stream=None):
+    return _lib.moe_rms_renorm(_ptr(x), T, D, _ptr(y), _stream(stream))
 
 
 def moe_swiglu_oai(g, u, h, n, h_dtype, alpha=1.702, limit=7.0, stream=None):

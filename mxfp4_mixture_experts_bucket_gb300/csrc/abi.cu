@@ -88,7 +88,8 @@ size_t max_rows_of(int T, int k, int E, int tile) {
 }
 
 int resolve_rail(int T, int rail) {
-  if (rail == MOE_RAIL_AUTO) return T <= MOE_GEMV_MAX_T ? MOE_RAIL_GEMV : MOE_RAIL_GROUPED_MM;
+  if (rail == MOE_RAIL_AUTO)
+    return T <= MOE_AUTO_GEMV_MAX_T ? MOE_RAIL_GEMV : T <= MOE_AUTO_MX_MAX_T ? MOE_RAIL_GROUPED_MX : MOE_RAIL_GROUPED_MM;
   return rail;
 }
 
@@ -313,6 +314,26 @@ int moe_swiglu_oai(const float* g, const float* u, void* h, int64_t n, int h_dty
   if (rc != MOE_OK) return rc;
   Launch L{stream, false};
   return cuda_status(launch_swiglu(g, u, h, n, h_dtype, alpha, limit, L));
+}
+
+int moe_selftest_wait_timeout(const void* src, cudaStream_t stream) {
+  MOE_REQUIRE(src && aligned(src, 16));
+  DeviceInfo* d = nullptr;
+  int rc = current_device(&d);
+  if (rc != MOE_OK) return rc;
+  Launch L{stream, false};
+  return cuda_status(launch_selftest_wait_timeout(static_cast<const uint8_t*>(src), d->status, L));
+}
+
+int moe_rms_renorm(const float* x, int T, int D, float* y, cudaStream_t stream) {
+  MOE_REQUIRE(T >= 0 && D >= 1);
+  if (T == 0) return MOE_OK;
+  MOE_REQUIRE(x && y);
+  DeviceInfo* d = nullptr;
+  int rc = current_device(&d);
+  if (rc != MOE_OK) return rc;
+  Launch L{stream, false};
+  return cuda_status(launch_rms_renorm(x, T, D, y, L));
 }
 
 int moe_gather_rows_bf16(const float* x, int T, int D, int k, const int32_t* rows,

@@ -148,4 +148,36 @@ cudaError_t launch_swiglu(const float* g, const float* u, void* h, int64_t n, in
                        alpha, limit);
 }
 
+// ---------------------------------------------------------------------------
+// RMS renormalisation of token rows, y[t] = x[t] / sqrt(mean_c x[t][c]^2) (a
+// zero row stays zero): the step between the layers of a stack of MoE layers.
+// One block per row; the sum of squares is added in a fixed order (strided
+// per-thread sums, then a tree over the threads), so the result is
+// deterministic. In place is allowed.
+// ---------------------------------------------------------------------------
+constexpr int kRmsThreads = 256;
+__global__ void __launch_bounds__(kRmsThreads) rms_renorm_kernel(const float* x, int D, float* y) {
+  __shared__ float part[kRmsThreads];
+  pdl_launch_dependents();
+  pdl_wait();
+  const float* xr = x + (size_t)blockIdx.x * D;
+  float* yr = y + (size_t)blockIdx.x * D;
+  float s = 0.f;
+  for (int c = threadIdx.x; c < D; c += kRmsThreads) s = fmaf(xr[c], xr[c], s);
+  part[threadIdx.x] = s;
+  __syncthreads();
+  for (int w = kRmsThreads / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) part[threadIdx.x] += part[threadIdx.x + w];
+    __syncthreads();
+  }
+  const float mean = part[0] / (float)D;
+  const float inv = mean > 0.f ? 1.f / sqrtf(mean) : 0.f;
+  for (int c = threadIdx.x; c < D; c += kRmsThreads) yr[c] = xr[c] * inv;
+}
+
+cudaError_t launch_rms_renorm(const float* x, int T, int D, float* y, Launch L) {
+  if (T <= 0) return cudaSuccess;
+  return launch_kernel(rms_renorm_kernel, dim3(T), dim3(kRmsThreads), 0, L, x, D, y);
+}
+
 }  // namespace moe

@@ -78,6 +78,8 @@ cudaError_t launch_gather_bf16(const float* x, int T, int D, int k, const int32_
 cudaError_t launch_mxfp4_gemv(const uint8_t* qs, const uint8_t* sc, int E, int R, int C,
                               const int32_t* experts, int n, const float* x, int64_t x_stride,
                               const float* bias, float* out, int* status, Launch L);
+cudaError_t launch_selftest_wait_timeout(const uint8_t* src, int* status, Launch L);
+cudaError_t launch_rms_renorm(const float* x, int T, int D, float* y, Launch L);
 cudaError_t launch_swiglu(const float* g, const float* u, void* h, int64_t n, int h_dtype,
                           float alpha, float limit, Launch L);
 

@@ -68,8 +68,18 @@ class MoeLayer:
                                                     w["bu"], pk["d_qs"], pk["d_sf"], w["bd"])
 
     def _use_packed(self, T: int, rail: int) -> bool:
-        return self.packed is not None and (rail == _lib.MOE_RAIL_DECODE_MX or
-                                            (rail == _lib.MOE_RAIL_AUTO and T <= _lib.MOE_GEMV_MAX_T))
+        # MOE_RAIL_AUTO with both sets of planes takes the rail measured fastest on
+        # GB300 at each T: the CUDA-core GEMV rail (canonical) at T = 1, the
+        # block-scaled decode rail (prepacked) for 2 <= T <= MOE_GEMV_MAX_T, the
+        # library's own choice (canonical) beyond. Without the canonical planes the
+        # prepacked rail serves every decode size.
+        if self.packed is None:
+            return False
+        if rail == _lib.MOE_RAIL_DECODE_MX:
+            return True
+        if rail != _lib.MOE_RAIL_AUTO or T > _lib.MOE_GEMV_MAX_T:
+            return False
+        return self.w["g_qs"] is None or T >= 2
 
     def workspace(self, T: int, rail: int) -> torch.Tensor:
         if self._use_packed(T, rail):

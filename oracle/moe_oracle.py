@@ -448,6 +448,18 @@ def moe_layer_decode_terms(layer: Dict[str, np.ndarray], x: np.ndarray, k: int, 
 # Comparison helpers used by the tests
 # ----------------------------------------------------------------------------
 
+def rms_renorm(y: np.ndarray) -> np.ndarray:
+    """Each row divided by its root mean square, in float64 (a zero row stays
+    zero): the renormalisation between the layers of a stack of MoE layers,
+    which keeps a deep stack's hidden state bounded. Not a step of the MoE
+    layer itself (gpt-oss puts an RMSNorm, with a learned gain not modelled
+    here, before each MoE block)."""
+    y64 = np.asarray(y, dtype=np.float64)
+    ms = np.mean(y64 * y64, axis=-1, keepdims=True)
+    inv = np.where(ms > 0, 1.0 / np.sqrt(np.where(ms > 0, ms, 1.0)), 0.0)
+    return y64 * inv
+
+
 def rownorm_rel_err(y: np.ndarray, y_ref: np.ndarray, floor: float = 1e-3) -> np.ndarray:
     """Per row t: max_c |y - y_ref| / max(max_c |y_ref|, floor)."""
     y = np.asarray(y, np.float64)

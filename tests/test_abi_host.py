@@ -4,6 +4,7 @@ Nothing here launches a kernel; every call either is a pure host query or is
 rejected on the host before the library touches the device.
 """
 
+import os
 import numpy as np
 import pytest
 
@@ -14,7 +15,7 @@ FAKE = 1 << 20  # a non-null, 256-byte aligned pointer value that is never deref
 
 def test_library_exports_every_declared_symbol(moe):
     names = moe._lib.declared_functions()
-    assert len(names) == 24
+    assert len(names) == 26
     assert set(names) <= set(moe._lib._SIGS), "every declared function has a binding"
     for n in names:
         assert hasattr(moe._lib._lib, n), n
@@ -89,6 +90,13 @@ def test_gemv_rejects_bad_arguments(moe):
 def test_swiglu_rejects_bad_dtype(moe):
     assert moe.moe_swiglu_oai(FAKE, FAKE, FAKE, 10, 5, stream=0) == moe.MOE_EINVAL
     assert moe.moe_swiglu_oai(None, FAKE, FAKE, 10, 0, stream=0) == moe.MOE_EINVAL
+
+
+def test_rms_renorm_rejects_bad_arguments(moe):
+    assert moe.moe_rms_renorm(None, 0, 64, None, stream=0) == moe.MOE_OK
+    assert moe.moe_rms_renorm(FAKE, -1, 64, FAKE, stream=0) == moe.MOE_EINVAL
+    assert moe.moe_rms_renorm(FAKE, 2, 0, FAKE, stream=0) == moe.MOE_EINVAL
+    assert moe.moe_rms_renorm(None, 2, 64, FAKE, stream=0) == moe.MOE_EINVAL
 
 
 def test_grouped_mm_rejects_bad_arguments(moe):
@@ -178,3 +186,24 @@ def test_packed_layer_rejects_on_the_host(moe):
     assert moe.moe_ffn_layer_packed(L, FAKE, 1, 0, FAKE, n, FAKE, stream=0) == moe.MOE_EINVAL
     L.D = 2880
     assert moe.moe_ffn_layer_packed(L, FAKE, 0, 0, FAKE, n, FAKE, stream=0) == moe.MOE_OK
+
+
+def test_binding_constants_match_the_header(moe):
+    import re
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    text = open(os.path.join(root, "include", "moe_mxfp4.h")).read()
+    checked = 0
+    for name, raw in re.findall(r"^#define (MOE_[A-Z0-9_]+)\s+([^/\n]+)", text, re.M):
+        v = raw.strip().strip("()").replace("u", "")
+        if re.fullmatch(r"-?(0x[0-9a-fA-F]+|\d+)", v):
+            val = int(v, 0)
+        elif re.fullmatch(r"\d+\s*\*\s*\d+", v):
+            a, b = (int(t) for t in v.split("*"))
+            val = a * b
+        else:
+            continue
+        if hasattr(moe, name):
+            assert getattr(moe, name) == val, name
+            checked += 1
+    assert checked >= 20

@@ -146,13 +146,18 @@ def test_decode_mx_is_deterministic(moe):
         assert torch.equal(y, ys[0])
 
 
-def test_decode_mx_auto_rail_and_gemv_rail_agree(moe):
+def test_decode_mx_rail_and_gemv_rail_agree(moe):
     spec, L, layer, _ = packed_layer(moe, 1)
     x = dev(make_tokens(spec, T=2, seed=78))
-    y_auto = layer(x)  # packed layer, T <= 8: the block-scaled decode rail
+    y_mx = layer(x, rail=moe.MOE_RAIL_DECODE_MX)
     y_gemv = layer(x, rail=moe.MOE_RAIL_GEMV)
+    y_auto = layer(x)  # both sets of planes, T = 2: the automatic choice is the block-scaled decode rail
+    x1 = x[:1]
+    y1_auto, y1_gemv = layer(x1), layer(x1, rail=moe.MOE_RAIL_GEMV)  # T = 1: the CUDA-core GEMV rail
     torch.cuda.synchronize()
-    assert O.rownorm_rel_err(y_auto.cpu().numpy(), y_gemv.cpu().numpy()).max() <= 2 * DECODE_TOL
+    assert O.rownorm_rel_err(y_mx.cpu().numpy(), y_gemv.cpu().numpy()).max() <= 2 * DECODE_TOL
+    assert torch.equal(y_auto, y_mx)
+    assert torch.equal(y1_auto, y1_gemv)
 
 
 @pytest.mark.parametrize("pinned", [True, False])
@@ -165,7 +170,7 @@ def test_decode_mx_host_io(moe, pinned):
         xh, yh = xh.pin_memory(), yh.pin_memory()
     stream = torch.cuda.current_stream()
     for _ in range(2):
-        layer.forward_host(xh, yh, stream=stream)
+        layer.forward_host(xh, yh, rail=moe.MOE_RAIL_DECODE_MX, stream=stream)
     stream.synchronize()
     assert status(moe) == 0
     y64, _, _, _ = O.moe_layer(L, x, spec.k, cache=cache)

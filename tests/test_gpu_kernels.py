@@ -226,6 +226,25 @@ def test_swiglu_parity(moe):
     assert np.all(np.abs(gotb - O.round_bf16(ref)) <= 2.0 ** -7 * np.abs(ref) + 1e-30)
 
 
+@pytest.mark.parametrize("T,D", [(1, 2880), (6, 2880), (3, 64), (2, 1000)])
+def test_rms_renorm_parity(moe, T, D):
+    rng = np.random.default_rng(T * 7 + D)
+    scale = np.array([1e-3, 1.0, 30.0, 1e4, 0.5, 2.0])[:T, None]
+    x = (rng.standard_normal((T, D)) * scale).astype(np.float32)
+    if T > 1:
+        x[T - 1] = 0.0  # a zero row stays zero
+    ref = O.rms_renorm(x)
+    y = empty((T, D), torch.float32)
+    assert moe.moe_rms_renorm(dev(x), T, D, y) == 0
+    got = y.cpu().numpy().astype(np.float64)
+    # fp32 sum of squares and one division per element: a few ulp of 1
+    assert np.all(np.abs(got - ref) <= 4e-6 * np.maximum(np.abs(ref), 1e-3))
+    xi = dev(x)
+    assert moe.moe_rms_renorm(xi, T, D, xi) == 0  # in place
+    assert np.array_equal(xi.cpu().numpy(), y.cpu().numpy())
+    assert status(moe) == 0
+
+
 # ---------------------------------------------------------------------------
 # gather + grouped GEMM (tcgen05)
 # ---------------------------------------------------------------------------

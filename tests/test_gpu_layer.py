@@ -39,8 +39,9 @@ def run_layer(moe, layer, x_np, rail, k):
 
 def check_layer(moe, cfg, T, rail, sample=None, seed=None):
     spec, L, layer, cache = layer_for(moe, cfg)
-    if rail == moe.MOE_RAIL_AUTO:
-        rail = moe.MOE_RAIL_GEMV if T <= moe.MOE_GEMV_MAX_T else moe.MOE_RAIL_GROUPED_MM
+    if rail == moe.MOE_RAIL_AUTO:  # the canonical planes' automatic choice by T
+        rail = (moe.MOE_RAIL_GEMV if T <= moe.MOE_AUTO_GEMV_MAX_T else
+                moe.MOE_RAIL_GROUPED_MX if T <= moe.MOE_AUTO_MX_MAX_T else moe.MOE_RAIL_GROUPED_MM)
     x = make_tokens(spec, T=T, seed=seed)
     y, ids, w = run_layer(moe, layer, x, rail, spec.k)
     logits = O.router_logits(x, L["w_router"], L["b_router"])

@@ -718,3 +718,17 @@ def test_decode_terms_layer_in_both_formats():
     for fmt, n in (("e2m1", 8), ("e4m3", 5)):
         y, _, _, _ = O.moe_layer_decode_terms(L, L["x"], spec.k, x_terms=n, h_terms=n, fmt=fmt)
         assert np.max(O.rownorm_rel_err(y, y_ref)) < 1e-5, fmt
+
+
+def test_rms_renorm_closed_forms():
+    # [3, 4]: mean square 12.5; a constant row becomes its sign; every nonzero
+    # row ends with mean square 1; a zero row stays zero; rows are independent.
+    y = O.rms_renorm(np.array([[3.0, 4.0], [-2.0, -2.0], [0.0, 0.0]]))
+    assert np.allclose(y[0], [3 / math.sqrt(12.5), 4 / math.sqrt(12.5)], rtol=0, atol=1e-15)
+    assert np.array_equal(y[1], [-1.0, -1.0])
+    assert np.array_equal(y[2], [0.0, 0.0])
+    rng = np.random.default_rng(5)
+    z = rng.standard_normal((4, 2880)) * np.array([[1e-3], [1.0], [7.0], [1e4]])
+    r = O.rms_renorm(z)
+    assert np.allclose(np.mean(r * r, axis=1), 1.0, rtol=1e-12)
+    assert np.allclose(r * np.sqrt(np.mean(z * z, axis=1, keepdims=True)), z, rtol=1e-12)
