@@ -61,6 +61,7 @@ def parse_args():
                     help="measure only the prefill step (profiling aid; the headline needs decode)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-stack", action="store_true", help="skip the 24-layer stack measurement")
+    ap.add_argument("--no-crossover", action="store_true", help="skip the T=1..512 rail crossover")
     ap.add_argument("--stack-steps", type=int, default=128, help="T=1 tokens through the 24-layer stack")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="minimum CPU time of the oracle sample (whole decode tokens)")
@@ -462,7 +463,7 @@ def run_ours(args, dist: Dist):
     mx_rate, _ = whole_job_rate(K, mx_secs, dist)
 
     # ---- rail crossover, T = 1 .. 64 (same layers) ----
-    crossover = run_crossover(moe, layers, stream, dev, dist)
+    crossover = None if args.no_crossover else run_crossover(moe, layers, stream, dev, dist)
 
     result = {
         "metric": METRIC, "value": round(rate, 1), "unit": "tokens/s", "n_gpus": dist.world, "steps": K,
