@@ -313,6 +313,97 @@ def split_e2m1_terms(v: np.ndarray, nterms: int) -> np.ndarray:
 # Projections and the expert FFN
 # ----------------------------------------------------------------------------
 
+# ----------------------------------------------------------------------------
+# Q8 activations and the MXFP4 x Q8 integer dot ("dasLLAMA gpt-oss arc": the
+# dot_mx4q8 template takes a weight block's nibbles through a table lookup, the
+# low nibble by masking with 15 and the high one by a shift of 4, and
+# accumulates integer dot products of four lanes; the fused MoE expert chain
+# commit requantises the activations of its first stage in blocks of 32)
+# ----------------------------------------------------------------------------
+# The E2M1 table doubled: every entry becomes an integer in [-12, 12], so a
+# block's products with int8 activations add up exactly in integers.
+E2M1_X2 = np.array([int(round(2.0 * e2m1_value(c))) for c in range(16)], dtype=np.int64)
+
+
+def quantize_q8(v: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """Blocks of 32 values as int8 codes and one float32 scale per block.
+
+    Reading (the pages name a 32-block requant and the Q8 format, not its
+    arithmetic): the scale is d = amax / 127 of the block's largest magnitude
+    and each code q = round(v * (127 / amax)), nearest with ties to even,
+    every step in float32; an all-zero block has d = 0 and q = 0. Returns
+    (q int8 [..., C], d float32 [..., C/32]).
+    """
+    v = np.asarray(v, dtype=np.float32)
+    C = v.shape[-1]
+    assert C % 32 == 0
+    blk = v.reshape(v.shape[:-1] + (C // 32, 32))
+    amax = np.max(np.abs(blk), axis=-1)
+    live = amax > 0
+    safe = np.where(live, amax, np.float32(1.0)).astype(np.float32)
+    inv = (np.float32(127.0) / safe).astype(np.float32)
+    q = np.rint((blk * inv[..., None]).astype(np.float32))
+    q = np.where(live[..., None], q, 0.0).astype(np.int8)
+    d = np.where(live, (safe / np.float32(127.0)).astype(np.float32), np.float32(0.0)).astype(np.float32)
+    return q.reshape(v.shape), d
+
+
+def dequant_q8(q: np.ndarray, d: np.ndarray) -> np.ndarray:
+    """The values that Q8 codes stand for, float64: q * d per block of 32."""
+    q = np.asarray(q, np.float64)
+    C = q.shape[-1]
+    blk = q.reshape(q.shape[:-1] + (C // 32, 32))
+    return (blk * np.asarray(d, np.float64)[..., None]).reshape(q.shape)
+
+
+def mxfp4_q8_block_dots(qs: np.ndarray, q: np.ndarray) -> np.ndarray:
+    """Integer dot of every 32-block of an MXFP4 matrix's rows with int8 codes:
+    isum[r, b] = sum_i E2M1_X2[code of column 32b+i of row r] * q[32b+i]
+    (byte j of a block: column j in the low nibble, column 16+j in the high).
+    qs [R, C/2] uint8, q [C] int8; returns int64 [R, C/32]."""
+    qs = np.asarray(qs, dtype=np.uint8)
+    R, half = qs.shape
+    nb = half // 16
+    blocks = qs.reshape(R, nb, 16)
+    w = np.concatenate([E2M1_X2[blocks & 0x0F], E2M1_X2[blocks >> 4]], axis=2)  # [R, nb, 32]
+    return np.einsum("rbi,bi->rb", w, np.asarray(q, np.int64).reshape(nb, 32))
+
+
+def q8_block_scales(sc: np.ndarray, d: np.ndarray) -> np.ndarray:
+    """Per (row, block) float32 factor d_b * 2**(s - 128): the activation
+    block scale times the weight block's E8M0 scale, halved for the doubled
+    table (E8M0 byte 255, NaN, stays NaN)."""
+    sc = np.asarray(sc, dtype=np.int64)
+    w = np.where(sc == 255, np.nan, np.ldexp(1.0, sc - 128)).astype(np.float32)
+    return (np.asarray(d, np.float32)[None, :] * w).astype(np.float32)
+
+
+def mxfp4_gemv_q8(qs: np.ndarray, sc: np.ndarray, q: np.ndarray, d: np.ndarray,
+                  bias: Optional[np.ndarray]) -> np.ndarray:
+    """out[r] = sum_b isum[r, b] * d_b * 2**(s[r, b] - 128) + bias[r], float32.
+
+    The float32 additions follow a fixed order (so that the result is a
+    function of the inputs alone, and a GPU warp can reproduce it exactly):
+    lane l of 32 adds the products of blocks l, l+32, l+64, ... in ascending
+    order, each product float32(isum) * factor rounded to float32; the 32
+    lane sums then meet in a butterfly over lane distances 16, 8, 4, 2, 1
+    (each lane adds its partner's sum), and the bias is added last."""
+    isum = mxfp4_q8_block_dots(qs, q).astype(np.float32)  # |isum| <= 12*127*32: exact
+    fac = q8_block_scales(sc, d)
+    R, nb = isum.shape
+    lanes = np.zeros((R, 32), dtype=np.float32)
+    for b in range(nb):
+        prod = (isum[:, b] * fac[:, b]).astype(np.float32)
+        lanes[:, b % 32] = (lanes[:, b % 32] + prod).astype(np.float32)
+    idx = np.arange(32)
+    for m in (16, 8, 4, 2, 1):
+        lanes = (lanes + lanes[:, idx ^ m]).astype(np.float32)
+    out = lanes[:, 0]
+    if bias is not None:
+        out = (out + np.asarray(bias, np.float32)).astype(np.float32)
+    return out
+
+
 def mxfp4_gemv(qs: np.ndarray, sc: np.ndarray, x: np.ndarray, bias: Optional[np.ndarray]) -> np.ndarray:
     """out = W x + bias for one MXFP4 matrix W [R, C] and vector(s) x [..., C]."""
     W = dequant_mxfp4(qs, sc)
@@ -335,7 +426,9 @@ def expert_ffn(x_rows: np.ndarray, Wg: np.ndarray, bg, Wu: np.ndarray, bu, Wd: n
                    lo = bf16(x - hi), so the gate/up operand is hi + lo;
                    h rounded to bfloat16;
       "e4m3_terms" the block-scaled rail's operands: x as three E4M3 terms
-                   and h as two (split_e4m3_terms).
+                   and h as two (split_e4m3_terms);
+      "q8"         the q8 rail's operands: x and h (rounded to float32)
+                   requantised in blocks of 32 (quantize_q8), exact products.
     """
     x = np.asarray(x_rows, np.float64)
     if operands == "bf16":
@@ -345,6 +438,8 @@ def expert_ffn(x_rows: np.ndarray, Wg: np.ndarray, bg, Wu: np.ndarray, bu, Wd: n
         x = hi + round_bf16(np.asarray(x, np.float64) - hi)
     elif operands == "e4m3_terms":
         x = split_e4m3_terms(x, 3)
+    elif operands == "q8":
+        x = dequant_q8(*quantize_q8(x))
     elif operands != "f64":
         raise ValueError(operands)
     g = x @ Wg.T + (0.0 if bg is None else np.asarray(bg, np.float64))
@@ -354,6 +449,8 @@ def expert_ffn(x_rows: np.ndarray, Wg: np.ndarray, bg, Wu: np.ndarray, bu, Wd: n
         h = round_bf16(h)
     elif operands == "e4m3_terms":
         h = split_e4m3_terms(h, 2)
+    elif operands == "q8":
+        h = dequant_q8(*quantize_q8(h.astype(np.float32)))
     return h @ Wd.T + (0.0 if bd is None else np.asarray(bd, np.float64))
 
 

@@ -12,6 +12,9 @@ from tests.test_oracle_pins import (
     check_bucket_max_rows,
     check_bucket_vs_brute,
     check_decode_terms_layer,
+    check_gemv_q8,
+    check_q8_block_dots,
+    check_quantize_q8,
     check_dequant_vs_brute,
     check_e2m1,
     check_layer_vs_brute,
@@ -39,6 +42,9 @@ def test_pins_pass_on_the_real_oracle():
     assert check_bucket_max_rows(O.bucket_max_rows)
     assert check_round_e2m1(O.round_e2m1)
     assert check_split_e2m1_vs_brute(O.split_e2m1_terms)
+    assert check_quantize_q8(O.quantize_q8)
+    assert check_q8_block_dots(O.mxfp4_q8_block_dots)
+    assert check_gemv_q8(O.mxfp4_gemv_q8)
 
 
 def test_e2m1_subnormal_mistake_is_caught():
@@ -359,3 +365,63 @@ def test_e2m1_terms_without_residual_are_caught():
     def bad(v, nterms):
         return O.split_e2m1_terms(v, 1) * nterms
     assert not check_split_e2m1_vs_brute(bad)
+
+
+def test_q8_truncating_codes_are_caught():
+    def bad(v):
+        v = np.asarray(v, np.float32)
+        q, d = O.quantize_q8(v)
+        blk = v.reshape(v.shape[:-1] + (-1, 32))
+        amax = np.abs(blk).max(-1)
+        inv = np.float32(127) / np.where(amax > 0, amax, 1).astype(np.float32)
+        qt = np.trunc(blk * inv[..., None]).astype(np.int8).reshape(v.shape)
+        return qt, d
+    assert not check_quantize_q8(bad)
+
+
+def test_q8_ties_away_from_zero_are_caught():
+    def bad(v):
+        v = np.asarray(v, np.float32)
+        _, d = O.quantize_q8(v)
+        blk = v.reshape(v.shape[:-1] + (-1, 32))
+        amax = np.abs(blk).max(-1)
+        inv = np.float32(127) / np.where(amax > 0, amax, 1).astype(np.float32)
+        t = (blk * inv[..., None]).astype(np.float32)
+        qa = (np.sign(t) * np.floor(np.abs(t) + 0.5)).astype(np.int8).reshape(v.shape)
+        return qa, d
+    assert not check_quantize_q8(bad)
+
+
+def test_q8_scale_of_255_is_caught():
+    def bad(v):
+        v = np.asarray(v, np.float32)
+        blk = v.reshape(v.shape[:-1] + (-1, 32))
+        amax = np.abs(blk).max(-1)
+        safe = np.where(amax > 0, amax, 1).astype(np.float32)
+        q = np.rint(blk * (np.float32(255) / safe)[..., None] / 2).astype(np.int8).reshape(v.shape)
+        return q, np.where(amax > 0, safe / np.float32(127), 0).astype(np.float32)
+    assert not check_quantize_q8(bad)
+
+
+def test_q8_dot_with_swapped_nibbles_is_caught():
+    def bad(qs, q):
+        return O.mxfp4_q8_block_dots((((qs & 0x0F) << 4) | (qs >> 4)).astype(np.uint8), q)
+    assert not check_q8_block_dots(bad)
+
+
+def test_q8_dot_with_the_plain_table_is_caught():
+    def bad(qs, q):  # the E2M1 table not doubled: the integer sums come out halved
+        return O.mxfp4_q8_block_dots(qs, q) // 2
+    assert not check_q8_block_dots(bad)
+
+
+def test_q8_gemv_with_the_undoubled_scale_is_caught():
+    def bad(qs, sc, q, d, bias):  # 2**(s-127): the doubled table not compensated
+        return O.mxfp4_gemv_q8(qs, (sc.astype(np.int64) + 1).clip(0, 254).astype(np.uint8), q, d, bias)
+    assert not check_gemv_q8(bad)
+
+
+def test_q8_gemv_without_the_bias_is_caught():
+    def bad(qs, sc, q, d, bias):
+        return O.mxfp4_gemv_q8(qs, sc, q, d, None)
+    assert not check_gemv_q8(bad)

@@ -732,3 +732,107 @@ def test_rms_renorm_closed_forms():
     r = O.rms_renorm(z)
     assert np.allclose(np.mean(r * r, axis=1), 1.0, rtol=1e-12)
     assert np.allclose(r * np.sqrt(np.mean(z * z, axis=1, keepdims=True)), z, rtol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# Q8 activations and the MXFP4 x Q8 integer dot
+# ---------------------------------------------------------------------------
+def check_quantize_q8(fn) -> bool:
+    """Closed forms of the 32-block requant: scale = block max / 127, codes
+    rounded to nearest with ties to even, zero blocks zero, scaling by a power
+    of two moves only the scale, and every code reconstructs within half a step."""
+    v = np.zeros((2, 64), np.float32)
+    v[0, :4] = [127.0, -63.5, 0.5, 1.5]  # scale 1: ties go to even codes
+    v[0, 32:35] = [-254.0, 127.0, 3.0]   # scale 2
+    q, d = fn(v)
+    ok = q.dtype == np.int8 and d.dtype == np.float32 and q.shape == (2, 64) and d.shape == (2, 2)
+    ok &= list(q[0, :4]) == [127, -64, 0, 2] and d[0, 0] == 1.0
+    ok &= list(q[0, 32:35]) == [-127, 64, 2] and d[0, 1] == 2.0  # 1.5 -> 2 (tie to even)
+    ok &= not q[1].any() and not d[1].any()  # all-zero blocks
+    rng = np.random.default_rng(17)
+    x = (rng.standard_normal((5, 2880)) * rng.uniform(1e-3, 1e3, (5, 1))).astype(np.float32)
+    q1, d1 = fn(x)
+    q2, d2 = fn((x * np.float32(2.0 ** -9)).astype(np.float32))
+    ok &= np.array_equal(q1, q2) and np.array_equal(d2, (d1 * np.float32(2.0 ** -9)).astype(np.float32))
+    blk_max = np.abs(q1.reshape(5, 90, 32)).max(axis=2)
+    ok &= bool(np.all(blk_max == 127))  # the largest element of a block takes the full code
+    rec = q1.reshape(5, 90, 32).astype(np.float64) * d1[..., None].astype(np.float64)
+    ok &= bool(np.all(np.abs(rec - x.reshape(5, 90, 32)) <= 0.5 * d1[..., None] * (1 + 1e-5) + 1e-30))
+    return bool(ok)
+
+
+def check_q8_block_dots(fn) -> bool:
+    """Brute force on small matrices: element by element, the stored byte
+    order of a block (column j low nibble, column 16+j high) and integer sums."""
+    rng = np.random.default_rng(23)
+    R, C = 3, 96
+    qs = rng.integers(0, 256, (R, C // 2), dtype=np.uint8)
+    q = rng.integers(-127, 128, C).astype(np.int8)
+    got = fn(qs, q)
+    ok = got.shape == (R, C // 32)
+    for r in range(R):
+        for b in range(C // 32):
+            s = 0
+            for j in range(32):
+                byte = int(qs[r, 16 * b + (j % 16)])
+                code = byte & 15 if j < 16 else byte >> 4
+                s += int(round(2 * O.e2m1_value(code))) * int(q[32 * b + j])
+            ok &= int(got[r, b]) == s
+    return bool(ok)
+
+
+def check_gemv_q8(fn) -> bool:
+    """The float32 result against the exact float64 sum of the block products
+    (within the rounding of 90 float32 additions), and the one-block case,
+    where the order leaves a single rounding: out = fl(fl(isum * factor) + bias)."""
+    rng = np.random.default_rng(29)
+    R, C = 5, 2880
+    qs = rng.integers(0, 256, (R, C // 2), dtype=np.uint8)
+    sc = rng.integers(118, 136, (R, C // 32), dtype=np.uint8)
+    x = rng.standard_normal(C).astype(np.float32)
+    q, d = O.quantize_q8(x)
+    bias = rng.standard_normal(R).astype(np.float32)
+    got = fn(qs, sc, q, d, bias)
+    isum = O.mxfp4_q8_block_dots(qs, q).astype(np.float64)
+    fac = d.astype(np.float64)[None, :] * np.ldexp(1.0, sc.astype(np.int64) - 128)
+    exact = (isum * fac).sum(axis=1) + bias
+    scale = np.abs(isum * fac).sum(axis=1) + np.abs(bias)
+    ok = got.dtype == np.float32 and bool(np.all(np.abs(got - exact) <= 2e-6 * scale))
+    q1 = np.zeros(C, np.int8)
+    q1[32:64] = q[32:64]  # only block 1 (lane 1) is live
+    d1 = d.copy()
+    one = fn(qs, sc, q1, d1, bias)
+    i1 = O.mxfp4_q8_block_dots(qs, q1)[:, 1].astype(np.float32)
+    f1 = (d1[1] * np.ldexp(np.float32(1.0), sc[:, 1].astype(np.int64) - 128)).astype(np.float32)
+    ok &= np.array_equal(one, ((i1 * f1).astype(np.float32) + bias).astype(np.float32))
+    # a sign flip of all codes flips the result without the bias exactly (no order effect)
+    neg = fn(qs, sc, (-q.astype(np.int16)).astype(np.int8), d, None)
+    pos = fn(qs, sc, q, d, None)
+    ok &= np.array_equal(neg, -pos)
+    return bool(ok)
+
+
+def test_quantize_q8_closed_forms():
+    assert check_quantize_q8(O.quantize_q8)
+
+
+def test_q8_block_dots_brute_force():
+    assert check_q8_block_dots(O.mxfp4_q8_block_dots)
+
+
+def test_gemv_q8_exact_sum_and_single_block():
+    assert check_gemv_q8(O.mxfp4_gemv_q8)
+
+
+def test_q8_operands_of_the_layer_reduce_to_requantised_inputs():
+    # the q8 operand model is the layer evaluated on requantised x and h: with
+    # activations already on the Q8 grid (codes times a power-of-two scale),
+    # the requant of x is exact and gate/up equal the float64 projections
+    spec = spec_for(0)
+    L = make_layer(spec, with_tokens=False)
+    rng = np.random.default_rng(31)
+    codes = rng.integers(-127, 128, (1, spec.D)).astype(np.float32)
+    codes[:, ::32] = 127  # every block reaches the full code
+    x = (codes * np.float32(2.0 ** -5)).astype(np.float32)
+    qx, dx = O.quantize_q8(x)
+    assert np.array_equal(O.dequant_q8(qx, dx), x.astype(np.float64))
