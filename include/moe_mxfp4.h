@@ -76,6 +76,7 @@ extern "C" {
 #define MOE_RAIL_GROUPED_MM 2
 #define MOE_RAIL_GROUPED_MX 3 /* grouped GEMM on the block-scaled (MXFP4 x E4M3) tensor cores */
 #define MOE_RAIL_DECODE_MX 4  /* T <= MOE_GEMV_MAX_T on the block-scaled tensor cores (prepacked weights) */
+#define MOE_RAIL_GEMV_Q8 5    /* T <= MOE_GEMV_MAX_T: x and h requantised to Q8, integer MXFP4 x Q8 dots */
 #define MOE_GEMV_MAX_T 8
 /*
  * MOE_RAIL_AUTO on the canonical planes (moe_ffn_layer and friends) takes the
@@ -155,6 +156,44 @@ int moe_bucket(const int32_t* ids, int T, int k, int E, int tile, int32_t* count
 int moe_mxfp4_gemv(const uint8_t* w_qs, const uint8_t* w_sc, int E, int R, int C,
                    const int32_t* experts, int n, const float* x, int64_t x_stride,
                    const float* bias, float* out, cudaStream_t stream);
+
+/*
+ * moe_quantize_q8 -- activations requantised in blocks of 32 (the 32-block
+ * requant of the first stage of the fused MoE expert chain, "dasLLAMA gpt-oss
+ * arc", fused MoE expert chain commit): for every block of 32 consecutive
+ * values of the rows x [rows][C], with amax its largest magnitude,
+ *   d = amax / 127,  q[c] = round(x[c] * (127 / amax))  (nearest, ties to even),
+ * each division and product rounded to float32; an all-zero block gives d = 0
+ * and zero codes. q: int8 [rows][C], d: float [rows][C/32], both device memory
+ * owned by the caller. Finite inputs. Requires C a multiple of 32; x and q
+ * 16-byte aligned. Deterministic, bit-exact.
+ */
+int moe_quantize_q8(const float* x, int64_t rows, int C, int8_t* q, float* d, cudaStream_t stream);
+
+/*
+ * moe_mxfp4_gemv_q8 -- n MXFP4 x Q8 matrix-vector products with bias, taken
+ * in integers (the dot_mx4q8 template of "dasLLAMA gpt-oss arc", commit
+ * "dot_mx4q8_template rewritten in plain das": the weight block's nibbles go
+ * through a table, the low one masked with 15, the high one shifted by 4, and
+ * four-lane integer dots accumulate):
+ *   isum[b] = sum_{i<32} T2[code(r, 32b+i)] * q_a[32b+i]       (exact, int32)
+ *   out[i][r] = sum_b isum[b] * (d_a[b] * 2^(s[r][b] - 128)) + bias[e][r]
+ * with T2 the E2M1 table doubled (integers in [-12, 12]), a = i / act_div the
+ * activation row (act_div = k: one row per token for the k slots of a token;
+ * 1: one row per output), e = experts[i], s the weight block's E8M0 byte (255:
+ * NaN). The float32 sum has a fixed order: lane l of 32 adds blocks l, l+32,
+ * ... in ascending order (each product and sum rounded to float32), then the
+ * 32 lane sums meet in a butterfly over lane distances 16, 8, 4, 2, 1, then the
+ * bias is added: the result is bit-exact and deterministic. W: w_qs
+ * [E][R][C/2], w_sc [E][R][C/32]; q: int8 [rows][C], d: float [rows][C/32]
+ * from moe_quantize_q8; bias float [E][R] or NULL; out float [n][R].
+ * Requires C a multiple of 32 and at most 4096 (MOE_EUNSUPPORTED beyond),
+ * act_div >= 1, q and w_qs 16-byte aligned. An expert id outside [0, E) gives
+ * a zero row and sets MOE_STATUS_BAD_EXPERT_ID.
+ */
+int moe_mxfp4_gemv_q8(const uint8_t* w_qs, const uint8_t* w_sc, int E, int R, int C, const int32_t* experts,
+                      int n, int act_div, const int8_t* q, const float* d, const float* bias, float* out,
+                      cudaStream_t stream);
 
 /*
  * moe_swiglu_oai -- h = min(g, limit) * sigmoid(alpha * min(g, limit))
@@ -290,6 +329,13 @@ int moe_expert_down_combine(const uint8_t* d_qs, const uint8_t* d_sc, const floa
  * scale, each term carrying the rounding residual of the ones before: about
  * 12 and 8 significant bits). Both grouped rails accumulate in fp32 and
  * scatter with float atomics (order not deterministic).
+ * MOE_RAIL_GEMV_Q8 (T <= MOE_GEMV_MAX_T, k <= 8) is the Q8 variant of the
+ * decode rail: x and h are requantised in blocks of 32 (moe_quantize_q8) and
+ * each projection is moe_mxfp4_gemv_q8 (integer block dots), then the
+ * slot-order combine; nine kernels, deterministic. It computes the layer on
+ * the requantised operands to float32 rounding; its distance from the float64
+ * layer is the requant's own (each activation rounded to 1/254 of its block's
+ * largest: large where a block of h spans several orders of magnitude).
  * MOE_RAIL_AUTO picks by T (MOE_AUTO_GEMV_MAX_T, MOE_AUTO_MX_MAX_T above).
  * x: float [T][D]; w_router [E][D]; b_router [E] or NULL; gate/up planes
  * [E][F][D/2], [E][F][D/32]; down planes [E][D][F/2], [E][D][F/32]; biases

@@ -42,6 +42,7 @@ MOE_RAIL_GEMV = 1
 MOE_RAIL_GROUPED_MM = 2
 MOE_RAIL_GROUPED_MX = 3
 MOE_RAIL_DECODE_MX = 4
+MOE_RAIL_GEMV_Q8 = 5
 MOE_STAGE_PROLOGUE = 1
 MOE_STAGE_GATEUP = 2
 MOE_STAGE_DOWN = 4
@@ -64,6 +65,8 @@ _SIGS = {
     "moe_mxfp4_gemv": (I, [P, P, I, I, I, P, I, P, I64, P, P, P]),
     "moe_swiglu_oai": (I, [P, P, P, I64, I, F, F, P]),
     "moe_rms_renorm": (I, [P, I, I, P, P]),
+    "moe_quantize_q8": (I, [P, I64, I, P, P, P]),
+    "moe_mxfp4_gemv_q8": (I, [P, P, I, I, I, P, I, I, P, P, P, P, P]),
     "moe_selftest_wait_timeout": (I, [P, P]),
     "moe_gather_rows_bf16": (I, [P, I, I, I, P, P, I, I, P, P, P, P]),
     "moe_mxfp4_grouped_mm": (I, [P, P, P, P, P, P, I, I, I, P, P, P, P, P, I, I, P, I, F, F, P, I64, P]),
@@ -157,6 +160,15 @@ def moe_mxfp4_gemv(w_qs, w_sc, E, R, C, experts, n, x, x_stride, bias, out, stre
 
 def moe_selftest_wait_timeout(src, stream=None):
     return _lib.moe_selftest_wait_timeout(_ptr(src), _stream(stream))
+
+
+def moe_quantize_q8(x, rows, C, q, d, stream=None):
+    return _lib.moe_quantize_q8(_ptr(x), rows, C, _ptr(q), _ptr(d), _stream(stream))
+
+
+def moe_mxfp4_gemv_q8(w_qs, w_sc, E, R, C, experts, n, act_div, q, d, bias, out, stream=None):
+    return _lib.moe_mxfp4_gemv_q8(_ptr(w_qs), _ptr(w_sc), E, R, C, _ptr(experts), n, act_div, _ptr(q), _ptr(d),
+                                  _ptr(bias), _ptr(out), _stream(stream))
 
 
 def moe_rms_renorm(x, T, D, y, stream=None):

@@ -110,12 +110,20 @@ struct Workspace {
   uint32_t* xs;      // [kMxXTerms][D/128 rounded up][max_rows]
   uint8_t* hq;       // [kMxHTerms][max_rows][F]
   uint32_t* hs;      // [kMxHTerms][F/128 rounded up][max_rows]
+  // Q8 rail
+  int8_t* x8;        // [T][D]
+  float* xd;         // [T][D/32]
+  float* gq;         // [T*k][F] gate, then h
+  float* uq;         // [T*k][F]
+  int8_t* h8;        // [T*k][F]
+  float* hd;         // [T*k][F/32]
+  float* od;         // [T*k][D] down rows + bias, per slot
   size_t max_rows;
 };
 
 // Lays the workspace out from `base` (nullptr: size only). Returns total bytes.
 size_t layout_workspace(int T, int D, int F, int E, int k, int rail, char* base, Workspace* ws) {
-  const int tile = (rail == MOE_RAIL_GEMV) ? 1 : MOE_MM_TILE;
+  const int tile = (rail == MOE_RAIL_GEMV || rail == MOE_RAIL_GEMV_Q8) ? 1 : MOE_MM_TILE;
   const size_t mr = max_rows_of(T, k, E, tile);
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -133,6 +141,15 @@ size_t layout_workspace(int T, int D, int F, int E, int k, int rail, char* base,
   w.inv = reinterpret_cast<int32_t*>(take((size_t)T * k * 4));
   if (rail == MOE_RAIL_GEMV) {
     w.h = reinterpret_cast<float*>(take((size_t)T * k * F * 4));
+  } else if (rail == MOE_RAIL_GEMV_Q8) {
+    const size_t TK = (size_t)T * k;
+    w.x8 = reinterpret_cast<int8_t*>(take((size_t)T * D));
+    w.xd = reinterpret_cast<float*>(take((size_t)T * (D / 32) * 4));
+    w.gq = reinterpret_cast<float*>(take(TK * F * 4));
+    w.uq = reinterpret_cast<float*>(take(TK * F * 4));
+    w.h8 = reinterpret_cast<int8_t*>(take(TK * F));
+    w.hd = reinterpret_cast<float*>(take(TK * (F / 32) * 4));
+    w.od = reinterpret_cast<float*>(take(TK * D * 4));
   } else if (rail == MOE_RAIL_GROUPED_MX) {
     const size_t nd = (size_t)(D / 32 + 3) / 4, nf = (size_t)(F / 32 + 3) / 4;
     w.xq = reinterpret_cast<uint8_t*>(take(kMxXTerms * mr * D));
@@ -253,7 +270,10 @@ size_t moe_bucket_max_rows(int T, int k, int E, int tile) {
 size_t moe_ffn_workspace_bytes(int T, int D, int F, int E, int k, int rail) {
   if (T < 0 || D < 1 || F < 1 || E < 1 || k < 1 || k > E) return 0;
   rail = resolve_rail(T, rail);
-  if (rail != MOE_RAIL_GEMV && rail != MOE_RAIL_GROUPED_MM && rail != MOE_RAIL_GROUPED_MX) return 0;
+  if (rail != MOE_RAIL_GEMV && rail != MOE_RAIL_GROUPED_MM && rail != MOE_RAIL_GROUPED_MX &&
+      rail != MOE_RAIL_GEMV_Q8)
+    return 0;
+  if (rail == MOE_RAIL_GEMV_Q8 && (T > MOE_GEMV_MAX_T || D % 32 || F % 32)) return 0;
   return layout_workspace(T, D, F, E, k, rail, nullptr, nullptr);
 }
 
@@ -302,6 +322,32 @@ int moe_mxfp4_gemv(const uint8_t* w_qs, const uint8_t* w_sc, int E, int R, int C
   Launch L{stream, false};
   return cuda_status(
       launch_mxfp4_gemv(w_qs, w_sc, E, R, C, experts, n, x, x_stride, bias, out, d->status, L));
+}
+
+int moe_quantize_q8(const float* x, int64_t rows, int C, int8_t* q, float* d, cudaStream_t stream) {
+  MOE_REQUIRE(rows >= 0 && C >= 32 && C % 32 == 0);
+  if (rows == 0) return MOE_OK;
+  MOE_REQUIRE(x && q && d && aligned(x, 16) && aligned(q, 16));
+  DeviceInfo* dv = nullptr;
+  int rc = current_device(&dv);
+  if (rc != MOE_OK) return rc;
+  Launch L{stream, false};
+  return cuda_status(launch_quant_q8(x, rows, C, q, d, L));
+}
+
+int moe_mxfp4_gemv_q8(const uint8_t* w_qs, const uint8_t* w_sc, int E, int R, int C, const int32_t* experts,
+                      int n, int act_div, const int8_t* q, const float* d, const float* bias, float* out,
+                      cudaStream_t stream) {
+  MOE_REQUIRE(E >= 1 && R >= 1 && C >= 32 && C % 32 == 0 && n >= 0 && act_div >= 1);
+  if (n == 0) return MOE_OK;
+  if (C > 4096) return MOE_EUNSUPPORTED;
+  MOE_REQUIRE(w_qs && w_sc && experts && q && d && out);
+  MOE_REQUIRE(aligned(w_qs, 16) && aligned(q, 16));
+  DeviceInfo* dv = nullptr;
+  int rc = current_device(&dv);
+  if (rc != MOE_OK) return rc;
+  Launch L{stream, false};
+  return cuda_status(launch_gemv_q8(w_qs, w_sc, E, R, C, experts, n, act_div, q, d, bias, out, dv->status, L));
 }
 
 int moe_swiglu_oai(const float* g, const float* u, void* h, int64_t n, int h_dtype, float alpha,
@@ -450,8 +496,9 @@ int ffn_layer_impl(const float* x, float* x_copy, int T, int D, int F, int E, in
   MOE_REQUIRE(T >= 0 && D >= 64 && F >= 64 && D % 64 == 0 && F % 64 == 0);
   MOE_REQUIRE(E >= 1 && E <= 256 && k >= 1 && k <= E && k <= 32);
   rail = resolve_rail(T, rail);
-  MOE_REQUIRE(rail == MOE_RAIL_GEMV || rail == MOE_RAIL_GROUPED_MM || rail == MOE_RAIL_GROUPED_MX);
-  if (rail == MOE_RAIL_GEMV) {
+  MOE_REQUIRE(rail == MOE_RAIL_GEMV || rail == MOE_RAIL_GROUPED_MM || rail == MOE_RAIL_GROUPED_MX ||
+              rail == MOE_RAIL_GEMV_Q8);
+  if (rail == MOE_RAIL_GEMV || rail == MOE_RAIL_GEMV_Q8) {
     MOE_REQUIRE(T <= MOE_GEMV_MAX_T && k <= 8);
     if (D > 4096 || F > 4096) return MOE_EUNSUPPORTED;
   } else {
@@ -490,6 +537,25 @@ int ffn_layer_impl(const float* x, float* x_copy, int T, int D, int F, int E, in
   }
   rc = cuda_status(launch_topk_softmax(ws.logits, T, E, k, ids, wts, L));
   if (rc != MOE_OK) return rc;
+  if (rail == MOE_RAIL_GEMV_Q8) {
+    // x -> Q8; gate and up per slot (the slot's token row); swiglu in place; h -> Q8; down per slot; combine
+    const int TK = T * k;
+    if ((rc = cuda_status(launch_quant_q8(x, T, D, ws.x8, ws.xd, L))) != MOE_OK) return rc;
+    if ((rc = cuda_status(launch_gemv_q8(g_qs, g_sc, E, F, D, ids, TK, k, ws.x8, ws.xd, bg, ws.gq, d->status, L))) !=
+        MOE_OK)
+      return rc;
+    if ((rc = cuda_status(launch_gemv_q8(u_qs, u_sc, E, F, D, ids, TK, k, ws.x8, ws.xd, bu, ws.uq, d->status, L))) !=
+        MOE_OK)
+      return rc;
+    if ((rc = cuda_status(launch_swiglu(ws.gq, ws.uq, ws.gq, (int64_t)TK * F, MOE_DTYPE_F32, alpha, limit, L))) !=
+        MOE_OK)
+      return rc;
+    if ((rc = cuda_status(launch_quant_q8(ws.gq, TK, F, ws.h8, ws.hd, L))) != MOE_OK) return rc;
+    if ((rc = cuda_status(launch_gemv_q8(d_qs, d_sc, E, D, F, ids, TK, 1, ws.h8, ws.hd, bd, ws.od, d->status, L))) !=
+        MOE_OK)
+      return rc;
+    return cuda_status(launch_combine_slots(ws.od, wts, ids, T, k, D, E, y, L));
+  }
   rc = cuda_status(launch_bucket(ids, T, k, E, MOE_MM_TILE, (int)ws.max_rows, ws.counts, ws.basep,
                                  ws.rows, ws.inv, d->status, L));
   if (rc != MOE_OK) return rc;

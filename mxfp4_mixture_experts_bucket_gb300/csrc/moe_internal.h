@@ -79,6 +79,12 @@ cudaError_t launch_mxfp4_gemv(const uint8_t* qs, const uint8_t* sc, int E, int R
                               const int32_t* experts, int n, const float* x, int64_t x_stride,
                               const float* bias, float* out, int* status, Launch L);
 cudaError_t launch_selftest_wait_timeout(const uint8_t* src, int* status, Launch L);
+cudaError_t launch_quant_q8(const float* v, int64_t rows, int C, int8_t* q, float* d, Launch L);
+cudaError_t launch_gemv_q8(const uint8_t* qs, const uint8_t* sc, int E, int R, int C, const int32_t* experts,
+                           int n, int act_div, const int8_t* aq, const float* ad, const float* bias, float* out,
+                           int* status, Launch L);
+cudaError_t launch_combine_slots(const float* o, const float* w, const int32_t* ids, int T, int k, int D, int E,
+                                 float* y, Launch L);
 cudaError_t launch_rms_renorm(const float* x, int T, int D, float* y, Launch L);
 cudaError_t launch_swiglu(const float* g, const float* u, void* h, int64_t n, int h_dtype,
                           float alpha, float limit, Launch L);

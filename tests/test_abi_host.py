@@ -15,7 +15,7 @@ FAKE = 1 << 20  # a non-null, 256-byte aligned pointer value that is never deref
 
 def test_library_exports_every_declared_symbol(moe):
     names = moe._lib.declared_functions()
-    assert len(names) == 26
+    assert len(names) == 28
     assert set(names) <= set(moe._lib._SIGS), "every declared function has a binding"
     for n in names:
         assert hasattr(moe._lib._lib, n), n
@@ -207,3 +207,16 @@ def test_binding_constants_match_the_header(moe):
             assert getattr(moe, name) == val, name
             checked += 1
     assert checked >= 20
+
+
+def test_q8_entry_points_reject_bad_arguments(moe):
+    EINVAL = moe.MOE_EINVAL
+    assert moe.moe_quantize_q8(None, 0, 64, None, None, stream=0) == moe.MOE_OK
+    assert moe.moe_quantize_q8(FAKE, 2, 48, FAKE, FAKE, stream=0) == EINVAL  # C not a multiple of 32
+    assert moe.moe_quantize_q8(None, 2, 64, FAKE, FAKE, stream=0) == EINVAL
+    assert moe.moe_mxfp4_gemv_q8(FAKE, FAKE, 2, 8, 64, FAKE, 0, 1, FAKE, FAKE, None, FAKE, stream=0) == moe.MOE_OK
+    assert moe.moe_mxfp4_gemv_q8(FAKE, FAKE, 2, 8, 64, FAKE, 1, 0, FAKE, FAKE, None, FAKE, stream=0) == EINVAL
+    assert moe.moe_mxfp4_gemv_q8(FAKE, FAKE, 2, 8, 8192, FAKE, 1, 1, FAKE, FAKE, None, FAKE,
+                                 stream=0) == moe.MOE_EUNSUPPORTED
+    assert moe.moe_ffn_workspace_bytes(1, 2880, 2880, 32, 4, moe.MOE_RAIL_GEMV_Q8) > 0
+    assert moe.moe_ffn_workspace_bytes(9, 2880, 2880, 32, 4, moe.MOE_RAIL_GEMV_Q8) == 0
