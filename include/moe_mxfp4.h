@@ -353,6 +353,25 @@ int moe_ffn_layer(const float* x, int T, int D, int F, int E, int k, const float
                   cudaStream_t stream);
 
 /*
+ * moe_ffn_layer_gu -- moe_ffn_layer with gate and up stored as gpt-oss stores
+ * them: one MXFP4 plane per expert of 2F rows, gate row f at row 2f and up row
+ * f at row 2f+1 (the pages' decode stage reads "gate+up rows" together:
+ * "dasLLAMA gpt-oss arc", fused MoE expert chain commit, stage 0). gu_qs
+ * [E][2F][D/2], gu_sc [E][2F][D/32], gu_b [E][2F] (interleaved the same way)
+ * or NULL; every other argument, the workspace (moe_ffn_workspace_bytes) and
+ * the results are those of moe_ffn_layer on the separated planes, bit for bit
+ * on the deterministic rails (GEMV, GEMV_Q8). The GEMV rail streams a
+ * sub-task's gate and up rows as one run of 2*8 rows (one copy for the
+ * nibbles, one for the scales); the grouped rails read the plane through
+ * strided tensor maps. Requires gu_qs 16-byte aligned and gu_sc 16-byte
+ * aligned; other requirements as moe_ffn_layer.
+ */
+int moe_ffn_layer_gu(const float* x, int T, int D, int F, int E, int k, const float* w_router,
+                     const float* b_router, const uint8_t* gu_qs, const uint8_t* gu_sc, const float* gu_b,
+                     const uint8_t* d_qs, const uint8_t* d_sc, const float* bd, int rail, void* workspace,
+                     size_t workspace_bytes, float* y, int32_t* ids_out, float* weights_out, cudaStream_t stream);
+
+/*
  * moe_ffn_args_t -- every argument of moe_ffn_layer that stays fixed from one
  * step to the next, plus two device staging buffers x_dev and y_dev of T*D
  * floats (16-byte aligned). Filled once by the caller; the library neither
@@ -426,6 +445,18 @@ size_t moe_mxfp4_packed_sf_bytes(int E, int R, int C);
  */
 int moe_mxfp4_prepack(const uint8_t* qs, const uint8_t* sc, int E, int R, int C, uint8_t* qs_p,
                       uint8_t* sf_p, cudaStream_t stream);
+
+/*
+ * moe_mxfp4_prepack_gu -- moe_mxfp4_prepack of the gate and the up matrices
+ * straight from one interleaved gate/up plane (gu_qs [E][2F][D/2], gu_sc
+ * [E][2F][D/32]: gate row f at row 2f, up row f at row 2f+1, as
+ * moe_ffn_layer_gu takes them) into the two prepacked pairs (g_qs_p, g_sf_p)
+ * and (u_qs_p, u_sf_p), each sized moe_mxfp4_packed_*_bytes(E, F, D). The
+ * packed planes equal those of moe_mxfp4_prepack on the separated planes.
+ * Requires F a multiple of 64, D of 32; gu_qs 16-byte aligned, *_qs_p 32, *_sf_p 16.
+ */
+int moe_mxfp4_prepack_gu(const uint8_t* gu_qs, const uint8_t* gu_sc, int E, int F, int D, uint8_t* g_qs_p,
+                         uint8_t* g_sf_p, uint8_t* u_qs_p, uint8_t* u_sf_p, cudaStream_t stream);
 
 /*
  * moe_packed_layer_t -- one layer's device weights with the three expert

@@ -65,6 +65,8 @@ _SIGS = {
     "moe_mxfp4_gemv": (I, [P, P, I, I, I, P, I, P, I64, P, P, P]),
     "moe_swiglu_oai": (I, [P, P, P, I64, I, F, F, P]),
     "moe_rms_renorm": (I, [P, I, I, P, P]),
+    "moe_ffn_layer_gu": (I, [P, I, I, I, I, I, P, P, P, P, P, P, P, P, I, P, SZ, P, P, P, P]),
+    "moe_mxfp4_prepack_gu": (I, [P, P, I, I, I, P, P, P, P, P]),
     "moe_quantize_q8": (I, [P, I64, I, P, P, P]),
     "moe_mxfp4_gemv_q8": (I, [P, P, I, I, I, P, I, I, P, P, P, P, P]),
     "moe_selftest_wait_timeout": (I, [P, P]),
@@ -169,6 +171,18 @@ def moe_quantize_q8(x, rows, C, q, d, stream=None):
 def moe_mxfp4_gemv_q8(w_qs, w_sc, E, R, C, experts, n, act_div, q, d, bias, out, stream=None):
     return _lib.moe_mxfp4_gemv_q8(_ptr(w_qs), _ptr(w_sc), E, R, C, _ptr(experts), n, act_div, _ptr(q), _ptr(d),
                                   _ptr(bias), _ptr(out), _stream(stream))
+
+
+def moe_ffn_layer_gu(x, T, D, F, E, k, w_router, b_router, gu_qs, gu_sc, gu_b, d_qs, d_sc, bd, rail,
+                     workspace, workspace_bytes, y, ids_out=None, weights_out=None, stream=None):
+    return _lib.moe_ffn_layer_gu(_ptr(x), T, D, F, E, k, _ptr(w_router), _ptr(b_router), _ptr(gu_qs), _ptr(gu_sc),
+                                 _ptr(gu_b), _ptr(d_qs), _ptr(d_sc), _ptr(bd), rail, _ptr(workspace),
+                                 workspace_bytes, _ptr(y), _ptr(ids_out), _ptr(weights_out), _stream(stream))
+
+
+def moe_mxfp4_prepack_gu(gu_qs, gu_sc, E, F, D, g_qs_p, g_sf_p, u_qs_p, u_sf_p, stream=None):
+    return _lib.moe_mxfp4_prepack_gu(_ptr(gu_qs), _ptr(gu_sc), E, F, D, _ptr(g_qs_p), _ptr(g_sf_p), _ptr(u_qs_p),
+                                     _ptr(u_sf_p), _stream(stream))
 
 
 def moe_rms_renorm(x, T, D, y, stream=None):

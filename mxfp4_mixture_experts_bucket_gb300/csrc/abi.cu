@@ -492,7 +492,9 @@ int ffn_layer_impl(const float* x, float* x_copy, int T, int D, int F, int E, in
                   const uint8_t* u_qs, const uint8_t* u_sc, const float* bu, const uint8_t* d_qs,
                   const uint8_t* d_sc, const float* bd, int rail, void* workspace,
                   size_t workspace_bytes, float* y, int32_t* ids_out, float* weights_out,
-                  cudaStream_t stream) {
+                  cudaStream_t stream, int gu_rs = 1) {
+  // gu_rs = 2: gate and up are one plane with interleaved rows; u_qs, u_sc, bu
+  // point one row (or one bias) past g_qs, g_sc, bg
   MOE_REQUIRE(T >= 0 && D >= 64 && F >= 64 && D % 64 == 0 && F % 64 == 0);
   MOE_REQUIRE(E >= 1 && E <= 256 && k >= 1 && k <= E && k <= 32);
   rail = resolve_rail(T, rail);
@@ -508,7 +510,7 @@ int ffn_layer_impl(const float* x, float* x_copy, int T, int D, int F, int E, in
   MOE_REQUIRE(x && w_router && g_qs && g_sc && u_qs && u_sc && d_qs && d_sc && y && workspace);
   MOE_REQUIRE(aligned(x, 16) && aligned(w_router, 16) && aligned(y, 16) && aligned(workspace, 256));
   MOE_REQUIRE(aligned(g_qs, 16) && aligned(u_qs, 16) && aligned(d_qs, 16));
-  MOE_REQUIRE(aligned(g_sc, 16) && aligned(u_sc, 16) && aligned(d_sc, 16));
+  MOE_REQUIRE(aligned(g_sc, 16) && (gu_rs == 2 || aligned(u_sc, 16)) && aligned(d_sc, 16));
   const size_t need = layout_workspace(T, D, F, E, k, rail, nullptr, nullptr);
   MOE_REQUIRE(workspace_bytes >= need);
   DeviceInfo* d = nullptr;
@@ -530,7 +532,7 @@ int ffn_layer_impl(const float* x, float* x_copy, int T, int D, int F, int E, in
     // decode: the two expert kernels take the top-k of the logits themselves
     rc = cuda_status(launch_gemv_gateup(g_qs, g_sc, bg, u_qs, u_sc, bu, E, F, D, T, k, x_copy ? x_copy : x,
                                         ws.logits, nullptr, ids_out, weights_out, alpha, limit, ws.h, d->status,
-                                        x_copy != nullptr, L));
+                                        x_copy != nullptr, L, gu_rs));
     if (rc != MOE_OK) return rc;
     return cuda_status(launch_gemv_down(d_qs, d_sc, bd, E, D, F, T, k, ws.h, ws.logits, nullptr,
                                         nullptr, y, d->status, L));
@@ -541,10 +543,10 @@ int ffn_layer_impl(const float* x, float* x_copy, int T, int D, int F, int E, in
     // x -> Q8; gate and up per slot (the slot's token row); swiglu in place; h -> Q8; down per slot; combine
     const int TK = T * k;
     if ((rc = cuda_status(launch_quant_q8(x, T, D, ws.x8, ws.xd, L))) != MOE_OK) return rc;
-    if ((rc = cuda_status(launch_gemv_q8(g_qs, g_sc, E, F, D, ids, TK, k, ws.x8, ws.xd, bg, ws.gq, d->status, L))) !=
+    if ((rc = cuda_status(launch_gemv_q8(g_qs, g_sc, E, F, D, ids, TK, k, ws.x8, ws.xd, bg, ws.gq, d->status, L, gu_rs))) !=
         MOE_OK)
       return rc;
-    if ((rc = cuda_status(launch_gemv_q8(u_qs, u_sc, E, F, D, ids, TK, k, ws.x8, ws.xd, bu, ws.uq, d->status, L))) !=
+    if ((rc = cuda_status(launch_gemv_q8(u_qs, u_sc, E, F, D, ids, TK, k, ws.x8, ws.xd, bu, ws.uq, d->status, L, gu_rs))) !=
         MOE_OK)
       return rc;
     if ((rc = cuda_status(launch_swiglu(ws.gq, ws.uq, ws.gq, (int64_t)TK * F, MOE_DTYPE_F32, alpha, limit, L))) !=
@@ -587,9 +589,11 @@ int ffn_layer_impl(const float* x, float* x_copy, int T, int D, int F, int E, in
     g.h_terms = ws.hq;
     g.h_sc = ws.hs;
     g.status = d->status;
+    g.rs = gu_rs;
     rc = cuda_status(launch_grouped_mx(g, L));
     if (rc != MOE_OK) return rc;
     GroupedMXArgs gd = g;
+    gd.rs = 1;
     gd.w_qs[0] = d_qs;
     gd.w_sc[0] = d_sc;
     gd.bias[0] = bd;
@@ -634,9 +638,11 @@ int ffn_layer_impl(const float* x, float* x_copy, int T, int D, int F, int E, in
   g.out = ws.hg;
   g.out_ld = F;
   g.status = d->status;
+  g.rs = gu_rs;
   rc = cuda_status(launch_grouped_mm(g, L));
   if (rc != MOE_OK) return rc;
   GroupedMMArgs gd = g;
+  gd.rs = 1;
   gd.w_qs[0] = d_qs;
   gd.w_sc[0] = d_sc;
   gd.bias[0] = bd;
@@ -666,6 +672,19 @@ int moe_ffn_layer(const float* x, int T, int D, int F, int E, int k, const float
                   cudaStream_t stream) {
   return ffn_layer_impl(x, nullptr, T, D, F, E, k, w_router, b_router, g_qs, g_sc, bg, u_qs, u_sc, bu, d_qs, d_sc,
                         bd, rail, workspace, workspace_bytes, y, ids_out, weights_out, stream);
+}
+
+int moe_ffn_layer_gu(const float* x, int T, int D, int F, int E, int k, const float* w_router,
+                     const float* b_router, const uint8_t* gu_qs, const uint8_t* gu_sc, const float* gu_b,
+                     const uint8_t* d_qs, const uint8_t* d_sc, const float* bd, int rail, void* workspace,
+                     size_t workspace_bytes, float* y, int32_t* ids_out, float* weights_out, cudaStream_t stream) {
+  MOE_REQUIRE(D >= 64 && D % 64 == 0);
+  MOE_REQUIRE(T == 0 || (gu_qs && gu_sc));
+  const uint8_t* u_qs = gu_qs ? gu_qs + D / 2 : nullptr;
+  const uint8_t* u_sc = gu_sc ? gu_sc + D / 32 : nullptr;
+  return ffn_layer_impl(x, nullptr, T, D, F, E, k, w_router, b_router, gu_qs, gu_sc, gu_b, u_qs, u_sc,
+                        gu_b ? gu_b + 1 : nullptr, d_qs, d_sc, bd, rail, workspace, workspace_bytes, y, ids_out,
+                        weights_out, stream, 2);
 }
 
 }  // extern "C"
@@ -734,6 +753,21 @@ int moe_mxfp4_prepack(const uint8_t* qs, const uint8_t* sc, int E, int R, int C,
   if (rc != MOE_OK) return rc;
   Launch L{stream, false};
   return cuda_status(launch_prepack(qs, sc, E, R, C, qs_p, sf_p, L));
+}
+
+int moe_mxfp4_prepack_gu(const uint8_t* gu_qs, const uint8_t* gu_sc, int E, int F, int D, uint8_t* g_qs_p,
+                         uint8_t* g_sf_p, uint8_t* u_qs_p, uint8_t* u_sf_p, cudaStream_t stream) {
+  MOE_REQUIRE(E >= 1 && F >= 64 && D >= 32 && F % 64 == 0 && D % 32 == 0);
+  MOE_REQUIRE(gu_qs && gu_sc && g_qs_p && g_sf_p && u_qs_p && u_sf_p);
+  MOE_REQUIRE(aligned(gu_qs, 16) && aligned(g_qs_p, 32) && aligned(u_qs_p, 32));
+  MOE_REQUIRE(aligned(g_sf_p, 16) && aligned(u_sf_p, 16));
+  DeviceInfo* d = nullptr;
+  int rc = current_device(&d);
+  if (rc != MOE_OK) return rc;
+  Launch L{stream, false};
+  rc = cuda_status(launch_prepack(gu_qs, gu_sc, E, F, D, g_qs_p, g_sf_p, L, 2));
+  if (rc != MOE_OK) return rc;
+  return cuda_status(launch_prepack(gu_qs + D / 2, gu_sc + D / 32, E, F, D, u_qs_p, u_sf_p, L, 2));
 }
 
 size_t moe_ffn_packed_workspace_bytes(int T, int D, int F, int E, int k, int rail) {

@@ -251,6 +251,8 @@ struct DecodeArgs {
   int spt;     // stages per team
   int staged;  // vectors split into shared memory once per CTA
   int vec_wait;  // gate/up: x is written by the previous kernel (read it after the wait)
+  int rs;        // gate/up rows: 1 = separate planes; 2 = one plane, rows interleaved (gate f = row 2f,
+                 // up f = row 2f+1; qs[1], sc[1], bias[1] point one row or one element further)
   uint32_t stage_bytes;
   int* status;
 };
@@ -414,16 +416,28 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_expert_kernel(const Dec
           const uint32_t fb = tc::smem_u32(&full_bar[s]);
           uint8_t* stage = ring + (size_t)s * A.stage_bytes;
           const size_t row0 = (size_t)e * R + st.r0;
-          const size_t sc0 = row0 * nb, sc1 = sc0 + (size_t)st.nr * nb;
-          const size_t w0 = sc0 & ~(size_t)15, w1 = (sc1 + 15) & ~(size_t)15;
-          const uint32_t qbytes = (uint32_t)st.nr * (C / 2);
-          tc::mbar_expect_tx(fb, NMAT * (qbytes + (uint32_t)(w1 - w0)));
-#pragma unroll
-          for (int m = 0; m < NMAT; ++m) {
-            tc::bulk_load_stream(tc::smem_u32(stage + m * qsb), A.qs[m] + row0 * (C / 2), qbytes, fb,
+          if (KIND == 0 && A.rs == 2) {
+            // interleaved gate/up: the sub-task's gate and up rows are one run of 2*nr rows,
+            // one copy for the nibbles and one for the scale window
+            const size_t sc0 = 2 * row0 * nb, sc1 = sc0 + 2 * (size_t)st.nr * nb;
+            const size_t w0 = sc0 & ~(size_t)15, w1 = (sc1 + 15) & ~(size_t)15;
+            const uint32_t qbytes = 2u * (uint32_t)st.nr * (C / 2);
+            tc::mbar_expect_tx(fb, qbytes + (uint32_t)(w1 - w0));
+            tc::bulk_load_stream(tc::smem_u32(stage), A.qs[0] + 2 * row0 * (C / 2), qbytes, fb, stream_policy);
+            tc::bulk_load_stream(tc::smem_u32(stage + NMAT * qsb), A.sc[0] + w0, (uint32_t)(w1 - w0), fb,
                                  stream_policy);
-            tc::bulk_load_stream(tc::smem_u32(stage + NMAT * qsb + m * scb), A.sc[m] + w0, (uint32_t)(w1 - w0),
-                                 fb, stream_policy);
+          } else {
+            const size_t sc0 = row0 * nb, sc1 = sc0 + (size_t)st.nr * nb;
+            const size_t w0 = sc0 & ~(size_t)15, w1 = (sc1 + 15) & ~(size_t)15;
+            const uint32_t qbytes = (uint32_t)st.nr * (C / 2);
+            tc::mbar_expect_tx(fb, NMAT * (qbytes + (uint32_t)(w1 - w0)));
+#pragma unroll
+            for (int m = 0; m < NMAT; ++m) {
+              tc::bulk_load_stream(tc::smem_u32(stage + m * qsb), A.qs[m] + row0 * (C / 2), qbytes, fb,
+                                   stream_policy);
+              tc::bulk_load_stream(tc::smem_u32(stage + NMAT * qsb + m * scb), A.sc[m] + w0, (uint32_t)(w1 - w0),
+                                   fb, stream_policy);
+            }
           }
           s_last[s] = n;
         }
@@ -474,14 +488,18 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_expert_kernel(const Dec
     const int e = Rt.act_e[st.ai];
     // biases of the sub-task's rows, in flight during the products
     float bias0 = 0.f, bias1 = 0.f;
+    const int rsv = (KIND == 0) ? A.rs : 1;
     if (lane < st.nr) {
-      const size_t ro = (size_t)e * R + st.r0 + lane;
+      const size_t ro = ((size_t)e * R + st.r0 + lane) * rsv;
       if (A.bias[0]) bias0 = __ldg(A.bias[0] + ro);
       if (KIND == 0 && A.bias[1]) bias1 = __ldg(A.bias[1] + ro);
     }
     team_wait(&full_bar[s], n & 1, 1);
     const uint8_t* stage = ring + (size_t)s * A.stage_bytes;
-    const int sc_skew = (int)((((size_t)e * R + st.r0) * nb) & 15);
+    const int sc_skew = (int)((((size_t)e * R + st.r0) * rsv * nb) & 15);
+    // stage strides: between a matrix's consecutive rows, and between the two matrices' row r
+    const uint32_t q_rs = (uint32_t)rsv * (C / 2), q_ms = rsv == 2 ? (uint32_t)(C / 2) : qsb;
+    const uint32_t s_rs = (uint32_t)(rsv * nb), s_ms = rsv == 2 ? (uint32_t)nb : scb;
     for (int li = Rt.act_off[st.ai]; li < Rt.act_off[st.ai + 1]; ++li, ++it) {
       const int a = Rt.lst[li];
       const int v = (KIND == 0) ? a / k : a;
@@ -495,13 +513,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_expert_kernel(const Dec
           split_block_lane(A.vec + (size_t)v * C + 32 * b, XH, XL, xf);
 #pragma unroll
         for (int m = 0; m < NMAT; ++m) {
-          const uint8_t* qrow = stage + m * qsb + b * 16;
-          const uint8_t* srow = stage + NMAT * qsb + m * scb + sc_skew + b;
+          const uint8_t* qrow = stage + m * q_ms + b * 16;
+          const uint8_t* srow = stage + NMAT * qsb + m * s_ms + sc_skew + b;
 #pragma unroll
           for (int r = 0; r < kDecRows; ++r) {
             if (r < st.nr) {
-              const uint4 q = *reinterpret_cast<const uint4*>(qrow + r * (C / 2));
-              const float sc = e8m0_scale(srow[r * nb]);
+              const uint4 q = *reinterpret_cast<const uint4*>(qrow + r * q_rs);
+              const float sc = e8m0_scale(srow[r * s_rs]);
               acc[m * kDecRows + r] = (block_dot_split(q, XH, XL) * xf) * sc;
             }
           }
@@ -607,11 +625,12 @@ cudaError_t launch_gemv_gateup(const uint8_t* g_qs, const uint8_t* g_sc, const f
                                const uint8_t* u_qs, const uint8_t* u_sc, const float* bu, int E,
                                int F, int D, int T, int k, const float* x, const float* logits,
                                const int32_t* ids_in, int32_t* ids_out, float* w_out, float alpha,
-                               float limit, float* h, int* status, bool x_from_prev, Launch L) {
+                               float limit, float* h, int* status, bool x_from_prev, Launch L, int rs) {
   if (T <= 0) return cudaSuccess;
-  if (T * k > kMaxAssign) return cudaErrorInvalidValue;
+  if (T * k > kMaxAssign || (rs != 1 && rs != 2)) return cudaErrorInvalidValue;
   DecodeArgs A = {};
   A.vec_wait = x_from_prev ? 1 : 0;
+  A.rs = rs;
   A.qs[0] = g_qs;
   A.qs[1] = u_qs;
   A.sc[0] = g_sc;
@@ -642,6 +661,7 @@ cudaError_t launch_gemv_down(const uint8_t* d_qs, const uint8_t* d_sc, const flo
   if (T <= 0) return cudaSuccess;
   if (T * k > kMaxAssign) return cudaErrorInvalidValue;
   DecodeArgs A = {};
+  A.rs = 1;
   A.qs[0] = d_qs;
   A.sc[0] = d_sc;
   A.bias[0] = bd;

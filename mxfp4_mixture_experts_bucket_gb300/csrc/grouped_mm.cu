@@ -62,6 +62,7 @@ struct Params {
   int64_t out_ld;
   int* status;
   int box_rows;  // rows of one weight TMA box: min(BM, R)
+  int wrs;       // weight row stride in rows: 1, or 2 for gate/up rows interleaved in one plane
 };
 
 // Shared-memory plan (identical on host and device): A ring, activation pool,
@@ -178,6 +179,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = tc::smem_u32(smem);
   const uint32_t sA = sbase + L.a, sB = sbase + L.b, sRaw = sbase + L.raw;
   const uint8_t* scs = smem + L.sc;
+  // the tile's scale rows in shared memory: separate planes one matrix after the
+  // other; interleaved gate/up rows alternating
+  const int sc_rs = p.wrs == 2 ? 2 * nbc : nbc;
+  const int sc_ms = p.wrs == 2 ? nbc : (int)L.sc_stride;
   const uint32_t bars = sbase + L.bars;
   int* s_rows = reinterpret_cast<int*>(smem + L.misc);
   float* s_w = reinterpret_cast<float*>(smem + L.misc + BN * 4);
@@ -230,9 +235,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (NMAT == 2) tc::prefetch_tmap(&tm_w1);
       const uint32_t sc_bytes = (uint32_t)(rows_here * nbc);
       tc::mbar_expect_tx(bar(kScFull), NMAT * sc_bytes);
-      for (int mat = 0; mat < NMAT; ++mat)
-        tc::bulk_load(sbase + L.sc + mat * L.sc_stride,
-                      p.w_sc[mat] + ((size_t)e * p.R + m0) * nbc, sc_bytes, bar(kScFull));
+      if (p.wrs == 2) {  // interleaved gate/up: both matrices' scale rows are one run
+        tc::bulk_load(sbase + L.sc, p.w_sc[0] + ((size_t)e * p.R + m0) * 2 * nbc, 2 * sc_bytes, bar(kScFull));
+      } else {
+        for (int mat = 0; mat < NMAT; ++mat)
+          tc::bulk_load(sbase + L.sc + mat * L.sc_stride,
+                        p.w_sc[mat] + ((size_t)e * p.R + m0) * nbc, sc_bytes, bar(kScFull));
+      }
       const uint32_t raw_bytes = (uint32_t)(NMAT * p.box_rows * (BK / 2));
       int issued = 0;
       for (int ks = 0; ks < nk; ++ks) {
@@ -327,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int f = m0 + trow;
     if (seeded && group == 0) {
       for (int mat = 0; mat < NMAT; ++mat) {
-        const float bv = (p.bias[mat] != nullptr && f < p.R) ? p.bias[mat][(size_t)e * p.R + f] : 0.f;
+        const float bv = (p.bias[mat] != nullptr && f < p.R) ? p.bias[mat][((size_t)e * p.R + f) * p.wrs] : 0.f;
         const int ncols = SPLIT ? 2 * hn : n_mma;
         for (int c = colhalf; c < ncols / 16; c += 2)
           tc::tmem_st16(tmem + ((uint32_t)(32 * q) << 16) + mat * AW + 16 * c,
@@ -356,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int mat = 0; mat < NMAT; ++mat) {
         const uint4 qv = *reinterpret_cast<const uint4*>(smem + L.raw + (rs * NMAT + mat) * kRawTile +
                                                          r * (BK / 2) + kb * 16);
-        const float scale = e8m0_to_f32(scs[mat * L.sc_stride + r * nbc + 2 * ks + kb]);
+        const float scale = e8m0_to_f32(scs[mat * sc_ms + r * sc_rs + 2 * ks + kb]);
         uint32_t o[16];
         dequant_block_bf16(qv, scale, o);
         uint8_t* arow = smem + L.a + (as * NMAT + mat) * kATile + r * 128;
@@ -487,11 +496,11 @@ bool encode_tiled_map(CUtensorMap* tm, CUtensorMapDataType dtype, int rank, cons
              swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-static bool make_weight_map(CUtensorMap* tm, const uint8_t* qs, int E, int R, int C, int box_rows) {
+static bool make_weight_map(CUtensorMap* tm, const uint8_t* qs, int E, int R, int C, int box_rows, int wrs) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
   cuuint64_t dims[3] = {(cuuint64_t)(C / 2), (cuuint64_t)R, (cuuint64_t)E};
-  cuuint64_t strides[2] = {(cuuint64_t)(C / 2), (cuuint64_t)R * (C / 2)};
+  cuuint64_t strides[2] = {(cuuint64_t)wrs * (C / 2), (cuuint64_t)wrs * R * (C / 2)};
   cuuint32_t box[3] = {(cuuint32_t)(mm::BK / 2), (cuuint32_t)box_rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   return enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(qs), dims, strides, box, es,
@@ -538,9 +547,10 @@ cudaError_t launch_grouped_mm(const GroupedMMArgs& g, Launch L) {
     return cudaErrorInvalidValue;
   const int box_rows = g.R < mm::BM ? g.R : mm::BM;
   CUtensorMap t0, t1, ta;
-  if (!make_weight_map(&t0, g.w_qs[0], g.E, g.R, g.C, box_rows)) return cudaErrorInvalidValue;
+  const int wrs = g.rs == 2 && g.nmat == 2 ? 2 : 1;
+  if (!make_weight_map(&t0, g.w_qs[0], g.E, g.R, g.C, box_rows, wrs)) return cudaErrorInvalidValue;
   if (g.nmat == 2) {
-    if (!make_weight_map(&t1, g.w_qs[1], g.E, g.R, g.C, box_rows)) return cudaErrorInvalidValue;
+    if (!make_weight_map(&t1, g.w_qs[1], g.E, g.R, g.C, box_rows, wrs)) return cudaErrorInvalidValue;
   } else {
     t1 = t0;
   }
@@ -552,6 +562,7 @@ cudaError_t launch_grouped_mm(const GroupedMMArgs& g, Launch L) {
   prm.w_sc[1] = g.nmat == 2 ? g.w_sc[1] : g.w_sc[0];
   prm.bias[0] = g.bias[0];
   prm.bias[1] = g.nmat == 2 ? g.bias[1] : nullptr;
+  prm.wrs = wrs;
   prm.E = g.E;
   prm.R = g.R;
   prm.C = g.C;

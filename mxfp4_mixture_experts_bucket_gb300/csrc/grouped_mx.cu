@@ -90,6 +90,7 @@ struct Params {
   float* y;              // down: [T][R]
   int* status;
   int box_rows;
+  int wrs;  // weight row stride in rows: 1, or 2 for gate/up rows interleaved in one plane
 };
 
 __device__ __forceinline__ uint32_t idesc_mx(int M, int N) {
@@ -364,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t qlane = (uint32_t)(32 * q) << 16;
     if (seeded && g == 0) {
       for (int mat = 0; mat < NMAT; ++mat) {
-        const float bv = (p.bias[mat] != nullptr && f < p.R) ? p.bias[mat][(size_t)e * p.R + f] : 0.f;
+        const float bv = (p.bias[mat] != nullptr && f < p.R) ? p.bias[mat][((size_t)e * p.R + f) * p.wrs] : 0.f;
         for (int c = 0; c < acc_w / 16; ++c)
           tc::tmem_st16(tmem + qlane + (uint32_t)(mat * acc_w) + 16 * c, __float_as_uint(16 * c < hn ? bv : 0.f));
       }
@@ -380,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint16_t* scrow[NMAT];
 #pragma unroll
     for (int mat = 0; mat < NMAT; ++mat)
-      scrow[mat] = reinterpret_cast<const uint16_t*>(p.w_sc[mat] + ((size_t)e * p.R + m0 + trow) * nbc);
+      scrow[mat] = reinterpret_cast<const uint16_t*>(p.w_sc[mat] + ((size_t)e * p.R + m0 + trow) * p.wrs * nbc);
     const bool sc_row = trow < rows_here;
     uint16_t sc_lo16[NMAT], sc_hi16[NMAT];
     auto sc_fetch = [&](int ks) {
@@ -624,8 +625,9 @@ cudaError_t launch_grouped_mx(const GroupedMXArgs& g, Launch L) {
   const int box_rows = g.R < mx::BM ? g.R : mx::BM;
   CUtensorMap t0, t1, tb;
   {
+    const uint64_t wrs = g.rs == 2 && g.nmat == 2 ? 2 : 1;
     const uint64_t dims[3] = {(uint64_t)(g.C / 2), (uint64_t)g.R, (uint64_t)g.E};
-    const uint64_t strides[2] = {(uint64_t)(g.C / 2), (uint64_t)g.R * (g.C / 2)};
+    const uint64_t strides[2] = {wrs * (g.C / 2), wrs * g.R * (g.C / 2)};
     const uint32_t box[3] = {(uint32_t)(mx::BK / 2), (uint32_t)box_rows, 1};
     if (!encode_tiled_map(&t0, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, g.w_qs[0], dims, strides, box,
                           CU_TENSOR_MAP_SWIZZLE_NONE))
@@ -651,6 +653,7 @@ cudaError_t launch_grouped_mx(const GroupedMXArgs& g, Launch L) {
   prm.w_sc[1] = g.nmat == 2 ? g.w_sc[1] : g.w_sc[0];
   prm.bias[0] = g.bias[0];
   prm.bias[1] = g.nmat == 2 ? g.bias[1] : nullptr;
+  prm.wrs = g.rs == 2 && g.nmat == 2 ? 2 : 1;
   prm.E = g.E;
   prm.R = g.R;
   prm.C = g.C;

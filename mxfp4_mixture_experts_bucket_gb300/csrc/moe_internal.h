@@ -82,7 +82,7 @@ cudaError_t launch_selftest_wait_timeout(const uint8_t* src, int* status, Launch
 cudaError_t launch_quant_q8(const float* v, int64_t rows, int C, int8_t* q, float* d, Launch L);
 cudaError_t launch_gemv_q8(const uint8_t* qs, const uint8_t* sc, int E, int R, int C, const int32_t* experts,
                            int n, int act_div, const int8_t* aq, const float* ad, const float* bias, float* out,
-                           int* status, Launch L);
+                           int* status, Launch L, int wrs = 1);
 cudaError_t launch_combine_slots(const float* o, const float* w, const int32_t* ids, int T, int k, int D, int E,
                                  float* y, Launch L);
 cudaError_t launch_rms_renorm(const float* x, int T, int D, float* y, Launch L);
@@ -99,7 +99,7 @@ cudaError_t launch_gemv_gateup(const uint8_t* g_qs, const uint8_t* g_sc, const f
                                const uint8_t* u_qs, const uint8_t* u_sc, const float* bu, int E,
                                int F, int D, int T, int k, const float* x, const float* logits,
                                const int32_t* ids_in, int32_t* ids_out, float* w_out, float alpha,
-                               float limit, float* h, int* status, bool x_from_prev, Launch L);
+                               float limit, float* h, int* status, bool x_from_prev, Launch L, int rs = 1);
 // Decode rail, stage 1: down projection + bias + router-weighted combine in slot
 // order. Routing from `logits` when not NULL, else from ids_in / w_in.
 cudaError_t launch_gemv_down(const uint8_t* d_qs, const uint8_t* d_sc, const float* bd, int E,
@@ -112,7 +112,7 @@ cudaError_t launch_gemv_down(const uint8_t* d_qs, const uint8_t* d_sc, const flo
 size_t packed_qs_bytes(int E, int R, int C);
 size_t packed_sf_bytes(int E, int R, int C);
 cudaError_t launch_prepack(const uint8_t* qs, const uint8_t* sc, int E, int R, int C, uint8_t* qs_p,
-                           uint8_t* sf_p, Launch L);
+                           uint8_t* sf_p, Launch L, int rs = 1);
 
 // ---- route_bucket.cu: prologue of the block-scaled decode rail ----
 // Router logits, x as E4M3 operand chunks xq [NK][npad][128] + atoms xsf [NK][512],
@@ -165,6 +165,8 @@ struct GroupedMMArgs {
   void* out;
   int64_t out_ld;
   int* status;
+  int rs = 1;  // nmat 2: 1 = separate planes; 2 = gate/up rows interleaved in one plane (w_qs[1], w_sc[1],
+               // bias[1] point one row or one element past w_qs[0], w_sc[0], bias[0])
 };
 // Returns cudaErrorInvalidValue for unsupported shapes (checked by the caller first).
 cudaError_t launch_grouped_mm(const GroupedMMArgs& args, Launch L);
@@ -198,6 +200,7 @@ struct GroupedMXArgs {
   uint32_t* h_sc;    // nmat 2: [2][R/128 rounded up][max_rows]
   float* y;          // nmat 1: [T][R], accumulated into (zeroed beforehand)
   int* status;
+  int rs = 1;        // as GroupedMMArgs::rs
 };
 constexpr int kMxXTerms = 3;
 constexpr int kMxHTerms = 2;

@@ -19,6 +19,11 @@
 //        chunk, byte 16*(m%32) + 4*(m/32) + kb = E8M0 of tile row m, block
 //        4j+kb; 127 (a scale of 1) where the row or the block does not exist.
 //
+// The source may hold two matrices' rows interleaved (gate/up of gpt-oss, one
+// [2R][C] plane per expert): with row stride rs = 2 row r of the matrix is
+// source row 2r of the plane starting at `qs` (pass qs one row further for
+// the odd rows).
+//
 // The atom is the order tcgen05.cp.32x128b.warpx4 copies into tensor memory
 // (32 rows of 16 bytes, each row replicated into the four lane quarters): row m
 // of the tile then finds its four scale bytes in lane m, column m/32.
@@ -29,7 +34,7 @@ namespace moe {
 // One thread per 16-byte block of the output (expert e, row, block b < 4*NK):
 // the stored block, or zero past the last column.
 __global__ void __launch_bounds__(256) prepack_qs_kernel(const uint8_t* __restrict__ qs, int E, int R, int C,
-                                                         uint8_t* __restrict__ qs_p) {
+                                                         int rs, uint8_t* __restrict__ qs_p) {
   const int nb = C / 32, NK = (C + 127) / 128, nbp = 4 * NK;
   const size_t total = (size_t)E * R * nbp;
   for (size_t p = (size_t)blockIdx.x * blockDim.x + threadIdx.x; p < total; p += (size_t)gridDim.x * blockDim.x) {
@@ -43,13 +48,13 @@ __global__ void __launch_bounds__(256) prepack_qs_kernel(const uint8_t* __restri
     const size_t dst = ((size_t)e * R + 128 * (size_t)t) * ((size_t)NK * 64) + (size_t)rows_t * 64 * j +
                        (size_t)(m * 64 + 16 * (kb ^ ((m >> 1) & 3)));
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (b < nb) v = __ldg(reinterpret_cast<const uint4*>(qs + ((size_t)e * R + row) * (C / 2)) + b);
+    if (b < nb) v = __ldg(reinterpret_cast<const uint4*>(qs + ((size_t)e * R + row) * rs * (C / 2)) + b);
     *reinterpret_cast<uint4*>(qs_p + dst) = v;
   }
 }
 
 __global__ void __launch_bounds__(256) prepack_sf_kernel(const uint8_t* __restrict__ sc, int E, int R, int C,
-                                                         uint8_t* __restrict__ sf_p) {
+                                                         int rs, uint8_t* __restrict__ sf_p) {
   const int NK = (C + 127) / 128, nb = C / 32, NT = (R + 127) / 128;
   const size_t total = (size_t)E * NT * NK * 512;
   for (size_t p = (size_t)blockIdx.x * blockDim.x + threadIdx.x; p < total; p += (size_t)gridDim.x * blockDim.x) {
@@ -62,7 +67,7 @@ __global__ void __launch_bounds__(256) prepack_sf_kernel(const uint8_t* __restri
     const int l = byte >> 4, q = (byte >> 2) & 3, kb = byte & 3;
     const int row = 128 * t + 32 * q + l, b = 4 * j + kb;
     uint8_t v = 127;
-    if (row < R && b < nb) v = sc[((size_t)e * R + row) * nb + b];
+    if (row < R && b < nb) v = sc[((size_t)e * R + row) * rs * nb + b];
     sf_p[p] = v;
   }
 }
@@ -73,7 +78,7 @@ size_t packed_sf_bytes(int E, int R, int C) {
 }
 
 cudaError_t launch_prepack(const uint8_t* qs, const uint8_t* sc, int E, int R, int C, uint8_t* qs_p,
-                           uint8_t* sf_p, Launch L) {
+                           uint8_t* sf_p, Launch L, int rs) {
   const int cap = device_sm_count() * 8;
   auto blocks_for = [&](size_t n) {
     size_t b = (n + 255) / 256;
@@ -81,9 +86,9 @@ cudaError_t launch_prepack(const uint8_t* qs, const uint8_t* sc, int E, int R, i
     return (int)(b < 1 ? 1 : b);
   };
   const size_t nq = (size_t)E * R * ((C + 127) / 128) * 4, ns = packed_sf_bytes(E, R, C);
-  cudaError_t err = launch_kernel(prepack_qs_kernel, dim3(blocks_for(nq)), dim3(256), 0, L, qs, E, R, C, qs_p);
+  cudaError_t err = launch_kernel(prepack_qs_kernel, dim3(blocks_for(nq)), dim3(256), 0, L, qs, E, R, C, rs, qs_p);
   if (err != cudaSuccess) return err;
-  return launch_kernel(prepack_sf_kernel, dim3(blocks_for(ns)), dim3(256), 0, L, sc, E, R, C, sf_p);
+  return launch_kernel(prepack_sf_kernel, dim3(blocks_for(ns)), dim3(256), 0, L, sc, E, R, C, rs, sf_p);
 }
 
 }  // namespace moe

@@ -75,7 +75,7 @@ template <int NBL>
 __global__ void __launch_bounds__(kQ8Warps * 32) gemv_q8_kernel(
     const uint8_t* __restrict__ qs, const uint8_t* __restrict__ sc, int E, int R, int C,
     const int32_t* __restrict__ experts, int act_div, const int8_t* __restrict__ aq, const float* __restrict__ ad,
-    const float* __restrict__ bias, float* __restrict__ out, int* status) {
+    const float* __restrict__ bias, float* __restrict__ out, int* status, int wrs) {
   pdl_launch_dependents();
   pdl_wait();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(kQ8Warps * 32) gemv_q8_kernel(
   const int a = i / act_div;
   const int8_t* qa = aq + (size_t)a * C;
   const float* da = ad + (size_t)a * nb;
-  const size_t row = (size_t)e * R + r;
+  const size_t row = ((size_t)e * R + r) * wrs;  // wrs = 2: gate/up rows interleaved in one plane
   float acc = 0.f;
 #pragma unroll
   for (int j = 0; j < NBL; ++j) {
@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(kQ8Warps * 32) gemv_q8_kernel(
   }
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, m));
-  if (lane == 0) out[(size_t)i * R + r] = bias ? __fadd_rn(acc, bias[(size_t)e * R + r]) : acc;
+  if (lane == 0) out[(size_t)i * R + r] = bias ? __fadd_rn(acc, bias[row]) : acc;
 }
 
 // ---------------------------------------------------------------------------
@@ -158,22 +158,23 @@ cudaError_t launch_quant_q8(const float* v, int64_t rows, int C, int8_t* q, floa
 
 cudaError_t launch_gemv_q8(const uint8_t* qs, const uint8_t* sc, int E, int R, int C, const int32_t* experts,
                            int n, int act_div, const int8_t* aq, const float* ad, const float* bias, float* out,
-                           int* status, Launch L) {
+                           int* status, Launch L, int wrs) {
   if (n <= 0 || R <= 0) return cudaSuccess;
+  if (wrs != 1 && wrs != 2) return cudaErrorInvalidValue;
   const dim3 grid((R + kQ8Warps - 1) / kQ8Warps, n);
   switch (((C >> 5) + 31) / 32) {
     case 1:
       return launch_kernel(gemv_q8_kernel<1>, grid, dim3(kQ8Warps * 32), 0, L, qs, sc, E, R, C, experts, act_div,
-                           aq, ad, bias, out, status);
+                           aq, ad, bias, out, status, wrs);
     case 2:
       return launch_kernel(gemv_q8_kernel<2>, grid, dim3(kQ8Warps * 32), 0, L, qs, sc, E, R, C, experts, act_div,
-                           aq, ad, bias, out, status);
+                           aq, ad, bias, out, status, wrs);
     case 3:
       return launch_kernel(gemv_q8_kernel<3>, grid, dim3(kQ8Warps * 32), 0, L, qs, sc, E, R, C, experts, act_div,
-                           aq, ad, bias, out, status);
+                           aq, ad, bias, out, status, wrs);
     case 4:
       return launch_kernel(gemv_q8_kernel<4>, grid, dim3(kQ8Warps * 32), 0, L, qs, sc, E, R, C, experts, act_div,
-                           aq, ad, bias, out, status);
+                           aq, ad, bias, out, status, wrs);
     default:
       return cudaErrorInvalidValue;
   }

@@ -13,7 +13,7 @@ import torch
 from . import _lib
 
 _WEIGHT_KEYS = ("w_router", "b_router", "g_qs", "g_sc", "u_qs", "u_sc", "d_qs", "d_sc",
-                "bg", "bu", "bd")
+                "bg", "bu", "bd", "gu_qs", "gu_sc", "gu_b")
 
 
 class MoeLayer:
@@ -22,6 +22,9 @@ class MoeLayer:
     weights: dict with w_router [E, D] f32, b_router [E] f32 (optional),
     g_qs/u_qs [E, F, D/2] u8, g_sc/u_sc [E, F, D/32] u8, d_qs [E, D, F/2] u8,
     d_sc [E, D, F/32] u8, bg/bu [E, F] f32, bd [E, D] f32 (biases optional).
+    Gate and up may instead come as gpt-oss stores them, one interleaved plane
+    per expert: gu_qs [E, 2F, D/2], gu_sc [E, 2F, D/32], gu_b [E, 2F] (gate row
+    f = row 2f, up row f = row 2f+1); the layer then runs moe_ffn_layer_gu.
     Host (numpy or torch CPU) arrays are copied to `device` once.
     """
 
@@ -37,7 +40,10 @@ class MoeLayer:
             t = v if isinstance(v, torch.Tensor) else torch.from_numpy(v)
             self.w[key] = t.to(self.device).contiguous()
         self.E, self.D = self.w["w_router"].shape
-        self.F = self.w["g_qs"].shape[1]
+        self.interleaved = self.w["gu_qs"] is not None
+        if self.interleaved and self.w["g_qs"] is not None:
+            raise ValueError("give gate/up either as g_*/u_* planes or as one interleaved gu_* plane")
+        self.F = self.w["gu_qs"].shape[1] // 2 if self.interleaved else self.w["g_qs"].shape[1]
         self.k = k
         self._ws: Dict[int, torch.Tensor] = {}
         self._io: Dict[tuple, tuple] = {}
@@ -45,7 +51,7 @@ class MoeLayer:
         if packed:
             self._prepack()
             if not keep_canonical:
-                for key in ("g_qs", "g_sc", "u_qs", "u_sc", "d_qs", "d_sc"):
+                for key in ("g_qs", "g_sc", "u_qs", "u_sc", "d_qs", "d_sc", "gu_qs", "gu_sc"):
                     self.w[key] = None
 
     def _prepack(self):
@@ -56,16 +62,25 @@ class MoeLayer:
             ns = _lib.moe_mxfp4_packed_sf_bytes(self.E, R, C)
             if nq == 0 or ns == 0:
                 raise _lib.MoeError(f"shape ({self.E}, {R}, {C}) cannot be prepacked")
-            qs_p = torch.empty(nq, dtype=torch.uint8, device=self.device)
-            sf_p = torch.empty(ns, dtype=torch.uint8, device=self.device)
-            _lib.check(_lib.moe_mxfp4_prepack(self.w[m + "_qs"], self.w[m + "_sc"], self.E, R, C, qs_p, sf_p),
-                       "moe_mxfp4_prepack")
-            pk[m + "_qs"], pk[m + "_sf"] = qs_p, sf_p
+            pk[m + "_qs"] = torch.empty(nq, dtype=torch.uint8, device=self.device)
+            pk[m + "_sf"] = torch.empty(ns, dtype=torch.uint8, device=self.device)
+            if m == "d" or not self.interleaved:
+                _lib.check(_lib.moe_mxfp4_prepack(self.w[m + "_qs"], self.w[m + "_sc"], self.E, R, C, pk[m + "_qs"],
+                                                  pk[m + "_sf"]), "moe_mxfp4_prepack")
+        if self.interleaved:
+            _lib.check(_lib.moe_mxfp4_prepack_gu(self.w["gu_qs"], self.w["gu_sc"], self.E, self.F, self.D,
+                                                 pk["g_qs"], pk["g_sf"], pk["u_qs"], pk["u_sf"]),
+                       "moe_mxfp4_prepack_gu")
         self.packed = pk
         w = self.w
+        bg, bu = w["bg"], w["bu"]
+        if self.interleaved and w["gu_b"] is not None:  # the packed layer struct takes separate bias rows
+            gb = w["gu_b"].view(self.E, self.F, 2)
+            self._bias_split = (gb[:, :, 0].contiguous(), gb[:, :, 1].contiguous())
+            bg, bu = self._bias_split
         self.packed_struct = _lib.make_packed_layer(self.D, self.F, self.E, self.k, w["w_router"], w["b_router"],
-                                                    pk["g_qs"], pk["g_sf"], w["bg"], pk["u_qs"], pk["u_sf"],
-                                                    w["bu"], pk["d_qs"], pk["d_sf"], w["bd"])
+                                                    pk["g_qs"], pk["g_sf"], bg, pk["u_qs"], pk["u_sf"],
+                                                    bu, pk["d_qs"], pk["d_sf"], w["bd"])
 
     def _use_packed(self, T: int, rail: int) -> bool:
         # MOE_RAIL_AUTO with both sets of planes takes the rail measured fastest on
@@ -79,7 +94,7 @@ class MoeLayer:
             return True
         if rail != _lib.MOE_RAIL_AUTO or T > _lib.MOE_GEMV_MAX_T:
             return False
-        return self.w["g_qs"] is None or T >= 2
+        return (self.w["g_qs"] is None and self.w["gu_qs"] is None) or T >= 2
 
     def workspace(self, T: int, rail: int) -> torch.Tensor:
         if self._use_packed(T, rail):
@@ -108,6 +123,12 @@ class MoeLayer:
             _lib.check(rc, "moe_ffn_layer_packed")
             return out
         w = self.w
+        if self.interleaved:
+            rc = _lib.moe_ffn_layer_gu(x, T, self.D, self.F, self.E, self.k, w["w_router"], w["b_router"],
+                                       w["gu_qs"], w["gu_sc"], w["gu_b"], w["d_qs"], w["d_sc"], w["bd"], rail, ws,
+                                       ws.numel(), out, ids_out, weights_out, stream)
+            _lib.check(rc, "moe_ffn_layer_gu")
+            return out
         rc = _lib.moe_ffn_layer(x, T, self.D, self.F, self.E, self.k, w["w_router"], w["b_router"],
                                 w["g_qs"], w["g_sc"], w["bg"], w["u_qs"], w["u_sc"], w["bu"],
                                 w["d_qs"], w["d_sc"], w["bd"], rail, ws, ws.numel(), out, ids_out,
@@ -136,6 +157,8 @@ class MoeLayer:
                                                   stream)
             _lib.check(rc, "moe_ffn_layer_packed_hostio")
             return y_host
+        if self.interleaved:
+            raise NotImplementedError("host I/O runs on separate gate/up planes or the prepacked rail")
         key = (T, rail)
         io = self._io.get(key)
         if io is None:  # staging buffers and the fixed arguments, once per (T, rail)

@@ -7,6 +7,7 @@ the CPU oracle and the CUDA path can take their inputs from it.
 
 from .moe_inputs import (  # noqa: F401
     CONFIGS,
+    interleave_gate_up,
     LayerSpec,
     make_layer,
     make_tokens,

@@ -152,3 +152,25 @@ def make_layer_torch(spec: LayerSpec, layer: int, device, with_tokens: bool = Fa
     if with_tokens:
         out["x"] = torch.randn((spec.T, D), generator=g, device=device, dtype=torch.float32)
     return out
+
+
+def interleave_gate_up(layer: Dict[str, object]) -> Dict[str, object]:
+    """The same layer with gate and up stored as gpt-oss stores them: one plane
+    per expert of 2F rows, gate row f at row 2f and up row f at row 2f+1
+    (gu_qs [E, 2F, D/2], gu_sc [E, 2F, D/32], gu_b [E, 2F]). A storage layout
+    only: numpy arrays stay numpy, torch tensors stay on their device."""
+    out = {k: v for k, v in layer.items() if k not in ("g_qs", "g_sc", "u_qs", "u_sc", "bg", "bu")}
+
+    def inter(a, b):
+        if isinstance(a, np.ndarray):
+            E, F = a.shape[:2]
+            return np.stack([a, b], axis=2).reshape((E, 2 * F) + a.shape[2:])
+        import torch
+        E, F = a.shape[:2]
+        return torch.stack([a, b], dim=2).reshape((E, 2 * F) + tuple(a.shape[2:])).contiguous()
+
+    out["gu_qs"] = inter(layer["g_qs"], layer["u_qs"])
+    out["gu_sc"] = inter(layer["g_sc"], layer["u_sc"])
+    if layer.get("bg") is not None and layer.get("bu") is not None:
+        out["gu_b"] = inter(layer["bg"], layer["bu"])
+    return out
