@@ -462,7 +462,26 @@ def run_ours(args, dist: Dist):
     del stage_ws
     mx_rate, _ = whole_job_rate(K, mx_secs, dist)
 
-    # ---- rail crossover, T = 1 .. 64 (same layers) ----
+    # ---- the same decode step with gate/up stored interleaved (one [2F][D] plane per expert) ----
+    from synthetic import interleave_gate_up
+    ilv_layers = [moe.MoeLayer(interleave_gate_up(make_layer_torch(spec, li + 17 * dist.rank, dev)), k=K_TOP,
+                               device=dev) for li in range(NL)]
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            ilv_layers[i % NL](xs[i:i + 1], rail=head_rail, out=ys[i:i + 1])
+    torch.cuda.synchronize()
+
+    def ilv_body():
+        for i in range(K):
+            j = W + i
+            ilv_layers[j % NL](xs[j:j + 1], rail=head_rail, out=ys[j:j + 1])
+
+    ilv_secs = graph_seconds(stream, ilv_body)[0]
+    check_status(moe, stream)
+    ilv_rate, _ = whole_job_rate(K, ilv_secs, dist)
+    del ilv_layers
+
+    # ---- rail crossover, T = 1 .. 512 (same layers) ----
     crossover = None if args.no_crossover else run_crossover(moe, layers, stream, dev, dist)
 
     result = {
@@ -489,6 +508,9 @@ def run_ours(args, dist: Dist):
             "rail": "decode_mx (block-scaled tcgen05 MMA on prepacked MXFP4 weights, activations as 8 E2M1 terms)",
             "gateup_kernel": "decode_mx_kernel<0>", "gateup_launch_us": round(mx_kern_s * 1e6, 3),
             "gateup_frac": round(gateup_bytes / mx_kern_s / 1e9 / hbm_peak, 4)},
+        "decode_t1_interleaved": {"tokens_per_s": round(ilv_rate, 1), "ms_per_step": round(ilv_secs / K * 1e3, 5),
+                                  "rail": "gemv on gate/up stored interleaved (moe_ffn_layer_gu: one copy of a "
+                                          "sub-task's 2x8 gate/up rows)"},
         "crossover": crossover,
         "clocks": clocks,
         "gpu_launches": int(round(launches_per_step * K)),
