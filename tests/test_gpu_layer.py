@@ -37,6 +37,22 @@ def run_layer(moe, layer, x_np, rail, k):
     return y.cpu().numpy(), ids.cpu().numpy(), w.cpu().numpy()
 
 
+def tile_boundary_tokens(ids, E, k, tile=128):
+    """Tokens whose assignments sit at the edges of the grouped GEMM's work: each
+    expert's first and last live bucket row, and the first and last live row of
+    every 128-row bucket tile (the oracle's CSR of the GPU's own routing)."""
+    csr = O.bucket_csr(ids, E, tile)
+    rows, basep, counts = csr["rows"], csr["basep"], csr["counts"]
+    picks = set()
+    for e in range(E):
+        n = int(counts[e])
+        for lo in range(0, n, tile):
+            hi = min(n, lo + tile) - 1
+            picks.add(int(rows[basep[e] + lo]) // k)
+            picks.add(int(rows[basep[e] + hi]) // k)
+    return np.array(sorted(picks), dtype=np.int64)
+
+
 def check_layer(moe, cfg, T, rail, sample=None, seed=None):
     spec, L, layer, cache = layer_for(moe, cfg)
     if rail == moe.MOE_RAIL_AUTO:  # the canonical planes' automatic choice by T
@@ -49,6 +65,9 @@ def check_layer(moe, cfg, T, rail, sample=None, seed=None):
     margin = O.routing_margins(logits, spec.k)
     clear = margin > 1e-4 * np.abs(logits).max()
     assert np.array_equal(ids[clear], ids_ref[clear])
+    if isinstance(sample, str) and sample == "tiles":
+        sample = tile_boundary_tokens(ids, spec.E, spec.k)
+        print(f"cfg {cfg} T {T}: {len(sample)} tokens sampled at bucket-tile edges")
     toks = np.arange(T) if sample is None else sample
     # evaluate the oracle on the GPU's routing for the sampled tokens (identical where clear)
     w_ref = np.take_along_axis(logits, ids.astype(np.int64), 1)
@@ -104,18 +123,24 @@ def test_decode_T8_full_size(moe):
 
 
 def test_prefill_T512_full_size_sampled(moe):
-    # the prefill workload (T=512), sampled tokens through the oracle
-    check_layer(moe, 2, 512, moe.MOE_RAIL_AUTO, sample=np.array([0, 1, 255, 511]))
+    # the prefill workload (T=512): the first and last token, and every token at
+    # an edge of a bucket tile (each expert's first and last live row, each
+    # 128-row tile's first and last), through the oracle
+    y, ids = check_layer(moe, 2, 512, moe.MOE_RAIL_GROUPED_MM, sample="tiles")
 
 
 def test_prefill_T512_full_size_sampled_mx(moe):
-    check_layer(moe, 2, 512, moe.MOE_RAIL_GROUPED_MX, sample=np.array([0, 1, 100, 255, 511]))
+    check_layer(moe, 2, 512, moe.MOE_RAIL_GROUPED_MX, sample="tiles")
+
+
+def test_prefill_T512_auto_rail(moe):
+    check_layer(moe, 2, 512, moe.MOE_RAIL_AUTO, sample=np.array([0, 1, 255, 511]))
 
 
 @pytest.mark.parametrize("rail_name", ["GROUPED_MM", "GROUPED_MX"])
 def test_skew_T4096_full_size_sampled(moe, rail_name):
     spec, L, layer, cache = layer_for(moe, 4)
-    y, ids = check_layer(moe, 4, 4096, getattr(moe, "MOE_RAIL_" + rail_name), sample=np.array([0, 777, 4095]))
+    y, ids = check_layer(moe, 4, 4096, getattr(moe, "MOE_RAIL_" + rail_name), sample="tiles")
     counts = np.bincount(ids.reshape(-1), minlength=spec.E)
     # the stated shape of the skewed workload: about half of the assignments on the
     # two hot experts, several experts nearly empty
