@@ -328,7 +328,9 @@ def run_ours(args, dist: Dist):
     if args.skip_decode:
         return {"prefill_t512": run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src),
                 "prefill_t512_mx": run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src,
-                                               rail=moe.MOE_RAIL_GROUPED_MX)}
+                                               rail=moe.MOE_RAIL_GROUPED_MX),
+                "prefill_t512_mx4": run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src,
+                                                rail=moe.MOE_RAIL_GROUPED_MX4)}
     K, W, NL = args.steps, args.warmup, args.layers
     spec = spec_for(1)
 
@@ -523,7 +525,11 @@ def run_ours(args, dist: Dist):
         result["prefill_t512"] = run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src)
         result["prefill_t512_mx"] = run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src,
                                                 rail=moe.MOE_RAIL_GROUPED_MX)
+        result["prefill_t512_mx4"] = run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src,
+                                                 rail=moe.MOE_RAIL_GROUPED_MX4)
         result["skew_t4096"] = run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src, cfg=4)
+        result["skew_t4096_mx4"] = run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src, cfg=4,
+                                               rail=moe.MOE_RAIL_GROUPED_MX4)
         result["skew_t4096_mx"] = run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src, cfg=4,
                                               rail=moe.MOE_RAIL_GROUPED_MX)
     if not args.no_stack:
@@ -537,7 +543,8 @@ def run_crossover(moe, layers, stream, dev, dist, Ts=(1, 2, 4, 8, 16, 32, 64, 12
     import torch
 
     rails = {"gemv": moe.MOE_RAIL_GEMV, "decode_mx": moe.MOE_RAIL_DECODE_MX,
-             "grouped_mm": moe.MOE_RAIL_GROUPED_MM, "grouped_mx": moe.MOE_RAIL_GROUPED_MX}
+             "grouped_mm": moe.MOE_RAIL_GROUPED_MM, "grouped_mx": moe.MOE_RAIL_GROUPED_MX,
+             "grouped_mx4": moe.MOE_RAIL_GROUPED_MX4}
     NL = len(layers)
     out = {"unit": "us per layer step", "layers_rotated": NL, "steps": steps}
     g = torch.Generator(device=dev)
@@ -580,7 +587,9 @@ def run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src, rai
     if rail is None:
         rail = moe.MOE_RAIL_GROUPED_MM
     NL = 2
-    layers = [moe.MoeLayer(make_layer_torch(spec, li + 31 * dist.rank, dev), k=K_TOP, device=dev) for li in range(NL)]
+    packed = rail == moe.MOE_RAIL_GROUPED_MX4
+    layers = [moe.MoeLayer(make_layer_torch(spec, li + 31 * dist.rank, dev), k=K_TOP, device=dev, packed=packed,
+                           keep_canonical=not packed) for li in range(NL)]
     g = torch.Generator(device=dev)
     g.manual_seed(777 + dist.rank)
     xs = [torch.randn((T, D), generator=g, device=dev) for _ in range(NL)]
@@ -621,9 +630,12 @@ def run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src, rai
     workload = WORKLOAD_PREFILL if cfg == 2 else WORKLOAD_SKEW
     return {"tokens_per_s": round(rate, 1), "ms_per_step": round(ms, 4), "steps": K, "workload": workload,
             "weight_gbs": round(weight_bytes / (ms / 1e3) / 1e9, 1),
-            "dtype": ("bf16 MMA, fp32 accumulate" if rail == moe.MOE_RAIL_GROUPED_MM else
-                      "MXFP4 x E4M3-term block-scaled MMA (x: 3 terms, h: 2), fp32 accumulate"),
-            "rail": "grouped_mm" if rail == moe.MOE_RAIL_GROUPED_MM else "grouped_mx",
+            "dtype": {moe.MOE_RAIL_GROUPED_MM: "bf16 MMA, fp32 accumulate",
+                      moe.MOE_RAIL_GROUPED_MX: "MXFP4 x E4M3-term block-scaled MMA (x: 3 terms, h: 2), fp32 accumulate",
+                      moe.MOE_RAIL_GROUPED_MX4: "MXFP4 x E2M1-term block-scaled MMA, kind::mxf4 on prepacked weights "
+                                                "(x: 6 terms, h: 3), fp32 accumulate"}[rail],
+            "rail": {moe.MOE_RAIL_GROUPED_MM: "grouped_mm", moe.MOE_RAIL_GROUPED_MX: "grouped_mx",
+                     moe.MOE_RAIL_GROUPED_MX4: "grouped_mx4"}[rail],
             "roofline_frac": round(t_roof / (ms / 1e3), 4),
             "roofline_bound": "hbm" if alg_bytes / (hbm_peak * 1e9) >= flops / (bf16_peak * 1e12) else "tensor",
             "roofline_us": round(t_roof * 1e6, 1),

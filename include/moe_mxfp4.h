@@ -77,6 +77,7 @@ extern "C" {
 #define MOE_RAIL_GROUPED_MX 3 /* grouped GEMM on the block-scaled (MXFP4 x E4M3) tensor cores */
 #define MOE_RAIL_DECODE_MX 4  /* T <= MOE_GEMV_MAX_T on the block-scaled tensor cores (prepacked weights) */
 #define MOE_RAIL_GEMV_Q8 5    /* T <= MOE_GEMV_MAX_T: x and h requantised to Q8, integer MXFP4 x Q8 dots */
+#define MOE_RAIL_GROUPED_MX4 6 /* prepacked weights, any T: grouped GEMMs on tcgen05.mma kind::mxf4 */
 #define MOE_GEMV_MAX_T 8
 /*
  * MOE_RAIL_AUTO on the canonical planes (moe_ffn_layer and friends) takes the
@@ -500,15 +501,23 @@ size_t moe_ffn_packed_workspace_bytes(int T, int D, int F, int E, int k, int rai
  * CTAs are summed in a fixed order, so results are deterministic.
  * h_out (may be NULL): receives the swiglu outputs h[t*k+j][F] of the
  * assignments (decode rail only). Other arguments and limits as in
- * moe_ffn_layer; D and F multiples of 64; k*T <= 64. Returns
- * MOE_EUNSUPPORTED for T > MOE_GEMV_MAX_T.
+ * moe_ffn_layer; D and F multiples of 64; k*T <= 64 on the decode rail.
+ * MOE_RAIL_GROUPED_MX4 (MOE_RAIL_AUTO for T > MOE_GEMV_MAX_T) runs the prefill
+ * chain of "dasLLAMA gpt-oss arc" (Metal fusion lane commit: router, the
+ * MoeBucket CSR with the prefix folded in, the MXFP4 grouped mul_mm for
+ * gate/up with bias and swiglu, then down with bias and the router-weighted
+ * scatter) on the same prepacked planes: x enters as four E2M1 terms per value
+ * in bucket order, each 128-row bucket tile meets 256 weight rows per MMA
+ * (gate/up: a gate tile and its up tile) on tcgen05.mma kind::mxf4, h leaves
+ * the gate/up epilogue as four E2M1 terms, and the down epilogue scatters
+ * w*(acc + bd) into y with float atomics (summation order not deterministic).
  */
 int moe_ffn_layer_packed(const moe_packed_layer_t* layer, const float* x, int T, int rail, void* workspace,
                          size_t workspace_bytes, float* y, int32_t* ids_out, float* weights_out, float* h_out,
                          cudaStream_t stream);
 
 /* Stages of the block-scaled decode rail (moe_ffn_layer_packed_stage, a bit mask). */
-#define MOE_STAGE_PROLOGUE 1 /* router logits, x as E4M3 operand terms, counters zeroed */
+#define MOE_STAGE_PROLOGUE 1 /* router logits, x as E2M1 operand terms, counters zeroed */
 #define MOE_STAGE_GATEUP 2   /* gate/up + bias + swiglu, the down operand written to the workspace */
 #define MOE_STAGE_DOWN 4     /* down + bias + router-weighted combine into y */
 

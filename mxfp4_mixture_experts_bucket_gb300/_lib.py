@@ -43,6 +43,7 @@ MOE_RAIL_GROUPED_MM = 2
 MOE_RAIL_GROUPED_MX = 3
 MOE_RAIL_DECODE_MX = 4
 MOE_RAIL_GEMV_Q8 = 5
+MOE_RAIL_GROUPED_MX4 = 6
 MOE_STAGE_PROLOGUE = 1
 MOE_STAGE_GATEUP = 2
 MOE_STAGE_DOWN = 4

@@ -21,7 +21,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe_mxfp4.so")
 
 SOURCES = ["abi.cu", "route_bucket.cu", "gemv.cu", "decode.cu", "decode_mx.cu", "prepack.cu", "grouped_mm.cu",
-           "grouped_mx.cu", "noalloc.cu", "selftest.cu", "q8.cu"]
+           "grouped_mx.cu", "noalloc.cu", "selftest.cu", "q8.cu", "grouped_mx4.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "-I" + INCLUDE, "-I" + CSRC] + ARCH

@@ -206,8 +206,53 @@ size_t layout_packed_workspace(int T, int D, int F, int k, int E, char* base, Pa
 }
 
 int resolve_packed_rail(int T, int rail) {
-  if (rail == MOE_RAIL_AUTO) return T <= MOE_GEMV_MAX_T ? MOE_RAIL_DECODE_MX : MOE_RAIL_GROUPED_MX;
+  if (rail == MOE_RAIL_AUTO) return T <= MOE_GEMV_MAX_T ? MOE_RAIL_DECODE_MX : MOE_RAIL_GROUPED_MX4;
   return rail;
+}
+
+// Workspace of the prefill rail on prepacked weights (MOE_RAIL_GROUPED_MX4).
+struct PackedPrefillWorkspace {
+  float* logits;
+  int32_t* ids;
+  float* w;
+  int32_t* counts;
+  int32_t* basep;
+  int32_t* rows;
+  int32_t* inv;
+  uint8_t* aq;   // x terms in bucket order, activation-chunk layout
+  uint8_t* asf;
+  uint8_t* hq;   // h terms, written by the gate/up GEMM
+  uint8_t* hsf;
+  float* xs;     // host-I/O staging [T][D]
+  float* ys;
+  size_t max_rows;
+};
+
+size_t layout_packed_prefill_workspace(int T, int D, int F, int k, int E, char* base, PackedPrefillWorkspace* ws) {
+  const size_t mr = max_rows_of(T, k, E, MOE_MM_TILE);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    char* p = base ? base + off : nullptr;
+    off = round_up(off + bytes, 256);
+    return p;
+  };
+  PackedPrefillWorkspace w{};
+  w.logits = reinterpret_cast<float*>(take((size_t)T * E * 4));
+  w.ids = reinterpret_cast<int32_t*>(take((size_t)T * k * 4));
+  w.w = reinterpret_cast<float*>(take((size_t)T * k * 4));
+  w.counts = reinterpret_cast<int32_t*>(take((size_t)E * 4));
+  w.basep = reinterpret_cast<int32_t*>(take((size_t)(E + 1) * 4));
+  w.rows = reinterpret_cast<int32_t*>(take(mr * 4));
+  w.inv = reinterpret_cast<int32_t*>(take((size_t)T * k * 4));
+  w.aq = reinterpret_cast<uint8_t*>(take(prefill_operand_bytes((int)mr, D, kPrefillXTerms)));
+  w.asf = reinterpret_cast<uint8_t*>(take(prefill_atom_bytes((int)mr, D, kPrefillXTerms)));
+  w.hq = reinterpret_cast<uint8_t*>(take(prefill_operand_bytes((int)mr, F, kPrefillHTerms)));
+  w.hsf = reinterpret_cast<uint8_t*>(take(prefill_atom_bytes((int)mr, F, kPrefillHTerms)));
+  w.xs = reinterpret_cast<float*>(take((size_t)T * D * 4));
+  w.ys = reinterpret_cast<float*>(take((size_t)T * D * 4));
+  w.max_rows = mr;
+  if (ws) *ws = w;
+  return off;
 }
 
 }  // namespace
@@ -772,13 +817,86 @@ int moe_mxfp4_prepack_gu(const uint8_t* gu_qs, const uint8_t* gu_sc, int E, int 
 
 size_t moe_ffn_packed_workspace_bytes(int T, int D, int F, int E, int k, int rail) {
   if (T < 0 || D < 64 || F < 64 || D % 64 != 0 || F % 64 != 0 || E < 1 || k < 1 || k > E) return 0;
-  if (resolve_packed_rail(T, rail) != MOE_RAIL_DECODE_MX || T > MOE_GEMV_MAX_T) return 0;
+  rail = resolve_packed_rail(T, rail);
+  if (rail == MOE_RAIL_GROUPED_MX4) return layout_packed_prefill_workspace(T, D, F, k, E, nullptr, nullptr);
+  if (rail != MOE_RAIL_DECODE_MX || T > MOE_GEMV_MAX_T) return 0;
   return layout_packed_workspace(T, D, F, k, E, nullptr, nullptr);
 }
 
 }  // extern "C"
 
 namespace {
+// The prefill chain on prepacked planes: router, top-k, bucket (128-row tiles),
+// x as E2M1 terms in bucket order (y zeroed), gate/up + swiglu, down + scatter.
+int packed_prefill_impl(const moe_packed_layer_t& P, const float* x, int T, void* workspace, size_t workspace_bytes,
+                        float* y, int32_t* ids_out, float* weights_out, cudaStream_t stream) {
+  if (P.D > 4096 || P.F > 4096) return MOE_EUNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  MOE_REQUIRE(x && y && workspace && P.w_router && P.g_qs && P.g_sf && P.u_qs && P.u_sf && P.d_qs && P.d_sf);
+  MOE_REQUIRE(aligned(x, 16) && aligned(y, 16) && aligned(P.w_router, 16) && aligned(workspace, 256));
+  MOE_REQUIRE(aligned(P.g_qs, 32) && aligned(P.u_qs, 32) && aligned(P.d_qs, 32));
+  MOE_REQUIRE(aligned(P.g_sf, 16) && aligned(P.u_sf, 16) && aligned(P.d_sf, 16));
+  MOE_REQUIRE(workspace_bytes >= layout_packed_prefill_workspace(T, P.D, P.F, P.k, P.E, nullptr, nullptr));
+  DeviceInfo* d = nullptr;
+  int rc = current_device(&d);
+  if (rc != MOE_OK) return rc;
+  PackedPrefillWorkspace ws;
+  layout_packed_prefill_workspace(T, P.D, P.F, P.k, P.E, static_cast<char*>(workspace), &ws);
+  int32_t* ids = ids_out ? ids_out : ws.ids;
+  float* wts = weights_out ? weights_out : ws.w;
+  Launch L{stream, false};
+  if ((rc = cuda_status(launch_router_logits(x, T, P.D, P.w_router, P.b_router, P.E, ws.logits, nullptr, L))) !=
+      MOE_OK)
+    return rc;
+  L.pdl = true;
+  if ((rc = cuda_status(launch_topk_softmax(ws.logits, T, P.E, P.k, ids, wts, L))) != MOE_OK) return rc;
+  if ((rc = cuda_status(launch_bucket(ids, T, P.k, P.E, MOE_MM_TILE, (int)ws.max_rows, ws.counts, ws.basep, ws.rows,
+                                      ws.inv, d->status, L))) != MOE_OK)
+    return rc;
+  if ((rc = cuda_status(launch_quant_rows_e2m1(x, T, P.D, P.k, ws.rows, ws.basep, P.E, (int)ws.max_rows, ws.aq,
+                                               ws.asf, y, L))) != MOE_OK)
+    return rc;
+  GroupedMX4Args g{};
+  g.kind = 0;
+  g.w_qs[0] = P.g_qs;
+  g.w_qs[1] = P.u_qs;
+  g.w_sf[0] = P.g_sf;
+  g.w_sf[1] = P.u_sf;
+  g.bias[0] = P.bg;
+  g.bias[1] = P.bu;
+  g.E = P.E;
+  g.R = P.F;
+  g.C = P.D;
+  g.counts = ws.counts;
+  g.basep = ws.basep;
+  g.rows = ws.rows;
+  g.max_rows = (int)ws.max_rows;
+  g.k = P.k;
+  g.weights = wts;
+  g.aq = ws.aq;
+  g.asf = ws.asf;
+  g.hq = ws.hq;
+  g.hsf = ws.hsf;
+  g.alpha = 1.702f;
+  g.limit = 7.0f;
+  g.status = d->status;
+  if ((rc = cuda_status(launch_grouped_mx4(g, L))) != MOE_OK) return rc;
+  GroupedMX4Args gd = g;
+  gd.kind = 1;
+  gd.w_qs[0] = gd.w_qs[1] = P.d_qs;
+  gd.w_sf[0] = gd.w_sf[1] = P.d_sf;
+  gd.bias[0] = P.bd;
+  gd.bias[1] = nullptr;
+  gd.R = P.D;
+  gd.C = P.F;
+  gd.aq = ws.hq;
+  gd.asf = ws.hsf;
+  gd.hq = nullptr;
+  gd.hsf = nullptr;
+  gd.y = y;
+  return cuda_status(launch_grouped_mx4(gd, L));
+}
+
 int packed_layer_impl(const moe_packed_layer_t* Lp, const float* x, int T, int rail, void* workspace,
                       size_t workspace_bytes, float* y, int32_t* ids_out, float* weights_out, float* h_out,
                       cudaStream_t stream, int stages = MOE_STAGE_PROLOGUE | MOE_STAGE_GATEUP | MOE_STAGE_DOWN) {
@@ -787,7 +905,9 @@ int packed_layer_impl(const moe_packed_layer_t* Lp, const float* x, int T, int r
   MOE_REQUIRE(P.D >= 64 && P.F >= 64 && P.D % 64 == 0 && P.F % 64 == 0);
   MOE_REQUIRE(P.E >= 1 && P.E <= 256 && P.k >= 1 && P.k <= P.E && P.k <= 32);
   rail = resolve_packed_rail(T, rail);
-  MOE_REQUIRE(rail == MOE_RAIL_DECODE_MX || rail == MOE_RAIL_GROUPED_MX);
+  MOE_REQUIRE(rail == MOE_RAIL_DECODE_MX || rail == MOE_RAIL_GROUPED_MX || rail == MOE_RAIL_GROUPED_MX4);
+  if (rail == MOE_RAIL_GROUPED_MX4) return packed_prefill_impl(P, x, T, workspace, workspace_bytes, y, ids_out,
+                                                               weights_out, stream);
   if (rail != MOE_RAIL_DECODE_MX || T > MOE_GEMV_MAX_T) return MOE_EUNSUPPORTED;
   MOE_REQUIRE(T * P.k <= 64);
   if (P.D > 4096 || P.F > 4096) return MOE_EUNSUPPORTED;
@@ -890,18 +1010,33 @@ int moe_ffn_layer_packed_hostio(const moe_packed_layer_t* layer, int T, int rail
   float* dy = static_cast<float*>(const_cast<void*>(mapped_host(y_host)));
   if (dx && dy && aligned(dx, 16))  // pinned: the kernels read x and write y through the mapping
     return packed_layer_impl(layer, dx, T, rail, workspace, workspace_bytes, dy, nullptr, nullptr, nullptr, stream);
-  if (resolve_packed_rail(T, rail) != MOE_RAIL_DECODE_MX || T > MOE_GEMV_MAX_T) return MOE_EUNSUPPORTED;
-  MOE_REQUIRE(workspace_bytes >= layout_packed_workspace(T, layer->D, layer->F, layer->k, layer->E, nullptr, nullptr));
+  const int prail = resolve_packed_rail(T, rail);
+  float* xs = nullptr;
+  float* ys = nullptr;
   MOE_REQUIRE(aligned(workspace, 256));
-  PackedWorkspace ws;
-  layout_packed_workspace(T, layer->D, layer->F, layer->k, layer->E, static_cast<char*>(workspace), &ws);
+  if (prail == MOE_RAIL_GROUPED_MX4) {
+    MOE_REQUIRE(workspace_bytes >=
+                layout_packed_prefill_workspace(T, layer->D, layer->F, layer->k, layer->E, nullptr, nullptr));
+    PackedPrefillWorkspace pw;
+    layout_packed_prefill_workspace(T, layer->D, layer->F, layer->k, layer->E, static_cast<char*>(workspace), &pw);
+    xs = pw.xs;
+    ys = pw.ys;
+  } else {
+    if (prail != MOE_RAIL_DECODE_MX || T > MOE_GEMV_MAX_T) return MOE_EUNSUPPORTED;
+    MOE_REQUIRE(workspace_bytes >=
+                layout_packed_workspace(T, layer->D, layer->F, layer->k, layer->E, nullptr, nullptr));
+    PackedWorkspace ws;
+    layout_packed_workspace(T, layer->D, layer->F, layer->k, layer->E, static_cast<char*>(workspace), &ws);
+    xs = ws.xs;
+    ys = ws.ys;
+  }
   const size_t bytes = (size_t)T * layer->D * sizeof(float);
-  cudaError_t err = cudaMemcpyAsync(ws.xs, x_host, bytes, cudaMemcpyHostToDevice, stream);
+  cudaError_t err = cudaMemcpyAsync(xs, x_host, bytes, cudaMemcpyHostToDevice, stream);
   if (err != cudaSuccess) return cuda_status(err);
-  const int rc = packed_layer_impl(layer, ws.xs, T, rail, workspace, workspace_bytes, ws.ys, nullptr, nullptr,
-                                   nullptr, stream);
+  const int rc = packed_layer_impl(layer, xs, T, rail, workspace, workspace_bytes, ys, nullptr, nullptr, nullptr,
+                                   stream);
   if (rc != MOE_OK) return rc;
-  return cuda_status(cudaMemcpyAsync(y_host, ws.ys, bytes, cudaMemcpyDeviceToHost, stream));
+  return cuda_status(cudaMemcpyAsync(y_host, ys, bytes, cudaMemcpyDeviceToHost, stream));
 }
 
 int moe_get_status(cudaStream_t stream, int* status) {

@@ -154,6 +154,14 @@ __device__ __forceinline__ float swiglu_oai_f(float g, float u, float alpha, flo
   return g * sigmoid_f(alpha * g) * (u + 1.f);
 }
 
+// The same with a fast reciprocal and no branch (a few ulp): 1/(1 + e^-z)
+// tends to 0 as z -> -inf (e^-z = inf, reciprocal 0), never NaN for finite g.
+__device__ __forceinline__ float swiglu_oai_fast(float g, float u, float alpha, float limit) {
+  g = fminf(g, limit);
+  u = fminf(fmaxf(u, -limit), limit);
+  return g * __fdividef(1.f, 1.f + __expf(-alpha * g)) * (u + 1.f);
+}
+
 // ---------------------------------------------------------------------------
 // warp helpers
 // ---------------------------------------------------------------------------

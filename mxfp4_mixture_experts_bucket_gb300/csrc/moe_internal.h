@@ -145,6 +145,34 @@ struct DecodeMXArgs {
 };
 cudaError_t launch_decode_mx(const DecodeMXArgs& a, Launch L);
 
+// ---- grouped_mx4.cu: prefill grouped GEMMs on prepacked planes (kind::mxf4) ----
+constexpr int kPrefillXTerms = 6;  // E2M1 terms of x (the gate/up operand)
+constexpr int kPrefillHTerms = 3;  // E2M1 terms of h (the down operand)
+struct GroupedMX4Args {
+  int kind;                 // 0: gate/up + swiglu -> h terms; 1: down + weighted scatter into y
+  const uint8_t* w_qs[2];   // prepacked planes (gate, up; or down, down)
+  const uint8_t* w_sf[2];
+  const float* bias[2];
+  int E, R, C;              // per-expert matrices [R][C]
+  const int32_t* counts;
+  const int32_t* basep;
+  const int32_t* rows;
+  int max_rows, k;
+  const float* weights;     // router weights [T*k] (down)
+  const uint8_t* aq;        // activation chunks [max_rows/128][ceil(C/128)][terms][8192] (x: 6 terms, h: 3)
+  const uint8_t* asf;       // [max_rows/128][ceil(C/128)][terms][512]
+  uint8_t* hq;              // gate/up output: the down GEMM's activation chunks (C of down = R here)
+  uint8_t* hsf;
+  float alpha, limit;
+  float* y;                 // down: [T][R], zeroed beforehand
+  int* status;
+};
+size_t prefill_operand_bytes(int max_rows, int C, int terms);
+size_t prefill_atom_bytes(int max_rows, int C, int terms);
+cudaError_t launch_quant_rows_e2m1(const float* x, int T, int D, int k, const int32_t* rows, const int32_t* basep,
+                                   int E, int max_rows, uint8_t* aq, uint8_t* asf, float* y, Launch L);
+cudaError_t launch_grouped_mx4(const GroupedMX4Args& a, Launch L);
+
 // ---- grouped_mm.cu ----
 struct GroupedMMArgs {
   const uint8_t* w_qs[2];

@@ -222,6 +222,18 @@ __device__ __forceinline__ uint64_t sw64_kmajor_desc(uint32_t saddr) {
   return d;
 }
 
+// The same with another distance between 8-row groups (a multiple of 512
+// bytes: groups of several operands interleaved).
+__device__ __forceinline__ uint64_t sw64_kmajor_desc_sbo(uint32_t saddr, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)4 << 61;
+  return d;
+}
+
 // Shared-memory descriptor of an unswizzled K-major operand built from core
 // matrices (8 rows x 16 bytes, 128 contiguous bytes): lbo = byte distance
 // between core matrices adjacent along K, sbo = along M (or N).

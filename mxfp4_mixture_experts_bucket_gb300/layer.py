@@ -90,7 +90,7 @@ class MoeLayer:
         # prepacked rail serves every decode size.
         if self.packed is None:
             return False
-        if rail == _lib.MOE_RAIL_DECODE_MX:
+        if rail in (_lib.MOE_RAIL_DECODE_MX, _lib.MOE_RAIL_GROUPED_MX4):
             return True
         if rail != _lib.MOE_RAIL_AUTO or T > _lib.MOE_GEMV_MAX_T:
             return False

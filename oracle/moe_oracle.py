@@ -429,6 +429,8 @@ def expert_ffn(x_rows: np.ndarray, Wg: np.ndarray, bg, Wu: np.ndarray, bu, Wd: n
                    and h as two (split_e4m3_terms);
       "q8"         the q8 rail's operands: x and h (rounded to float32)
                    requantised in blocks of 32 (quantize_q8), exact products.
+      "e2m1_terms" the prefill rail on prepacked planes: x as six E2M1 terms
+                   and h as three (split_e2m1_terms), exact products.
     """
     x = np.asarray(x_rows, np.float64)
     if operands == "bf16":
@@ -440,6 +442,8 @@ def expert_ffn(x_rows: np.ndarray, Wg: np.ndarray, bg, Wu: np.ndarray, bu, Wd: n
         x = split_e4m3_terms(x, 3)
     elif operands == "q8":
         x = dequant_q8(*quantize_q8(x))
+    elif operands == "e2m1_terms":
+        x = split_e2m1_terms(x, 6)
     elif operands != "f64":
         raise ValueError(operands)
     g = x @ Wg.T + (0.0 if bg is None else np.asarray(bg, np.float64))
@@ -451,6 +455,8 @@ def expert_ffn(x_rows: np.ndarray, Wg: np.ndarray, bg, Wu: np.ndarray, bu, Wd: n
         h = split_e4m3_terms(h, 2)
     elif operands == "q8":
         h = dequant_q8(*quantize_q8(h.astype(np.float32)))
+    elif operands == "e2m1_terms":
+        h = split_e2m1_terms(h, 3)
     return h @ Wd.T + (0.0 if bd is None else np.asarray(bd, np.float64))
 
 

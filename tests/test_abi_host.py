@@ -170,7 +170,10 @@ def test_packed_sizes(moe):
     assert moe.moe_mxfp4_packed_sf_bytes(3, 192, 48) == 0
     assert moe.moe_ffn_packed_workspace_bytes(1, 2880, 2880, 32, 4, moe.MOE_RAIL_AUTO) > 0
     assert moe.moe_ffn_packed_workspace_bytes(1, 2880, 2880, 32, 4, moe.MOE_RAIL_DECODE_MX) % 256 == 0
-    assert moe.moe_ffn_packed_workspace_bytes(9, 2880, 2880, 32, 4, moe.MOE_RAIL_AUTO) == 0
+    # beyond decode sizes the packed layer runs the prefill rail on the same planes
+    assert moe.moe_ffn_packed_workspace_bytes(9, 2880, 2880, 32, 4, moe.MOE_RAIL_AUTO) == \
+        moe.moe_ffn_packed_workspace_bytes(9, 2880, 2880, 32, 4, moe.MOE_RAIL_GROUPED_MX4) > 0
+    assert moe.moe_ffn_packed_workspace_bytes(9, 2880, 2880, 32, 4, moe.MOE_RAIL_DECODE_MX) == 0
 
 
 def test_packed_layer_rejects_on_the_host(moe):

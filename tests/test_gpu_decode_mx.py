@@ -179,13 +179,13 @@ def test_decode_mx_host_io(moe, pinned):
 
 def test_decode_mx_workspace_and_rail_limits(moe):
     spec, L, layer, _ = packed_layer(moe, 0)
-    assert moe.moe_ffn_packed_workspace_bytes(9, 64, 64, 4, 2, moe.MOE_RAIL_AUTO) == 0  # prefill not on this rail
+    assert moe.moe_ffn_packed_workspace_bytes(9, 64, 64, 4, 2, moe.MOE_RAIL_DECODE_MX) == 0  # decode sizes only
     ws = layer.workspace(1, moe.MOE_RAIL_DECODE_MX)
     x = dev(make_tokens(spec, T=1, seed=1))
     y = empty((1, spec.D), torch.float32)
     rc = moe.moe_ffn_layer_packed(layer.packed_struct, x, 1, moe.MOE_RAIL_DECODE_MX, ws, 16, y)
     assert rc == moe.MOE_EINVAL  # workspace too small, rejected before anything is enqueued
-    rc = moe.moe_ffn_layer_packed(layer.packed_struct, x, 9, moe.MOE_RAIL_AUTO, ws, ws.numel(), y)
+    rc = moe.moe_ffn_layer_packed(layer.packed_struct, x, 9, moe.MOE_RAIL_DECODE_MX, ws, ws.numel(), y)
     assert rc == moe.MOE_EUNSUPPORTED
 
 
