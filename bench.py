@@ -633,7 +633,7 @@ def run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src, rai
             "dtype": {moe.MOE_RAIL_GROUPED_MM: "bf16 MMA, fp32 accumulate",
                       moe.MOE_RAIL_GROUPED_MX: "MXFP4 x E4M3-term block-scaled MMA (x: 3 terms, h: 2), fp32 accumulate",
                       moe.MOE_RAIL_GROUPED_MX4: "MXFP4 x E2M1-term block-scaled MMA, kind::mxf4 on prepacked weights "
-                                                "(x: 6 terms, h: 3), fp32 accumulate"}[rail],
+                                                "(x: 6 terms, h: 4), fp32 accumulate"}[rail],
             "rail": {moe.MOE_RAIL_GROUPED_MM: "grouped_mm", moe.MOE_RAIL_GROUPED_MX: "grouped_mx",
                      moe.MOE_RAIL_GROUPED_MX4: "grouped_mx4"}[rail],
             "roofline_frac": round(t_roof / (ms / 1e3), 4),

@@ -506,11 +506,13 @@ size_t moe_ffn_packed_workspace_bytes(int T, int D, int F, int E, int k, int rai
  * chain of "dasLLAMA gpt-oss arc" (Metal fusion lane commit: router, the
  * MoeBucket CSR with the prefix folded in, the MXFP4 grouped mul_mm for
  * gate/up with bias and swiglu, then down with bias and the router-weighted
- * scatter) on the same prepacked planes: x enters as four E2M1 terms per value
- * in bucket order, each 128-row bucket tile meets 256 weight rows per MMA
- * (gate/up: a gate tile and its up tile) on tcgen05.mma kind::mxf4, h leaves
- * the gate/up epilogue as four E2M1 terms, and the down epilogue scatters
- * w*(acc + bd) into y with float atomics (summation order not deterministic).
+ * scatter) on the same prepacked planes: x enters as six E2M1 terms per value
+ * in bucket order; on tcgen05.mma kind::mxf4 each 128-row weight tile is the A
+ * operand and a bucket segment of at most 96 live rows (two terms stacked per
+ * MMA) the B operand, so the MMA work follows the live rows, not the 128-row
+ * padding; h leaves the gate/up epilogue as four E2M1 terms, and the down
+ * epilogue scatters w*(acc + bd) into y with float atomics (summation order not
+ * deterministic).
  */
 int moe_ffn_layer_packed(const moe_packed_layer_t* layer, const float* x, int T, int rail, void* workspace,
                          size_t workspace_bytes, float* y, int32_t* ids_out, float* weights_out, float* h_out,

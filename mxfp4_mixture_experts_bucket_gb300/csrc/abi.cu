@@ -221,7 +221,8 @@ struct PackedPrefillWorkspace {
   int32_t* inv;
   uint8_t* aq;   // x terms in bucket order, activation-chunk layout
   uint8_t* asf;
-  uint8_t* hq;   // h terms, written by the gate/up GEMM
+  float* hf;     // h as float rows, written by the gate/up GEMM
+  uint8_t* hq;   // h terms
   uint8_t* hsf;
   float* xs;     // host-I/O staging [T][D]
   float* ys;
@@ -246,6 +247,7 @@ size_t layout_packed_prefill_workspace(int T, int D, int F, int k, int E, char* 
   w.inv = reinterpret_cast<int32_t*>(take((size_t)T * k * 4));
   w.aq = reinterpret_cast<uint8_t*>(take(prefill_operand_bytes((int)mr, D, kPrefillXTerms)));
   w.asf = reinterpret_cast<uint8_t*>(take(prefill_atom_bytes((int)mr, D, kPrefillXTerms)));
+  w.hf = reinterpret_cast<float*>(take(mr * (size_t)F * 4));
   w.hq = reinterpret_cast<uint8_t*>(take(prefill_operand_bytes((int)mr, F, kPrefillHTerms)));
   w.hsf = reinterpret_cast<uint8_t*>(take(prefill_atom_bytes((int)mr, F, kPrefillHTerms)));
   w.xs = reinterpret_cast<float*>(take((size_t)T * D * 4));
@@ -853,7 +855,7 @@ int packed_prefill_impl(const moe_packed_layer_t& P, const float* x, int T, void
   if ((rc = cuda_status(launch_bucket(ids, T, P.k, P.E, MOE_MM_TILE, (int)ws.max_rows, ws.counts, ws.basep, ws.rows,
                                       ws.inv, d->status, L))) != MOE_OK)
     return rc;
-  if ((rc = cuda_status(launch_quant_rows_e2m1(x, T, P.D, P.k, ws.rows, ws.basep, P.E, (int)ws.max_rows, ws.aq,
+  if ((rc = cuda_status(launch_quant_rows_e2m1(x, T, P.D, P.k, ws.rows, ws.counts, ws.basep, P.E, (int)ws.max_rows, ws.aq,
                                                ws.asf, y, L))) != MOE_OK)
     return rc;
   GroupedMX4Args g{};
@@ -875,8 +877,7 @@ int packed_prefill_impl(const moe_packed_layer_t& P, const float* x, int T, void
   g.weights = wts;
   g.aq = ws.aq;
   g.asf = ws.asf;
-  g.hq = ws.hq;
-  g.hsf = ws.hsf;
+  g.hf = ws.hf;
   g.alpha = 1.702f;
   g.limit = 7.0f;
   g.status = d->status;
@@ -889,10 +890,12 @@ int packed_prefill_impl(const moe_packed_layer_t& P, const float* x, int T, void
   gd.bias[1] = nullptr;
   gd.R = P.D;
   gd.C = P.F;
+  if ((rc = cuda_status(launch_quant_h_e2m1(ws.hf, P.F, ws.rows, ws.counts, ws.basep, P.E, (int)ws.max_rows, ws.hq,
+                                            ws.hsf, L))) != MOE_OK)
+    return rc;
   gd.aq = ws.hq;
   gd.asf = ws.hsf;
-  gd.hq = nullptr;
-  gd.hsf = nullptr;
+  gd.hf = nullptr;
   gd.y = y;
   return cuda_status(launch_grouped_mx4(gd, L));
 }

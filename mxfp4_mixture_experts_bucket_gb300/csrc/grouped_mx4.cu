@@ -6,30 +6,44 @@
 // commit: gate+up rows, bias, activation, then down rows, bias and the
 // router-weighted sum) with neither operand dequantised.
 //
-// Tile of one work unit: M = the 128 rows of one bucket tile (the tokens'
-// activations), N = 256 weight rows (gate/up: 128 gate rows and the same 128
-// up rows; down: two 128-row tiles of D), K walked in 128-column chunks. The
-// activations enter as E2M1 terms (x: six, h: three; each block of 32 on its own E8M0
-// scale, each term the rounded residual of the ones before), and the terms of
-// a row accumulate into the same fp32 accumulator, one MMA per term and K
-// half. The weights come from the prepacked planes (one bulk copy per 128-row
-// tile and chunk lands the 64-byte-swizzled image the MMA reads); the
-// activation chunks of a bucket tile (all terms) and their scale atoms are
-// laid out the same way by quant_rows_e2m1_kernel (x) or by the gate/up
-// epilogue (h).
+// Orientation: the weights are the MMA's A operand (M = 128 weight rows of one
+// tile) and the bucket rows its B operand, so N follows the live rows instead
+// of the 128-row padding of a bucket tile. The activations enter as E2M1 terms
+// (x: six, h: four; each block of 32 on its own E8M0 scale, each term the
+// rounded residual of the ones before), and m terms share one MMA: B holds
+// term t's rows, then term t+1's, ... (N = m * rn), and the groups of m terms
+// accumulate into the same columns, so accumulator column j * rn + n holds the
+// sum over the terms congruent to j mod m for row n; the epilogue adds the m
+// slots, all in the thread that owns the weight row. m is the largest divisor
+// of the term count with m * rn <= 192 (the tensor memory of one accumulator).
 //
-// Warps: 0..5 producers (one copy of every step each; warps 0..3, one per
-// tensor-memory lane quarter, also store the previous step's scale atoms into
-// tensor memory with tcgen05.st and signal the MMA thread), 6 MMA issuer,
-// 7..10 epilogue (one per lane quarter; warp 7 owns tensor memory). Units are
-// dealt round-robin to the CTAs; every role walks the same unit sequence. The
-// accumulator is freed as soon as the epilogue has read it, so the epilogue's
-// arithmetic overlaps the next unit's MMAs.
-//   gate/up epilogue: bias, swiglu_oai, h as three E2M1 terms per 32-block
-//     (computed by each thread over its row's 32 columns), written as the down
-//     GEMM's activation chunks.
-//   down epilogue: y[t] += w_a * (acc + bd) for the bucket row's assignment a
-//     (float atomics, as the pages' weighted scatter).
+// A bucket tile with L live rows is one segment when L <= 96, else two (rows
+// 0..63 and 64..L-1); rn = the segment's rows rounded up to 16. A work unit is
+// (segment, weight tile pair): gate/up: the gate and up tiles of 128 features
+// (two accumulators); down: two 128-row tiles of D.
+//
+// Activation chunk layout (one per bucket tile and 128-column chunk): term t's
+// 8192-byte image of the tile's 128 rows (64-byte-swizzled, block kb of row n
+// at 64*n + 16*(kb ^ ((n>>1)&3))), terms one after the other, so a segment's
+// rows of a term are one contiguous run. Its scale atoms: one run of `terms`
+// atoms per segment; term t's scales for segment row r sit in atom
+// 2*(t / m) + (n >> 7) at row n & 127, n = (t % m) * rn + r (B row n of the
+// term group's MMA). Written by quant_rows_e2m1_kernel: x from the token rows,
+// h from the float rows the gate/up epilogue leaves.
+//
+// Warps: 0..3 scale loaders (one per tensor-memory lane quarter: each step's
+// scale atoms into tensor memory with tcgen05.st once its data has landed,
+// then a signal to the MMA thread), 4..5 copy issuers (activations; weights),
+// 6 MMA issuer, 7..14 epilogue (two per lane quarter; warp 7 owns tensor
+// memory). Units are dealt round-robin to the CTAs; every role walks the same
+// unit sequence. The accumulators are freed as soon as the epilogue has read
+// them, so the epilogue's remaining work overlaps the next unit's MMAs.
+//   gate/up epilogue: bias, swiglu_oai of every (feature, row) into registers,
+//     accumulators freed, then h stored as float rows (32 consecutive
+//     features per warp and row).
+//   down epilogue: y[t] += w_a * (acc + bd) for each row's assignment a (float
+//     atomics over 32 consecutive outputs per warp, as the pages' weighted
+//     scatter).
 #include <cuda.h>
 
 #include "decode_mx.cuh"
@@ -42,36 +56,43 @@ namespace gx4 {
 constexpr int kProd = 6;
 constexpr int kMmaWarp = 6;
 constexpr int kEpiWarp0 = 7;
-constexpr int kEpiWarps = 8;  // two per tensor-memory lane quarter, each taking half of the columns
+constexpr int kEpiWarps = 8;  // two per tensor-memory lane quarter
 constexpr int kTmemWarp = 7;
 constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
-constexpr int kChunk = 8192;  // 128 rows x 64 bytes: one term's (or one weight tile's) chunk
+constexpr int kTermBytes = 8192;  // one term's image of a bucket tile chunk: 128 rows x 64 bytes
+constexpr int kTileBytes = 8192;  // one weight tile chunk: 128 rows x 64 bytes
 constexpr int kAtom = 512;
-constexpr uint32_t kAccCols = 256;
+constexpr int kSegMax = 96;          // most rows in one segment
+constexpr uint32_t kAccStride = 192;  // tensor-memory columns of one accumulator: m * rn <= 192
+constexpr uint32_t kSfBase = 2 * kAccStride;  // scale atoms after the two accumulators
 constexpr uint32_t kTmemCols = 512;
 
+__host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
+
 // Per-kernel plan: the activation operand's terms (x: kPrefillXTerms, h:
-// kPrefillHTerms), the ring depth that fits 227 KB, the stage layout
-// [terms][two weight tiles][term atoms][two weight atoms] and its scale columns.
+// kPrefillHTerms), the stage layout [two weight tiles][terms x kSegMax rows]
+// [activation atoms][two weight atoms], its scale columns, and the ring depth
+// that fits both 227 KB of shared memory and the tensor memory left for scales.
 template <int KIND>
 struct Plan {
   static constexpr int kTerms = KIND == 0 ? kPrefillXTerms : kPrefillHTerms;
-  static constexpr uint32_t kOffB = kTerms * kChunk;
-  static constexpr uint32_t kOffSfa = kOffB + 2 * kChunk;
-  static constexpr uint32_t kOffSfb = kOffSfa + kTerms * kAtom;
-  static constexpr uint32_t kStageBytes = ((kOffSfb + 2 * kAtom) + 1023u) & ~1023u;
-  static constexpr int kStages = (int)((226u * 1024u) / kStageBytes) > 6 ? 6 : (int)((226u * 1024u) / kStageBytes);
-  static constexpr uint32_t kDynSmem = kStages * kStageBytes + 1024;
-  static constexpr uint32_t kSfCols = 4 * kTerms + 8;  // per stage: the term atoms, then the two weight atoms
-  static constexpr int kScaleBatch = kStages - 1;
+  static constexpr uint32_t kOffAct = 2 * kTileBytes;
+  static constexpr uint32_t kOffSfa = kOffAct + kTerms * kSegMax * 64;
+  static constexpr uint32_t kOffSfw = kOffSfa + kTerms * kAtom;
+  static constexpr uint32_t kStageBytes = ((kOffSfw + 2 * kAtom) + 1023u) & ~1023u;
+  static constexpr uint32_t kSfCols = 4 * kTerms + 8;  // per stage: the activation atoms, then the two weight atoms
+  static constexpr int kStages =
+      cmin(6, cmin((int)((226u * 1024u) / kStageBytes), (int)((kTmemCols - kSfBase) / kSfCols)));
+  static constexpr uint32_t kDynSmem = kStages * kStageBytes + 512;
 };
+static_assert(kPrefillXTerms % 2 == 0 && kPrefillHTerms % 2 == 0, "terms enter the MMA in pairs");
 static_assert(Plan<0>::kStages >= 3 && Plan<1>::kStages >= 3, "ring depth");
-static_assert(kAccCols + Plan<0>::kStages * Plan<0>::kSfCols <= kTmemCols, "tensor memory plan");
-static_assert(kAccCols + Plan<1>::kStages * Plan<1>::kSfCols <= kTmemCols, "tensor memory plan");
+static_assert(kSfBase + Plan<0>::kStages * Plan<0>::kSfCols <= kTmemCols, "tensor memory plan");
+static_assert(kSfBase + Plan<1>::kStages * Plan<1>::kSfCols <= kTmemCols, "tensor memory plan");
 
 struct Params {
   int E, R, C, NK, NT;  // weight matrices [R][C]: NT tiles of 128 rows, NK chunks of 128 columns
-  int npair;            // N tile pairs per bucket tile
+  int npair;            // weight tile pairs per segment (gate/up: NT; down: ceil(NT / 2))
   int ntiles;           // bucket tiles (max_rows / 128)
   const uint8_t* w_qs[2];
   const uint8_t* w_sf[2];
@@ -82,9 +103,8 @@ struct Params {
   int k;
   const float* weights;
   const uint8_t* aq;   // activation chunks [ntiles][NK][terms][8192]
-  const uint8_t* asf;  // [ntiles][NK][terms][512]
-  uint8_t* hq;         // gate/up: down operand chunks [ntiles][NT][kPrefillHTerms][8192]
-  uint8_t* hsf;        // [ntiles][NT][kPrefillHTerms][512]
+  const uint8_t* asf;  // [ntiles][NK][2 segments][terms][512]
+  float* hf;           // gate/up: h as float rows [ntiles * 128][R]
   float alpha, limit;
   float* y;  // down: [T][R], accumulated into (zeroed beforehand)
   int* status;
@@ -103,67 +123,127 @@ __device__ __forceinline__ void mma_mxf4(uint32_t tmem_d, uint64_t adesc, uint64
       : "memory");
 }
 
-// Activation chunk layout (one per bucket tile and 128-column chunk, all terms
-// of its rows): 16 groups of 8 rows, each group holding the terms one after
-// the other, every (group, term) the 512-byte 64-byte-swizzled image of those
-// 8 rows (block kb of row n at 64*(n%8) + 16*(kb ^ ((n>>1)&3))). The live rows'
-// groups are then one contiguous run for every term, and a term's rows are
-// `terms` x 512 bytes apart group to group (the MMA descriptor's stride).
-__host__ __device__ __forceinline__ size_t act_off(int n, int t, int terms, int kb, int i) {
-  return ((size_t)(n >> 3) * terms + t) * 512 + dmx::chunk_off(n & 7, kb, i);
+// Byte offset of (row n, term t, block kb, byte i) in one activation chunk.
+__host__ __device__ __forceinline__ size_t act_off(int n, int t, int kb, int i) {
+  return (size_t)t * kTermBytes + dmx::chunk_off(n, kb, i);
 }
 
-// A work unit: bucket tile b (its expert e and live rows) and N tile pair t.
+// Segments of a bucket tile with `live` rows: segment s's first row, row
+// count, and rows rounded up to 16 (0 rows: no such segment).
+struct Segment {
+  int base, rows, rn;
+};
+__host__ __device__ __forceinline__ Segment segment_of(int live, int s) {
+  Segment g{64 * s, 0, 0};
+  if (live > kSegMax) g.rows = s == 0 ? 64 : live - 64;
+  else g.rows = s == 0 ? live : 0;
+  g.rn = (g.rows + 15) & ~15;
+  return g;
+}
+// Terms per MMA for a segment of rn rows: the largest divisor of `terms` with
+// m * rn <= kAccStride (at least 2: rn <= 96).
+template <int TERMS>
+__host__ __device__ __forceinline__ int slots_of(int rn) {
+  int m = 2;
+#pragma unroll
+  for (int d = 3; d <= TERMS; ++d)
+    if (TERMS % d == 0 && d * rn <= (int)kAccStride) m = d;
+  return m;
+}
+// Atom (within the segment's run) and atom row of the scales of term t, segment row r.
+__host__ __device__ __forceinline__ int atom_index(int t, int m, int rn, int r, int& n) {
+  const int nn = (t % m) * rn + r;
+  n = nn & 127;
+  return 2 * (t / m) + (nn >> 7);
+}
+
+// Live rows of the bucket tile starting at row0 (< basep[E]) and its expert.
+__device__ __forceinline__ int tile_live(const int32_t* __restrict__ basep, const int32_t* __restrict__ counts, int E,
+                                         int row0, int& e) {
+  int lo = 0, hi = E - 1;  // basep[e] <= row0 < basep[e + 1]
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(basep + mid) <= row0) lo = mid; else hi = mid - 1;
+  }
+  e = lo;
+  return min(128, __ldg(counts + lo) - (row0 - __ldg(basep + lo)));
+}
+
+// A work unit: bucket tile b (expert e), segment s, weight tile pair t.
 struct Unit {
-  int b, t, e, live;
+  int b, s, t, e;
+  Segment g;
 };
 
-// The i-th unit of this CTA that is not a ghost (past the padded end of the
-// last bucket); false when there is none. `cursor` walks the unit indices.
+// The next unit of this CTA that is not a ghost (past the padded end of the
+// last bucket, or a second segment its tile does not have); false when there
+// is none. `cursor` walks the unit indices ((tile, segment) major).
 __device__ __forceinline__ bool next_unit(const Params& p, int mpad, int& cursor, Unit& u) {
-  const int nunits = p.ntiles * p.npair;
+  const int nunits = p.ntiles * 2 * p.npair;
   for (; cursor < nunits; cursor += gridDim.x) {
-    const int b = cursor / p.npair, t = cursor - b * p.npair;
+    const int bs = cursor / p.npair, t = cursor - bs * p.npair;
+    const int b = bs >> 1, s = bs & 1;
     const int row0 = 128 * b;
     if (row0 >= mpad) continue;
-    int lo = 0, hi = p.E - 1;  // basep[e] <= row0 < basep[e + 1]
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (__ldg(p.basep + mid) <= row0) lo = mid; else hi = mid - 1;
-    }
-    const int live = min(128, __ldg(p.counts + lo) - (row0 - __ldg(p.basep + lo)));
+    int e;
+    const int live = tile_live(p.basep, p.counts, p.E, row0, e);
     if (live <= 0) continue;
+    const Segment g = segment_of(live, s);
+    if (g.rows <= 0) continue;
     u.b = b;
+    u.s = s;
     u.t = t;
-    u.e = lo;
-    u.live = live;
+    u.e = e;
+    u.g = g;
     cursor += gridDim.x;
     return true;
   }
   return false;
 }
 
+// 16 columns from column c0 of the accumulator at `acc` (this warp's lanes),
+// summed over its m term slots (slot j at column j * rn + c0).
+__device__ __forceinline__ void slot_sum16(uint32_t acc, int c0, int rn, int m, float (&out)[16]) {
+  uint32_t a0[16], a1[16];
+  tc::tmem_ld16x2_wait(acc + c0, acc + rn + c0, a0, a1);
+#pragma unroll
+  for (int k = 0; k < 16; ++k) out[k] = __uint_as_float(a0[k]) + __uint_as_float(a1[k]);
+  for (int j = 2; j < m; j += 2) {
+    if (j + 1 < m) {
+      tc::tmem_ld16x2_wait(acc + j * rn + c0, acc + (j + 1) * rn + c0, a0, a1);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) out[k] += __uint_as_float(a0[k]) + __uint_as_float(a1[k]);
+    } else {
+      tc::tmem_ld16_wait(acc + j * rn + c0, a0);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) out[k] += __uint_as_float(a0[k]);
+    }
+  }
+}
+
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p) {
   using PL = Plan<KIND>;
-  constexpr int kTerms = PL::kTerms, kStages = PL::kStages, kScaleBatch = PL::kScaleBatch;
-  constexpr uint32_t kOffB = PL::kOffB, kOffSfa = PL::kOffSfa, kOffSfb = PL::kOffSfb;
+  constexpr int kTerms = PL::kTerms, kStages = PL::kStages;
+  constexpr uint32_t kOffAct = PL::kOffAct, kOffSfa = PL::kOffSfa, kOffSfw = PL::kOffSfw;
   constexpr uint32_t kStageBytes = PL::kStageBytes, kSfCols = PL::kSfCols;
   extern __shared__ uint8_t smem_dyn[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 511) &
+                                             ~static_cast<uintptr_t>(511));
   __shared__ __align__(8) uint64_t full_bar[kStages];
   __shared__ __align__(8) uint64_t empty_bar[kStages];
   __shared__ __align__(8) uint64_t sfr_bar[kStages];
   __shared__ __align__(8) uint64_t accf_bar, acce_bar, drain_bar, tfree_bar;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ float s_bias[256];  // the epilogue's unit biases (gate/up: 128 gate, 128 up; down: 256)
+  __shared__ float s_bias[256];  // the unit's biases (gate/up: 128 gate, 128 up; down: 256)
+  __shared__ int s_tok[KIND == 1 ? kSegMax : 1];    // down: each segment row's token (-1: none)
+  __shared__ float s_w[KIND == 1 ? kSegMax : 1];    // and its router weight
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (warp == 1 && lane == 0) {
     for (int i = 0; i < kStages; ++i) {
-      tc::mbar_init(tc::smem_u32(&full_bar[i]), kProd);
+      tc::mbar_init(tc::smem_u32(&full_bar[i]), 2);  // the two copy issuers
       tc::mbar_init(tc::smem_u32(&empty_bar[i]), 1);
       tc::mbar_init(tc::smem_u32(&sfr_bar[i]), 4);
     }
@@ -189,120 +269,105 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
     report_timeout(p.status, 7 + KIND, role, 0, seq);
   };
   const int nbc = p.C / 32;
+  // weight tile h of unit u's pair (gate/up: matrix h of tile t; down: tile 2t + h), or -1
+  auto wtile = [&](const Unit& u, int h) { return KIND == 0 ? u.t : (2 * u.t + h < p.NT ? 2 * u.t + h : -1); };
 
-  if (warp < kProd) {
-    // ------------------------------------------------ producers: copy `warp` of every step;
-    // warps 0..3 (one per tensor-memory lane quarter) also store the scale atoms of the
-    // step before into tensor memory once its data has landed, and signal the MMA thread
-    const bool loader = warp < 4;
+  if (warp < 4) {
+    // ------------------------------------------------ scale loaders, one per tensor-memory lane
+    // quarter: step by step, once a step's data has landed, its scale atoms go into this
+    // warp's lane quarter (tcgen05.st) and the MMA thread is signalled. They never hold up
+    // the copies, which run up to kStages steps ahead.
     const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
-    uint64_t pol = 0;
-    if (lane == 0) pol = tc::l2_policy_evict_first();
-    int cursor = blockIdx.x, i = 0, issued = 0;
+    int cursor = blockIdx.x, i = 0;
     Unit u;
     bool ok = true;
-    // scale atoms of step s (stage s % kStages) into this warp's lane quarter
-    auto load_scales = [&](int s) -> bool {
-      const int st = s % kStages, n = s / kStages;
-      // (sleeping between probes: these warps share their SM sub-partitions with the epilogue warps)
-      const bool okw = tc::mbar_wait_sleep(tc::smem_u32(&full_bar[st]), n & 1, abort_flag, 64);
-      if (!__all_sync(0xffffffffu, okw)) {
-        if (lane == 0) fail(3, s);
-        return false;
-      }
-      const uint8_t* sbp = smem + (size_t)st * kStageBytes;
-      const uint32_t sfs = lane_base + kAccCols + (uint32_t)st * kSfCols;
-#pragma unroll
-      for (int a = 0; a < kTerms + 2; ++a) {  // activation atoms, then the two weight atoms
-        const uint8_t* atom = sbp + (a < kTerms ? kOffSfa + a * kAtom : kOffSfb + (a - kTerms) * kAtom);
-        const uint4 w = *reinterpret_cast<const uint4*>(atom + 16 * lane);
-        tc::tmem_st4(sfs + 4 * a, w.x, w.y, w.z, w.w);
-      }
-      tc::tmem_wait_st();
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&sfr_bar[st]));
-      return true;
-    };
     while (ok && next_unit(p, mpad, cursor, u)) {
-      const int live_groups = (u.live + 7) >> 3;
-      for (int j = 0; j < NK && ok; ++j, ++i) {
+      for (int j = 0; j < NK; ++j, ++i) {
         const int st = i % kStages, n = i / kStages;
-        if (lane == 0) {
+        const bool okw = tc::mbar_wait_sleep(tc::smem_u32(&full_bar[st]), n & 1, abort_flag, 32);
+        if (!__all_sync(0xffffffffu, okw)) {
+          if (lane == 0) fail(3, i);
+          ok = false;
+          break;
+        }
+        const uint8_t* sbp = smem + (size_t)st * kStageBytes;
+        const uint32_t sfs = lane_base + kSfBase + (uint32_t)st * kSfCols;
+#pragma unroll
+        for (int a = 0; a < kTerms + 2; ++a) {  // activation atoms, then the two weight atoms
+          const uint8_t* atom = sbp + (a < kTerms ? kOffSfa + a * kAtom : kOffSfw + (a - kTerms) * kAtom);
+          const uint4 w = *reinterpret_cast<const uint4*>(atom + 16 * lane);
+          tc::tmem_st4(sfs + 4 * a, w.x, w.y, w.z, w.w);
+        }
+        tc::tmem_wait_st();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(tc::smem_u32(&sfr_bar[st]));
+      }
+    }
+    tc::fence_before_sync();  // this warp's tensor-memory stores are complete
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(tc::smem_u32(&tfree_bar));
+  } else if (warp < kProd) {
+    // ------------------------------------------------ copy issuers (lane 0): warp 4 the
+    // segment's rows of every activation term and their atoms, warp 5 the two weight
+    // tiles and their atoms
+    if (lane == 0) {
+      uint64_t pol = tc::l2_policy_evict_first();
+      int cursor = blockIdx.x, i = 0, issued = 0;
+      Unit u;
+      bool ok = true;
+      while (ok && next_unit(p, mpad, cursor, u)) {
+        const uint32_t run = (uint32_t)u.g.rn * 64;  // one term's rows of the segment
+        for (int j = 0; j < NK; ++j, ++i) {
+          const int st = i % kStages, n = i / kStages;
           if (n > 0 && !tc::mbar_wait_sleep(tc::smem_u32(&empty_bar[st]), (n - 1) & 1, abort_flag, 32)) {
             fail(0, i);
             ok = false;
+            break;
           }
-        }
-        if (loader) ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
-        if (lane == 0) {
           const uint32_t fb = tc::smem_u32(&full_bar[st]);
           const uint32_t sb = tc::smem_u32(smem) + (uint32_t)st * kStageBytes;
-          const size_t achunk = (size_t)u.b * NK + j;
-          if (warp < 2) {  // the live rows' groups of all terms, in two runs
-            const int g0 = (live_groups + 1) >> 1;
-            const int ga = warp == 0 ? 0 : g0, gn = warp == 0 ? g0 : live_groups - g0;
-            const uint32_t bytes = (uint32_t)(gn * kTerms * 512);
-            tc::mbar_expect_tx(fb, bytes);
-            if (bytes)
-              tc::bulk_load(sb + (uint32_t)(ga * kTerms * 512),
-                            p.aq + achunk * (size_t)(kTerms * kChunk) + (size_t)ga * kTerms * 512, bytes, fb);
-          } else if (warp == 4) {  // the activation atoms of all terms
-            tc::mbar_expect_tx(fb, kTerms * kAtom);
-            tc::bulk_load(sb + kOffSfa, p.asf + achunk * kTerms * kAtom, kTerms * kAtom, fb);
-          } else if (warp < 4) {
-            // weight tile h of the pair (gate/up: matrix h of tile t; down: tile 2t + h); a
-            // missing tile leaves its rows stale: they only feed accumulator columns nobody reads
-            const int h = warp - 2;
-            const int tile = KIND == 0 ? u.t : 2 * u.t + h;
-            if (tile < p.NT) {
-              const int rows_t = min(128, p.R - 128 * tile);
-              const uint32_t bytes = (uint32_t)(rows_t * 64);
-              const uint8_t* src = p.w_qs[KIND == 0 ? h : 0] +
-                                   ((size_t)u.e * p.R + 128 * (size_t)tile) * ((size_t)NK * 64) + (size_t)rows_t * 64 * j;
-              tc::mbar_expect_tx(fb, bytes);
-              tc::bulk_load_stream(sb + kOffB + (uint32_t)(h * kChunk), src, bytes, fb, pol);
-            } else {
-              tc::mbar_expect_tx(fb, 0);
-            }
-          } else {  // warp 5: the weight tiles' scale atoms
+          if (warp == 4) {
+            const size_t achunk = (size_t)u.b * NK + j;
+            const uint8_t* src = p.aq + achunk * (size_t)(kTerms * kTermBytes) + (size_t)u.g.base * 64;
+            tc::mbar_expect_tx(fb, (uint32_t)kTerms * run + kTerms * kAtom);
+            for (int t = 0; t < kTerms; ++t)
+              tc::bulk_load(sb + kOffAct + (uint32_t)t * run, src + (size_t)t * kTermBytes, run, fb);
+            tc::bulk_load(sb + kOffSfa, p.asf + (achunk * 2 + u.s) * (kTerms * kAtom), kTerms * kAtom, fb);
+          } else {
+            // a tile shorter than 128 rows leaves the rest stale: those rows only feed
+            // accumulator lanes nobody reads
             uint32_t bytes = 0;
-            for (int h = 0; h < 2; ++h) bytes += (KIND == 0 || 2 * u.t + h < p.NT) ? kAtom : 0u;
+            for (int h = 0; h < 2; ++h) {
+              const int tile = wtile(u, h);
+              if (tile >= 0) bytes += (uint32_t)(min(128, p.R - 128 * tile) * 64) + kAtom;
+            }
             tc::mbar_expect_tx(fb, bytes);
             for (int h = 0; h < 2; ++h) {
-              const int tile = KIND == 0 ? u.t : 2 * u.t + h;
-              if (tile >= p.NT) continue;
-              tc::bulk_load_stream(sb + kOffSfb + (uint32_t)(h * kAtom),
+              const int tile = wtile(u, h);
+              if (tile < 0) continue;
+              const int rows_t = min(128, p.R - 128 * tile);
+              const uint8_t* src = p.w_qs[KIND == 0 ? h : 0] +
+                                   ((size_t)u.e * p.R + 128 * (size_t)tile) * ((size_t)NK * 64) + (size_t)rows_t * 64 * j;
+              tc::bulk_load_stream(sb + (uint32_t)(h * kTileBytes), src, (uint32_t)(rows_t * 64), fb, pol);
+              tc::bulk_load_stream(sb + kOffSfw + (uint32_t)(h * kAtom),
                                    p.w_sf[KIND == 0 ? h : 0] + (((size_t)u.e * p.NT + tile) * NK + j) * kAtom, kAtom,
                                    fb, pol);
             }
           }
           issued = i + 1;
         }
-        if (loader) {
-          __syncwarp();
-          if (i >= 1 && !load_scales(i - 1)) ok = false;
-        }
       }
-    }
-    if (loader) {
-      issued = __shfl_sync(0xffffffffu, issued, 0);
-      if (ok && issued >= 1) ok = load_scales(issued - 1);  // the last step's scales
-      tc::fence_before_sync();  // this warp's tensor-memory stores are complete
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&tfree_bar));
-    }
-    if (lane == 0 && *abort_flag) {  // every copy already issued lands before shared memory goes away
-      for (int st = 0; st < kStages; ++st) {
-        const int n = issued > st ? (issued - 1 - st) / kStages + 1 : 0;
-        if (n > 0) tc::mbar_wait(tc::smem_u32(&full_bar[st]), (n - 1) & 1, nullptr);
+      if (*abort_flag) {  // every copy already issued lands before shared memory goes away
+        for (int st = 0; st < kStages; ++st) {
+          const int n = issued > st ? (issued - 1 - st) / kStages + 1 : 0;
+          if (n > 0) tc::mbar_wait(tc::smem_u32(&full_bar[st]), (n - 1) & 1, nullptr);
+        }
       }
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_mxf4(128, 256);
       int cursor = blockIdx.x, i = 0, lu = 0;
       Unit u;
       bool ok = true;
@@ -312,6 +377,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
           break;
         }
         tc::fence_after_sync();
+        const int m = slots_of<kTerms>(u.g.rn), ngrp = kTerms / m;
+        const uint32_t idesc = idesc_mxf4(128, m * u.g.rn);
+        const bool two = wtile(u, 1) >= 0;
+        const uint32_t grp_step = (uint32_t)(m * u.g.rn * 64) >> 4;  // descriptor units between term groups
         for (int j = 0; j < NK; ++j, ++i) {
           const int st = i % kStages, n = i / kStages;
           if (!tc::mbar_wait(tc::smem_u32(&sfr_bar[st]), n & 1, abort_flag)) {
@@ -321,18 +390,23 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
           }
           tc::fence_after_sync();
           const uint32_t sb = tc::smem_u32(smem) + (uint32_t)st * kStageBytes;
-          const uint32_t sfs = tmem + kAccCols + (uint32_t)st * kSfCols;
+          const uint32_t sfs = tmem + kSfBase + (uint32_t)st * kSfCols;
           const int nkb = min(4, nbc - 4 * j);  // 32-blocks in this chunk: 2 or 4 (widths are multiples of 64)
-          const uint64_t bdesc = tc::sw64_kmajor_desc(sb + kOffB);
-          const uint64_t adesc = tc::sw64_kmajor_desc_sbo(sb, kTerms * 512);  // term t starts t*512 further
+          const uint64_t adesc0 = tc::sw64_kmajor_desc(sb);
+          const uint64_t adesc1 = tc::sw64_kmajor_desc(sb + kTileBytes);
+          const uint64_t bdesc = tc::sw64_kmajor_desc(sb + kOffAct);
 #pragma unroll
           for (int kh = 0; kh < 2; ++kh) {
             if (2 * kh >= nkb) continue;
             const uint32_t id = idesc | (kh ? ((2u << 4) | (2u << 29)) : 0u);
-#pragma unroll
-            for (int term = 0; term < kTerms; ++term)
-              mma_mxf4(tmem, adesc + (uint64_t)(term * (512 >> 4) + 2 * kh), bdesc + (uint64_t)(2 * kh), id,
-                       sfs + 4 * term, sfs + 4 * kTerms, (j == 0 && kh == 0 && term == 0) ? 0u : 1u);
+#pragma unroll 1
+            for (int q = 0; q < ngrp; ++q) {
+              const uint64_t bq = bdesc + (uint64_t)(q * grp_step + 2 * kh);
+              const uint32_t sfb = sfs + 8 * q;
+              const uint32_t acc = (j == 0 && kh == 0 && q == 0) ? 0u : 1u;
+              mma_mxf4(tmem, adesc0 + (uint64_t)(2 * kh), bq, id, sfs + 4 * kTerms, sfb, acc);
+              if (two) mma_mxf4(tmem + kAccStride, adesc1 + (uint64_t)(2 * kh), bq, id, sfs + 4 * kTerms + 4, sfb, acc);
+            }
           }
           tc::mma_commit(tc::smem_u32(&empty_bar[st]));
           if (j == NK - 1) tc::mma_commit(tc::smem_u32(&accf_bar));
@@ -347,9 +421,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
   } else {
     // ------------------------------------------------ epilogue (warps 7..14)
     const int q = warp & 3;
-    const int half = (warp - kEpiWarp0) >> 2;  // which half of the unit's columns
-    const int row = 32 * q + lane;  // bucket row within the tile = tensor-memory lane
+    const int hh = (warp - kEpiWarp0) >> 2;  // gate/up: which row chunks; down: which tile of the pair
     const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
+    const int et = threadIdx.x - kEpiWarp0 * 32;  // 0..255
     int cur_epi = blockIdx.x;
     Unit ue{};
     int ldone = 0;  // units whose epilogue has run
@@ -357,23 +431,25 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
     while (have_e) {
       // ---- the epilogue of unit ldone (ue)
       const int e = ue.e;
-      const int prow = 128 * ue.b + row;  // bucket row
-      // the unit's biases into shared memory (the four epilogue warps; every
-      // reader of the previous unit's is past the first barrier)
+      const Segment g = ue.g;
+      // the unit's biases (and, down, its rows' tokens) into shared memory; every
+      // reader of the previous unit's is past the first barrier
       tc::named_sync(1, 32 * kEpiWarps);
       {
-        const int c = 32 * q + lane;  // 128 columns per pass
-        for (int h2 = half; h2 < 2; h2 += 2) {
-          float bv = 0.f;
-          if (KIND == 0) {
-            const int f = 128 * ue.t + c;
-            if (p.bias[h2] && f < p.R) bv = __ldg(p.bias[h2] + (size_t)e * p.R + f);
-          } else {
-            const int col = 256 * ue.t + 128 * h2 + c;
-            if (p.bias[0] && col < p.R) bv = __ldg(p.bias[0] + (size_t)e * p.R + col);
+        float bv = 0.f;
+        if (KIND == 0) {
+          const int h2 = et >> 7, f = 128 * ue.t + (et & 127);
+          if (p.bias[h2] && f < p.R) bv = __ldg(p.bias[h2] + (size_t)e * p.R + f);
+        } else {
+          const int col = 256 * ue.t + et;
+          if (p.bias[0] && col < p.R) bv = __ldg(p.bias[0] + (size_t)e * p.R + col);
+          if (et < kSegMax) {
+            const int a = et < g.rows ? __ldg(p.rows + 128 * ue.b + g.base + et) : -1;
+            s_tok[et] = a >= 0 ? a / p.k : -1;
+            s_w[et] = a >= 0 ? __ldg(p.weights + a) : 0.f;
           }
-          s_bias[128 * h2 + c] = bv;
         }
+        s_bias[et] = bv;
       }
       tc::named_sync(1, 32 * kEpiWarps);
       const bool okw = tc::mbar_wait_sleep(tc::smem_u32(&accf_bar), ldone & 1, abort_flag, 128);
@@ -383,65 +459,67 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
       }
       tc::fence_after_sync();
       if constexpr (KIND == 0) {
-        // ---- gate/up: bias + swiglu of all 128 columns into registers, the
-        // accumulator released, then h as E2M1 terms per 32-column block
-        const int F = p.R;
-        uint8_t* hq = p.hq + ((size_t)ue.b * p.NT + ue.t) * (size_t)(kPrefillHTerms * kChunk);
-        uint8_t* hsf = p.hsf + (((size_t)ue.b * p.NT + ue.t) * kPrefillHTerms) * kAtom;
-        const bool live = row < ue.live;
-        float h[2][32];  // column groups 2*half, 2*half+1
+        // ---- gate/up: this lane's feature f; rows in 16-row chunks hh, hh + 2, hh + 4
+        const int m = slots_of<kPrefillXTerms>(g.rn);
+        const int fl = 32 * q + lane, f = 128 * ue.t + fl;
+        const bool fvalid = f < p.R;
+        const float bg = s_bias[fl], bu = s_bias[128 + fl];
+        float hv[3][16];
 #pragma unroll
-        for (int gg = 0; gg < 2; ++gg) {
-          const int g = 2 * half + gg;
+        for (int ci = 0; ci < 3; ++ci) {
+          const int c = hh + 2 * ci;
+          if (16 * c < g.rn) {
+            float gs[16], us[16];
+            slot_sum16(lane_base, 16 * c, g.rn, m, gs);
+            slot_sum16(lane_base + kAccStride, 16 * c, g.rn, m, us);
 #pragma unroll
-          for (int hb = 0; hb < 2; ++hb) {
-            uint32_t gv[16], uv[16];
-            tc::tmem_ld16x2_wait(lane_base + 32 * g + 16 * hb, lane_base + 128 + 32 * g + 16 * hb, gv, uv);
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              const int cc = 32 * g + 16 * hb + c;
-              h[gg][16 * hb + c] = (live && 128 * ue.t + cc < F)
-                                      ? swiglu_oai_fast(__uint_as_float(gv[c]) + s_bias[cc],
-                                                        __uint_as_float(uv[c]) + s_bias[128 + cc], p.alpha, p.limit)
-                                      : 0.f;
-            }
+            for (int k = 0; k < 16; ++k) hv[ci][k] = swiglu_oai_fast(gs[k] + bg, us[k] + bu, p.alpha, p.limit);
           }
         }
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(tc::smem_u32(&acce_bar));  // the next unit's MMAs may start
+        // h rows: 32 consecutive features per warp and row
+        float* hrow = p.hf + (size_t)(128 * ue.b + g.base) * p.R + f;
 #pragma unroll
-        for (int gg = 0; gg < 2; ++gg) {
-          const int g = 2 * half + gg;
-          uint4 packed[kPrefillHTerms];
-          uint32_t sc[kPrefillHTerms];
-          mx::split_block_e2m1<kPrefillHTerms>(h[gg], packed, sc);
+        for (int ci = 0; ci < 3; ++ci) {
+          const int c = hh + 2 * ci;
+          if (16 * c >= g.rows) continue;
 #pragma unroll
-          for (int term = 0; term < kPrefillHTerms; ++term) {
-            *reinterpret_cast<uint4*>(hq + act_off(row, term, kPrefillHTerms, g, 0)) = packed[term];
-            hsf[(size_t)term * kAtom + dmx::atom_off(row, g)] = (uint8_t)sc[term];
+          for (int k = 0; k < 16; ++k) {
+            const int r = 16 * c + k;
+            if (fvalid && r < g.rows) hrow[(size_t)r * p.R] = hv[ci][k];
           }
         }
       } else {
-        // ---- down: y[token] += w_a * (acc + bd) over the pair's valid columns
+        // ---- down: output d of tile hh; y[token] += w_a * (acc + bd) for the segment's rows
+        const int m = slots_of<kPrefillHTerms>(g.rn);
         const int D = p.R;
-        const int a = row < ue.live ? __ldg(p.rows + prow) : -1;
-        const int tok = a >= 0 ? a / p.k : 0;
-        const float wa = a >= 0 ? __ldg(p.weights + a) : 0.f;
+        const int dl = 128 * hh + 32 * q + lane, d = 256 * ue.t + dl;
+        const bool has = wtile(ue, hh) >= 0;
+        const bool dvalid = has && d < D;
+        const float bd = s_bias[dl];
+        const uint32_t acc = lane_base + kAccStride * hh;
+        const int nch = (g.rows + 15) >> 4;
+        if (!has) {
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(tc::smem_u32(&acce_bar));
+        } else {
 #pragma unroll 1
-        for (int g = 8 * half; g < 8 * half + 8; ++g) {
-          uint32_t v[16];
-          tc::tmem_ld16_wait(lane_base + 16 * g, v);
-          if (g == 8 * half + 7) {
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(tc::smem_u32(&acce_bar));
-          }
-          if (a >= 0) {
+          for (int c = 0; c < nch; ++c) {
+            float v[16];
+            slot_sum16(acc, 16 * c, g.rn, m, v);
+            if (c == nch - 1) {
+              tc::fence_before_sync();
+              __syncwarp();
+              if (lane == 0) tc::mbar_arrive(tc::smem_u32(&acce_bar));
+            }
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              const int col = 256 * ue.t + 16 * g + c;
-              if (col < D) atomicAdd(p.y + (size_t)tok * D + col, wa * (__uint_as_float(v[c]) + s_bias[16 * g + c]));
+            for (int k = 0; k < 16; ++k) {
+              const int r = 16 * c + k;
+              const int tok = r < g.rows ? s_tok[r] : -1;
+              if (dvalid && tok >= 0) atomicAdd(p.y + (size_t)tok * D + d, s_w[r] * (v[k] + bd));
             }
           }
         }
@@ -465,64 +543,111 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
 }
 
 // ---------------------------------------------------------------------------
-// x rows in bucket order as kPrefillXTerms E2M1 terms, in the activation-chunk
-// layout: one warp per (bucket row, 32-block); pad rows and blocks past D are
-// zero. y[0 .. T*D) is zeroed (the down GEMM accumulates into it).
+// Bucket rows as NT E2M1 terms, in the activation-chunk layout: one thread per
+// (bucket row, 32-block), which loads the block's 128 bytes, splits it
+// (split_block_e2m1), stores each term's 16 bytes with one store and its scale
+// byte into its segment's atoms. GATHER: the rows are x's token rows (x: the
+// gate/up operand) and y[0 .. T*C) is zeroed (the down GEMM accumulates into
+// it); else the rows are src's own bucket rows (h: the down operand). Pad rows
+// and blocks past C are zero.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) quant_rows_e2m1_kernel(const float* __restrict__ x, int T, int D, int k,
+template <int NT, bool GATHER>
+__global__ void __launch_bounds__(256) quant_rows_e2m1_kernel(const float* __restrict__ src, int T, int C, int k,
                                                               const int32_t* __restrict__ rows,
+                                                              const int32_t* __restrict__ counts,
                                                               const int32_t* __restrict__ basep, int E, int NK,
                                                               uint8_t* __restrict__ aq, uint8_t* __restrict__ asf,
                                                               float* __restrict__ y) {
   pdl_launch_dependents();
   pdl_wait();
-  const int lane = threadIdx.x & 31;
-  const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
   const int mpad = basep[E];
-  const int nbp = 4 * NK, nb = D / 32;
-  for (int64_t w = gw; w < (int64_t)mpad * nbp; w += nw) {
+  const int nbp = 4 * NK, nb = C / 32;
+  for (int64_t w = tid; w < (int64_t)mpad * nbp; w += nthr) {
     const int p = (int)(w / nbp), blk = (int)(w - (int64_t)p * nbp);
     const int a = rows[p];
-    float v = 0.f;
-    if (a >= 0 && blk < nb) v = x[(size_t)(a / k) * D + 32 * blk + lane];
-    uint32_t qv[kPrefillXTerms], sv[kPrefillXTerms];
-    mx::split_terms_e2m1<kPrefillXTerms>(v, qv, sv);
-    const int b = p >> 7, r = p & 127, j = blk >> 2, kb = blk & 3;
-    const size_t base = ((size_t)b * NK + j) * kPrefillXTerms;
+    const int b = p >> 7, rt = p & 127, j = blk >> 2, kb = blk & 3;
+    int e;
+    const int live = tile_live(basep, counts, E, 128 * b, e);
+    const int s = live > kSegMax ? (rt >> 6) : 0;
+    const Segment g = segment_of(live, s);
+    const int r = rt - g.base;
+    const int m = slots_of<NT>(g.rn);
+    uint8_t* chunk = aq + ((size_t)b * NK + j) * (NT * kTermBytes);
+    uint8_t* atoms = asf + (((size_t)b * NK + j) * 2 + s) * (NT * kAtom);
+    uint4 packed[NT];
+    uint32_t sc[NT];
+    if (a >= 0 && blk < nb) {
+      float v[32];
+      const float* row = GATHER ? src + (size_t)(a / k) * C : src + (size_t)p * C;
+      const float4* s4 = reinterpret_cast<const float4*>(row + 32 * blk);
 #pragma unroll
-    for (int term = 0; term < kPrefillXTerms; ++term) {
-      const uint32_t byte = mx::pack_e2m1_block(qv[term]);
-      if (lane < 16) aq[((size_t)b * NK + j) * (kPrefillXTerms * kChunk) + act_off(r, term, kPrefillXTerms, kb, lane)] =
-          (uint8_t)byte;
-      if (lane == 0) asf[(base + term) * kAtom + dmx::atom_off(r, kb)] = (uint8_t)sv[term];
+      for (int i = 0; i < 8; ++i) {
+        const float4 f = __ldg(s4 + i);
+        v[4 * i] = f.x;
+        v[4 * i + 1] = f.y;
+        v[4 * i + 2] = f.z;
+        v[4 * i + 3] = f.w;
+      }
+      mx::split_block_e2m1<NT>(v, packed, sc);
+    } else {
+#pragma unroll
+      for (int term = 0; term < NT; ++term) {
+        packed[term] = make_uint4(0u, 0u, 0u, 0u);
+        sc[term] = 0u;
+      }
+    }
+#pragma unroll
+    for (int term = 0; term < NT; ++term) {
+      *reinterpret_cast<uint4*>(chunk + act_off(rt, term, kb, 0)) = packed[term];
+      if (r < g.rn) {  // rows past the segment's rounded end are never read
+        int n;
+        const int ai = atom_index(term, m, g.rn, r, n);
+        atoms[(size_t)ai * kAtom + dmx::atom_off(n, kb)] = (uint8_t)sc[term];
+      }
     }
   }
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < (int64_t)T * D;
-       i += (int64_t)gridDim.x * blockDim.x)
-    y[i] = 0.f;
+  if (GATHER) {
+    const int64_t n4 = (int64_t)T * C / 4;
+    float4* y4 = reinterpret_cast<float4*>(y);
+    for (int64_t i = tid; i < n4; i += nthr) y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int64_t i = 4 * n4 + tid; i < (int64_t)T * C; i += nthr) y[i] = 0.f;
+  }
   asm volatile("fence.proxy.async.global;" ::: "memory");  // read next by the copy engine
 }
 
 }  // namespace gx4
 
 size_t prefill_operand_bytes(int max_rows, int C, int terms) {
-  return (size_t)(max_rows / 128) * ((C + 127) / 128) * terms * gx4::kChunk;
+  return (size_t)(max_rows / 128) * ((C + 127) / 128) * terms * gx4::kTermBytes;
 }
 size_t prefill_atom_bytes(int max_rows, int C, int terms) {
-  return (size_t)(max_rows / 128) * ((C + 127) / 128) * terms * gx4::kAtom;
+  return (size_t)(max_rows / 128) * ((C + 127) / 128) * 2 * terms * gx4::kAtom;
 }
 
-cudaError_t launch_quant_rows_e2m1(const float* x, int T, int D, int k, const int32_t* rows, const int32_t* basep,
-                                   int E, int max_rows, uint8_t* aq, uint8_t* asf, float* y, Launch L) {
-  const int NK = (D + 127) / 128;
-  const int64_t warps = (int64_t)max_rows * 4 * NK;
-  int64_t blocks = (warps * 32 + 255) / 256;
+namespace {
+int quant_blocks(int max_rows, int C) {
+  const int64_t threads = (int64_t)max_rows * 4 * ((C + 127) / 128);
+  int64_t blocks = (threads + 255) / 256;
   const int64_t cap = (int64_t)device_sm_count() * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  return launch_kernel(gx4::quant_rows_e2m1_kernel, dim3((unsigned)blocks), dim3(256), 0, L, x, T, D, k, rows, basep,
-                       E, NK, aq, asf, y);
+  return (int)blocks;
+}
+}  // namespace
+
+cudaError_t launch_quant_rows_e2m1(const float* x, int T, int D, int k, const int32_t* rows, const int32_t* counts,
+                                   const int32_t* basep, int E, int max_rows, uint8_t* aq, uint8_t* asf, float* y,
+                                   Launch L) {
+  return launch_kernel(gx4::quant_rows_e2m1_kernel<kPrefillXTerms, true>, dim3(quant_blocks(max_rows, D)), dim3(256), 0,
+                       L, x, T, D, k, rows, counts, basep, E, (D + 127) / 128, aq, asf, y);
+}
+
+cudaError_t launch_quant_h_e2m1(const float* hf, int F, const int32_t* rows, const int32_t* counts,
+                                const int32_t* basep, int E, int max_rows, uint8_t* hq, uint8_t* hsf, Launch L) {
+  return launch_kernel(gx4::quant_rows_e2m1_kernel<kPrefillHTerms, false>, dim3(quant_blocks(max_rows, F)), dim3(256),
+                       0, L, hf, 0, F, 1, rows, counts, basep, E, (F + 127) / 128, hq, hsf, nullptr);
 }
 
 cudaError_t launch_grouped_mx4(const GroupedMX4Args& a, Launch L) {
@@ -550,13 +675,12 @@ cudaError_t launch_grouped_mx4(const GroupedMX4Args& a, Launch L) {
   prm.weights = a.weights;
   prm.aq = a.aq;
   prm.asf = a.asf;
-  prm.hq = a.hq;
-  prm.hsf = a.hsf;
+  prm.hf = a.hf;
   prm.alpha = a.alpha;
   prm.limit = a.limit;
   prm.y = a.y;
   prm.status = a.status;
-  const int nunits = prm.ntiles * prm.npair;
+  const int nunits = prm.ntiles * 2 * prm.npair;
   int grid = device_sm_count();
   if (grid > nunits) grid = nunits;
   if (a.kind == 0) {

@@ -147,9 +147,9 @@ cudaError_t launch_decode_mx(const DecodeMXArgs& a, Launch L);
 
 // ---- grouped_mx4.cu: prefill grouped GEMMs on prepacked planes (kind::mxf4) ----
 constexpr int kPrefillXTerms = 6;  // E2M1 terms of x (the gate/up operand)
-constexpr int kPrefillHTerms = 3;  // E2M1 terms of h (the down operand)
+constexpr int kPrefillHTerms = 4;  // E2M1 terms of h (the down operand)
 struct GroupedMX4Args {
-  int kind;                 // 0: gate/up + swiglu -> h terms; 1: down + weighted scatter into y
+  int kind;                 // 0: gate/up + swiglu -> h rows; 1: down + weighted scatter into y
   const uint8_t* w_qs[2];   // prepacked planes (gate, up; or down, down)
   const uint8_t* w_sf[2];
   const float* bias[2];
@@ -159,18 +159,22 @@ struct GroupedMX4Args {
   const int32_t* rows;
   int max_rows, k;
   const float* weights;     // router weights [T*k] (down)
-  const uint8_t* aq;        // activation chunks [max_rows/128][ceil(C/128)][terms][8192] (x: 6 terms, h: 3)
-  const uint8_t* asf;       // [max_rows/128][ceil(C/128)][terms][512]
-  uint8_t* hq;              // gate/up output: the down GEMM's activation chunks (C of down = R here)
-  uint8_t* hsf;
+  const uint8_t* aq;        // activation chunks [max_rows/128][ceil(C/128)][terms][8192] (x: 6 terms, h: 4)
+  const uint8_t* asf;       // their scale atoms [max_rows/128][ceil(C/128)][2 segments][terms][512]
+  float* hf;                // gate/up output: h as float rows [max_rows][R]
   float alpha, limit;
   float* y;                 // down: [T][R], zeroed beforehand
   int* status;
 };
 size_t prefill_operand_bytes(int max_rows, int C, int terms);
 size_t prefill_atom_bytes(int max_rows, int C, int terms);
-cudaError_t launch_quant_rows_e2m1(const float* x, int T, int D, int k, const int32_t* rows, const int32_t* basep,
-                                   int E, int max_rows, uint8_t* aq, uint8_t* asf, float* y, Launch L);
+// x's token rows in bucket order as kPrefillXTerms E2M1 terms (and y zeroed)
+cudaError_t launch_quant_rows_e2m1(const float* x, int T, int D, int k, const int32_t* rows, const int32_t* counts,
+                                   const int32_t* basep, int E, int max_rows, uint8_t* aq, uint8_t* asf, float* y,
+                                   Launch L);
+// h's bucket rows (float [max_rows][F]) as kPrefillHTerms E2M1 terms
+cudaError_t launch_quant_h_e2m1(const float* hf, int F, const int32_t* rows, const int32_t* counts,
+                                const int32_t* basep, int E, int max_rows, uint8_t* hq, uint8_t* hsf, Launch L);
 cudaError_t launch_grouped_mx4(const GroupedMX4Args& a, Launch L);
 
 // ---- grouped_mm.cu ----

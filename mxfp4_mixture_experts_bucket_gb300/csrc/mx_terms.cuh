@@ -83,6 +83,14 @@ __device__ __forceinline__ float e2m1_to_f32(uint32_t q) {
   return __uint_as_float(bits | ((q & 8u) << 28));
 }
 
+// Two E2M1 codes (one byte: low nibble, high nibble) to their exact values as
+// an f16 pair (low nibble in the low half); every E2M1 value is an f16 value.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t h2;
+  asm("{\n .reg .b8 t;\n cvt.u8.u32 t, %1;\n cvt.rn.f16x2.e2m1x2 %0, t;\n}" : "=r"(h2) : "r"(byte));
+  return h2;
+}
+
 // One block of 32 values, one per lane (all lanes of the warp take part): v as
 // NT E2M1 terms, q[t] the lane's code and s[t] the block's E8M0 code of term t;
 // each term rounds the exact residual of the ones before it.
@@ -121,8 +129,9 @@ __device__ __forceinline__ void split_block_e2m1(float (&r)[32], uint4 (&packed)
           : "f"(__fmul_rn(r[16 + i], inv)), "f"(__fmul_rn(r[i], inv)));
       w[i >> 2] |= (uint32_t)(b & 0xFFu) << (8 * (i & 3));
       if (t + 1 < NT) {
-        r[i] = __fmaf_rn(-e2m1_to_f32(b & 0xFu), fwd, r[i]);
-        r[16 + i] = __fmaf_rn(-e2m1_to_f32((b >> 4) & 0xFu), fwd, r[16 + i]);
+        const uint32_t h2 = e2m1x2_to_f16x2(b);  // both codes exactly, low nibble in the low half
+        r[i] = __fmaf_rn(-__half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))), fwd, r[i]);
+        r[16 + i] = __fmaf_rn(-__half2float(__ushort_as_half((unsigned short)(h2 >> 16))), fwd, r[16 + i]);
       }
     }
     packed[t] = make_uint4(w[0], w[1], w[2], w[3]);

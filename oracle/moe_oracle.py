@@ -430,7 +430,7 @@ def expert_ffn(x_rows: np.ndarray, Wg: np.ndarray, bg, Wu: np.ndarray, bu, Wd: n
       "q8"         the q8 rail's operands: x and h (rounded to float32)
                    requantised in blocks of 32 (quantize_q8), exact products.
       "e2m1_terms" the prefill rail on prepacked planes: x as six E2M1 terms
-                   and h as three (split_e2m1_terms), exact products.
+                   and h as four (split_e2m1_terms), exact products.
     """
     x = np.asarray(x_rows, np.float64)
     if operands == "bf16":
@@ -456,7 +456,7 @@ def expert_ffn(x_rows: np.ndarray, Wg: np.ndarray, bg, Wu: np.ndarray, bu, Wd: n
     elif operands == "q8":
         h = dequant_q8(*quantize_q8(h.astype(np.float32)))
     elif operands == "e2m1_terms":
-        h = split_e2m1_terms(h, 3)
+        h = split_e2m1_terms(h, 4)
     return h @ Wd.T + (0.0 if bd is None else np.asarray(bd, np.float64))
 
 

@@ -1,5 +1,5 @@
 """GPU parity of the prefill rail on prepacked weights (MOE_RAIL_GROUPED_MX4:
-tcgen05.mma kind::mxf4 with x and h as four E2M1 terms) against the float64
+tcgen05.mma kind::mxf4 with x as six E2M1 terms and h as four) against the float64
 layer and against the oracle evaluated on the same E2M1-term operands."""
 
 import numpy as np
