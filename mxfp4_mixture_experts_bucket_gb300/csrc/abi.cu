@@ -221,6 +221,7 @@ struct PackedPrefillWorkspace {
   int32_t* inv;
   uint8_t* aq;   // x terms in bucket order, activation-chunk layout
   uint8_t* asf;
+  int2* segs;    // segment table of the bucket
   float* hf;     // h as float rows, written by the gate/up GEMM
   uint8_t* hq;   // h terms
   uint8_t* hsf;
@@ -247,6 +248,7 @@ size_t layout_packed_prefill_workspace(int T, int D, int F, int k, int E, char* 
   w.inv = reinterpret_cast<int32_t*>(take((size_t)T * k * 4));
   w.aq = reinterpret_cast<uint8_t*>(take(prefill_operand_bytes((int)mr, D, kPrefillXTerms)));
   w.asf = reinterpret_cast<uint8_t*>(take(prefill_atom_bytes((int)mr, D, kPrefillXTerms)));
+  w.segs = reinterpret_cast<int2*>(take((2 * (mr / 128) + 1) * sizeof(int2)));
   w.hf = reinterpret_cast<float*>(take(mr * (size_t)F * 4));
   w.hq = reinterpret_cast<uint8_t*>(take(prefill_operand_bytes((int)mr, F, kPrefillHTerms)));
   w.hsf = reinterpret_cast<uint8_t*>(take(prefill_atom_bytes((int)mr, F, kPrefillHTerms)));
@@ -856,7 +858,7 @@ int packed_prefill_impl(const moe_packed_layer_t& P, const float* x, int T, void
                                       ws.inv, d->status, L))) != MOE_OK)
     return rc;
   if ((rc = cuda_status(launch_quant_rows_e2m1(x, T, P.D, P.k, ws.rows, ws.counts, ws.basep, P.E, (int)ws.max_rows, ws.aq,
-                                               ws.asf, y, L))) != MOE_OK)
+                                               ws.asf, y, ws.segs, L))) != MOE_OK)
     return rc;
   GroupedMX4Args g{};
   g.kind = 0;
@@ -872,6 +874,7 @@ int packed_prefill_impl(const moe_packed_layer_t& P, const float* x, int T, void
   g.counts = ws.counts;
   g.basep = ws.basep;
   g.rows = ws.rows;
+  g.segs = ws.segs;
   g.max_rows = (int)ws.max_rows;
   g.k = P.k;
   g.weights = wts;

@@ -100,6 +100,7 @@ struct Params {
   const int32_t* counts;
   const int32_t* basep;
   const int32_t* rows;
+  const int2* segs;    // the segment table: segs[0].x = count; segs[1 + i] = ((b << 1) | s, (e << 8) | live)
   int k;
   const float* weights;
   const uint8_t* aq;   // activation chunks [ntiles][NK][terms][8192]
@@ -175,30 +176,21 @@ struct Unit {
   Segment g;
 };
 
-// The next unit of this CTA that is not a ghost (past the padded end of the
-// last bucket, or a second segment its tile does not have); false when there
-// is none. `cursor` walks the unit indices ((tile, segment) major).
-__device__ __forceinline__ bool next_unit(const Params& p, int mpad, int& cursor, Unit& u) {
-  const int nunits = p.ntiles * 2 * p.npair;
-  for (; cursor < nunits; cursor += gridDim.x) {
-    const int bs = cursor / p.npair, t = cursor - bs * p.npair;
-    const int b = bs >> 1, s = bs & 1;
-    const int row0 = 128 * b;
-    if (row0 >= mpad) continue;
-    int e;
-    const int live = tile_live(p.basep, p.counts, p.E, row0, e);
-    if (live <= 0) continue;
-    const Segment g = segment_of(live, s);
-    if (g.rows <= 0) continue;
-    u.b = b;
-    u.s = s;
-    u.t = t;
-    u.e = e;
-    u.g = g;
-    cursor += gridDim.x;
-    return true;
-  }
-  return false;
+// The next unit of this CTA, or false when there is none: unit i is segment
+// i / npair of the segment table (every segment of every live bucket tile, in
+// bucket order) and weight tile pair i % npair; the CTAs take units
+// blockIdx.x, blockIdx.x + gridDim.x, ...
+__device__ __forceinline__ bool next_unit(const Params& p, int nseg, int& cursor, Unit& u) {
+  if (cursor >= nseg * p.npair) return false;
+  const int si = cursor / p.npair;
+  const int2 sg = __ldg(p.segs + 1 + si);
+  u.b = sg.x >> 1;
+  u.s = sg.x & 1;
+  u.t = cursor - si * p.npair;
+  u.e = sg.y >> 8;
+  u.g = segment_of(sg.y & 255, u.s);
+  cursor += gridDim.x;
+  return true;
 }
 
 // 16 columns from column c0 of the accumulator at `acc` (this warp's lanes),
@@ -261,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = s_tmem;
-  const int mpad = __ldg(p.basep + p.E);
+  const int nseg = __ldg(&p.segs[0].x);
   const int NK = p.NK;
   const volatile int* abort_flag = &s_abort;
   auto fail = [&](int role, int seq) {
@@ -281,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
     int cursor = blockIdx.x, i = 0;
     Unit u;
     bool ok = true;
-    while (ok && next_unit(p, mpad, cursor, u)) {
+    while (ok && next_unit(p, nseg, cursor, u)) {
       for (int j = 0; j < NK; ++j, ++i) {
         const int st = i % kStages, n = i / kStages;
         const bool okw = tc::mbar_wait_sleep(tc::smem_u32(&full_bar[st]), n & 1, abort_flag, 32);
@@ -316,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
       int cursor = blockIdx.x, i = 0, issued = 0;
       Unit u;
       bool ok = true;
-      while (ok && next_unit(p, mpad, cursor, u)) {
+      while (ok && next_unit(p, nseg, cursor, u)) {
         const uint32_t run = (uint32_t)u.g.rn * 64;  // one term's rows of the segment
         for (int j = 0; j < NK; ++j, ++i) {
           const int st = i % kStages, n = i / kStages;
@@ -371,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
       int cursor = blockIdx.x, i = 0, lu = 0;
       Unit u;
       bool ok = true;
-      while (ok && next_unit(p, mpad, cursor, u)) {
+      while (ok && next_unit(p, nseg, cursor, u)) {
         if (lu > 0 && !tc::mbar_wait_sleep(tc::smem_u32(&acce_bar), (lu - 1) & 1, abort_flag, 32)) {
           fail(1, i);
           break;
@@ -427,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
     int cur_epi = blockIdx.x;
     Unit ue{};
     int ldone = 0;  // units whose epilogue has run
-    bool have_e = next_unit(p, mpad, cur_epi, ue);
+    bool have_e = next_unit(p, nseg, cur_epi, ue);
     while (have_e) {
       // ---- the epilogue of unit ldone (ue)
       const int e = ue.e;
@@ -525,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
         }
       }
       ++ldone;
-      have_e = next_unit(p, mpad, cur_epi, ue);
+      have_e = next_unit(p, nseg, cur_epi, ue);
     }
     tc::fence_before_sync();
     __syncwarp();
@@ -547,9 +539,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
 // (bucket row, 32-block), which loads the block's 128 bytes, splits it
 // (split_block_e2m1), stores each term's 16 bytes with one store and its scale
 // byte into its segment's atoms. GATHER: the rows are x's token rows (x: the
-// gate/up operand) and y[0 .. T*C) is zeroed (the down GEMM accumulates into
-// it); else the rows are src's own bucket rows (h: the down operand). Pad rows
-// and blocks past C are zero.
+// gate/up operand), y[0 .. T*C) is zeroed (the down GEMM accumulates into it)
+// and block 0 writes the segment table; else the rows are src's own bucket rows
+// (h: the down operand). Pad rows up to the segment's rounded end and blocks
+// past C are zero; rows past that end are never read and not written.
 // ---------------------------------------------------------------------------
 template <int NT, bool GATHER>
 __global__ void __launch_bounds__(256) quant_rows_e2m1_kernel(const float* __restrict__ src, int T, int C, int k,
@@ -557,9 +550,36 @@ __global__ void __launch_bounds__(256) quant_rows_e2m1_kernel(const float* __res
                                                               const int32_t* __restrict__ counts,
                                                               const int32_t* __restrict__ basep, int E, int NK,
                                                               uint8_t* __restrict__ aq, uint8_t* __restrict__ asf,
-                                                              float* __restrict__ y) {
+                                                              float* __restrict__ y, int2* __restrict__ segs) {
   pdl_launch_dependents();
   pdl_wait();
+  if (GATHER && blockIdx.x == 0 && threadIdx.x < 32) {
+    // the segment table: one lane per expert, a warp prefix over the experts' segment counts
+    const int lane = threadIdx.x;
+    int total = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const int cnt = e < E ? counts[e] : 0;
+      const int t0 = e < E ? (basep[e] >> 7) : 0;
+      const int ntl = (cnt + 127) >> 7;
+      int ns = 0;
+      for (int i = 0; i < ntl; ++i) ns += min(128, cnt - 128 * i) > kSegMax ? 2 : 1;
+      int incl = ns;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      int pos = total + incl - ns;
+      for (int i = 0; i < ntl; ++i) {
+        const int live = min(128, cnt - 128 * i);
+        for (int sg = 0; sg < (live > kSegMax ? 2 : 1); ++sg)
+          segs[1 + pos++] = make_int2(((t0 + i) << 1) | sg, (e << 8) | live);
+      }
+      total += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) segs[0] = make_int2(total, 0);
+  }
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
   const int mpad = basep[E];
@@ -573,6 +593,7 @@ __global__ void __launch_bounds__(256) quant_rows_e2m1_kernel(const float* __res
     const int s = live > kSegMax ? (rt >> 6) : 0;
     const Segment g = segment_of(live, s);
     const int r = rt - g.base;
+    if (r >= g.rn) continue;  // rows past the segment's rounded end are never read
     const int m = slots_of<NT>(g.rn);
     uint8_t* chunk = aq + ((size_t)b * NK + j) * (NT * kTermBytes);
     uint8_t* atoms = asf + (((size_t)b * NK + j) * 2 + s) * (NT * kAtom);
@@ -601,11 +622,9 @@ __global__ void __launch_bounds__(256) quant_rows_e2m1_kernel(const float* __res
 #pragma unroll
     for (int term = 0; term < NT; ++term) {
       *reinterpret_cast<uint4*>(chunk + act_off(rt, term, kb, 0)) = packed[term];
-      if (r < g.rn) {  // rows past the segment's rounded end are never read
-        int n;
-        const int ai = atom_index(term, m, g.rn, r, n);
-        atoms[(size_t)ai * kAtom + dmx::atom_off(n, kb)] = (uint8_t)sc[term];
-      }
+      int n;
+      const int ai = atom_index(term, m, g.rn, r, n);
+      atoms[(size_t)ai * kAtom + dmx::atom_off(n, kb)] = (uint8_t)sc[term];
     }
   }
   if (GATHER) {
@@ -639,15 +658,15 @@ int quant_blocks(int max_rows, int C) {
 
 cudaError_t launch_quant_rows_e2m1(const float* x, int T, int D, int k, const int32_t* rows, const int32_t* counts,
                                    const int32_t* basep, int E, int max_rows, uint8_t* aq, uint8_t* asf, float* y,
-                                   Launch L) {
+                                   int2* segs, Launch L) {
   return launch_kernel(gx4::quant_rows_e2m1_kernel<kPrefillXTerms, true>, dim3(quant_blocks(max_rows, D)), dim3(256), 0,
-                       L, x, T, D, k, rows, counts, basep, E, (D + 127) / 128, aq, asf, y);
+                       L, x, T, D, k, rows, counts, basep, E, (D + 127) / 128, aq, asf, y, segs);
 }
 
 cudaError_t launch_quant_h_e2m1(const float* hf, int F, const int32_t* rows, const int32_t* counts,
                                 const int32_t* basep, int E, int max_rows, uint8_t* hq, uint8_t* hsf, Launch L) {
   return launch_kernel(gx4::quant_rows_e2m1_kernel<kPrefillHTerms, false>, dim3(quant_blocks(max_rows, F)), dim3(256),
-                       0, L, hf, 0, F, 1, rows, counts, basep, E, (F + 127) / 128, hq, hsf, nullptr);
+                       0, L, hf, 0, F, 1, rows, counts, basep, E, (F + 127) / 128, hq, hsf, nullptr, nullptr);
 }
 
 cudaError_t launch_grouped_mx4(const GroupedMX4Args& a, Launch L) {
@@ -671,6 +690,7 @@ cudaError_t launch_grouped_mx4(const GroupedMX4Args& a, Launch L) {
   prm.counts = a.counts;
   prm.basep = a.basep;
   prm.rows = a.rows;
+  prm.segs = a.segs;
   prm.k = a.k;
   prm.weights = a.weights;
   prm.aq = a.aq;
