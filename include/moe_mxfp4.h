@@ -510,7 +510,7 @@ size_t moe_ffn_packed_workspace_bytes(int T, int D, int F, int E, int k, int rai
  * in bucket order; on tcgen05.mma kind::mxf4 each 128-row weight tile is the A
  * operand and a bucket segment of at most 96 live rows (two terms stacked per
  * MMA) the B operand, so the MMA work follows the live rows, not the 128-row
- * padding; h leaves the gate/up epilogue as four E2M1 terms, and the down
+ * padding; h leaves the gate/up epilogue as float rows split into four E2M1 terms, and the down
  * epilogue scatters w*(acc + bd) into y with float atomics (summation order not
  * deterministic).
  */

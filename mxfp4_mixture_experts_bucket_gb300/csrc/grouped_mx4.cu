@@ -16,6 +16,8 @@
 // sum over the terms congruent to j mod m for row n; the epilogue adds the m
 // slots, all in the thread that owns the weight row. m is the largest divisor
 // of the term count with m * rn <= 192 (the tensor memory of one accumulator).
+// An MMA costs about N / 2 cycles down to a floor near N = 110, so stacking
+// terms keeps small segments off that floor.
 //
 // A bucket tile with L live rows is one segment when L <= 96, else two (rows
 // 0..63 and 64..L-1); rn = the segment's rows rounded up to 16. A work unit is
@@ -27,8 +29,8 @@
 // at 64*n + 16*(kb ^ ((n>>1)&3))), terms one after the other, so a segment's
 // rows of a term are one contiguous run. Its scale atoms: one run of `terms`
 // atoms per segment; term t's scales for segment row r sit in atom
-// 2*(t / m) + (n >> 7) at row n & 127, n = (t % m) * rn + r (B row n of the
-// term group's MMA). Written by quant_rows_e2m1_kernel: x from the token rows,
+// (t / m) * ceil(m * rn / 128) + (n >> 7) at row n & 127, n = (t % m) * rn + r
+// (B row n of the term group's MMA). Written by quant_rows_e2m1_kernel: x from the token rows,
 // h from the float rows the gate/up epilogue leaves.
 //
 // Warps: 0..3 scale loaders (one per tensor-memory lane quarter: each step's
@@ -85,7 +87,6 @@ struct Plan {
       cmin(6, cmin((int)((226u * 1024u) / kStageBytes), (int)((kTmemCols - kSfBase) / kSfCols)));
   static constexpr uint32_t kDynSmem = kStages * kStageBytes + 512;
 };
-static_assert(kPrefillXTerms % 2 == 0 && kPrefillHTerms % 2 == 0, "terms enter the MMA in pairs");
 static_assert(Plan<0>::kStages >= 3 && Plan<1>::kStages >= 3, "ring depth");
 static_assert(kSfBase + Plan<0>::kStages * Plan<0>::kSfCols <= kTmemCols, "tensor memory plan");
 static_assert(kSfBase + Plan<1>::kStages * Plan<1>::kSfCols <= kTmemCols, "tensor memory plan");
@@ -141,21 +142,34 @@ __host__ __device__ __forceinline__ Segment segment_of(int live, int s) {
   g.rn = (g.rows + 15) & ~15;
   return g;
 }
-// Terms per MMA for a segment of rn rows: the largest divisor of `terms` with
-// m * rn <= kAccStride (at least 2: rn <= 96).
+// Terms per MMA for a segment of rn rows: the largest divisor m of `terms`
+// with m * rn <= kAccStride (m = 1 always fits: rn <= 96).
 template <int TERMS>
 __host__ __device__ __forceinline__ int slots_of(int rn) {
-  int m = 2;
+  int m = 1;
 #pragma unroll
-  for (int d = 3; d <= TERMS; ++d)
+  for (int d = 2; d <= TERMS; ++d)
     if (TERMS % d == 0 && d * rn <= (int)kAccStride) m = d;
   return m;
 }
-// Atom (within the segment's run) and atom row of the scales of term t, segment row r.
+// Scale atoms per term group (one per 128 B rows of the group's MMA).
+__host__ __device__ __forceinline__ int atoms_per_group(int m, int rn) { return (m * rn + 127) >> 7; }
+// Atom (within the segment's run) and atom row of the scales of term t,
+// segment row r: B row n = (t % m) * rn + r of group t / m. At most `terms`
+// atoms: a group of m >= 2 terms takes at most 2 (m * rn <= 192), a single
+// term 1 (rn <= 96).
 __host__ __device__ __forceinline__ int atom_index(int t, int m, int rn, int r, int& n) {
   const int nn = (t % m) * rn + r;
   n = nn & 127;
-  return 2 * (t / m) + (nn >> 7);
+  return (t / m) * atoms_per_group(m, rn) + (nn >> 7);
+}
+
+// Atoms a segment of rn rows uses: the first (terms / m) * ceil(m * rn / 128)
+// of its run.
+template <int TERMS>
+__host__ __device__ __forceinline__ int used_atoms(int rn) {
+  const int m = slots_of<TERMS>(rn);
+  return (TERMS / m) * atoms_per_group(m, rn);
 }
 
 // Live rows of the bucket tile starting at row0 (< basep[E]) and its expert.
@@ -197,6 +211,12 @@ __device__ __forceinline__ bool next_unit(const Params& p, int nseg, int& cursor
 // summed over its m term slots (slot j at column j * rn + c0).
 __device__ __forceinline__ void slot_sum16(uint32_t acc, int c0, int rn, int m, float (&out)[16]) {
   uint32_t a0[16], a1[16];
+  if (m == 1) {
+    tc::tmem_ld16_wait(acc + c0, a0);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) out[k] = __uint_as_float(a0[k]);
+    return;
+  }
   tc::tmem_ld16x2_wait(acc + c0, acc + rn + c0, a0, a1);
 #pragma unroll
   for (int k = 0; k < 16; ++k) out[k] = __uint_as_float(a0[k]) + __uint_as_float(a1[k]);
@@ -274,6 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
     Unit u;
     bool ok = true;
     while (ok && next_unit(p, nseg, cursor, u)) {
+      const int na = used_atoms<kTerms>(u.g.rn);
       for (int j = 0; j < NK; ++j, ++i) {
         const int st = i % kStages, n = i / kStages;
         const bool okw = tc::mbar_wait_sleep(tc::smem_u32(&full_bar[st]), n & 1, abort_flag, 32);
@@ -284,11 +305,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
         }
         const uint8_t* sbp = smem + (size_t)st * kStageBytes;
         const uint32_t sfs = lane_base + kSfBase + (uint32_t)st * kSfCols;
-#pragma unroll
-        for (int a = 0; a < kTerms + 2; ++a) {  // activation atoms, then the two weight atoms
-          const uint8_t* atom = sbp + (a < kTerms ? kOffSfa + a * kAtom : kOffSfw + (a - kTerms) * kAtom);
-          const uint4 w = *reinterpret_cast<const uint4*>(atom + 16 * lane);
+#pragma unroll 1
+        for (int a = 0; a < na; ++a) {  // the activation atoms the segment's MMAs read
+          const uint4 w = *reinterpret_cast<const uint4*>(sbp + kOffSfa + a * kAtom + 16 * lane);
           tc::tmem_st4(sfs + 4 * a, w.x, w.y, w.z, w.w);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {  // the two weight atoms
+          const uint4 w = *reinterpret_cast<const uint4*>(sbp + kOffSfw + h * kAtom + 16 * lane);
+          tc::tmem_st4(sfs + 4 * (kTerms + h), w.x, w.y, w.z, w.w);
         }
         tc::tmem_wait_st();
         tc::fence_before_sync();
@@ -322,10 +347,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
           if (warp == 4) {
             const size_t achunk = (size_t)u.b * NK + j;
             const uint8_t* src = p.aq + achunk * (size_t)(kTerms * kTermBytes) + (size_t)u.g.base * 64;
-            tc::mbar_expect_tx(fb, (uint32_t)kTerms * run + kTerms * kAtom);
+            const uint32_t abytes = (uint32_t)used_atoms<kTerms>(u.g.rn) * kAtom;
+            tc::mbar_expect_tx(fb, (uint32_t)kTerms * run + abytes);
             for (int t = 0; t < kTerms; ++t)
               tc::bulk_load(sb + kOffAct + (uint32_t)t * run, src + (size_t)t * kTermBytes, run, fb);
-            tc::bulk_load(sb + kOffSfa, p.asf + (achunk * 2 + u.s) * (kTerms * kAtom), kTerms * kAtom, fb);
+            tc::bulk_load(sb + kOffSfa, p.asf + (achunk * 2 + u.s) * (kTerms * kAtom), abytes, fb);
           } else {
             // a tile shorter than 128 rows leaves the rest stale: those rows only feed
             // accumulator lanes nobody reads
@@ -369,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
           break;
         }
         tc::fence_after_sync();
-        const int m = slots_of<kTerms>(u.g.rn), ngrp = kTerms / m;
+        const int m = slots_of<kTerms>(u.g.rn), ngrp = kTerms / m, apg = atoms_per_group(m, u.g.rn);
         const uint32_t idesc = idesc_mxf4(128, m * u.g.rn);
         const bool two = wtile(u, 1) >= 0;
         const uint32_t grp_step = (uint32_t)(m * u.g.rn * 64) >> 4;  // descriptor units between term groups
@@ -394,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
 #pragma unroll 1
             for (int q = 0; q < ngrp; ++q) {
               const uint64_t bq = bdesc + (uint64_t)(q * grp_step + 2 * kh);
-              const uint32_t sfb = sfs + 8 * q;
+              const uint32_t sfb = sfs + 4 * q * apg;
               const uint32_t acc = (j == 0 && kh == 0 && q == 0) ? 0u : 1u;
               mma_mxf4(tmem, adesc0 + (uint64_t)(2 * kh), bq, id, sfs + 4 * kTerms, sfb, acc);
               if (two) mma_mxf4(tmem + kAccStride, adesc1 + (uint64_t)(2 * kh), bq, id, sfs + 4 * kTerms + 4, sfb, acc);
@@ -545,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
 // past C are zero; rows past that end are never read and not written.
 // ---------------------------------------------------------------------------
 template <int NT, bool GATHER>
-__global__ void __launch_bounds__(256) quant_rows_e2m1_kernel(const float* __restrict__ src, int T, int C, int k,
+__global__ void __launch_bounds__(256, 3) quant_rows_e2m1_kernel(const float* __restrict__ src, int T, int C, int k,
                                                               const int32_t* __restrict__ rows,
                                                               const int32_t* __restrict__ counts,
                                                               const int32_t* __restrict__ basep, int E, int NK,
@@ -597,8 +623,6 @@ __global__ void __launch_bounds__(256) quant_rows_e2m1_kernel(const float* __res
     const int m = slots_of<NT>(g.rn);
     uint8_t* chunk = aq + ((size_t)b * NK + j) * (NT * kTermBytes);
     uint8_t* atoms = asf + (((size_t)b * NK + j) * 2 + s) * (NT * kAtom);
-    uint4 packed[NT];
-    uint32_t sc[NT];
     if (a >= 0 && blk < nb) {
       float v[32];
       const float* row = GATHER ? src + (size_t)(a / k) * C : src + (size_t)p * C;
@@ -611,20 +635,24 @@ __global__ void __launch_bounds__(256) quant_rows_e2m1_kernel(const float* __res
         v[4 * i + 2] = f.z;
         v[4 * i + 3] = f.w;
       }
-      mx::split_block_e2m1<NT>(v, packed, sc);
+#pragma unroll
+      for (int term = 0; term < NT; ++term) {  // each term stored as soon as it is split
+        uint4 packed;
+        uint32_t sc;
+        mx::split_block_e2m1_term(v, term + 1 == NT, packed, sc);
+        *reinterpret_cast<uint4*>(chunk + act_off(rt, term, kb, 0)) = packed;
+        int n;
+        const int ai = atom_index(term, m, g.rn, r, n);
+        atoms[(size_t)ai * kAtom + dmx::atom_off(n, kb)] = (uint8_t)sc;
+      }
     } else {
 #pragma unroll
       for (int term = 0; term < NT; ++term) {
-        packed[term] = make_uint4(0u, 0u, 0u, 0u);
-        sc[term] = 0u;
+        *reinterpret_cast<uint4*>(chunk + act_off(rt, term, kb, 0)) = make_uint4(0u, 0u, 0u, 0u);
+        int n;
+        const int ai = atom_index(term, m, g.rn, r, n);
+        atoms[(size_t)ai * kAtom + dmx::atom_off(n, kb)] = 0;
       }
-    }
-#pragma unroll
-    for (int term = 0; term < NT; ++term) {
-      *reinterpret_cast<uint4*>(chunk + act_off(rt, term, kb, 0)) = packed[term];
-      int n;
-      const int ai = atom_index(term, m, g.rn, r, n);
-      atoms[(size_t)ai * kAtom + dmx::atom_off(n, kb)] = (uint8_t)sc[term];
     }
   }
   if (GATHER) {

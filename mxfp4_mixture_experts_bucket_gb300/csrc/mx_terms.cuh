@@ -107,35 +107,38 @@ __device__ __forceinline__ void split_terms_e2m1(float v, uint32_t (&q)[NT], uin
 }
 
 // The same split for a block of 32 values held by one thread (r[i] = column i),
-// with the same arithmetic: each term's 32 codes come back packed in the MXFP4
-// block layout (byte i = column i low nibble, column 16 + i high), r keeps the
-// last residual.
+// with the same arithmetic, one term at a time: the term's 32 codes come back
+// packed in the MXFP4 block layout (byte i = column i low nibble, column 16 + i
+// high) with its E8M0 code s; r becomes the residual unless `last`.
+__device__ __forceinline__ void split_block_e2m1_term(float (&r)[32], bool last, uint4& packed, uint32_t& s) {
+  uint32_t am = 0;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) am = max(am, __float_as_uint(r[i]) & 0x7FFFFFFFu);
+  s = e2m1_block_code(am);
+  const float inv = inv_scale(s), fwd = fwd_scale(s);
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    // columns i and 16 + i in one conversion: the byte of the block layout
+    uint16_t b;
+    asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n cvt.u16.u8 %0, t;\n}"
+        : "=h"(b)
+        : "f"(__fmul_rn(r[16 + i], inv)), "f"(__fmul_rn(r[i], inv)));
+    w[i >> 2] |= (uint32_t)(b & 0xFFu) << (8 * (i & 3));
+    if (!last) {
+      const uint32_t h2 = e2m1x2_to_f16x2(b);  // both codes exactly, low nibble in the low half
+      r[i] = __fmaf_rn(-__half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))), fwd, r[i]);
+      r[16 + i] = __fmaf_rn(-__half2float(__ushort_as_half((unsigned short)(h2 >> 16))), fwd, r[16 + i]);
+    }
+  }
+  packed = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// All NT terms of one thread's block at once; r keeps the last residual.
 template <int NT>
 __device__ __forceinline__ void split_block_e2m1(float (&r)[32], uint4 (&packed)[NT], uint32_t (&s)[NT]) {
 #pragma unroll
-  for (int t = 0; t < NT; ++t) {
-    uint32_t am = 0;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) am = max(am, __float_as_uint(r[i]) & 0x7FFFFFFFu);
-    s[t] = e2m1_block_code(am);
-    const float inv = inv_scale(s[t]), fwd = fwd_scale(s[t]);
-    uint32_t w[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      // columns i and 16 + i in one conversion: the byte of the block layout
-      uint16_t b;
-      asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n cvt.u16.u8 %0, t;\n}"
-          : "=h"(b)
-          : "f"(__fmul_rn(r[16 + i], inv)), "f"(__fmul_rn(r[i], inv)));
-      w[i >> 2] |= (uint32_t)(b & 0xFFu) << (8 * (i & 3));
-      if (t + 1 < NT) {
-        const uint32_t h2 = e2m1x2_to_f16x2(b);  // both codes exactly, low nibble in the low half
-        r[i] = __fmaf_rn(-__half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))), fwd, r[i]);
-        r[16 + i] = __fmaf_rn(-__half2float(__ushort_as_half((unsigned short)(h2 >> 16))), fwd, r[16 + i]);
-      }
-    }
-    packed[t] = make_uint4(w[0], w[1], w[2], w[3]);
-  }
+  for (int t = 0; t < NT; ++t) split_block_e2m1_term(r, t + 1 == NT, packed[t], s[t]);
 }
 
 // A warp's block of E2M1 codes (lane l holds column l) packed as the MXFP4 block
