@@ -95,6 +95,7 @@ int resolve_rail(int T, int rail) {
 
 struct Workspace {
   float* logits;
+  float* rpart;    // grouped rails: the split router's partial dots
   int32_t* ids;
   float* w;
   int32_t* counts;
@@ -133,6 +134,7 @@ size_t layout_workspace(int T, int D, int F, int E, int k, int rail, char* base,
   };
   Workspace w{};
   w.logits = reinterpret_cast<float*>(take((size_t)T * E * 4));
+  if (tile != 1) w.rpart = reinterpret_cast<float*>(take(router_partials_bytes(T, E)));
   w.ids = reinterpret_cast<int32_t*>(take((size_t)T * k * 4));
   w.w = reinterpret_cast<float*>(take((size_t)T * k * 4));
   w.counts = reinterpret_cast<int32_t*>(take((size_t)E * 4));
@@ -221,6 +223,7 @@ struct PackedPrefillWorkspace {
   int32_t* inv;
   uint8_t* aq;   // x terms in bucket order, activation-chunk layout
   uint8_t* asf;
+  float* rpart;  // the split router's partial dots
   int2* segs;    // segment table of the bucket
   float* hf;     // h as float rows, written by the gate/up GEMM
   uint8_t* hq;   // h terms
@@ -248,6 +251,7 @@ size_t layout_packed_prefill_workspace(int T, int D, int F, int k, int E, char* 
   w.inv = reinterpret_cast<int32_t*>(take((size_t)T * k * 4));
   w.aq = reinterpret_cast<uint8_t*>(take(prefill_operand_bytes((int)mr, D, kPrefillXTerms)));
   w.asf = reinterpret_cast<uint8_t*>(take(prefill_atom_bytes((int)mr, D, kPrefillXTerms)));
+  w.rpart = reinterpret_cast<float*>(take(router_partials_bytes(T, E)));
   w.segs = reinterpret_cast<int2*>(take((2 * (mr / 128) + 1) * sizeof(int2)));
   w.hf = reinterpret_cast<float*>(take(mr * (size_t)F * 4));
   w.hq = reinterpret_cast<uint8_t*>(take(prefill_operand_bytes((int)mr, F, kPrefillHTerms)));
@@ -574,9 +578,16 @@ int ffn_layer_impl(const float* x, float* x_copy, int T, int D, int F, int E, in
   Launch L{stream, false};
   if (rail != MOE_RAIL_GEMV) x_copy = nullptr;  // prefill sizes read x from device memory
   MOE_REQUIRE(x_copy == nullptr || aligned(x_copy, 16));
-  rc = cuda_status(launch_router_logits(x, T, D, w_router, b_router, E, ws.logits, x_copy, L));
-  if (rc != MOE_OK) return rc;
-  L.pdl = true;
+  if (ws.rpart) {  // grouped rails: router split over D, then top-k
+    if ((rc = cuda_status(launch_route_topk(x, T, D, w_router, b_router, E, k, ws.logits, ws.rpart, ids, wts, L))) !=
+        MOE_OK)
+      return rc;
+    L.pdl = true;
+  } else {
+    rc = cuda_status(launch_router_logits(x, T, D, w_router, b_router, E, ws.logits, x_copy, L));
+    if (rc != MOE_OK) return rc;
+    L.pdl = true;
+  }
   if (rail == MOE_RAIL_GEMV) {
     // decode: the two expert kernels take the top-k of the logits themselves
     rc = cuda_status(launch_gemv_gateup(g_qs, g_sc, bg, u_qs, u_sc, bu, E, F, D, T, k, x_copy ? x_copy : x,
@@ -586,8 +597,7 @@ int ffn_layer_impl(const float* x, float* x_copy, int T, int D, int F, int E, in
     return cuda_status(launch_gemv_down(d_qs, d_sc, bd, E, D, F, T, k, ws.h, ws.logits, nullptr,
                                         nullptr, y, d->status, L));
   }
-  rc = cuda_status(launch_topk_softmax(ws.logits, T, E, k, ids, wts, L));
-  if (rc != MOE_OK) return rc;
+  if (!ws.rpart && (rc = cuda_status(launch_topk_softmax(ws.logits, T, E, k, ids, wts, L))) != MOE_OK) return rc;
   if (rail == MOE_RAIL_GEMV_Q8) {
     // x -> Q8; gate and up per slot (the slot's token row); swiglu in place; h -> Q8; down per slot; combine
     const int TK = T * k;
@@ -849,11 +859,10 @@ int packed_prefill_impl(const moe_packed_layer_t& P, const float* x, int T, void
   int32_t* ids = ids_out ? ids_out : ws.ids;
   float* wts = weights_out ? weights_out : ws.w;
   Launch L{stream, false};
-  if ((rc = cuda_status(launch_router_logits(x, T, P.D, P.w_router, P.b_router, P.E, ws.logits, nullptr, L))) !=
-      MOE_OK)
+  if ((rc = cuda_status(launch_route_topk(x, T, P.D, P.w_router, P.b_router, P.E, P.k, ws.logits, ws.rpart, ids, wts,
+                                          L))) != MOE_OK)
     return rc;
   L.pdl = true;
-  if ((rc = cuda_status(launch_topk_softmax(ws.logits, T, P.E, P.k, ids, wts, L))) != MOE_OK) return rc;
   if ((rc = cuda_status(launch_bucket(ids, T, P.k, P.E, MOE_MM_TILE, (int)ws.max_rows, ws.counts, ws.basep, ws.rows,
                                       ws.inv, d->status, L))) != MOE_OK)
     return rc;

@@ -67,6 +67,14 @@ cudaError_t launch_router_logits(const float* x, int T, int D, const float* wr, 
                                  int E, float* logits, float* x_copy, Launch L);
 cudaError_t launch_topk_softmax(const float* logits, int T, int E, int k, int32_t* ids, float* w,
                                 Launch L);
+// Router and top-k-then-softmax in one call. T > 8 with `part` given: the
+// router split over D (partial dots in part, kRouterMaxSplits x T x E floats at
+// most), the slices added in order by the top-k kernel, which also writes
+// logits. Else the single-pass router and topk_softmax.
+constexpr int kRouterMaxSplits = 32;
+size_t router_partials_bytes(int T, int E);
+cudaError_t launch_route_topk(const float* x, int T, int D, const float* wr, const float* br, int E, int k,
+                              float* logits, float* part, int32_t* ids, float* w, Launch L);
 cudaError_t launch_bucket(const int32_t* ids, int T, int k, int E, int tile, int max_rows,
                           int32_t* counts, int32_t* basep, int32_t* rows, int32_t* inv,
                           int* status, Launch L);

@@ -5,7 +5,10 @@
 // folded into the bucket kernel, each expert's block computing its own padded
 // base in-block and publishing basep[e]; the resulting CSR is bit-identical
 // to the two-pass one.
+#include <algorithm>
+
 #include "decode_mx.cuh"
+
 #include "moe_common.cuh"
 #include "mx_terms.cuh"
 
@@ -252,6 +255,117 @@ __global__ void __launch_bounds__(512) router_logits_tile_kernel(const float* __
 }
 
 // ---------------------------------------------------------------------------
+// Prefill sizes, split over the dot length: block (token tile of 64, slice s
+// of D, expert tile of 32) writes part[s][t][e], the slice's partial dot, and
+// the top-k kernel adds the slices in slice order (so the result does not
+// depend on scheduling). Each thread holds 4 tokens x 4 experts (tokens
+// tt + 16 i, experts te + 8 j) and reads them from shared-memory tiles of
+// 32 columns staged by the whole block, the next tile's loads in flight
+// while the current one is used. Row pitch 36 floats: a quarter-warp's
+// float4 reads of 8 consecutive rows fall in 8 different bank groups.
+// ---------------------------------------------------------------------------
+constexpr int kRsT = 64, kRsE = 32, kRsPitch = 36;
+__global__ void __launch_bounds__(128) router_splitk_kernel(const float* __restrict__ x, int T, int D,
+                                                            const float* __restrict__ wr, int E, int ks,
+                                                            float* __restrict__ part) {
+  pdl_launch_dependents();
+  pdl_wait();
+  __shared__ __align__(16) float xs[kRsT][kRsPitch];
+  __shared__ __align__(16) float ws[kRsE][kRsPitch];
+  const int t0 = blockIdx.x * kRsT, s = blockIdx.y, e0 = blockIdx.z * kRsE;
+  const int kb = s * ks, ke = min(D, kb + ks);
+  const int tid = threadIdx.x, tt = tid >> 3, te = tid & 7;
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  float4 xr[4], wv[2];
+  auto gload = [&](int k0) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int idx = tid + 128 * i, r = idx >> 3, k = k0 + 4 * (idx & 7);
+      xr[i] = (t0 + r < T && k < ke) ? __ldg(reinterpret_cast<const float4*>(x + (size_t)(t0 + r) * D + k))
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int idx = tid + 128 * i, r = idx >> 3, k = k0 + 4 * (idx & 7);
+      wv[i] = (e0 + r < E && k < ke) ? __ldg(reinterpret_cast<const float4*>(wr + (size_t)(e0 + r) * D + k))
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  };
+  gload(kb);
+  for (int k0 = kb; k0 < ke; k0 += 32) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int idx = tid + 128 * i;
+      *reinterpret_cast<float4*>(&xs[idx >> 3][4 * (idx & 7)]) = xr[i];
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int idx = tid + 128 * i;
+      *reinterpret_cast<float4*>(&ws[idx >> 3][4 * (idx & 7)]) = wv[i];
+    }
+    __syncthreads();
+    if (k0 + 32 < ke) gload(k0 + 32);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      float4 a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4*>(&xs[tt + 16 * i][4 * c]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = *reinterpret_cast<const float4*>(&ws[te + 8 * j][4 * c]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float v = acc[i][j];
+          v = fmaf(a[i].x, b[j].x, v);
+          v = fmaf(a[i].y, b[j].y, v);
+          v = fmaf(a[i].z, b[j].z, v);
+          v = fmaf(a[i].w, b[j].w, v);
+          acc[i][j] = v;
+        }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int t = t0 + tt + 16 * i, e = e0 + te + 8 * j;
+      if (t < T && e < E) part[((size_t)s * T + t) * E + e] = acc[i][j];
+    }
+}
+
+// The slices' partial dots added in slice order, plus the bias, into
+// logits[t][e]; then top-k and softmax as topk_softmax_kernel. One warp per token.
+__global__ void __launch_bounds__(256) topk_partials_kernel(const float* __restrict__ part, int S,
+                                                            const float* __restrict__ br, int T, int E, int k,
+                                                            float* __restrict__ logits, int32_t* __restrict__ ids,
+                                                            float* __restrict__ w) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  for (int e = lane; e < E; e += 32) {
+    float v = 0.f;
+    for (int q = 0; q < S; ++q) v += part[((size_t)q * T + t) * E + e];
+    logits[(size_t)t * E + e] = v + (br ? br[e] : 0.f);
+  }
+  __syncwarp();
+  int my_id;
+  float my_w;
+  warp_topk_softmax(logits + (size_t)t * E, E, k, lane, my_id, my_w);
+  if (lane < k) {
+    ids[(size_t)t * k + lane] = my_id;
+    w[(size_t)t * k + lane] = my_w;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Top-k then softmax over the k selected; one warp per token.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) topk_softmax_kernel(const float* __restrict__ logits, int T,
@@ -460,6 +574,39 @@ cudaError_t launch_decode_prologue(const float* x, int T, int D, const float* wr
   const int nlx = (T + 1) / 2, nlog = nlx * ((E + 1) / 2);
   return launch_kernel(decode_prologue_kernel<2, 2>, dim3(nlog + nq), dim3(128), 0, L, x, T, D, wr, br, E,
                        logits, nlx, nlog, xq, xsf, npad, zero, nzero);
+}
+
+namespace {
+// Slices of D for the split router: about four blocks per SM, slices a
+// multiple of 32 wide, at most kRouterMaxSplits of them.
+void router_split(int T, int D, int E, int& S, int& ks) {
+  const int tiles = ((T + kRsT - 1) / kRsT) * ((E + kRsE - 1) / kRsE);
+  int s = (4 * device_sm_count() + tiles - 1) / tiles;
+  s = std::max(1, std::min(s, std::min(kRouterMaxSplits, D / 32)));
+  ks = ((D + s - 1) / s + 31) / 32 * 32;
+  S = (D + ks - 1) / ks;
+}
+}  // namespace
+
+size_t router_partials_bytes(int T, int E) { return (size_t)kRouterMaxSplits * T * E * sizeof(float); }
+
+cudaError_t launch_route_topk(const float* x, int T, int D, const float* wr, const float* br, int E, int k,
+                              float* logits, float* part, int32_t* ids, float* w, Launch L) {
+  if (T <= 0) return cudaSuccess;
+  if (T <= 8 || part == nullptr) {
+    cudaError_t err = launch_router_logits(x, T, D, wr, br, E, logits, nullptr, L);
+    if (err != cudaSuccess) return err;
+    L.pdl = true;
+    return launch_topk_softmax(logits, T, E, k, ids, w, L);
+  }
+  int S = 1, ks = D;
+  router_split(T, D, E, S, ks);
+  dim3 grid((T + kRsT - 1) / kRsT, S, (E + kRsE - 1) / kRsE);
+  cudaError_t err = launch_kernel(router_splitk_kernel, grid, dim3(128), 0, L, x, T, D, wr, E, ks, part);
+  if (err != cudaSuccess) return err;
+  L.pdl = true;
+  return launch_kernel(topk_partials_kernel, dim3((T + 7) / 8), dim3(256), 0, L, (const float*)part, S, br, T, E, k,
+                       logits, ids, w);
 }
 
 cudaError_t launch_topk_softmax(const float* logits, int T, int E, int k, int32_t* ids, float* w,

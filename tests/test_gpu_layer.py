@@ -322,7 +322,9 @@ def test_mx_activation_terms_are_exact(moe, cfg, T):
     mr = ru(T * k + E * 127, 128)
     nd = (D // 32 + 3) // 4
     off, parts = 0, {}
-    for name, nbytes in (("logits", T * E * 4), ("ids", T * k * 4), ("w", T * k * 4), ("counts", E * 4),
+    # the grouped rails' workspace: logits, the split router's partial dots (32 slices at most), the route
+    for name, nbytes in (("logits", T * E * 4), ("rpart", 32 * T * E * 4), ("ids", T * k * 4), ("w", T * k * 4),
+                         ("counts", E * 4),
                          ("basep", (E + 1) * 4), ("rows", mr * 4), ("inv", T * k * 4),
                          ("xq", 3 * mr * D), ("xs", 3 * nd * mr * 4)):
         parts[name] = ws[off:off + nbytes]
