@@ -111,27 +111,40 @@ __device__ __forceinline__ void split_terms_e2m1(float v, uint32_t (&q)[NT], uin
 // packed in the MXFP4 block layout (byte i = column i low nibble, column 16 + i
 // high) with its E8M0 code s; r becomes the residual unless `last`.
 __device__ __forceinline__ void split_block_e2m1_term(float (&r)[32], bool last, uint4& packed, uint32_t& s) {
-  uint32_t am = 0;
+  // the largest magnitude (a tree of depth 5; for finite values the float order
+  // of magnitudes is the integer order of their bit patterns)
+  float am[16];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) am = max(am, __float_as_uint(r[i]) & 0x7FFFFFFFu);
-  s = e2m1_block_code(am);
+  for (int i = 0; i < 16; ++i) am[i] = fmaxf(fabsf(r[i]), fabsf(r[16 + i]));
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) am[i] = fmaxf(am[i], am[i + w]);
+  s = e2m1_block_code(__float_as_uint(am[0]));
   const float inv = inv_scale(s), fwd = fwd_scale(s);
-  uint32_t w[4] = {0u, 0u, 0u, 0u};
+  uint32_t b[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     // columns i and 16 + i in one conversion: the byte of the block layout
-    uint16_t b;
-    asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n cvt.u16.u8 %0, t;\n}"
-        : "=h"(b)
-        : "f"(__fmul_rn(r[16 + i], inv)), "f"(__fmul_rn(r[i], inv)));
-    w[i >> 2] |= (uint32_t)(b & 0xFFu) << (8 * (i & 3));
-    if (!last) {
-      const uint32_t h2 = e2m1x2_to_f16x2(b);  // both codes exactly, low nibble in the low half
-      r[i] = __fmaf_rn(-__half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))), fwd, r[i]);
-      r[16 + i] = __fmaf_rn(-__half2float(__ushort_as_half((unsigned short)(h2 >> 16))), fwd, r[16 + i]);
+    const float2 v = __fmul2_rn(make_float2(r[i], r[16 + i]), make_float2(inv, inv));
+    asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n cvt.u32.u8 %0, t;\n}" : "=r"(b[i]) : "f"(v.y), "f"(v.x));
+  }
+  uint32_t w[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    w[q] = __byte_perm(__byte_perm(b[4 * q], b[4 * q + 1], 0x0040), __byte_perm(b[4 * q + 2], b[4 * q + 3], 0x0040),
+                       0x5410);
+  packed = make_uint4(w[0], w[1], w[2], w[3]);
+  if (!last) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t h2 = e2m1x2_to_f16x2(b[i]);  // both codes exactly, low nibble in the low half
+      const float2 d = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+      const float2 rr = __ffma2_rn(d, make_float2(-fwd, -fwd), make_float2(r[i], r[16 + i]));
+      r[i] = rr.x;
+      r[16 + i] = rr.y;
     }
   }
-  packed = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // All NT terms of one thread's block at once; r keeps the last residual.

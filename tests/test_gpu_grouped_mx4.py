@@ -77,3 +77,72 @@ def test_mx4_rail_is_the_packed_automatic_choice_beyond_decode_sizes(moe):
     yb = layer(x, rail=moe.MOE_RAIL_GROUPED_MX4)
     torch.cuda.synchronize()
     assert O.rownorm_rel_err(ya.cpu().numpy(), yb.cpu().numpy().astype(np.float64)).max() <= 1e-5
+
+
+def _ru(v, a):
+    return (v + a - 1) // a * a
+
+
+def _read_x_terms(moe, layer, spec, T):
+    """x as the prefill rail's quantiser left it in the layer workspace: for every
+    live bucket row, the sum of its six E2M1 terms, decoded from the activation
+    chunks (term-major 8192-byte images of 128 rows, 64-byte swizzle) and the
+    scale atoms of the row's segment."""
+    E, k, D = spec.E, spec.k, spec.D
+    ws = layer.workspace(T, moe.MOE_RAIL_GROUPED_MX4).cpu().numpy()
+    mr = _ru(T * k + E * 127, 128)
+    ntiles, NK, NT = mr // 128, (D + 127) // 128, 6
+    off, parts = 0, {}
+    for name, nbytes in (("logits", T * E * 4), ("ids", T * k * 4), ("w", T * k * 4), ("counts", E * 4),
+                         ("basep", (E + 1) * 4), ("rows", mr * 4), ("inv", T * k * 4),
+                         ("aq", ntiles * NK * NT * 8192), ("asf", ntiles * NK * 2 * NT * 512)):
+        parts[name] = ws[off:off + nbytes]
+        off = _ru(off + nbytes, 256)
+    counts, basep = parts["counts"].view(np.int32), parts["basep"].view(np.int32)
+    rows = parts["rows"].view(np.int32)
+    aq = parts["aq"].reshape(ntiles, NK, NT, 128, 64)
+    asf = parts["asf"].reshape(ntiles, NK, 2, NT, 512)
+    got = {}
+    for b in range(int(basep[E]) // 128):
+        e = int(np.searchsorted(basep, 128 * b, side="right")) - 1
+        live = min(128, int(counts[e]) - (128 * b - int(basep[e])))
+        for rt in range(live):
+            p = 128 * b + rt
+            s = (rt >> 6) if live > 96 else 0
+            nrows = (64 if s == 0 else live - 64) if live > 96 else live
+            rn = _ru(nrows, 16)
+            r = rt - 64 * s
+            m = max([d for d in range(1, NT + 1) if NT % d == 0 and d * rn <= 192])
+            apg = (m * rn + 127) // 128
+            blk = np.arange(D // 32)
+            j, kb = blk // 4, blk % 4
+            col = (16 * (kb ^ ((rt >> 1) & 3)))[:, None] + np.arange(16)[None, :]
+            row = np.zeros((D // 32, 32))
+            for t in range(NT):
+                byts = aq[b, j[:, None], t, rt, col].astype(np.int64)  # [block][16]
+                codes = np.concatenate([byts & 15, byts >> 4], axis=1)  # columns 0..15, then 16..31
+                nn = (t % m) * rn + r
+                ai, n = (t // m) * apg + (nn >> 7), nn & 127
+                sc = asf[b, j, s, ai, 16 * (n & 31) + 4 * (n >> 5) + kb].astype(np.int64)
+                row += O.E2M1_LUT[codes] * np.exp2(sc - 127.0)[:, None]
+            row = row.reshape(D)
+            got[p] = (int(rows[p]), row)
+    return got
+
+
+@pytest.mark.parametrize("key,T,seed", [(0, 37, 21), ("rect", 300, 22), (2, 96, 23)])
+def test_mx4_x_terms_are_exact(moe, key, T, seed):
+    """The quantiser's x operand (six E2M1 terms per value, bucket order, the
+    segment-stacked atoms) equals the oracle's split_e2m1_terms(x, 6) bit for bit
+    on every live bucket row; single-segment and two-segment tiles both occur."""
+    spec, L, layer, _ = packed_layer(moe, key)
+    x = make_tokens(spec, T=T, seed=seed)
+    layer(dev(x), rail=moe.MOE_RAIL_GROUPED_MX4)
+    torch.cuda.synchronize()
+    assert status(moe) == 0
+    got = _read_x_terms(moe, layer, spec, T)
+    ref = O.split_e2m1_terms(x, 6)
+    assert len(got) == T * spec.k
+    for p, (a, row) in got.items():
+        assert a >= 0, p
+        assert np.array_equal(row, ref[a // spec.k]), (p, a)
