@@ -606,16 +606,22 @@ __global__ void __launch_bounds__(256, 3) quant_rows_e2m1_kernel(const float* __
     }
     if (lane == 0) segs[0] = make_int2(total, 0);
   }
-  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
+  // every bucket tile's live rows, once per block
+  extern __shared__ int s_live[];
   const int mpad = basep[E];
+  for (int i = threadIdx.x; i < (mpad >> 7); i += blockDim.x) {
+    int e;
+    s_live[i] = tile_live(basep, counts, E, 128 * i, e);
+  }
+  __syncthreads();
+  const int tid = blockIdx.x * blockDim.x + threadIdx.x;
+  const int nthr = gridDim.x * blockDim.x;
   const int nbp = 4 * NK, nb = C / 32;
-  for (int64_t w = tid; w < (int64_t)mpad * nbp; w += nthr) {
-    const int p = (int)(w / nbp), blk = (int)(w - (int64_t)p * nbp);
+  for (int w = tid; w < mpad * nbp; w += nthr) {
+    const int p = w / nbp, blk = w - p * nbp;
     const int a = rows[p];
     const int b = p >> 7, rt = p & 127, j = blk >> 2, kb = blk & 3;
-    int e;
-    const int live = tile_live(basep, counts, E, 128 * b, e);
+    const int live = s_live[b];
     const int s = live > kSegMax ? (rt >> 6) : 0;
     const Segment g = segment_of(live, s);
     const int r = rt - g.base;
@@ -657,6 +663,8 @@ __global__ void __launch_bounds__(256, 3) quant_rows_e2m1_kernel(const float* __
   }
   if (GATHER) {
     const int64_t n4 = (int64_t)T * C / 4;
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
     float4* y4 = reinterpret_cast<float4*>(y);
     for (int64_t i = tid; i < n4; i += nthr) y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int64_t i = 4 * n4 + tid; i < (int64_t)T * C; i += nthr) y[i] = 0.f;
@@ -674,8 +682,10 @@ size_t prefill_atom_bytes(int max_rows, int C, int terms) {
 }
 
 namespace {
+// Blocks of the row quantiser; 0 when its 32-bit item index would overflow.
 int quant_blocks(int max_rows, int C) {
   const int64_t threads = (int64_t)max_rows * 4 * ((C + 127) / 128);
+  if (threads > 0x7fffffffLL) return 0;
   int64_t blocks = (threads + 255) / 256;
   const int64_t cap = (int64_t)device_sm_count() * 8;
   if (blocks > cap) blocks = cap;
@@ -687,14 +697,18 @@ int quant_blocks(int max_rows, int C) {
 cudaError_t launch_quant_rows_e2m1(const float* x, int T, int D, int k, const int32_t* rows, const int32_t* counts,
                                    const int32_t* basep, int E, int max_rows, uint8_t* aq, uint8_t* asf, float* y,
                                    int2* segs, Launch L) {
-  return launch_kernel(gx4::quant_rows_e2m1_kernel<kPrefillXTerms, true>, dim3(quant_blocks(max_rows, D)), dim3(256), 0,
-                       L, x, T, D, k, rows, counts, basep, E, (D + 127) / 128, aq, asf, y, segs);
+  if (quant_blocks(max_rows, D) == 0) return cudaErrorInvalidValue;
+  return launch_kernel(gx4::quant_rows_e2m1_kernel<kPrefillXTerms, true>, dim3(quant_blocks(max_rows, D)), dim3(256),
+                       (size_t)(max_rows / 128) * sizeof(int), L, x, T, D, k, rows, counts, basep, E, (D + 127) / 128, aq,
+                       asf, y, segs);
 }
 
 cudaError_t launch_quant_h_e2m1(const float* hf, int F, const int32_t* rows, const int32_t* counts,
                                 const int32_t* basep, int E, int max_rows, uint8_t* hq, uint8_t* hsf, Launch L) {
+  if (quant_blocks(max_rows, F) == 0) return cudaErrorInvalidValue;
   return launch_kernel(gx4::quant_rows_e2m1_kernel<kPrefillHTerms, false>, dim3(quant_blocks(max_rows, F)), dim3(256),
-                       0, L, hf, 0, F, 1, rows, counts, basep, E, (F + 127) / 128, hq, hsf, nullptr, nullptr);
+                       (size_t)(max_rows / 128) * sizeof(int), L, hf, 0, F, 1, rows, counts, basep, E, (F + 127) / 128, hq,
+                       hsf, nullptr, nullptr);
 }
 
 cudaError_t launch_grouped_mx4(const GroupedMX4Args& a, Launch L) {
