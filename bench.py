@@ -6,8 +6,10 @@ shaped decode step (E=32 experts, top-4, D=F=2880, MXFP4 weights, T=1), the
 weight GB/s it streams, the dominant kernel's roofline fraction, the same
 metric end to end through the public API with host buffers, and the CPU
 oracle as a baseline. The prefill step (T=512) is measured in the same run
-and reported under "prefill_t512" (bf16 grouped GEMM) and "prefill_t512_mx"
-(block-scaled MXFP4 grouped GEMM).
+and reported under "prefill_t512" (the fastest rail: grouped GEMMs on
+tcgen05.mma kind::mxf4 over prepacked MXFP4 weights), with the bf16 rail
+("prefill_t512_bf16") and the E4M3-term block-scaled rail ("prefill_t512_mx")
+beside it; likewise the skewed T=4096 layer ("skew_t4096", ...).
 
 Timing: CUDA events on the launching stream around exactly --steps steps,
 captured in one CUDA graph, after --warmup eager steps; every step uses the
@@ -326,11 +328,12 @@ def run_ours(args, dist: Dist):
     hbm_peak, bf16_peak, bf16_sus, peak_src = load_peaks()
     stream = torch.cuda.Stream(device=dev)
     if args.skip_decode:
-        return {"prefill_t512": run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src),
+        return {"prefill_t512": run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src,
+                                            rail=moe.MOE_RAIL_GROUPED_MX4),
+                "prefill_t512_bf16": run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src,
+                                                 rail=moe.MOE_RAIL_GROUPED_MM),
                 "prefill_t512_mx": run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src,
-                                               rail=moe.MOE_RAIL_GROUPED_MX),
-                "prefill_t512_mx4": run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src,
-                                                rail=moe.MOE_RAIL_GROUPED_MX4)}
+                                               rail=moe.MOE_RAIL_GROUPED_MX)}
     K, W, NL = args.steps, args.warmup, args.layers
     spec = spec_for(1)
 
@@ -522,14 +525,16 @@ def run_ours(args, dist: Dist):
     torch.cuda.empty_cache()
 
     if not args.no_prefill:
-        result["prefill_t512"] = run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src)
+        result["prefill_t512"] = run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src,
+                                             rail=moe.MOE_RAIL_GROUPED_MX4)
+        result["prefill_t512_bf16"] = run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src,
+                                                  rail=moe.MOE_RAIL_GROUPED_MM)
         result["prefill_t512_mx"] = run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src,
                                                 rail=moe.MOE_RAIL_GROUPED_MX)
-        result["prefill_t512_mx4"] = run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src,
-                                                 rail=moe.MOE_RAIL_GROUPED_MX4)
-        result["skew_t4096"] = run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src, cfg=4)
-        result["skew_t4096_mx4"] = run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src, cfg=4,
-                                               rail=moe.MOE_RAIL_GROUPED_MX4)
+        result["skew_t4096"] = run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src, cfg=4,
+                                           rail=moe.MOE_RAIL_GROUPED_MX4)
+        result["skew_t4096_bf16"] = run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src, cfg=4,
+                                                rail=moe.MOE_RAIL_GROUPED_MM)
         result["skew_t4096_mx"] = run_prefill(args, dist, moe, dev, stream, hbm_peak, bf16_peak, peak_src, cfg=4,
                                               rail=moe.MOE_RAIL_GROUPED_MX)
     if not args.no_stack:
@@ -652,13 +657,14 @@ def run_stack(args, dist, moe, dev, stream, hbm_peak, NLS=24):
     from synthetic import make_layer_torch, spec_for
 
     spec = spec_for(3)
-    layers = [moe.MoeLayer(make_layer_torch(spec, li + 101 * dist.rank, dev), k=K_TOP, device=dev)
+    # canonical planes (the T=1 GEMV rail) and the prepacked copy (the T=512 kind::mxf4 rail)
+    layers = [moe.MoeLayer(make_layer_torch(spec, li + 101 * dist.rank, dev), k=K_TOP, device=dev, packed=True)
               for li in range(NLS)]
     res = {"workload": WORKLOAD_STACK, "layers": NLS,
            "resident_weight_gb": round(NLS * E * EXPERT_BYTES / 1e9, 2)}
     g = torch.Generator(device=dev)
     g.manual_seed(2024 + dist.rank)
-    for T, steps, rail in ((1, args.stack_steps, moe.MOE_RAIL_GEMV), (512, 3, moe.MOE_RAIL_GROUPED_MM)):
+    for T, steps, rail in ((1, args.stack_steps, moe.MOE_RAIL_GEMV), (512, 3, moe.MOE_RAIL_GROUPED_MX4)):
         h = [torch.randn((T, D), generator=g, device=dev), torch.empty((T, D), device=dev)]
 
         def one_pass():
@@ -678,7 +684,7 @@ def run_stack(args, dist, moe, dev, stream, hbm_peak, NLS=24):
         touched = E if T > 8 else K_TOP
         per_pass = secs_max / steps
         res[f"T{T}"] = {"tokens_per_s": round(rate, 2), "ms_per_token_pass" if T == 1 else "ms_per_pass":
-                        round(per_pass * 1e3, 4), "passes": steps, "rail": "gemv" if T == 1 else "grouped_mm",
+                        round(per_pass * 1e3, 4), "passes": steps, "rail": "gemv" if T == 1 else "grouped_mx4",
                         "us_per_layer": round(per_pass / NLS * 1e6, 2),
                         "weight_gbs": round(NLS * touched * EXPERT_BYTES / per_pass / 1e9, 1),
                         "weight_roofline_frac": round(NLS * touched * EXPERT_BYTES / per_pass / 1e9 / hbm_peak, 4),

@@ -208,7 +208,7 @@ size_t layout_packed_workspace(int T, int D, int F, int k, int E, char* base, Pa
 }
 
 int resolve_packed_rail(int T, int rail) {
-  if (rail == MOE_RAIL_AUTO) return T <= MOE_GEMV_MAX_T ? MOE_RAIL_DECODE_MX : MOE_RAIL_GROUPED_MX4;
+  if (rail == MOE_RAIL_AUTO) return T <= MOE_AUTO_DECODE_MX_MAX_T ? MOE_RAIL_DECODE_MX : MOE_RAIL_GROUPED_MX4;
   return rail;
 }
 

@@ -85,14 +85,15 @@ class MoeLayer:
     def _use_packed(self, T: int, rail: int) -> bool:
         # MOE_RAIL_AUTO with both sets of planes takes the rail measured fastest on
         # GB300 at each T: the CUDA-core GEMV rail (canonical) at T = 1, the
-        # block-scaled decode rail (prepacked) for 2 <= T <= MOE_GEMV_MAX_T, the
-        # library's own choice (canonical) beyond. Without the canonical planes the
-        # prepacked rail serves every decode size.
+        # prepacked planes beyond (the library's choice there: the block-scaled
+        # decode rail for T <= MOE_AUTO_DECODE_MX_MAX_T, the kind::mxf4 grouped
+        # rail after it). Without the canonical planes the prepacked planes serve
+        # every T.
         if self.packed is None:
             return False
         if rail in (_lib.MOE_RAIL_DECODE_MX, _lib.MOE_RAIL_GROUPED_MX4):
             return True
-        if rail != _lib.MOE_RAIL_AUTO or T > _lib.MOE_GEMV_MAX_T:
+        if rail != _lib.MOE_RAIL_AUTO:
             return False
         return (self.w["g_qs"] is None and self.w["gu_qs"] is None) or T >= 2
 
