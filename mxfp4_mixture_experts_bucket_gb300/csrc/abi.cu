@@ -866,7 +866,7 @@ int packed_prefill_impl(const moe_packed_layer_t& P, const float* x, int T, void
   if ((rc = cuda_status(launch_bucket(ids, T, P.k, P.E, MOE_MM_TILE, (int)ws.max_rows, ws.counts, ws.basep, ws.rows,
                                       ws.inv, d->status, L))) != MOE_OK)
     return rc;
-  if ((rc = cuda_status(launch_quant_rows_e2m1(x, T, P.D, P.k, ws.rows, ws.counts, ws.basep, P.E, (int)ws.max_rows, ws.aq,
+  if ((rc = cuda_status(launch_quant_rows_e2m1(x, T, P.D, P.k, ws.rows, ws.inv, ws.counts, ws.basep, P.E, (int)ws.max_rows, ws.aq,
                                                ws.asf, y, ws.segs, L))) != MOE_OK)
     return rc;
   GroupedMX4Args g{};

@@ -561,14 +561,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
 }
 
 // ---------------------------------------------------------------------------
-// Bucket rows as NT E2M1 terms, in the activation-chunk layout: one thread per
-// (bucket row, 32-block), which loads the block's 128 bytes, splits it
-// (split_block_e2m1), stores each term's 16 bytes with one store and its scale
-// byte into its segment's atoms. GATHER: the rows are x's token rows (x: the
-// gate/up operand), y[0 .. T*C) is zeroed (the down GEMM accumulates into it)
-// and block 0 writes the segment table; else the rows are src's own bucket rows
-// (h: the down operand). Pad rows up to the segment's rounded end and blocks
-// past C are zero; rows past that end are never read and not written.
+// Bucket rows as NT E2M1 terms, in the activation-chunk layout: each 32-block
+// is loaded (128 bytes), split (split_block_e2m1_term) and each term's 16
+// bytes stored with one store, its scale byte into the segment's atoms.
+// GATHER (x, the gate/up operand): one thread per (token, 32-block) splits the
+// block once and stores it into each of the token's k bucket rows (inv); pad
+// rows up to each segment's rounded end are zeroed; y[0 .. T*C) is zeroed (the
+// down GEMM accumulates into it) and block 0 writes the segment table. Else
+// (h, the down operand): one thread per (bucket row, 32-block) of src's own
+// rows, pad rows zero. Blocks past C are zero; rows past a segment's rounded
+// end are never read and not written.
 // ---------------------------------------------------------------------------
 template <int NT, bool GATHER>
 __global__ void __launch_bounds__(256, 3) quant_rows_e2m1_kernel(const float* __restrict__ src, int T, int C, int k,
@@ -576,7 +578,8 @@ __global__ void __launch_bounds__(256, 3) quant_rows_e2m1_kernel(const float* __
                                                               const int32_t* __restrict__ counts,
                                                               const int32_t* __restrict__ basep, int E, int NK,
                                                               uint8_t* __restrict__ aq, uint8_t* __restrict__ asf,
-                                                              float* __restrict__ y, int2* __restrict__ segs) {
+                                                              float* __restrict__ y, int2* __restrict__ segs,
+                                                              const int32_t* __restrict__ inv) {
   pdl_launch_dependents();
   pdl_wait();
   if (GATHER && blockIdx.x == 0 && threadIdx.x < 32) {
@@ -617,47 +620,106 @@ __global__ void __launch_bounds__(256, 3) quant_rows_e2m1_kernel(const float* __
   const int tid = blockIdx.x * blockDim.x + threadIdx.x;
   const int nthr = gridDim.x * blockDim.x;
   const int nbp = 4 * NK, nb = C / 32;
-  for (int w = tid; w < mpad * nbp; w += nthr) {
-    const int p = w / nbp, blk = w - p * nbp;
-    const int a = rows[p];
-    const int b = p >> 7, rt = p & 127, j = blk >> 2, kb = blk & 3;
-    const int live = s_live[b];
-    const int s = live > kSegMax ? (rt >> 6) : 0;
-    const Segment g = segment_of(live, s);
-    const int r = rt - g.base;
-    if (r >= g.rn) continue;  // rows past the segment's rounded end are never read
-    const int m = slots_of<NT>(g.rn);
-    uint8_t* chunk = aq + ((size_t)b * NK + j) * (NT * kTermBytes);
-    uint8_t* atoms = asf + (((size_t)b * NK + j) * 2 + s) * (NT * kAtom);
-    if (a >= 0 && blk < nb) {
+  if constexpr (GATHER) {
+    // the tokens: each block split once, its terms stored into the token's k bucket rows
+    for (int w = tid; w < T * nbp; w += nthr) {
+      const int t = w / nbp, blk = w - t * nbp, j = blk >> 2, kb = blk & 3;
       float v[32];
-      const float* row = GATHER ? src + (size_t)(a / k) * C : src + (size_t)p * C;
-      const float4* s4 = reinterpret_cast<const float4*>(row + 32 * blk);
+      if (blk < nb) {
+        const float4* s4 = reinterpret_cast<const float4*>(src + (size_t)t * C + 32 * blk);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float4 f = __ldg(s4 + i);
-        v[4 * i] = f.x;
-        v[4 * i + 1] = f.y;
-        v[4 * i + 2] = f.z;
-        v[4 * i + 3] = f.w;
+        for (int i = 0; i < 8; ++i) {
+          const float4 f = __ldg(s4 + i);
+          v[4 * i] = f.x;
+          v[4 * i + 1] = f.y;
+          v[4 * i + 2] = f.z;
+          v[4 * i + 3] = f.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0.f;
       }
 #pragma unroll
-      for (int term = 0; term < NT; ++term) {  // each term stored as soon as it is split
+      for (int term = 0; term < NT; ++term) {
         uint4 packed;
         uint32_t sc;
         mx::split_block_e2m1_term(v, term + 1 == NT, packed, sc);
-        *reinterpret_cast<uint4*>(chunk + act_off(rt, term, kb, 0)) = packed;
-        int n;
-        const int ai = atom_index(term, m, g.rn, r, n);
-        atoms[(size_t)ai * kAtom + dmx::atom_off(n, kb)] = (uint8_t)sc;
+        for (int jj = 0; jj < k; ++jj) {
+          const int p = __ldg(inv + (size_t)t * k + jj);
+          if (p < 0) continue;  // an invalid expert id: the assignment has no bucket row
+          const int b = p >> 7, rt = p & 127;
+          const int live = s_live[b];
+          const int s = live > kSegMax ? (rt >> 6) : 0;
+          const Segment g = segment_of(live, s);
+          const int r = rt - g.base;
+          *reinterpret_cast<uint4*>(aq + ((size_t)b * NK + j) * (NT * kTermBytes) + act_off(rt, term, kb, 0)) = packed;
+          int n;
+          const int ai = atom_index(term, slots_of<NT>(g.rn), g.rn, r, n);
+          asf[(((size_t)b * NK + j) * 2 + s) * (NT * kAtom) + (size_t)ai * kAtom + dmx::atom_off(n, kb)] = (uint8_t)sc;
+        }
       }
-    } else {
+    }
+    // the pad rows of every segment, up to its rounded end: zero terms, scale code 0
+    for (int w = tid; w < (mpad >> 7) * 16 * nbp; w += nthr) {
+      const int b = w / (16 * nbp), rem = w - b * (16 * nbp), pr = rem / nbp, blk = rem - pr * nbp;
+      const int live = s_live[b];
+      const int s = live > kSegMax ? 1 : 0;
+      const Segment g = segment_of(live, s);
+      const int rt = live + pr;
+      if (rt >= g.base + g.rn) continue;
+      const int r = rt - g.base, j = blk >> 2, kb = blk & 3, m = slots_of<NT>(g.rn);
 #pragma unroll
       for (int term = 0; term < NT; ++term) {
-        *reinterpret_cast<uint4*>(chunk + act_off(rt, term, kb, 0)) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(aq + ((size_t)b * NK + j) * (NT * kTermBytes) + act_off(rt, term, kb, 0)) =
+            make_uint4(0u, 0u, 0u, 0u);
         int n;
         const int ai = atom_index(term, m, g.rn, r, n);
-        atoms[(size_t)ai * kAtom + dmx::atom_off(n, kb)] = 0;
+        asf[(((size_t)b * NK + j) * 2 + s) * (NT * kAtom) + (size_t)ai * kAtom + dmx::atom_off(n, kb)] = 0;
+      }
+    }
+  } else {
+    for (int w = tid; w < mpad * nbp; w += nthr) {
+      const int p = w / nbp, blk = w - p * nbp;
+      const int a = rows[p];
+      const int b = p >> 7, rt = p & 127, j = blk >> 2, kb = blk & 3;
+      const int live = s_live[b];
+      const int s = live > kSegMax ? (rt >> 6) : 0;
+      const Segment g = segment_of(live, s);
+      const int r = rt - g.base;
+      if (r >= g.rn) continue;  // rows past the segment's rounded end are never read
+      const int m = slots_of<NT>(g.rn);
+      uint8_t* chunk = aq + ((size_t)b * NK + j) * (NT * kTermBytes);
+      uint8_t* atoms = asf + (((size_t)b * NK + j) * 2 + s) * (NT * kAtom);
+      if (a >= 0 && blk < nb) {
+        float v[32];
+        const float* row = GATHER ? src + (size_t)(a / k) * C : src + (size_t)p * C;
+        const float4* s4 = reinterpret_cast<const float4*>(row + 32 * blk);
+  #pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 f = __ldg(s4 + i);
+          v[4 * i] = f.x;
+          v[4 * i + 1] = f.y;
+          v[4 * i + 2] = f.z;
+          v[4 * i + 3] = f.w;
+        }
+  #pragma unroll
+        for (int term = 0; term < NT; ++term) {  // each term stored as soon as it is split
+          uint4 packed;
+          uint32_t sc;
+          mx::split_block_e2m1_term(v, term + 1 == NT, packed, sc);
+          *reinterpret_cast<uint4*>(chunk + act_off(rt, term, kb, 0)) = packed;
+          int n;
+          const int ai = atom_index(term, m, g.rn, r, n);
+          atoms[(size_t)ai * kAtom + dmx::atom_off(n, kb)] = (uint8_t)sc;
+        }
+      } else {
+  #pragma unroll
+        for (int term = 0; term < NT; ++term) {
+          *reinterpret_cast<uint4*>(chunk + act_off(rt, term, kb, 0)) = make_uint4(0u, 0u, 0u, 0u);
+          int n;
+          const int ai = atom_index(term, m, g.rn, r, n);
+          atoms[(size_t)ai * kAtom + dmx::atom_off(n, kb)] = 0;
+        }
       }
     }
   }
@@ -694,13 +756,13 @@ int quant_blocks(int max_rows, int C) {
 }
 }  // namespace
 
-cudaError_t launch_quant_rows_e2m1(const float* x, int T, int D, int k, const int32_t* rows, const int32_t* counts,
-                                   const int32_t* basep, int E, int max_rows, uint8_t* aq, uint8_t* asf, float* y,
-                                   int2* segs, Launch L) {
+cudaError_t launch_quant_rows_e2m1(const float* x, int T, int D, int k, const int32_t* rows, const int32_t* inv,
+                                   const int32_t* counts, const int32_t* basep, int E, int max_rows, uint8_t* aq,
+                                   uint8_t* asf, float* y, int2* segs, Launch L) {
   if (quant_blocks(max_rows, D) == 0) return cudaErrorInvalidValue;
   return launch_kernel(gx4::quant_rows_e2m1_kernel<kPrefillXTerms, true>, dim3(quant_blocks(max_rows, D)), dim3(256),
                        (size_t)(max_rows / 128) * sizeof(int), L, x, T, D, k, rows, counts, basep, E, (D + 127) / 128, aq,
-                       asf, y, segs);
+                       asf, y, segs, inv);
 }
 
 cudaError_t launch_quant_h_e2m1(const float* hf, int F, const int32_t* rows, const int32_t* counts,
@@ -708,7 +770,7 @@ cudaError_t launch_quant_h_e2m1(const float* hf, int F, const int32_t* rows, con
   if (quant_blocks(max_rows, F) == 0) return cudaErrorInvalidValue;
   return launch_kernel(gx4::quant_rows_e2m1_kernel<kPrefillHTerms, false>, dim3(quant_blocks(max_rows, F)), dim3(256),
                        (size_t)(max_rows / 128) * sizeof(int), L, hf, 0, F, 1, rows, counts, basep, E, (F + 127) / 128, hq,
-                       hsf, nullptr, nullptr);
+                       hsf, nullptr, nullptr, nullptr);
 }
 
 cudaError_t launch_grouped_mx4(const GroupedMX4Args& a, Launch L) {
