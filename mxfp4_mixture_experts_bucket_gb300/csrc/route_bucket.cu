@@ -577,11 +577,11 @@ cudaError_t launch_decode_prologue(const float* x, int T, int D, const float* wr
 }
 
 namespace {
-// Slices of D for the split router: about four blocks per SM, slices a
+// Slices of D for the split router: about eight blocks per SM, slices a
 // multiple of 32 wide, at most kRouterMaxSplits of them.
 void router_split(int T, int D, int E, int& S, int& ks) {
   const int tiles = ((T + kRsT - 1) / kRsT) * ((E + kRsE - 1) / kRsE);
-  int s = (4 * device_sm_count() + tiles - 1) / tiles;
+  int s = (8 * device_sm_count() + tiles - 1) / tiles;
   s = std::max(1, std::min(s, std::min(kRouterMaxSplits, D / 32)));
   ks = ((D + s - 1) / s + 31) / 32 * 32;
   S = (D + ks - 1) / ks;
