@@ -225,6 +225,7 @@ struct PackedPrefillWorkspace {
   uint8_t* asf;
   float* rpart;  // the split router's partial dots
   int2* segs;    // segment table of the bucket
+  int* ctr;      // the two GEMMs' unit counters
   float* hf;     // h as float rows, written by the gate/up GEMM
   uint8_t* hq;   // h terms
   uint8_t* hsf;
@@ -253,6 +254,7 @@ size_t layout_packed_prefill_workspace(int T, int D, int F, int k, int E, char* 
   w.asf = reinterpret_cast<uint8_t*>(take(prefill_atom_bytes((int)mr, D, kPrefillXTerms)));
   w.rpart = reinterpret_cast<float*>(take(router_partials_bytes(T, E)));
   w.segs = reinterpret_cast<int2*>(take((2 * (mr / 128) + 1) * sizeof(int2)));
+  w.ctr = reinterpret_cast<int*>(take(2 * sizeof(int)));
   w.hf = reinterpret_cast<float*>(take(mr * (size_t)F * 4));
   w.hq = reinterpret_cast<uint8_t*>(take(prefill_operand_bytes((int)mr, F, kPrefillHTerms)));
   w.hsf = reinterpret_cast<uint8_t*>(take(prefill_atom_bytes((int)mr, F, kPrefillHTerms)));
@@ -867,7 +869,7 @@ int packed_prefill_impl(const moe_packed_layer_t& P, const float* x, int T, void
                                       ws.inv, d->status, L))) != MOE_OK)
     return rc;
   if ((rc = cuda_status(launch_quant_rows_e2m1(x, T, P.D, P.k, ws.rows, ws.inv, ws.counts, ws.basep, P.E, (int)ws.max_rows, ws.aq,
-                                               ws.asf, y, ws.segs, L))) != MOE_OK)
+                                               ws.asf, y, ws.segs, ws.ctr, L))) != MOE_OK)
     return rc;
   GroupedMX4Args g{};
   g.kind = 0;
@@ -884,6 +886,7 @@ int packed_prefill_impl(const moe_packed_layer_t& P, const float* x, int T, void
   g.basep = ws.basep;
   g.rows = ws.rows;
   g.segs = ws.segs;
+  g.ctr = ws.ctr;
   g.max_rows = (int)ws.max_rows;
   g.k = P.k;
   g.weights = wts;
@@ -905,6 +908,7 @@ int packed_prefill_impl(const moe_packed_layer_t& P, const float* x, int T, void
   if ((rc = cuda_status(launch_quant_h_e2m1(ws.hf, P.F, ws.rows, ws.counts, ws.basep, P.E, (int)ws.max_rows, ws.hq,
                                             ws.hsf, L))) != MOE_OK)
     return rc;
+  gd.ctr = ws.ctr + 1;
   gd.aq = ws.hq;
   gd.asf = ws.hsf;
   gd.hf = nullptr;

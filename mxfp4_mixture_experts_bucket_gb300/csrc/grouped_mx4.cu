@@ -102,6 +102,7 @@ struct Params {
   const int32_t* basep;
   const int32_t* rows;
   const int2* segs;    // the segment table: segs[0].x = count; segs[1 + i] = ((b << 1) | s, (e << 8) | live)
+  int* ctr;            // units handed out so far (zeroed by the x quantiser)
   int k;
   const float* weights;
   const uint8_t* aq;   // activation chunks [ntiles][NK][terms][8192]
@@ -190,22 +191,23 @@ struct Unit {
   Segment g;
 };
 
-// The next unit of this CTA, or false when there is none: unit i is segment
-// i / npair of the segment table (every segment of every live bucket tile, in
-// bucket order) and weight tile pair i % npair; the CTAs take units
-// blockIdx.x, blockIdx.x + gridDim.x, ...
-__device__ __forceinline__ bool next_unit(const Params& p, int nseg, int& cursor, Unit& u) {
-  if (cursor >= nseg * p.npair) return false;
-  const int si = cursor / p.npair;
+// Unit v: segment v / npair of the segment table (every segment of every live
+// bucket tile, in bucket order) and weight tile pair v % npair.
+__device__ __forceinline__ void decode_unit(const Params& p, int v, Unit& u) {
+  const int si = v / p.npair;
   const int2 sg = __ldg(p.segs + 1 + si);
   u.b = sg.x >> 1;
   u.s = sg.x & 1;
-  u.t = cursor - si * p.npair;
+  u.t = v - si * p.npair;
   u.e = sg.y >> 8;
   u.g = segment_of(sg.y & 255, u.s);
-  cursor += gridDim.x;
-  return true;
 }
+
+// Units are handed out dynamically: the activation copy issuer of each CTA takes
+// the next index from a global counter and publishes it in a small ring in
+// shared memory; every other role reads the CTA's units from the ring in order.
+constexpr int kUnitRing = 4;
+constexpr int kUnitReaders = 1 + 4 + 1 + kEpiWarps;  // weight copies, scale loaders, MMA thread, epilogue warps
 
 // 16 columns from column c0 of the accumulator at `acc` (this warp's lanes),
 // summed over its m term slots (slot j at column j * rn + c0).
@@ -248,6 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
   __shared__ __align__(8) uint64_t accf_bar, acce_bar, drain_bar, tfree_bar;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ int s_unit[kUnitRing];
+  __shared__ __align__(8) uint64_t ufull_bar[kUnitRing], uempty_bar[kUnitRing];
   __shared__ float s_bias[256];  // the unit's biases (gate/up: 128 gate, 128 up; down: 256)
   __shared__ int s_tok[KIND == 1 ? kSegMax : 1];    // down: each segment row's token (-1: none)
   __shared__ float s_w[KIND == 1 ? kSegMax : 1];    // and its router weight
@@ -262,6 +266,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
     tc::mbar_init(tc::smem_u32(&accf_bar), 1);
     tc::mbar_init(tc::smem_u32(&acce_bar), kEpiWarps);
     tc::mbar_init(tc::smem_u32(&drain_bar), 1);
+    for (int i = 0; i < kUnitRing; ++i) {
+      tc::mbar_init(tc::smem_u32(&ufull_bar[i]), 1);
+      tc::mbar_init(tc::smem_u32(&uempty_bar[i]), kUnitReaders);
+    }
     tc::mbar_init(tc::smem_u32(&tfree_bar), 5 + kEpiWarps);  // 4 scale-loading producers, the MMA thread, the epilogue warps
     s_abort = 0;
     tc::fence_mbar_init();
@@ -281,6 +289,37 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
     report_timeout(p.status, 7 + KIND, role, 0, seq);
   };
   const int nbc = p.C / 32;
+  const int nunits = nseg * p.npair;
+  // the issuer publishes the CTA's unit n (the counter's next index, -1 once they are all
+  // handed out); returns it, or -2 if the wait for the ring slot gave up
+  auto publish = [&](int n) -> int {
+    const int slot = n % kUnitRing;
+    if (n >= kUnitRing &&
+        !tc::mbar_wait_sleep(tc::smem_u32(&uempty_bar[slot]), (n / kUnitRing - 1) & 1, abort_flag, 32))
+      return -2;
+    int v = atomicAdd(p.ctr, 1);
+    if (v >= nunits) v = -1;
+    *reinterpret_cast<volatile int*>(&s_unit[slot]) = v;
+    tc::mbar_arrive(tc::smem_u32(&ufull_bar[slot]));
+    return v;
+  };
+  // a reader takes the CTA's unit n (one lane, or every lane of a warp); false at the end
+  // of the units or if the wait gave up (then *abort_flag is set)
+  auto take = [&](int n, Unit& u, bool warp_wide, int role) -> bool {
+    const int slot = n % kUnitRing;
+    bool okw = tc::mbar_wait_sleep(tc::smem_u32(&ufull_bar[slot]), (n / kUnitRing) & 1, abort_flag, 32);
+    if (warp_wide) okw = __all_sync(0xffffffffu, okw);
+    if (!okw) {
+      if (!warp_wide || lane == 0) fail(role, n);
+      return false;
+    }
+    const int v = *reinterpret_cast<volatile int*>(&s_unit[slot]);
+    if (warp_wide) __syncwarp();
+    if (!warp_wide || lane == 0) tc::mbar_arrive(tc::smem_u32(&uempty_bar[slot]));
+    if (v < 0) return false;
+    decode_unit(p, v, u);
+    return true;
+  };
   // weight tile h of unit u's pair (gate/up: matrix h of tile t; down: tile 2t + h), or -1
   auto wtile = [&](const Unit& u, int h) { return KIND == 0 ? u.t : (2 * u.t + h < p.NT ? 2 * u.t + h : -1); };
 
@@ -290,10 +329,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
     // warp's lane quarter (tcgen05.st) and the MMA thread is signalled. They never hold up
     // the copies, which run up to kStages steps ahead.
     const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
-    int cursor = blockIdx.x, i = 0;
+    int un = 0, i = 0;
     Unit u;
     bool ok = true;
-    while (ok && next_unit(p, nseg, cursor, u)) {
+    while (ok && take(un++, u, true, 4)) {
       const int na = used_atoms<kTerms>(u.g.rn);
       for (int j = 0; j < NK; ++j, ++i) {
         const int st = i % kStages, n = i / kStages;
@@ -330,10 +369,18 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
     // tiles and their atoms
     if (lane == 0) {
       uint64_t pol = tc::l2_policy_evict_first();
-      int cursor = blockIdx.x, i = 0, issued = 0;
+      int un = 0, i = 0, issued = 0;
       Unit u;
       bool ok = true;
-      while (ok && next_unit(p, nseg, cursor, u)) {
+      while (ok) {
+        if (warp == 4) {  // the scheduler
+          const int v = publish(un++);
+          if (v == -2) fail(5, un - 1);
+          if (v < 0) break;
+          decode_unit(p, v, u);
+        } else if (!take(un++, u, false, 5)) {
+          break;
+        }
         const uint32_t run = (uint32_t)u.g.rn * 64;  // one term's rows of the segment
         for (int j = 0; j < NK; ++j, ++i) {
           const int st = i % kStages, n = i / kStages;
@@ -386,10 +433,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int cursor = blockIdx.x, i = 0, lu = 0;
+      int i = 0, lu = 0;
       Unit u;
       bool ok = true;
-      while (ok && next_unit(p, nseg, cursor, u)) {
+      while (ok && take(lu, u, false, 1)) {
         if (lu > 0 && !tc::mbar_wait_sleep(tc::smem_u32(&acce_bar), (lu - 1) & 1, abort_flag, 32)) {
           fail(1, i);
           break;
@@ -442,10 +489,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
     const int hh = (warp - kEpiWarp0) >> 2;  // gate/up: which row chunks; down: which tile of the pair
     const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
     const int et = threadIdx.x - kEpiWarp0 * 32;  // 0..255
-    int cur_epi = blockIdx.x;
     Unit ue{};
     int ldone = 0;  // units whose epilogue has run
-    bool have_e = next_unit(p, nseg, cur_epi, ue);
+    bool have_e = take(0, ue, true, 2);
     while (have_e) {
       // ---- the epilogue of unit ldone (ue)
       const int e = ue.e;
@@ -543,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
         }
       }
       ++ldone;
-      have_e = next_unit(p, nseg, cur_epi, ue);
+      have_e = take(ldone, ue, true, 2);
     }
     tc::fence_before_sync();
     __syncwarp();
@@ -579,9 +625,13 @@ __global__ void __launch_bounds__(256, 3) quant_rows_e2m1_kernel(const float* __
                                                               const int32_t* __restrict__ basep, int E, int NK,
                                                               uint8_t* __restrict__ aq, uint8_t* __restrict__ asf,
                                                               float* __restrict__ y, int2* __restrict__ segs,
-                                                              const int32_t* __restrict__ inv) {
+                                                              const int32_t* __restrict__ inv, int* __restrict__ ctr) {
   pdl_launch_dependents();
   pdl_wait();
+  if (GATHER && blockIdx.x == 0 && threadIdx.x == 32) {  // the GEMMs' unit counters
+    ctr[0] = 0;
+    ctr[1] = 0;
+  }
   if (GATHER && blockIdx.x == 0 && threadIdx.x < 32) {
     // the segment table: one lane per expert, a warp prefix over the experts' segment counts
     const int lane = threadIdx.x;
@@ -758,11 +808,11 @@ int quant_blocks(int max_rows, int C) {
 
 cudaError_t launch_quant_rows_e2m1(const float* x, int T, int D, int k, const int32_t* rows, const int32_t* inv,
                                    const int32_t* counts, const int32_t* basep, int E, int max_rows, uint8_t* aq,
-                                   uint8_t* asf, float* y, int2* segs, Launch L) {
+                                   uint8_t* asf, float* y, int2* segs, int* ctr, Launch L) {
   if (quant_blocks(max_rows, D) == 0) return cudaErrorInvalidValue;
   return launch_kernel(gx4::quant_rows_e2m1_kernel<kPrefillXTerms, true>, dim3(quant_blocks(max_rows, D)), dim3(256),
                        (size_t)(max_rows / 128) * sizeof(int), L, x, T, D, k, rows, counts, basep, E, (D + 127) / 128, aq,
-                       asf, y, segs, inv);
+                       asf, y, segs, inv, ctr);
 }
 
 cudaError_t launch_quant_h_e2m1(const float* hf, int F, const int32_t* rows, const int32_t* counts,
@@ -770,7 +820,7 @@ cudaError_t launch_quant_h_e2m1(const float* hf, int F, const int32_t* rows, con
   if (quant_blocks(max_rows, F) == 0) return cudaErrorInvalidValue;
   return launch_kernel(gx4::quant_rows_e2m1_kernel<kPrefillHTerms, false>, dim3(quant_blocks(max_rows, F)), dim3(256),
                        (size_t)(max_rows / 128) * sizeof(int), L, hf, 0, F, 1, rows, counts, basep, E, (F + 127) / 128, hq,
-                       hsf, nullptr, nullptr, nullptr);
+                       hsf, nullptr, nullptr, nullptr, nullptr);
 }
 
 cudaError_t launch_grouped_mx4(const GroupedMX4Args& a, Launch L) {
@@ -795,6 +845,7 @@ cudaError_t launch_grouped_mx4(const GroupedMX4Args& a, Launch L) {
   prm.basep = a.basep;
   prm.rows = a.rows;
   prm.segs = a.segs;
+  prm.ctr = a.ctr;
   prm.k = a.k;
   prm.weights = a.weights;
   prm.aq = a.aq;

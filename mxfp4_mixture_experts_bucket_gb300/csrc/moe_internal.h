@@ -166,6 +166,7 @@ struct GroupedMX4Args {
   const int32_t* basep;
   const int32_t* rows;
   const int2* segs;         // segment table written by launch_quant_rows_e2m1 (2 * max_rows / 128 + 1 entries)
+  int* ctr;                 // this GEMM's unit counter (zeroed by launch_quant_rows_e2m1)
   int max_rows, k;
   const float* weights;     // router weights [T*k] (down)
   const uint8_t* aq;        // activation chunks [max_rows/128][ceil(C/128)][terms][8192] (x: 6 terms, h: 4)
@@ -179,10 +180,11 @@ size_t prefill_operand_bytes(int max_rows, int C, int terms);
 size_t prefill_atom_bytes(int max_rows, int C, int terms);
 // x's token rows in bucket order as kPrefillXTerms E2M1 terms (each token split once, stored into
 // its k bucket rows via inv), y zeroed, and
-// the segment table of the bucket (segs: 2 * max_rows / 128 + 1 entries)
+// the segment table of the bucket (segs: 2 * max_rows / 128 + 1 entries); ctr[0..1] (the GEMMs'
+// unit counters) zeroed
 cudaError_t launch_quant_rows_e2m1(const float* x, int T, int D, int k, const int32_t* rows, const int32_t* inv,
                                    const int32_t* counts, const int32_t* basep, int E, int max_rows, uint8_t* aq,
-                                   uint8_t* asf, float* y, int2* segs, Launch L);
+                                   uint8_t* asf, float* y, int2* segs, int* ctr, Launch L);
 // h's bucket rows (float [max_rows][F]) as kPrefillHTerms E2M1 terms
 cudaError_t launch_quant_h_e2m1(const float* hf, int F, const int32_t* rows, const int32_t* counts,
                                 const int32_t* basep, int E, int max_rows, uint8_t* hq, uint8_t* hsf, Launch L);
