@@ -570,20 +570,23 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(tc::smem_u32(&acce_bar));
         } else {
-#pragma unroll 1
-          for (int c = 0; c < nch; ++c) {
-            float v[16];
-            slot_sum16(acc, 16 * c, g.rn, m, v);
-            if (c == nch - 1) {
-              tc::fence_before_sync();
-              __syncwarp();
-              if (lane == 0) tc::mbar_arrive(tc::smem_u32(&acce_bar));
-            }
+          // every chunk is read out before the accumulator goes back, so the next
+          // unit's MMAs need not wait for this unit's scatter
+          float v[kSegMax / 16][16];
+#pragma unroll
+          for (int c = 0; c < kSegMax / 16; ++c)
+            if (c < nch) slot_sum16(acc, 16 * c, g.rn, m, v[c]);
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(tc::smem_u32(&acce_bar));
+#pragma unroll
+          for (int c = 0; c < kSegMax / 16; ++c) {
+            if (c >= nch) break;
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
               const int r = 16 * c + k;
               const int tok = r < g.rows ? s_tok[r] : -1;
-              if (dvalid && tok >= 0) atomicAdd(p.y + (size_t)tok * D + d, s_w[r] * (v[k] + bd));
+              if (dvalid && tok >= 0) atomicAdd(p.y + (size_t)tok * D + d, s_w[r] * (v[c][k] + bd));
             }
           }
         }
