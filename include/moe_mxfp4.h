@@ -573,9 +573,8 @@ int moe_ffn_layer_packed_hostio(const moe_packed_layer_t* layer, int T, int rail
  * rejected with MOE_ESCRATCH before anything is enqueued (T = 8, k = 4,
  * D = F = 2880 needs about 370 KB; T = 8, k = 8 at that width does not fit).
  * The first call on each device looks up the array's device address (with
- * that device current) and keeps it for the life of the process; make that
- * first call before any stream capture, and do not use the library across
- * cudaDeviceReset. All calls on a device share the array and it keeps the last
+ * that device current) and keeps it for the life of the process; do not use
+ * the library across cudaDeviceReset. All calls on a device share the array and it keeps the last
  * call's contents; nothing in it needs to start at zero (every byte a call
  * reads it first writes). Calls whose executions overlap on the GPU (different
  * streams, or concurrent host threads) race on the array: serialise them.

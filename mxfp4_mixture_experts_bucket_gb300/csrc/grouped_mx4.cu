@@ -126,11 +126,6 @@ __device__ __forceinline__ void mma_mxf4(uint32_t tmem_d, uint64_t adesc, uint64
       : "memory");
 }
 
-// Byte offset of (row n, term t, block kb, byte i) in one activation chunk.
-__host__ __device__ __forceinline__ size_t act_off(int n, int t, int kb, int i) {
-  return (size_t)t * kTermBytes + dmx::chunk_off(n, kb, i);
-}
-
 // Segments of a bucket tile with `live` rows: segment s's first row, row
 // count, and rows rounded up to 16 (0 rows: no such segment).
 struct Segment {
@@ -155,6 +150,7 @@ __host__ __device__ __forceinline__ int slots_of(int rn) {
 }
 // Scale atoms per term group (one per 128 B rows of the group's MMA).
 __host__ __device__ __forceinline__ int atoms_per_group(int m, int rn) { return (m * rn + 127) >> 7; }
+
 // Atom (within the segment's run) and atom row of the scales of term t,
 // segment row r: B row n = (t % m) * rn + r of group t / m. At most `terms`
 // atoms: a group of m >= 2 terms takes at most 2 (m * rn <= 192), a single
@@ -171,18 +167,6 @@ template <int TERMS>
 __host__ __device__ __forceinline__ int used_atoms(int rn) {
   const int m = slots_of<TERMS>(rn);
   return (TERMS / m) * atoms_per_group(m, rn);
-}
-
-// Live rows of the bucket tile starting at row0 (< basep[E]) and its expert.
-__device__ __forceinline__ int tile_live(const int32_t* __restrict__ basep, const int32_t* __restrict__ counts, int E,
-                                         int row0, int& e) {
-  int lo = 0, hi = E - 1;  // basep[e] <= row0 < basep[e + 1]
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(basep + mid) <= row0) lo = mid; else hi = mid - 1;
-  }
-  e = lo;
-  return min(128, __ldg(counts + lo) - (row0 - __ldg(basep + lo)));
 }
 
 // A work unit: bucket tile b (expert e), segment s, weight tile pair t.
@@ -621,6 +605,27 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
 // rows, pad rows zero. Blocks past C are zero; rows past a segment's rounded
 // end are never read and not written.
 // ---------------------------------------------------------------------------
+// Stores a row's NT terms of one 32-block: the codes at `row` (the row's 16
+// bytes of block kb in term 0's image; term t sits t * kTermBytes further) and
+// the scale codes into the segment's atoms (segment of rn rows, segment row r;
+// atom_index's placement, the term groups walked in order instead of divided).
+template <int NT>
+__device__ __forceinline__ void store_terms(uint8_t* row, uint8_t* atoms, int rn, int r, int kb,
+                                            const uint4 (&packed)[NT], const uint32_t (&sc)[NT]) {
+  const int m = slots_of<NT>(rn), apg = atoms_per_group(m, rn);
+  int slot = 0, grp = 0;
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    *reinterpret_cast<uint4*>(row + (size_t)t * kTermBytes) = packed[t];
+    const int nn = slot * rn + r;  // B row of the group's MMA
+    atoms[(size_t)(grp * apg + (nn >> 7)) * kAtom + dmx::atom_off(nn & 127, kb)] = (uint8_t)sc[t];
+    if (++slot == m) {
+      slot = 0;
+      ++grp;
+    }
+  }
+}
+
 template <int NT, bool GATHER>
 __global__ void __launch_bounds__(256, 3) quant_rows_e2m1_kernel(const float* __restrict__ src, int T, int C, int k,
                                                               const int32_t* __restrict__ rows,
@@ -662,17 +667,25 @@ __global__ void __launch_bounds__(256, 3) quant_rows_e2m1_kernel(const float* __
     }
     if (lane == 0) segs[0] = make_int2(total, 0);
   }
-  // every bucket tile's live rows, once per block
+  // every bucket tile's live rows, once per block: each expert's tiles follow
+  // one another from its padded base
   extern __shared__ int s_live[];
   const int mpad = basep[E];
-  for (int i = threadIdx.x; i < (mpad >> 7); i += blockDim.x) {
-    int e;
-    s_live[i] = tile_live(basep, counts, E, 128 * i, e);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int cnt = counts[e], b0 = basep[e] >> 7;
+    for (int i = 0; 128 * i < cnt; ++i) s_live[b0 + i] = min(128, cnt - 128 * i);
   }
   __syncthreads();
   const int tid = blockIdx.x * blockDim.x + threadIdx.x;
   const int nthr = gridDim.x * blockDim.x;
   const int nbp = 4 * NK, nb = C / 32;
+  uint4 zq[NT];  // a zero row: every code 0, every scale code 0
+  uint32_t zs[NT];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    zq[t] = make_uint4(0u, 0u, 0u, 0u);
+    zs[t] = 0u;
+  }
   if constexpr (GATHER) {
     // the tokens: each block split once, its terms stored into the token's k bucket rows
     for (int w = tid; w < T * nbp; w += nthr) {
@@ -692,24 +705,19 @@ __global__ void __launch_bounds__(256, 3) quant_rows_e2m1_kernel(const float* __
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = 0.f;
       }
+      uint4 packed[NT];
+      uint32_t sc[NT];
 #pragma unroll
-      for (int term = 0; term < NT; ++term) {
-        uint4 packed;
-        uint32_t sc;
-        mx::split_block_e2m1_term(v, term + 1 == NT, packed, sc);
-        for (int jj = 0; jj < k; ++jj) {
-          const int p = __ldg(inv + (size_t)t * k + jj);
-          if (p < 0) continue;  // an invalid expert id: the assignment has no bucket row
-          const int b = p >> 7, rt = p & 127;
-          const int live = s_live[b];
-          const int s = live > kSegMax ? (rt >> 6) : 0;
-          const Segment g = segment_of(live, s);
-          const int r = rt - g.base;
-          *reinterpret_cast<uint4*>(aq + ((size_t)b * NK + j) * (NT * kTermBytes) + act_off(rt, term, kb, 0)) = packed;
-          int n;
-          const int ai = atom_index(term, slots_of<NT>(g.rn), g.rn, r, n);
-          asf[(((size_t)b * NK + j) * 2 + s) * (NT * kAtom) + (size_t)ai * kAtom + dmx::atom_off(n, kb)] = (uint8_t)sc;
-        }
+      for (int term = 0; term < NT; ++term) mx::split_block_e2m1_term(v, term + 1 == NT, packed[term], sc[term]);
+      for (int jj = 0; jj < k; ++jj) {
+        const int p = __ldg(inv + (size_t)t * k + jj);
+        if (p < 0) continue;  // an invalid expert id: the assignment has no bucket row
+        const int b = p >> 7, rt = p & 127;
+        const int live = s_live[b];
+        const int s = live > kSegMax ? (rt >> 6) : 0;
+        const Segment g = segment_of(live, s);
+        store_terms<NT>(aq + ((size_t)b * NK + j) * (NT * kTermBytes) + dmx::chunk_off(rt, kb, 0),
+                        asf + (((size_t)b * NK + j) * 2 + s) * (NT * kAtom), g.rn, rt - g.base, kb, packed, sc);
       }
     }
     // the pad rows of every segment, up to its rounded end: zero terms, scale code 0
@@ -720,15 +728,9 @@ __global__ void __launch_bounds__(256, 3) quant_rows_e2m1_kernel(const float* __
       const Segment g = segment_of(live, s);
       const int rt = live + pr;
       if (rt >= g.base + g.rn) continue;
-      const int r = rt - g.base, j = blk >> 2, kb = blk & 3, m = slots_of<NT>(g.rn);
-#pragma unroll
-      for (int term = 0; term < NT; ++term) {
-        *reinterpret_cast<uint4*>(aq + ((size_t)b * NK + j) * (NT * kTermBytes) + act_off(rt, term, kb, 0)) =
-            make_uint4(0u, 0u, 0u, 0u);
-        int n;
-        const int ai = atom_index(term, m, g.rn, r, n);
-        asf[(((size_t)b * NK + j) * 2 + s) * (NT * kAtom) + (size_t)ai * kAtom + dmx::atom_off(n, kb)] = 0;
-      }
+      const int j = blk >> 2, kb = blk & 3;
+      store_terms<NT>(aq + ((size_t)b * NK + j) * (NT * kTermBytes) + dmx::chunk_off(rt, kb, 0),
+                      asf + (((size_t)b * NK + j) * 2 + s) * (NT * kAtom), g.rn, rt - g.base, kb, zq, zs);
     }
   } else {
     for (int w = tid; w < mpad * nbp; w += nthr) {
@@ -760,7 +762,7 @@ __global__ void __launch_bounds__(256, 3) quant_rows_e2m1_kernel(const float* __
           uint4 packed;
           uint32_t sc;
           mx::split_block_e2m1_term(v, term + 1 == NT, packed, sc);
-          *reinterpret_cast<uint4*>(chunk + act_off(rt, term, kb, 0)) = packed;
+          *reinterpret_cast<uint4*>(chunk + (size_t)term * kTermBytes + dmx::chunk_off(rt, kb, 0)) = packed;
           int n;
           const int ai = atom_index(term, m, g.rn, r, n);
           atoms[(size_t)ai * kAtom + dmx::atom_off(n, kb)] = (uint8_t)sc;
@@ -768,7 +770,7 @@ __global__ void __launch_bounds__(256, 3) quant_rows_e2m1_kernel(const float* __
       } else {
   #pragma unroll
         for (int term = 0; term < NT; ++term) {
-          *reinterpret_cast<uint4*>(chunk + act_off(rt, term, kb, 0)) = make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(chunk + (size_t)term * kTermBytes + dmx::chunk_off(rt, kb, 0)) = make_uint4(0u, 0u, 0u, 0u);
           int n;
           const int ai = atom_index(term, m, g.rn, r, n);
           atoms[(size_t)ai * kAtom + dmx::atom_off(n, kb)] = 0;
@@ -798,6 +800,9 @@ size_t prefill_atom_bytes(int max_rows, int C, int terms) {
 
 namespace {
 // Blocks of the row quantiser; 0 when its 32-bit item index would overflow.
+// Blocks for the row quantisers: one thread per item of the h operand, at
+// most eight blocks per SM (about three are resident; later waves hide the
+// per-item load and split latency better than longer grid-stride loops).
 int quant_blocks(int max_rows, int C) {
   const int64_t threads = (int64_t)max_rows * 4 * ((C + 127) / 128);
   if (threads > 0x7fffffffLL) return 0;
@@ -812,16 +817,20 @@ int quant_blocks(int max_rows, int C) {
 cudaError_t launch_quant_rows_e2m1(const float* x, int T, int D, int k, const int32_t* rows, const int32_t* inv,
                                    const int32_t* counts, const int32_t* basep, int E, int max_rows, uint8_t* aq,
                                    uint8_t* asf, float* y, int2* segs, int* ctr, Launch L) {
-  if (quant_blocks(max_rows, D) == 0) return cudaErrorInvalidValue;
-  return launch_kernel(gx4::quant_rows_e2m1_kernel<kPrefillXTerms, true>, dim3(quant_blocks(max_rows, D)), dim3(256),
+  const auto kern = gx4::quant_rows_e2m1_kernel<kPrefillXTerms, true>;
+  const int blocks = quant_blocks(max_rows, D);
+  if (blocks == 0) return cudaErrorInvalidValue;
+  return launch_kernel(kern, dim3(blocks), dim3(256),
                        (size_t)(max_rows / 128) * sizeof(int), L, x, T, D, k, rows, counts, basep, E, (D + 127) / 128, aq,
                        asf, y, segs, inv, ctr);
 }
 
 cudaError_t launch_quant_h_e2m1(const float* hf, int F, const int32_t* rows, const int32_t* counts,
                                 const int32_t* basep, int E, int max_rows, uint8_t* hq, uint8_t* hsf, Launch L) {
-  if (quant_blocks(max_rows, F) == 0) return cudaErrorInvalidValue;
-  return launch_kernel(gx4::quant_rows_e2m1_kernel<kPrefillHTerms, false>, dim3(quant_blocks(max_rows, F)), dim3(256),
+  const auto kern = gx4::quant_rows_e2m1_kernel<kPrefillHTerms, false>;
+  const int blocks = quant_blocks(max_rows, F);
+  if (blocks == 0) return cudaErrorInvalidValue;
+  return launch_kernel(kern, dim3(blocks), dim3(256),
                        (size_t)(max_rows / 128) * sizeof(int), L, hf, 0, F, 1, rows, counts, basep, E, (F + 127) / 128, hq,
                        hsf, nullptr, nullptr, nullptr, nullptr);
 }
