@@ -869,7 +869,7 @@ int packed_prefill_impl(const moe_packed_layer_t& P, const float* x, int T, void
                                       ws.inv, d->status, L))) != MOE_OK)
     return rc;
   if ((rc = cuda_status(launch_quant_rows_e2m1(x, T, P.D, P.k, ws.rows, ws.inv, ws.counts, ws.basep, P.E, (int)ws.max_rows, ws.aq,
-                                               ws.asf, y, ws.segs, ws.ctr, L))) != MOE_OK)
+                                               ws.asf, nullptr, ws.segs, ws.ctr, L))) != MOE_OK)
     return rc;
   GroupedMX4Args g{};
   g.kind = 0;
@@ -896,6 +896,8 @@ int packed_prefill_impl(const moe_packed_layer_t& P, const float* x, int T, void
   g.alpha = 1.702f;
   g.limit = 7.0f;
   g.status = d->status;
+  g.y = y;  // zeroed by the gate/up kernel, accumulated into by the down kernel
+  g.ny = (int64_t)T * P.D;
   if ((rc = cuda_status(launch_grouped_mx4(g, L))) != MOE_OK) return rc;
   GroupedMX4Args gd = g;
   gd.kind = 1;

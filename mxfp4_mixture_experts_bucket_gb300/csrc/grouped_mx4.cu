@@ -109,7 +109,8 @@ struct Params {
   const uint8_t* asf;  // [ntiles][NK][2 segments][terms][512]
   float* hf;           // gate/up: h as float rows [ntiles * 128][R]
   float alpha, limit;
-  float* y;  // down: [T][R], accumulated into (zeroed beforehand)
+  float* y;  // down: [T][R], accumulated into; gate/up: zeroed (ny floats) by the epilogue warps
+  int64_t ny;
   int* status;
 };
 
@@ -473,6 +474,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
     const int hh = (warp - kEpiWarp0) >> 2;  // gate/up: which row chunks; down: which tile of the pair
     const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
     const int et = threadIdx.x - kEpiWarp0 * 32;  // 0..255
+    if (KIND == 0 && p.y) {
+      // the down GEMM's output, zeroed while the first unit's MMAs run (the down
+      // kernel starts after this one has completed)
+      const int64_t n4 = p.ny >> 2, stride = (int64_t)gridDim.x * 32 * kEpiWarps;
+      float4* y4 = reinterpret_cast<float4*>(p.y);
+      for (int64_t i = (int64_t)blockIdx.x * 32 * kEpiWarps + et; i < n4; i += stride)
+        y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int64_t i = 4 * n4 + (int64_t)blockIdx.x * 32 * kEpiWarps + et; i < p.ny; i += stride) p.y[i] = 0.f;
+    }
     Unit ue{};
     int ldone = 0;  // units whose epilogue has run
     bool have_e = take(0, ue, true, 2);
@@ -599,8 +609,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
 // bytes stored with one store, its scale byte into the segment's atoms.
 // GATHER (x, the gate/up operand): one thread per (token, 32-block) splits the
 // block once and stores it into each of the token's k bucket rows (inv); pad
-// rows up to each segment's rounded end are zeroed; y[0 .. T*C) is zeroed (the
-// down GEMM accumulates into it) and block 0 writes the segment table. Else
+// rows up to each segment's rounded end are zeroed; y[0 .. T*C) is zeroed
+// unless null (the down GEMM accumulates into it) and block 0 writes the
+// segment table. Else
 // (h, the down operand): one thread per (bucket row, 32-block) of src's own
 // rows, pad rows zero. Blocks past C are zero; rows past a segment's rounded
 // end are never read and not written.
@@ -778,7 +789,7 @@ __global__ void __launch_bounds__(256, 3) quant_rows_e2m1_kernel(const float* __
       }
     }
   }
-  if (GATHER) {
+  if (GATHER && y) {
     const int64_t n4 = (int64_t)T * C / 4;
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t nthr = (int64_t)gridDim.x * blockDim.x;
@@ -866,6 +877,7 @@ cudaError_t launch_grouped_mx4(const GroupedMX4Args& a, Launch L) {
   prm.alpha = a.alpha;
   prm.limit = a.limit;
   prm.y = a.y;
+  prm.ny = a.ny;
   prm.status = a.status;
   const int nunits = prm.ntiles * 2 * prm.npair;
   int grid = device_sm_count();

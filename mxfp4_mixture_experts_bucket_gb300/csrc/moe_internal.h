@@ -173,13 +173,14 @@ struct GroupedMX4Args {
   const uint8_t* asf;       // their scale atoms [max_rows/128][ceil(C/128)][2 segments][terms][512]
   float* hf;                // gate/up output: h as float rows [max_rows][R]
   float alpha, limit;
-  float* y;                 // down: [T][R], zeroed beforehand
+  float* y;                 // down: [T][R], accumulated into; gate/up: zeroed (ny floats) while its first unit streams
+  int64_t ny;
   int* status;
 };
 size_t prefill_operand_bytes(int max_rows, int C, int terms);
 size_t prefill_atom_bytes(int max_rows, int C, int terms);
 // x's token rows in bucket order as kPrefillXTerms E2M1 terms (each token split once, stored into
-// its k bucket rows via inv), y zeroed, and
+// its k bucket rows via inv), y zeroed unless null, and
 // the segment table of the bucket (segs: 2 * max_rows / 128 + 1 entries); ctr[0..1] (the GEMMs'
 // unit counters) zeroed
 cudaError_t launch_quant_rows_e2m1(const float* x, int T, int D, int k, const int32_t* rows, const int32_t* inv,

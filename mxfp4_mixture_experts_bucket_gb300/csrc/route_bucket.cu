@@ -408,6 +408,7 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(const int32_t* _
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int i = tid; i < E; i += kBucketThreads) hist[i] = 0;
   __syncthreads();
+#pragma unroll 4
   for (int a = tid; a < n; a += kBucketThreads) {
     const int id = ids[a];
     if (id >= 0 && id < E) {
@@ -441,28 +442,34 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(const int32_t* _
   __syncthreads();
   const int base = s_base;
   const int mine = hist[e];
-  // stable compaction of the assignments that chose expert e
-  int running = 0;
-  for (int c0 = 0; c0 < n; c0 += kBucketThreads) {
-    const int a = c0 + tid;
-    const bool match = (a < n) && (ids[a] == e);
+  // stable compaction of the assignments that chose expert e: warp w owns the
+  // ids [w L, (w + 1) L); it counts its matches, a prefix over the warps gives
+  // its first row, and a second pass over its ids writes them in order (one
+  // block barrier in all)
+  constexpr int kWarps = kBucketThreads / 32;
+  const int L = ((n + kWarps - 1) / kWarps + 31) & ~31;
+  const int a0 = warp * L, a1 = min(n, a0 + L);
+  int cnt = 0;
+#pragma unroll 8
+  for (int c = a0; c < a1; c += 32) {
+    const int a = c + lane;
+    cnt += __popc(__ballot_sync(0xffffffffu, a < a1 && ids[a] == e));
+  }
+  if (lane == 0) s_wtot[warp] = cnt;
+  __syncthreads();
+  int p0 = base;
+  for (int w = 0; w < warp; ++w) p0 += s_wtot[w];
+#pragma unroll 8
+  for (int c = a0; c < a1; c += 32) {
+    const int a = c + lane;
+    const bool match = a < a1 && ids[a] == e;
     const uint32_t ballot = __ballot_sync(0xffffffffu, match);
-    if (lane == 0) s_wtot[warp] = __popc(ballot);
-    __syncthreads();
-    int before = 0, total = 0;
-#pragma unroll
-    for (int w = 0; w < kBucketThreads / 32; ++w) {
-      const int c = s_wtot[w];
-      before += (w < warp) ? c : 0;
-      total += c;
-    }
     if (match) {
-      const int p = base + running + before + __popc(ballot & ((1u << lane) - 1u));
+      const int p = p0 + __popc(ballot & ((1u << lane) - 1u));
       rows[p] = a;
       inv[a] = p;
     }
-    running += total;
-    __syncthreads();
+    p0 += __popc(ballot);
   }
   // pad rows of this expert's last tile
   const int padded = ((mine + tile - 1) / tile) * tile;
