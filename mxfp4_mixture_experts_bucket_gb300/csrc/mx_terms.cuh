@@ -109,7 +109,11 @@ __device__ __forceinline__ void split_terms_e2m1(float v, uint32_t (&q)[NT], uin
 // The same split for a block of 32 values held by one thread (r[i] = column i),
 // with the same arithmetic, one term at a time: the term's 32 codes come back
 // packed in the MXFP4 block layout (byte i = column i low nibble, column 16 + i
-// high) with its E8M0 code s; r becomes the residual unless `last`.
+// high) with its E8M0 code s; r becomes the residual unless `last` (then r is
+// left scaled). The residual is taken in the scaled domain: v = r * 2^-e is
+// exact, v - code (the code's value exact in f16, one mixed-precision FMA) is
+// exact because the code is v's nearest E2M1 value, and * 2^e rounds once, as
+// r - code * 2^e would.
 __device__ __forceinline__ void split_block_e2m1_term(float (&r)[32], bool last, uint4& packed, uint32_t& s) {
   // the largest magnitude (a tree of depth 5; for finite values the float order
   // of magnitudes is the integer order of their bit patterns)
@@ -127,6 +131,8 @@ __device__ __forceinline__ void split_block_e2m1_term(float (&r)[32], bool last,
   for (int i = 0; i < 16; ++i) {
     // columns i and 16 + i in one conversion: the byte of the block layout
     const float2 v = __fmul2_rn(make_float2(r[i], r[16 + i]), make_float2(inv, inv));
+    r[i] = v.x;
+    r[16 + i] = v.y;
     asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n cvt.u32.u8 %0, t;\n}" : "=r"(b[i]) : "f"(v.y), "f"(v.x));
   }
   uint32_t w[4];
@@ -139,15 +145,19 @@ __device__ __forceinline__ void split_block_e2m1_term(float (&r)[32], bool last,
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const uint32_t h2 = e2m1x2_to_f16x2(b[i]);  // both codes exactly, low nibble in the low half
-      const float2 d = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-      const float2 rr = __ffma2_rn(d, make_float2(-fwd, -fwd), make_float2(r[i], r[16 + i]));
+      float d0, d1;
+      asm("{\n .reg .b16 c0, c1, m;\n mov.b32 {c0, c1}, %2;\n mov.b16 m, 0xBC00;\n"
+          " fma.rn.f32.f16 %0, c0, m, %3;\n fma.rn.f32.f16 %1, c1, m, %4;\n}"
+          : "=f"(d0), "=f"(d1)
+          : "r"(h2), "f"(r[i]), "f"(r[16 + i]));  // v - code, exact
+      const float2 rr = __fmul2_rn(make_float2(d0, d1), make_float2(fwd, fwd));
       r[i] = rr.x;
       r[16 + i] = rr.y;
     }
   }
 }
 
-// All NT terms of one thread's block at once; r keeps the last residual.
+// All NT terms of one thread's block at once.
 template <int NT>
 __device__ __forceinline__ void split_block_e2m1(float (&r)[32], uint4 (&packed)[NT], uint32_t (&s)[NT]) {
 #pragma unroll
