@@ -612,8 +612,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
 // rows up to each segment's rounded end are zeroed; y[0 .. T*C) is zeroed
 // unless null (the down GEMM accumulates into it) and block 0 writes the
 // segment table. Else
-// (h, the down operand): one thread per (bucket row, 32-block) of src's own
-// rows, pad rows zero. Blocks past C are zero; rows past a segment's rounded
+// (h, the down operand): a lane pair per (bucket row, 32-block) of src's own
+// rows (split_half_block_e2m1_term), pad rows zero. Blocks past C are zero; rows past a segment's rounded
 // end are never read and not written.
 // ---------------------------------------------------------------------------
 // Stores a row's NT terms of one 32-block: the codes at `row` (the row's 16
@@ -744,47 +744,44 @@ __global__ void __launch_bounds__(256, 3) quant_rows_e2m1_kernel(const float* __
                       asf + (((size_t)b * NK + j) * 2 + s) * (NT * kAtom), g.rn, rt - g.base, kb, zq, zs);
     }
   } else {
-    for (int w = tid; w < mpad * nbp; w += nthr) {
+    // a lane pair per (bucket row, 32-block): both lanes of a pair always take
+    // the same item (nthr and tid keep their parity), so they skip or split it together
+    const int hf = threadIdx.x & 1;
+    const uint32_t pair = 3u << (threadIdx.x & 30);
+    const int64_t nitem = 2 * (int64_t)mpad * nbp;
+    for (int64_t w2 = tid; w2 < nitem; w2 += nthr) {
+      const int w = (int)(w2 >> 1);
       const int p = w / nbp, blk = w - p * nbp;
-      const int a = rows[p];
       const int b = p >> 7, rt = p & 127, j = blk >> 2, kb = blk & 3;
       const int live = s_live[b];
       const int s = live > kSegMax ? (rt >> 6) : 0;
       const Segment g = segment_of(live, s);
       const int r = rt - g.base;
       if (r >= g.rn) continue;  // rows past the segment's rounded end are never read
+      const int a = rows[p];
       const int m = slots_of<NT>(g.rn);
-      uint8_t* chunk = aq + ((size_t)b * NK + j) * (NT * kTermBytes);
+      uint8_t* chunk = aq + ((size_t)b * NK + j) * (NT * kTermBytes) + dmx::chunk_off(rt, kb, 8 * hf);
       uint8_t* atoms = asf + (((size_t)b * NK + j) * 2 + s) * (NT * kAtom);
+      float v[16];
       if (a >= 0 && blk < nb) {
-        float v[32];
-        const float* row = GATHER ? src + (size_t)(a / k) * C : src + (size_t)p * C;
-        const float4* s4 = reinterpret_cast<const float4*>(row + 32 * blk);
-  #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 f = __ldg(s4 + i);
-          v[4 * i] = f.x;
-          v[4 * i + 1] = f.y;
-          v[4 * i + 2] = f.z;
-          v[4 * i + 3] = f.w;
-        }
-  #pragma unroll
-        for (int term = 0; term < NT; ++term) {  // each term stored as soon as it is split
-          uint4 packed;
-          uint32_t sc;
-          mx::split_block_e2m1_term(v, term + 1 == NT, packed, sc);
-          *reinterpret_cast<uint4*>(chunk + (size_t)term * kTermBytes + dmx::chunk_off(rt, kb, 0)) = packed;
+        const float4* s4 = reinterpret_cast<const float4*>(src + (size_t)p * C + 32 * blk + 8 * hf);
+        const float4 f0 = __ldg(s4), f1 = __ldg(s4 + 1), f2 = __ldg(s4 + 4), f3 = __ldg(s4 + 5);
+        v[0] = f0.x; v[1] = f0.y; v[2] = f0.z; v[3] = f0.w; v[4] = f1.x; v[5] = f1.y; v[6] = f1.z; v[7] = f1.w;
+        v[8] = f2.x; v[9] = f2.y; v[10] = f2.z; v[11] = f2.w; v[12] = f3.x; v[13] = f3.y; v[14] = f3.z; v[15] = f3.w;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = 0.f;
+      }
+#pragma unroll
+      for (int term = 0; term < NT; ++term) {  // each term stored as soon as it is split
+        uint2 packed;
+        uint32_t sc;
+        mx::split_half_block_e2m1_term(v, term + 1 == NT, pair, packed, sc);
+        *reinterpret_cast<uint2*>(chunk + (size_t)term * kTermBytes) = packed;
+        if (hf == 0) {
           int n;
           const int ai = atom_index(term, m, g.rn, r, n);
           atoms[(size_t)ai * kAtom + dmx::atom_off(n, kb)] = (uint8_t)sc;
-        }
-      } else {
-  #pragma unroll
-        for (int term = 0; term < NT; ++term) {
-          *reinterpret_cast<uint4*>(chunk + (size_t)term * kTermBytes + dmx::chunk_off(rt, kb, 0)) = make_uint4(0u, 0u, 0u, 0u);
-          int n;
-          const int ai = atom_index(term, m, g.rn, r, n);
-          atoms[(size_t)ai * kAtom + dmx::atom_off(n, kb)] = 0;
         }
       }
     }
@@ -839,7 +836,7 @@ cudaError_t launch_quant_rows_e2m1(const float* x, int T, int D, int k, const in
 cudaError_t launch_quant_h_e2m1(const float* hf, int F, const int32_t* rows, const int32_t* counts,
                                 const int32_t* basep, int E, int max_rows, uint8_t* hq, uint8_t* hsf, Launch L) {
   const auto kern = gx4::quant_rows_e2m1_kernel<kPrefillHTerms, false>;
-  const int blocks = quant_blocks(max_rows, F);
+  const int blocks = quant_blocks(2 * max_rows, F);  // a lane pair per item
   if (blocks == 0) return cudaErrorInvalidValue;
   return launch_kernel(kern, dim3(blocks), dim3(256),
                        (size_t)(max_rows / 128) * sizeof(int), L, hf, 0, F, 1, rows, counts, basep, E, (F + 127) / 128, hq,

@@ -157,6 +157,49 @@ __device__ __forceinline__ void split_block_e2m1_term(float (&r)[32], bool last,
   }
 }
 
+// The same split with a block held by a lane pair (lanes 2i and 2i + 1, both
+// calling it; pair = the pair's lane mask): lane h holds columns 8h .. 8h + 7 in r[0..7]
+// and 16 + 8h .. 16 + 8h + 7 in r[8..15]; the pair exchanges its largest
+// magnitudes once, so both lanes take the same scale. The lane's 8 bytes of
+// the packed block (bytes 8h .. 8h + 7) come back in `packed`.
+__device__ __forceinline__ void split_half_block_e2m1_term(float (&r)[16], bool last, uint32_t pair, uint2& packed,
+                                                           uint32_t& s) {
+  float am[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) am[i] = fmaxf(fabsf(r[i]), fabsf(r[8 + i]));
+#pragma unroll
+  for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) am[i] = fmaxf(am[i], am[i + w]);
+  const float m = fmaxf(am[0], __shfl_xor_sync(pair, am[0], 1));
+  s = e2m1_block_code(__float_as_uint(m));
+  const float inv = inv_scale(s), fwd = fwd_scale(s);
+  uint32_t b[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float2 v = __fmul2_rn(make_float2(r[i], r[8 + i]), make_float2(inv, inv));
+    r[i] = v.x;
+    r[8 + i] = v.y;
+    asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n cvt.u32.u8 %0, t;\n}" : "=r"(b[i]) : "f"(v.y), "f"(v.x));
+  }
+  packed = make_uint2(__byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410),
+                      __byte_perm(__byte_perm(b[4], b[5], 0x0040), __byte_perm(b[6], b[7], 0x0040), 0x5410));
+  if (!last) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t h2 = e2m1x2_to_f16x2(b[i]);
+      float d0, d1;
+      asm("{\n .reg .b16 c0, c1, m;\n mov.b32 {c0, c1}, %2;\n mov.b16 m, 0xBC00;\n"
+          " fma.rn.f32.f16 %0, c0, m, %3;\n fma.rn.f32.f16 %1, c1, m, %4;\n}"
+          : "=f"(d0), "=f"(d1)
+          : "r"(h2), "f"(r[i]), "f"(r[8 + i]));  // v - code, exact
+      const float2 rr = __fmul2_rn(make_float2(d0, d1), make_float2(fwd, fwd));
+      r[i] = rr.x;
+      r[8 + i] = rr.y;
+    }
+  }
+}
+
 // All NT terms of one thread's block at once.
 template <int NT>
 __device__ __forceinline__ void split_block_e2m1(float (&r)[32], uint4 (&packed)[NT], uint32_t (&s)[NT]) {
