@@ -607,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
 // Bucket rows as NT E2M1 terms, in the activation-chunk layout: each 32-block
 // is loaded (128 bytes), split (split_block_e2m1_term) and each term's 16
 // bytes stored with one store, its scale byte into the segment's atoms.
-// GATHER (x, the gate/up operand): one thread per (token, 32-block) splits the
+// GATHER (x, the gate/up operand): a lane pair per (token, 32-block) splits the
 // block once and stores it into each of the token's k bucket rows (inv); pad
 // rows up to each segment's rounded end are zeroed; y[0 .. T*C) is zeroed
 // unless null (the down GEMM accumulates into it) and block 0 writes the
@@ -630,6 +630,26 @@ __device__ __forceinline__ void store_terms(uint8_t* row, uint8_t* atoms, int rn
     *reinterpret_cast<uint4*>(row + (size_t)t * kTermBytes) = packed[t];
     const int nn = slot * rn + r;  // B row of the group's MMA
     atoms[(size_t)(grp * apg + (nn >> 7)) * kAtom + dmx::atom_off(nn & 127, kb)] = (uint8_t)sc[t];
+    if (++slot == m) {
+      slot = 0;
+      ++grp;
+    }
+  }
+}
+
+// The same for a lane pair's half of the block: this lane's 8 bytes of each
+// term at `row` (already offset to the lane's half); the scale codes only if
+// `scales` (one lane of the pair).
+template <int NT>
+__device__ __forceinline__ void store_half_terms(uint8_t* row, uint8_t* atoms, int rn, int r, int kb, bool scales,
+                                                 const uint2 (&packed)[NT], const uint32_t (&sc)[NT]) {
+  const int m = slots_of<NT>(rn), apg = atoms_per_group(m, rn);
+  int slot = 0, grp = 0;
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    *reinterpret_cast<uint2*>(row + (size_t)t * kTermBytes) = packed[t];
+    const int nn = slot * rn + r;
+    if (scales) atoms[(size_t)(grp * apg + (nn >> 7)) * kAtom + dmx::atom_off(nn & 127, kb)] = (uint8_t)sc[t];
     if (++slot == m) {
       slot = 0;
       ++grp;
@@ -698,28 +718,29 @@ __global__ void __launch_bounds__(256, 3) quant_rows_e2m1_kernel(const float* __
     zs[t] = 0u;
   }
   if constexpr (GATHER) {
-    // the tokens: each block split once, its terms stored into the token's k bucket rows
-    for (int w = tid; w < T * nbp; w += nthr) {
+    // the tokens: each block split once by a lane pair (both lanes of a pair take the
+    // same item: nthr and tid keep their parity), its terms stored into the token's
+    // k bucket rows
+    const int hf = threadIdx.x & 1;
+    const uint32_t pair = 3u << (threadIdx.x & 30);
+    for (int64_t w2 = tid; w2 < 2 * (int64_t)T * nbp; w2 += nthr) {
+      const int w = (int)(w2 >> 1);
       const int t = w / nbp, blk = w - t * nbp, j = blk >> 2, kb = blk & 3;
-      float v[32];
+      float v[16];
       if (blk < nb) {
-        const float4* s4 = reinterpret_cast<const float4*>(src + (size_t)t * C + 32 * blk);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 f = __ldg(s4 + i);
-          v[4 * i] = f.x;
-          v[4 * i + 1] = f.y;
-          v[4 * i + 2] = f.z;
-          v[4 * i + 3] = f.w;
-        }
+        const float4* s4 = reinterpret_cast<const float4*>(src + (size_t)t * C + 32 * blk + 8 * hf);
+        const float4 f0 = __ldg(s4), f1 = __ldg(s4 + 1), f2 = __ldg(s4 + 4), f3 = __ldg(s4 + 5);
+        v[0] = f0.x; v[1] = f0.y; v[2] = f0.z; v[3] = f0.w; v[4] = f1.x; v[5] = f1.y; v[6] = f1.z; v[7] = f1.w;
+        v[8] = f2.x; v[9] = f2.y; v[10] = f2.z; v[11] = f2.w; v[12] = f3.x; v[13] = f3.y; v[14] = f3.z; v[15] = f3.w;
       } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+        for (int i = 0; i < 16; ++i) v[i] = 0.f;
       }
-      uint4 packed[NT];
+      uint2 packed[NT];
       uint32_t sc[NT];
 #pragma unroll
-      for (int term = 0; term < NT; ++term) mx::split_block_e2m1_term(v, term + 1 == NT, packed[term], sc[term]);
+      for (int term = 0; term < NT; ++term)
+        mx::split_half_block_e2m1_term(v, term + 1 == NT, pair, packed[term], sc[term]);
       for (int jj = 0; jj < k; ++jj) {
         const int p = __ldg(inv + (size_t)t * k + jj);
         if (p < 0) continue;  // an invalid expert id: the assignment has no bucket row
@@ -727,8 +748,9 @@ __global__ void __launch_bounds__(256, 3) quant_rows_e2m1_kernel(const float* __
         const int live = s_live[b];
         const int s = live > kSegMax ? (rt >> 6) : 0;
         const Segment g = segment_of(live, s);
-        store_terms<NT>(aq + ((size_t)b * NK + j) * (NT * kTermBytes) + dmx::chunk_off(rt, kb, 0),
-                        asf + (((size_t)b * NK + j) * 2 + s) * (NT * kAtom), g.rn, rt - g.base, kb, packed, sc);
+        store_half_terms<NT>(aq + ((size_t)b * NK + j) * (NT * kTermBytes) + dmx::chunk_off(rt, kb, 8 * hf),
+                             asf + (((size_t)b * NK + j) * 2 + s) * (NT * kAtom), g.rn, rt - g.base, kb, hf == 0,
+                             packed, sc);
       }
     }
     // the pad rows of every segment, up to its rounded end: zero terms, scale code 0
@@ -826,7 +848,7 @@ cudaError_t launch_quant_rows_e2m1(const float* x, int T, int D, int k, const in
                                    const int32_t* counts, const int32_t* basep, int E, int max_rows, uint8_t* aq,
                                    uint8_t* asf, float* y, int2* segs, int* ctr, Launch L) {
   const auto kern = gx4::quant_rows_e2m1_kernel<kPrefillXTerms, true>;
-  const int blocks = quant_blocks(max_rows, D);
+  const int blocks = quant_blocks(2 * max_rows, D);  // a lane pair per item
   if (blocks == 0) return cudaErrorInvalidValue;
   return launch_kernel(kern, dim3(blocks), dim3(256),
                        (size_t)(max_rows / 128) * sizeof(int), L, x, T, D, k, rows, counts, basep, E, (D + 127) / 128, aq,
