@@ -605,16 +605,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
 
 // ---------------------------------------------------------------------------
 // Bucket rows as NT E2M1 terms, in the activation-chunk layout: each 32-block
-// is loaded (128 bytes), split (split_block_e2m1_term) and each term's 16
-// bytes stored with one store, its scale byte into the segment's atoms.
+// is loaded (128 bytes) and split (split_half_block_e2m1_term) by a lane pair,
+// each lane storing its 8 bytes of every term, one lane the scale bytes into
+// the segment's atoms.
 // GATHER (x, the gate/up operand): a lane pair per (token, 32-block) splits the
 // block once and stores it into each of the token's k bucket rows (inv); pad
 // rows up to each segment's rounded end are zeroed; y[0 .. T*C) is zeroed
 // unless null (the down GEMM accumulates into it) and block 0 writes the
-// segment table. Else
-// (h, the down operand): a lane pair per (bucket row, 32-block) of src's own
-// rows (split_half_block_e2m1_term), pad rows zero. Blocks past C are zero; rows past a segment's rounded
-// end are never read and not written.
+// segment table. Else (h, the down operand): a lane pair per (bucket row,
+// 32-block) of src's own rows, pad rows zero. Blocks past C are zero; rows
+// past a segment's rounded end are never read and not written.
 // ---------------------------------------------------------------------------
 // Stores a row's NT terms of one 32-block: the codes at `row` (the row's 16
 // bytes of block kb in term 0's image; term t sits t * kTermBytes further) and

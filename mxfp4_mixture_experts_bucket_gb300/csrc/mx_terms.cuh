@@ -106,62 +106,17 @@ __device__ __forceinline__ void split_terms_e2m1(float v, uint32_t (&q)[NT], uin
   }
 }
 
-// The same split for a block of 32 values held by one thread (r[i] = column i),
-// with the same arithmetic, one term at a time: the term's 32 codes come back
-// packed in the MXFP4 block layout (byte i = column i low nibble, column 16 + i
-// high) with its E8M0 code s; r becomes the residual unless `last` (then r is
-// left scaled). The residual is taken in the scaled domain: v = r * 2^-e is
-// exact, v - code (the code's value exact in f16, one mixed-precision FMA) is
-// exact because the code is v's nearest E2M1 value, and * 2^e rounds once, as
-// r - code * 2^e would.
-__device__ __forceinline__ void split_block_e2m1_term(float (&r)[32], bool last, uint4& packed, uint32_t& s) {
-  // the largest magnitude (a tree of depth 5; for finite values the float order
-  // of magnitudes is the integer order of their bit patterns)
-  float am[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) am[i] = fmaxf(fabsf(r[i]), fabsf(r[16 + i]));
-#pragma unroll
-  for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-    for (int i = 0; i < w; ++i) am[i] = fmaxf(am[i], am[i + w]);
-  s = e2m1_block_code(__float_as_uint(am[0]));
-  const float inv = inv_scale(s), fwd = fwd_scale(s);
-  uint32_t b[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    // columns i and 16 + i in one conversion: the byte of the block layout
-    const float2 v = __fmul2_rn(make_float2(r[i], r[16 + i]), make_float2(inv, inv));
-    r[i] = v.x;
-    r[16 + i] = v.y;
-    asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n cvt.u32.u8 %0, t;\n}" : "=r"(b[i]) : "f"(v.y), "f"(v.x));
-  }
-  uint32_t w[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-    w[q] = __byte_perm(__byte_perm(b[4 * q], b[4 * q + 1], 0x0040), __byte_perm(b[4 * q + 2], b[4 * q + 3], 0x0040),
-                       0x5410);
-  packed = make_uint4(w[0], w[1], w[2], w[3]);
-  if (!last) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t h2 = e2m1x2_to_f16x2(b[i]);  // both codes exactly, low nibble in the low half
-      float d0, d1;
-      asm("{\n .reg .b16 c0, c1, m;\n mov.b32 {c0, c1}, %2;\n mov.b16 m, 0xBC00;\n"
-          " fma.rn.f32.f16 %0, c0, m, %3;\n fma.rn.f32.f16 %1, c1, m, %4;\n}"
-          : "=f"(d0), "=f"(d1)
-          : "r"(h2), "f"(r[i]), "f"(r[16 + i]));  // v - code, exact
-      const float2 rr = __fmul2_rn(make_float2(d0, d1), make_float2(fwd, fwd));
-      r[i] = rr.x;
-      r[16 + i] = rr.y;
-    }
-  }
-}
-
 // The same split with a block held by a lane pair (lanes 2i and 2i + 1, both
-// calling it; pair = the pair's lane mask): lane h holds columns 8h .. 8h + 7 in r[0..7]
-// and 16 + 8h .. 16 + 8h + 7 in r[8..15]; the pair exchanges its largest
-// magnitudes once, so both lanes take the same scale. The lane's 8 bytes of
-// the packed block (bytes 8h .. 8h + 7) come back in `packed`.
+// calling it; pair = the pair's lane mask), one term at a time, with the same
+// arithmetic: lane h holds columns 8h .. 8h + 7 in r[0..7] and 16 + 8h ..
+// 16 + 8h + 7 in r[8..15]; the pair exchanges its largest magnitudes once, so
+// both lanes take the same scale code s. The lane's 8 bytes of the packed
+// block (byte i = column i low nibble, column 16 + i high; bytes 8h .. 8h + 7)
+// come back in `packed`; r becomes the residual unless `last` (then r is left
+// scaled). The residual is taken in the scaled domain: v = r * 2^-e is exact,
+// v - code (the code's value exact in f16, one mixed-precision FMA) is exact
+// because the code is v's nearest E2M1 value, and * 2^e rounds once, as
+// r - code * 2^e would.
 __device__ __forceinline__ void split_half_block_e2m1_term(float (&r)[16], bool last, uint32_t pair, uint2& packed,
                                                            uint32_t& s) {
   float am[8];
@@ -198,13 +153,6 @@ __device__ __forceinline__ void split_half_block_e2m1_term(float (&r)[16], bool 
       r[8 + i] = rr.y;
     }
   }
-}
-
-// All NT terms of one thread's block at once.
-template <int NT>
-__device__ __forceinline__ void split_block_e2m1(float (&r)[32], uint4 (&packed)[NT], uint32_t (&s)[NT]) {
-#pragma unroll
-  for (int t = 0; t < NT; ++t) split_block_e2m1_term(r, t + 1 == NT, packed[t], s[t]);
 }
 
 // A warp's block of E2M1 codes (lane l holds column l) packed as the MXFP4 block
