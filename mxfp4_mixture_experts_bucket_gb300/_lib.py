@@ -249,6 +249,18 @@ def moe_ffn_layer_hostio(args, x_host, y_host, stream=None):
                                      _ptr(y_host), _stream(stream))
 
 
+def byref_args(args):
+    """A reference to an argument struct that can be passed again without rebuilding it
+    (keep `args` alive as long as the reference is used)."""
+    return ctypes.byref(args)
+
+
+def moe_ffn_layer_hostio_ref(args_ref, x_host_ptr, y_host_ptr, stream_handle):
+    """moe_ffn_layer_hostio with everything already converted: args_ref from byref_args,
+    host addresses and the stream handle as ints (the per-step path of MoeLayer.forward_host)."""
+    return _lib.moe_ffn_layer_hostio(args_ref, x_host_ptr, y_host_ptr, stream_handle)
+
+
 def moe_ffn_layer_decode_static(x, T, D, F, E, k, w_router, b_router, g_qs, g_sc, bg, u_qs, u_sc, bu,
                                 d_qs, d_sc, bd, y, ids_out=None, weights_out=None, stream=None):
     return _lib.moe_ffn_layer_decode_static(_ptr(x), T, D, F, E, k, _ptr(w_router), _ptr(b_router),

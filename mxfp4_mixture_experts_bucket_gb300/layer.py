@@ -145,34 +145,42 @@ class MoeLayer:
         if None): [T, D] float32 CPU tensor. The copies and the layer are only
         enqueued on the stream: synchronise it before reading y_host.
         """
+        if x_host.dim() != 2 or x_host.shape[1] != self.D:
+            raise ValueError(f"x_host must be [T, {self.D}]")
         T = x_host.shape[0]
-        if x_host.device.type != "cpu" or x_host.dtype != torch.float32 or not x_host.is_contiguous():
+        if x_host.is_cuda or x_host.dtype is not torch.float32 or not x_host.is_contiguous():
             raise ValueError("x_host must be a contiguous float32 CPU tensor")
         if y_host is None:
             y_host = torch.empty((T, self.D), dtype=torch.float32, pin_memory=True)
-        if y_host.device.type != "cpu" or y_host.dtype != torch.float32 or not y_host.is_contiguous():
-            raise ValueError("y_host must be a contiguous float32 CPU tensor")
+        elif (y_host.is_cuda or y_host.dtype is not torch.float32 or not y_host.is_contiguous()
+              or y_host.shape != x_host.shape):
+            raise ValueError(f"y_host must be a contiguous float32 CPU tensor of shape [{T}, {self.D}]")
+        sp = _lib._stream(stream)
+        io = self._io.get((T, rail))
+        if io is not None:  # staging buffers and the C arguments of this (T, rail) exist already
+            rc = _lib.moe_ffn_layer_hostio_ref(io[2], x_host.data_ptr(), y_host.data_ptr(), sp)
+            if rc:
+                _lib.check(rc, "moe_ffn_layer_hostio")
+            return y_host
         if self._use_packed(T, rail):
             ws = self.workspace(T, rail)
             rc = _lib.moe_ffn_layer_packed_hostio(self.packed_struct, T, rail, ws, ws.numel(), x_host, y_host,
-                                                  stream)
+                                                  sp)
             _lib.check(rc, "moe_ffn_layer_packed_hostio")
             return y_host
         if self.interleaved:
             raise NotImplementedError("host I/O runs on separate gate/up planes or the prepacked rail")
-        key = (T, rail)
-        io = self._io.get(key)
-        if io is None:  # staging buffers and the fixed arguments, once per (T, rail)
-            xd = torch.empty((T, self.D), dtype=torch.float32, device=self.device)
-            yd = torch.empty((T, self.D), dtype=torch.float32, device=self.device)
-            ws = self.workspace(T, rail)
-            w = self.w
-            args = _lib.make_ffn_args(T, self.D, self.F, self.E, self.k, rail, w["w_router"], w["b_router"],
-                                      w["g_qs"], w["g_sc"], w["bg"], w["u_qs"], w["u_sc"], w["bu"],
-                                      w["d_qs"], w["d_sc"], w["bd"], ws, ws.numel(), xd, yd)
-            io = (xd, yd, args)
-            self._io[key] = io
-        rc = _lib.moe_ffn_layer_hostio(io[2], x_host, y_host, stream)
+        # staging buffers and the fixed arguments, once per (T, rail)
+        xd = torch.empty((T, self.D), dtype=torch.float32, device=self.device)
+        yd = torch.empty((T, self.D), dtype=torch.float32, device=self.device)
+        ws = self.workspace(T, rail)
+        w = self.w
+        args = _lib.make_ffn_args(T, self.D, self.F, self.E, self.k, rail, w["w_router"], w["b_router"],
+                                  w["g_qs"], w["g_sc"], w["bg"], w["u_qs"], w["u_sc"], w["bu"],
+                                  w["d_qs"], w["d_sc"], w["bd"], ws, ws.numel(), xd, yd)
+        io = (xd, yd, _lib.byref_args(args), args)
+        self._io[(T, rail)] = io
+        rc = _lib.moe_ffn_layer_hostio_ref(io[2], x_host.data_ptr(), y_host.data_ptr(), sp)
         _lib.check(rc, "moe_ffn_layer_hostio")
         return y_host
 

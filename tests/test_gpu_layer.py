@@ -295,6 +295,27 @@ def test_forward_host_pinned_and_pageable(moe):
         assert torch.equal(y, layer(dev(x.numpy()), rail=rail).cpu())
 
 
+def test_forward_host_rejects_mismatched_buffers(moe):
+    """Host buffers whose shape, dtype, layout or device do not fit the layer are
+    refused before anything is enqueued (a short y would otherwise be written
+    past its end)."""
+    spec, L, layer, _ = layer_for(moe, 1)
+    x = torch.from_numpy(make_tokens(spec, T=2, seed=410)).pin_memory()
+    bad = [
+        (x, torch.empty((1, spec.D)).pin_memory()),                 # y too short
+        (x, torch.empty((2, spec.D + 32)).pin_memory()),            # y too wide
+        (x, torch.empty((2, spec.D), dtype=torch.float64)),         # y not float32
+        (x, torch.empty((spec.D, 2)).t()),                          # y not contiguous
+        (x[:, :64].contiguous(), torch.empty((2, 64))),             # x of the wrong width
+        (x.cuda(), torch.empty((2, spec.D))),                       # x on the device
+    ]
+    for xb, yb in bad:
+        with pytest.raises(ValueError):
+            layer.forward_host(xb, yb, rail=moe.MOE_RAIL_GEMV)
+    torch.cuda.synchronize()
+    assert status(moe) == 0
+
+
 def _e4m3_values():
     vals = np.empty(256)
     for c in range(256):
