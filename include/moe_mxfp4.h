@@ -89,8 +89,8 @@ extern "C" {
  * needs the tighter bound names MOE_RAIL_GEMV. On prepacked planes
  * (moe_ffn_layer_packed) MOE_RAIL_AUTO is MOE_RAIL_DECODE_MX for
  * T <= MOE_AUTO_DECODE_MX_MAX_T and MOE_RAIL_GROUPED_MX4 beyond (measured:
- * at T = 2 the two are within 1%, from T = 4 the grouped rail leads, 70 us
- * against 83 us per layer step, 197 us at T = 512).
+ * at T = 2 the decode rail leads by about 6%, from T = 4 the grouped rail
+ * leads, 72 us against 84 us per layer step, 183 us at T = 512).
  */
 #define MOE_AUTO_GEMV_MAX_T 3
 #define MOE_AUTO_MX_MAX_T 320
@@ -505,15 +505,16 @@ size_t moe_ffn_packed_workspace_bytes(int T, int D, int F, int E, int k, int rai
  * h_out (may be NULL): receives the swiglu outputs h[t*k+j][F] of the
  * assignments (decode rail only). Other arguments and limits as in
  * moe_ffn_layer; D and F multiples of 64; k*T <= 64 on the decode rail.
- * MOE_RAIL_GROUPED_MX4 (MOE_RAIL_AUTO for T > MOE_GEMV_MAX_T) runs the prefill
+ * MOE_RAIL_GROUPED_MX4 (MOE_RAIL_AUTO for T > MOE_AUTO_DECODE_MX_MAX_T) runs the prefill
  * chain of "dasLLAMA gpt-oss arc" (Metal fusion lane commit: router, the
  * MoeBucket CSR with the prefix folded in, the MXFP4 grouped mul_mm for
  * gate/up with bias and swiglu, then down with bias and the router-weighted
  * scatter) on the same prepacked planes: x enters as six E2M1 terms per value
  * in bucket order; on tcgen05.mma kind::mxf4 each 128-row weight tile is the A
- * operand and a bucket segment of at most 96 live rows (two terms stacked per
- * MMA) the B operand, so the MMA work follows the live rows, not the 128-row
- * padding; h leaves the gate/up epilogue as float rows split into four E2M1 terms, and the down
+ * operand and a bucket segment of at most 96 live rows (as many of its terms
+ * stacked per MMA as fit 192 columns) the B operand, so the MMA work follows
+ * the live rows, not the 128-row padding; h leaves the gate/up epilogue as
+ * float rows split into four E2M1 terms, and the down
  * epilogue scatters w*(acc + bd) into y with float atomics (summation order not
  * deterministic).
  */
