@@ -200,6 +200,19 @@ __device__ __forceinline__ float block_dot_split(uint4 q, const uint32_t (&XH)[1
   return add_f16x2_f32(hadd2_u32(lo0, lo1), (h0 + h1) + (h2 + h3));
 }
 
+// One m16n8k16 tensor-core product (f16 operands, fp32 accumulators, d += a b)
+// with the register fragments of mma.sync: lane (g, q) = (lane / 4, lane % 4)
+// holds A rows g and g + 8 at k = 2q, 2q + 1 (a0, a1) and k = 2q + 8, 2q + 9
+// (a2, a3), B column g at the same k (b0, b1), and D rows g, g + 8 at columns
+// 2q, 2q + 1.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // 2^(s-127) with s = 0 -> 2^-127 and s = 255 -> NaN, as an fp32 bit pattern.
 __device__ __forceinline__ float e8m0_scale(uint32_t s) {
   const uint32_t special = (((s + 1u) & 0xFEu) == 0u) ? 0x00400000u : 0u;
@@ -328,7 +341,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_expert_kernel(const Dec
   __shared__ DecodeRouting Rt;
   __shared__ __align__(8) uint64_t full_bar[kDecMaxStages];
   __shared__ __align__(8) uint64_t empty_bar[kDecMaxStages];
-  __shared__ float s_part[2][kDecConsumers][16];
+  __shared__ float s_part[2][kDecConsumers][64];  // per warp: 16 row results, or 4 assignments x 8 rows x 2
   __shared__ __align__(8) uint64_t xfull_bar[kDecConsumers][2];  // per team and buffer: partials written
   __shared__ __align__(8) uint64_t xfree_bar[kDecConsumers][2];  // per team and buffer: leader done with them
   __shared__ SubWalk s_walk[kDecConsumers];
@@ -500,6 +513,84 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_expert_kernel(const Dec
     // stage strides: between a matrix's consecutive rows, and between the two matrices' row r
     const uint32_t q_rs = (uint32_t)rsv * (C / 2), q_ms = rsv == 2 ? (uint32_t)(C / 2) : qsb;
     const uint32_t s_rs = (uint32_t)(rsv * nb), s_ms = rsv == 2 ? (uint32_t)nb : scb;
+    if (KIND == 0 && A.staged) {
+      // Tensor cores (mma.sync m16n8k16, f16 in, fp32 out): A = the sub-task's rows
+      // (gate/up: gate rows 0..7, up rows 8..15; down: rows 0..7 twice), each lane
+      // decoding one 32-bit word of two rows per block; B = up to four
+      // assignments' split vectors (column 2j: high part of assignment j, 2j + 1:
+      // its low part), read as stored; per block the two k16 products are scaled
+      // by the block factors and added in fp32. This warp takes blocks
+      // [kb0, kb1) of the row; the team adds its warps' partials as below.
+      const int g = lane >> 2, tq = lane & 3;
+      const int kbw = (nb + tw - 1) / tw, kb0 = wt * kbw, kb1 = min(nb, kb0 + kbw);
+      const uint8_t* qa = stage + g * q_rs + 4 * tq;
+      const uint8_t* qb = qa + (KIND == 0 ? q_ms : 0u);
+      const uint8_t* sa = stage + NMAT * qsb + sc_skew + g * s_rs;
+      const uint8_t* sb = sa + (KIND == 0 ? s_ms : 0u);
+      // biases of the rows the leader's lanes finish: row lane % 8
+      float lb0 = 0.f, lb1 = 0.f;
+      if ((lane & 7) < st.nr) {
+        const size_t ro = ((size_t)e * R + st.r0 + (lane & 7)) * rsv;
+        if (A.bias[0]) lb0 = __ldg(A.bias[0] + ro);
+        if (KIND == 0 && A.bias[1]) lb1 = __ldg(A.bias[1] + ro);
+      }
+      const int l0 = Rt.act_off[st.ai], nas = Rt.act_off[st.ai + 1] - l0;
+      for (int g0 = 0; g0 < nas; g0 += 4, ++it) {
+        const int ng = min(4, nas - g0);
+        const int ab = Rt.lst[l0 + g0 + ((g >> 1) < ng ? (g >> 1) : 0)];  // this lane's B column
+        const int ac = Rt.lst[l0 + g0 + (tq < ng ? tq : 0)];              // its D columns
+        const uint32_t* xw = vwords + (size_t)((KIND == 0) ? ab / k : ab) * nb * 32;
+        const int cx = 4 * (g & 1) + tq;  // the 16-byte piece: high (g even) or low words 4q .. 4q + 3
+        const float* xfa = vfac + (size_t)((KIND == 0) ? ac / k : ac) * nb;
+        float acc0 = 0.f, acc1 = 0.f;
+        if (!__any_sync(0xffffffffu, dead)) {  // mma.sync wants the whole warp
+#pragma unroll 2
+          for (int blk = kb0; blk < kb1; ++blk) {
+            uint32_t ha[4], hb[4];
+            e2m1x8_to_f16x2x4(*reinterpret_cast<const uint32_t*>(qa + 16 * blk), ha);
+            if (KIND == 0) e2m1x8_to_f16x2x4(*reinterpret_cast<const uint32_t*>(qb + 16 * blk), hb);
+            const uint4 xq = *reinterpret_cast<const uint4*>(xw + 32 * blk + 4 * (cx ^ (blk & 7)));
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            if (KIND == 0) {
+              mma_f16_16816(d, ha[0], hb[0], ha[1], hb[1], xq.x, xq.y);
+              mma_f16_16816(d, ha[2], hb[2], ha[3], hb[3], xq.z, xq.w);
+            } else {
+              mma_f16_16816(d, ha[0], ha[0], ha[1], ha[1], xq.x, xq.y);
+              mma_f16_16816(d, ha[2], ha[2], ha[3], ha[3], xq.z, xq.w);
+            }
+            const float xf = xfa[blk];
+            acc0 = fmaf(d[0] + d[1], xf * e8m0_scale(sa[blk]), acc0);
+            if (KIND == 0) acc1 = fmaf(d[2] + d[3], xf * e8m0_scale(sb[blk]), acc1);
+          }
+        }
+        // exchange: lane (g, q) holds row g of assignment g0 + q
+        const int buf = it & 1, ph = it >> 1;
+        if (it >= 2) team_wait(&xfree_bar[team][buf], (ph - 1) & 1, 2);
+        s_part[buf][cw][16 * tq + 2 * g] = acc0;
+        s_part[buf][cw][16 * tq + 2 * g + 1] = acc1;
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(tc::smem_u32(&xfull_bar[team][buf]));
+        if (wt == it % tw) {
+          team_wait(&xfull_bar[team][buf], ph & 1, 3);
+          const int jj = lane >> 3, r = lane & 7;  // the leader's lane: assignment g0 + jj, row r
+          if (jj < ng && r < st.nr) {
+            const int a = Rt.lst[l0 + g0 + jj];
+            const int c0 = team * tw;
+            float v0 = 0.f, v1 = 0.f;
+            for (int w2 = 0; w2 < tw; ++w2) {
+              v0 += s_part[buf][c0 + w2][16 * jj + 2 * r];
+              v1 += s_part[buf][c0 + w2][16 * jj + 2 * r + 1];
+            }
+            if (KIND == 0)
+              A.out[(size_t)a * R + st.r0 + r] = swiglu_oai_f(v0 + lb0, v1 + lb1, A.alpha, A.limit);
+            else
+              so[a * kDecRows + r] = v0 + lb0;
+          }
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(tc::smem_u32(&xfree_bar[team][buf]));
+        }
+      }
+    } else
     for (int li = Rt.act_off[st.ai]; li < Rt.act_off[st.ai + 1]; ++li, ++it) {
       const int a = Rt.lst[li];
       const int v = (KIND == 0) ? a / k : a;
@@ -586,7 +677,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_expert_kernel(const Dec
 // Shared memory: stages (an equal number per team, 2..4) first, then the split
 // vectors if they still fit, then the down kernel's per-team row results.
 static cudaError_t decode_plan(int KIND, int C, int nvec, int TK, DecodeArgs& A, size_t& smem) {
-  constexpr size_t kBudget = 220 * 1024;
+  constexpr size_t kBudget = 216 * 1024;  // with the kernel's static shared memory, under 227 KB
   const int nb = C >> 5;
   const int tw = (nb + 31) / 32;
   if (tw < 1 || tw > 4) return cudaErrorInvalidValue;
