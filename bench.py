@@ -499,7 +499,7 @@ def run_ours(args, dist: Dist):
                                 f"inputs larger than L2: {NL} distinct layer weight sets "
                                 f"({NL * E * EXPERT_BYTES / 1e9:.1f} GB) rotated every step",
                                 "one CUDA graph of the timed steps, CUDA events on its stream"),
-        "rail": "gemv (CUDA cores: router, fused gate/up + swiglu, fused down + combine)",
+        "rail": "gemv (router; fused gate/up + swiglu with mma.sync inner products; fused down + combine on the CUDA cores)",
         "weight_gbs": round(weight_bytes_step * K / secs_max * dist.world / 1e9, 1),
         "layer_roofline_frac": round((step_bytes / (hbm_peak * 1e9)) / (secs_max / K), 4),
         "roofline": roofline,

@@ -321,8 +321,10 @@ int moe_expert_down_combine(const uint8_t* d_qs, const uint8_t* d_sc, const floa
  *   y[t] = sum_j weights[t][j] * (Wd[e] h_j + bd[e]),  e = ids[t][j],
  *   h_j  = swiglu_oai(Wg[e] x_t + bg[e], Wu[e] x_t + bu[e])  (alpha 1.702, limit 7)
  * Rails: MOE_RAIL_GEMV (T <= MOE_GEMV_MAX_T) streams the touched experts'
- * weights through fp32 CUDA-core GEMVs (gate/up + swiglu fused, down + bias +
- * slot-order combine fused; deterministic); its two expert kernels take the
+ * weights through fused GEMVs with fp32 accumulation (gate/up + swiglu, its
+ * inner products on the tensor pipe with mma.sync when the activations fit in
+ * shared memory; down + bias + slot-order combine on the CUDA cores;
+ * deterministic); its two expert kernels take the
  * top-k of the router logits themselves, so a decode step is three kernels. MOE_RAIL_GROUPED_MM runs the
  * tcgen05 grouped GEMM with bf16 MMAs (x enters gate/up split into bf16 high
  * and low parts, h enters down rounded to bf16), the swiglu fused into the
