@@ -601,12 +601,16 @@ int moe_get_status(cudaStream_t stream, int* status);
  * moe_get_timeout_site -- waits for `stream`, then reads and clears the site of
  * the first pipeline wait that gave up on the calling device since the last
  * read (0: none): kernel << 24 | role << 20 | stage << 12 | sequence index,
- * kernel 1 = decode gate/up, 2 = decode down (CUDA-core GEMV rail), 3 = grouped
- * GEMM (bf16), 4 = grouped GEMM (block-scaled), 5 = decode gate/up, 6 = decode
- * down (block-scaled decode rail); role 0 = a producer waiting for a free
- * stage, 1 = a consumer waiting for data, 2 = an epilogue waiting for its
- * accumulator (grouped GEMMs: the warp index of the waiting role, 3 or 4 = the
- * dequantising or expanding warps). For diagnosis only.
+ * kernel 1 = decode gate/up, 2 = decode down (GEMV rail), 3 = grouped GEMM
+ * (bf16), 4 = grouped GEMM (block-scaled), 5 = decode gate/up, 6 = decode down
+ * (block-scaled decode rail), 7 = gate/up, 8 = down (kind::mxf4 grouped rail);
+ * role 0 = a producer waiting for a free stage, 1 = a consumer waiting for
+ * data, 2 = an epilogue waiting for its accumulator (grouped GEMMs: the warp
+ * index of the waiting role, 3 or 4 = the dequantising or expanding warps;
+ * kind::mxf4 rail: 0 = a copy issuer waiting for a free stage, 1 = the MMA
+ * thread, 2 = an epilogue warp, 3 = a scale loader waiting for data, 4 = a
+ * scale loader and 5 = a copy issuer waiting for its next work unit). For
+ * diagnosis only.
  */
 int moe_get_timeout_site(cudaStream_t stream, int* site);
 
