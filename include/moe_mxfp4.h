@@ -60,6 +60,8 @@ extern "C" {
 /* ---- device status bits (moe_get_status) ---- */
 #define MOE_STATUS_BAD_EXPERT_ID 0x1 /* an id outside [0, E) reached a kernel */
 #define MOE_STATUS_WAIT_TIMEOUT 0x2  /* a pipeline wait gave up; outputs are invalid */
+#define MOE_STATUS_OUT_OF_BOUNDS 0x4 /* checked build only: an index a kernel formed fell outside its
+                                        buffer; that access was skipped, outputs are invalid */
 
 /* ---- activation element types ---- */
 #define MOE_DTYPE_F32 0
@@ -589,6 +591,16 @@ int moe_ffn_layer_decode_static(const float* x, int T, int D, int F, int E, int 
                                 const uint8_t* u_sc, const float* bu, const uint8_t* d_qs,
                                 const uint8_t* d_sc, const float* bd, float* y, int32_t* ids_out,
                                 float* weights_out, cudaStream_t stream);
+
+/*
+ * moe_checked_build -- 1 if this library was compiled with MOE_CHECKED
+ * (libmoe_mxfp4_checked.so: the kernels check the indices they form from
+ * routing, bucket and segment data against their buffers before each global
+ * access or bulk copy and set MOE_STATUS_OUT_OF_BOUNDS instead of touching
+ * memory outside them; a skipped copy still completes its pipeline stage, so
+ * nothing waits on it), 0 for the regular build. Same ABI in both.
+ */
+int moe_checked_build(void);
 
 /*
  * moe_get_status -- waits for `stream`, then reads and clears the calling

@@ -13,7 +13,9 @@ import os
 import re
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libmoe_mxfp4.so")
+# MOE_MXFP4_CHECKED=1 loads the checked build (libmoe_mxfp4_checked.so: device-side bounds checks)
+LIB_PATH = os.path.join(HERE, "libmoe_mxfp4_checked.so" if os.environ.get("MOE_MXFP4_CHECKED") == "1"
+                        else "libmoe_mxfp4.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "moe_mxfp4.h")
 
 if not os.path.exists(LIB_PATH):
@@ -32,6 +34,7 @@ MOE_ESCRATCH = -4
 MOE_DECODE_SCRATCH_BYTES = 512 * 1024
 MOE_STATUS_BAD_EXPERT_ID = 0x1
 MOE_STATUS_WAIT_TIMEOUT = 0x2
+MOE_STATUS_OUT_OF_BOUNDS = 0x4
 MOE_DTYPE_F32 = 0
 MOE_DTYPE_BF16 = 1
 MOE_EPI_STORE_BF16 = 0
@@ -86,6 +89,7 @@ _SIGS = {
     "moe_ffn_layer_packed": (I, [P, P, I, I, P, SZ, P, P, P, P, P]),
     "moe_ffn_layer_packed_hostio": (I, [P, I, I, P, SZ, P, P, P]),
     "moe_ffn_layer_packed_stage": (I, [P, P, I, P, SZ, I, P, P, P, P, P]),
+    "moe_checked_build": (I, []),
     "moe_get_status": (I, [P, ctypes.POINTER(ctypes.c_int)]),
     "moe_get_timeout_site": (I, [P, ctypes.POINTER(ctypes.c_int)]),
     "moe_last_cuda_error": (I, []),
@@ -316,6 +320,10 @@ def moe_ffn_layer_packed_hostio(layer, T, rail, workspace, workspace_bytes, x_ho
     return _lib.moe_ffn_layer_packed_hostio(None if layer is None else ctypes.byref(layer), T, rail,
                                             _ptr(workspace), workspace_bytes, _ptr(x_host), _ptr(y_host),
                                             _stream(stream))
+
+
+def moe_checked_build():
+    return _lib.moe_checked_build()
 
 
 def moe_get_status(stream=None):

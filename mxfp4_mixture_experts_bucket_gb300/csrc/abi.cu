@@ -496,6 +496,7 @@ int moe_mxfp4_grouped_mm(const uint8_t* w_qs, const uint8_t* w_sc, const float* 
   g.limit = limit;
   g.out = out;
   g.out_ld = out_ld;
+  g.out_rows = epilogue == MOE_EPI_SCATTER_WEIGHTED ? 0 : max_rows;  // the scatter's token count is not passed
   g.status = d->status;
   Launch L{stream, false};
   return cuda_status(launch_grouped_mm(g, L));
@@ -698,6 +699,7 @@ int ffn_layer_impl(const float* x, float* x_copy, int T, int D, int F, int E, in
   g.limit = limit;
   g.out = ws.hg;
   g.out_ld = F;
+  g.out_rows = (int64_t)ws.max_rows;
   g.status = d->status;
   g.rs = gu_rs;
   rc = cuda_status(launch_grouped_mm(g, L));
@@ -718,6 +720,7 @@ int ffn_layer_impl(const float* x, float* x_copy, int T, int D, int F, int E, in
   gd.epilogue = MOE_EPI_SCATTER_WEIGHTED;
   gd.out = y;
   gd.out_ld = D;
+  gd.out_rows = T;
   return cuda_status(launch_grouped_mm(gd, L));
 }
 
@@ -869,7 +872,7 @@ int packed_prefill_impl(const moe_packed_layer_t& P, const float* x, int T, void
                                       ws.inv, d->status, L))) != MOE_OK)
     return rc;
   if ((rc = cuda_status(launch_quant_rows_e2m1(x, T, P.D, P.k, ws.rows, ws.inv, ws.counts, ws.basep, P.E, (int)ws.max_rows, ws.aq,
-                                               ws.asf, nullptr, ws.segs, ws.ctr, L))) != MOE_OK)
+                                               ws.asf, nullptr, ws.segs, ws.ctr, d->status, L))) != MOE_OK)
     return rc;
   GroupedMX4Args g{};
   g.kind = 0;
@@ -908,7 +911,7 @@ int packed_prefill_impl(const moe_packed_layer_t& P, const float* x, int T, void
   gd.R = P.D;
   gd.C = P.F;
   if ((rc = cuda_status(launch_quant_h_e2m1(ws.hf, P.F, ws.rows, ws.counts, ws.basep, P.E, (int)ws.max_rows, ws.hq,
-                                            ws.hsf, L))) != MOE_OK)
+                                            ws.hsf, d->status, L))) != MOE_OK)
     return rc;
   gd.ctr = ws.ctr + 1;
   gd.aq = ws.hq;
@@ -1058,6 +1061,14 @@ int moe_ffn_layer_packed_hostio(const moe_packed_layer_t* layer, int T, int rail
                                    stream);
   if (rc != MOE_OK) return rc;
   return cuda_status(cudaMemcpyAsync(y_host, ys, bytes, cudaMemcpyDeviceToHost, stream));
+}
+
+int moe_checked_build(void) {
+#ifdef MOE_CHECKED
+  return 1;
+#else
+  return 0;
+#endif
 }
 
 int moe_get_status(cudaStream_t stream, int* status) {

@@ -429,7 +429,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_expert_kernel(const Dec
           const uint32_t fb = tc::smem_u32(&full_bar[s]);
           uint8_t* stage = ring + (size_t)s * A.stage_bytes;
           const size_t row0 = (size_t)e * R + st.r0;
-          if (KIND == 0 && A.rs == 2) {
+          if (!MOE_IN_BOUNDS(A.status, e >= 0 && e < E && st.r0 >= 0 && st.nr >= 1 && st.r0 + st.nr <= R)) {
+            tc::mbar_expect_tx(fb, 0);  // the stage completes without data
+          } else if (KIND == 0 && A.rs == 2) {
             // interleaved gate/up: the sub-task's gate and up rows are one run of 2*nr rows,
             // one copy for the nibbles and one for the scale window
             const size_t sc0 = 2 * row0 * nb, sc1 = sc0 + 2 * (size_t)st.nr * nb;
@@ -502,7 +504,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_expert_kernel(const Dec
     // biases of the sub-task's rows, in flight during the products
     float bias0 = 0.f, bias1 = 0.f;
     const int rsv = (KIND == 0) ? A.rs : 1;
-    if (lane < st.nr) {
+    if (lane < st.nr && MOE_IN_BOUNDS(A.status, e >= 0 && e < E)) {
       const size_t ro = ((size_t)e * R + st.r0 + lane) * rsv;
       if (A.bias[0]) bias0 = __ldg(A.bias[0] + ro);
       if (KIND == 0 && A.bias[1]) bias1 = __ldg(A.bias[1] + ro);
@@ -529,7 +531,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_expert_kernel(const Dec
       const uint8_t* sb = sa + (KIND == 0 ? s_ms : 0u);
       // biases of the rows the leader's lanes finish: row lane % 8
       float lb0 = 0.f, lb1 = 0.f;
-      if ((lane & 7) < st.nr) {
+      if ((lane & 7) < st.nr && MOE_IN_BOUNDS(A.status, e >= 0 && e < E)) {
         const size_t ro = ((size_t)e * R + st.r0 + (lane & 7)) * rsv;
         if (A.bias[0]) lb0 = __ldg(A.bias[0] + ro);
         if (KIND == 0 && A.bias[1]) lb1 = __ldg(A.bias[1] + ro);
@@ -581,10 +583,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_expert_kernel(const Dec
               v0 += s_part[buf][c0 + w2][16 * jj + 2 * r];
               v1 += s_part[buf][c0 + w2][16 * jj + 2 * r + 1];
             }
-            if (KIND == 0)
+            if (!MOE_IN_BOUNDS(A.status, a >= 0 && a < TK && st.r0 + r < R)) {
+            } else if (KIND == 0) {
               A.out[(size_t)a * R + st.r0 + r] = swiglu_oai_f(v0 + lb0, v1 + lb1, A.alpha, A.limit);
-            else
+            } else {
               so[a * kDecRows + r] = v0 + lb0;
+            }
           }
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(tc::smem_u32(&xfree_bar[team][buf]));
@@ -637,11 +641,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_expert_kernel(const Dec
               g += s_part[buf][c0 + w2][lane];
               u += s_part[buf][c0 + w2][kDecRows + lane];
             }
-            A.out[(size_t)a * R + st.r0 + lane] = swiglu_oai_f(g + bias0, u + bias1, A.alpha, A.limit);
+            if (MOE_IN_BOUNDS(A.status, a >= 0 && a < TK && st.r0 + lane < R))
+              A.out[(size_t)a * R + st.r0 + lane] = swiglu_oai_f(g + bias0, u + bias1, A.alpha, A.limit);
           } else {
             float d = 0.f;
             for (int w2 = 0; w2 < tw; ++w2) d += s_part[buf][c0 + w2][lane];
-            so[a * kDecRows + lane] = d + bias0;
+            if (MOE_IN_BOUNDS(A.status, a >= 0 && a < TK)) so[a * kDecRows + lane] = d + bias0;
           }
         }
         __syncwarp();
@@ -665,7 +670,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_expert_kernel(const Dec
           if (ej < 0 || ej >= E) continue;
           yv = fmaf(Rt.w[a], so[a * kDecRows + r], yv);
         }
-        A.out[(size_t)t * R + st.r0 + r] = yv;
+        if (MOE_IN_BOUNDS(A.status, st.r0 + r < R)) A.out[(size_t)t * R + st.r0 + r] = yv;
       }
     }
   }

@@ -60,6 +60,7 @@ struct Params {
   float alpha, limit;
   void* out;
   int64_t out_ld;
+  int64_t out_rows;  // rows of out, 0 if unknown (bounds checks of the checked build)
   int* status;
   int box_rows;  // rows of one weight TMA box: min(BM, R)
   int wrs;       // weight row stride in rows: 1, or 2 for gate/up rows interleaved in one plane
@@ -422,13 +423,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float g = __uint_as_float(v0[i]);
               if (EPI == MOE_EPI_SCATTER_WEIGHTED_ID) {
                 const int a = s_rows[n];
-                float* dst = static_cast<float*>(p.out) + (size_t)(a / p.k) * p.out_ld + f;
-                atomicAdd(dst, s_w[n] * g);
+                if (MOE_IN_BOUNDS(p.status, a >= 0 && (p.out_rows == 0 || a / p.k < p.out_rows))) {
+                  float* dst = static_cast<float*>(p.out) + (size_t)(a / p.k) * p.out_ld + f;
+                  atomicAdd(dst, s_w[n] * g);
+                }
               } else {
                 float v = g;
                 if (EPI == MOE_EPI_SWIGLU_BF16_ID) v = swiglu_oai_f(g, __uint_as_float(v1[i]), p.alpha, p.limit);
-                static_cast<__nv_bfloat16*>(p.out)[(size_t)(tile_row0 + n) * p.out_ld + f] =
-                    __float2bfloat16_rn(v);
+                if (MOE_IN_BOUNDS(p.status, p.out_rows == 0 || tile_row0 + n < p.out_rows))
+                  static_cast<__nv_bfloat16*>(p.out)[(size_t)(tile_row0 + n) * p.out_ld + f] =
+                      __float2bfloat16_rn(v);
               }
             }
           }
@@ -575,6 +579,7 @@ cudaError_t launch_grouped_mm(const GroupedMMArgs& g, Launch L) {
   prm.limit = g.limit;
   prm.out = g.out;
   prm.out_ld = g.out_ld;
+  prm.out_rows = g.out_rows;
   prm.status = g.status;
   prm.box_rows = box_rows;
   if (g.nmat == 2) {

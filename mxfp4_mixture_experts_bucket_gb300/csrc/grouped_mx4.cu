@@ -380,22 +380,27 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
             const size_t achunk = (size_t)u.b * NK + j;
             const uint8_t* src = p.aq + achunk * (size_t)(kTerms * kTermBytes) + (size_t)u.g.base * 64;
             const uint32_t abytes = (uint32_t)used_atoms<kTerms>(u.g.rn) * kAtom;
-            tc::mbar_expect_tx(fb, (uint32_t)kTerms * run + abytes);
-            for (int t = 0; t < kTerms; ++t)
-              tc::bulk_load(sb + kOffAct + (uint32_t)t * run, src + (size_t)t * kTermBytes, run, fb);
-            tc::bulk_load(sb + kOffSfa, p.asf + (achunk * 2 + u.s) * (kTerms * kAtom), abytes, fb);
+            if (!MOE_IN_BOUNDS(p.status, u.b >= 0 && u.b < p.ntiles && u.g.base + u.g.rn <= 128)) {
+              tc::mbar_expect_tx(fb, 0);  // the stage completes without this part
+            } else {
+              tc::mbar_expect_tx(fb, (uint32_t)kTerms * run + abytes);
+              for (int t = 0; t < kTerms; ++t)
+                tc::bulk_load(sb + kOffAct + (uint32_t)t * run, src + (size_t)t * kTermBytes, run, fb);
+              tc::bulk_load(sb + kOffSfa, p.asf + (achunk * 2 + u.s) * (kTerms * kAtom), abytes, fb);
+            }
           } else {
             // a tile shorter than 128 rows leaves the rest stale: those rows only feed
             // accumulator lanes nobody reads
+            const bool wok = MOE_IN_BOUNDS(p.status, u.e >= 0 && u.e < p.E && wtile(u, 0) < p.NT);
             uint32_t bytes = 0;
             for (int h = 0; h < 2; ++h) {
               const int tile = wtile(u, h);
-              if (tile >= 0) bytes += (uint32_t)(min(128, p.R - 128 * tile) * 64) + kAtom;
+              if (tile >= 0 && wok) bytes += (uint32_t)(min(128, p.R - 128 * tile) * 64) + kAtom;
             }
             tc::mbar_expect_tx(fb, bytes);
             for (int h = 0; h < 2; ++h) {
               const int tile = wtile(u, h);
-              if (tile < 0) continue;
+              if (tile < 0 || !wok) continue;
               const int rows_t = min(128, p.R - 128 * tile);
               const uint8_t* src = p.w_qs[KIND == 0 ? h : 0] +
                                    ((size_t)u.e * p.R + 128 * (size_t)tile) * ((size_t)NK * 64) + (size_t)rows_t * 64 * j;
@@ -497,10 +502,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
         float bv = 0.f;
         if (KIND == 0) {
           const int h2 = et >> 7, f = 128 * ue.t + (et & 127);
-          if (p.bias[h2] && f < p.R) bv = __ldg(p.bias[h2] + (size_t)e * p.R + f);
+          if (p.bias[h2] && f < p.R && MOE_IN_BOUNDS(p.status, e >= 0 && e < p.E)) bv = __ldg(p.bias[h2] + (size_t)e * p.R + f);
         } else {
           const int col = 256 * ue.t + et;
-          if (p.bias[0] && col < p.R) bv = __ldg(p.bias[0] + (size_t)e * p.R + col);
+          if (p.bias[0] && col < p.R && MOE_IN_BOUNDS(p.status, e >= 0 && e < p.E)) bv = __ldg(p.bias[0] + (size_t)e * p.R + col);
           if (et < kSegMax) {
             const int a = et < g.rows ? __ldg(p.rows + 128 * ue.b + g.base + et) : -1;
             s_tok[et] = a >= 0 ? a / p.k : -1;
@@ -546,7 +551,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
             const int r = 16 * c + k;
-            if (fvalid && r < g.rows) hrow[(size_t)r * p.R] = hv[ci][k];
+            if (fvalid && r < g.rows && MOE_IN_BOUNDS(p.status, 128 * ue.b + g.base + r < 128 * p.ntiles))
+              hrow[(size_t)r * p.R] = hv[ci][k];
           }
         }
       } else {
@@ -580,7 +586,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_mx4_kernel(const Params p
             for (int k = 0; k < 16; ++k) {
               const int r = 16 * c + k;
               const int tok = r < g.rows ? s_tok[r] : -1;
-              if (dvalid && tok >= 0) atomicAdd(p.y + (size_t)tok * D + d, s_w[r] * (v[c][k] + bd));
+              if (dvalid && tok >= 0 && MOE_IN_BOUNDS(p.status, (int64_t)tok * D + d < p.ny))
+                atomicAdd(p.y + (size_t)tok * D + d, s_w[r] * (v[c][k] + bd));
             }
           }
         }
@@ -664,7 +671,8 @@ __global__ void __launch_bounds__(256, 3) quant_rows_e2m1_kernel(const float* __
                                                               const int32_t* __restrict__ basep, int E, int NK,
                                                               uint8_t* __restrict__ aq, uint8_t* __restrict__ asf,
                                                               float* __restrict__ y, int2* __restrict__ segs,
-                                                              const int32_t* __restrict__ inv, int* __restrict__ ctr) {
+                                                              const int32_t* __restrict__ inv, int* __restrict__ ctr,
+                                                              int* status) {
   pdl_launch_dependents();
   pdl_wait();
   if (GATHER && blockIdx.x == 0 && threadIdx.x == 32) {  // the GEMMs' unit counters
@@ -744,6 +752,7 @@ __global__ void __launch_bounds__(256, 3) quant_rows_e2m1_kernel(const float* __
       for (int jj = 0; jj < k; ++jj) {
         const int p = __ldg(inv + (size_t)t * k + jj);
         if (p < 0) continue;  // an invalid expert id: the assignment has no bucket row
+        if (!MOE_IN_BOUNDS(status, p < mpad)) continue;
         const int b = p >> 7, rt = p & 127;
         const int live = s_live[b];
         const int s = live > kSegMax ? (rt >> 6) : 0;
@@ -846,23 +855,24 @@ int quant_blocks(int max_rows, int C) {
 
 cudaError_t launch_quant_rows_e2m1(const float* x, int T, int D, int k, const int32_t* rows, const int32_t* inv,
                                    const int32_t* counts, const int32_t* basep, int E, int max_rows, uint8_t* aq,
-                                   uint8_t* asf, float* y, int2* segs, int* ctr, Launch L) {
+                                   uint8_t* asf, float* y, int2* segs, int* ctr, int* status, Launch L) {
   const auto kern = gx4::quant_rows_e2m1_kernel<kPrefillXTerms, true>;
   const int blocks = quant_blocks(2 * max_rows, D);  // a lane pair per item
   if (blocks == 0) return cudaErrorInvalidValue;
   return launch_kernel(kern, dim3(blocks), dim3(256),
                        (size_t)(max_rows / 128) * sizeof(int), L, x, T, D, k, rows, counts, basep, E, (D + 127) / 128, aq,
-                       asf, y, segs, inv, ctr);
+                       asf, y, segs, inv, ctr, status);
 }
 
 cudaError_t launch_quant_h_e2m1(const float* hf, int F, const int32_t* rows, const int32_t* counts,
-                                const int32_t* basep, int E, int max_rows, uint8_t* hq, uint8_t* hsf, Launch L) {
+                                const int32_t* basep, int E, int max_rows, uint8_t* hq, uint8_t* hsf, int* status,
+                                Launch L) {
   const auto kern = gx4::quant_rows_e2m1_kernel<kPrefillHTerms, false>;
   const int blocks = quant_blocks(2 * max_rows, F);  // a lane pair per item
   if (blocks == 0) return cudaErrorInvalidValue;
   return launch_kernel(kern, dim3(blocks), dim3(256),
                        (size_t)(max_rows / 128) * sizeof(int), L, hf, 0, F, 1, rows, counts, basep, E, (F + 127) / 128, hq,
-                       hsf, nullptr, nullptr, nullptr, nullptr);
+                       hsf, nullptr, nullptr, nullptr, nullptr, status);
 }
 
 cudaError_t launch_grouped_mx4(const GroupedMX4Args& a, Launch L) {

@@ -14,6 +14,7 @@
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
 
+#include "../../include/moe_mxfp4.h"
 #include "moe_internal.h"
 
 namespace moe {
@@ -24,6 +25,19 @@ namespace moe {
 __device__ __forceinline__ void set_status(int* status, int bits) {
   if (status) atomicOr(status, bits);
 }
+
+// Device-side bounds checks of the checked build (-DMOE_CHECKED): a failed
+// check sets MOE_STATUS_OUT_OF_BOUNDS and the caller skips the access. In the
+// regular build the condition is not evaluated.
+__device__ __forceinline__ bool check_bounds(int* status, bool ok) {
+  if (!ok) set_status(status, MOE_STATUS_OUT_OF_BOUNDS);
+  return ok;
+}
+#ifdef MOE_CHECKED
+#define MOE_IN_BOUNDS(status, cond) (::moe::check_bounds((status), (cond)))
+#else
+#define MOE_IN_BOUNDS(status, cond) true
+#endif
 
 // A bounded wait gave up: set the timeout bit and keep the first site that did
 // (status[1], see moe_get_timeout_site): kernel << 24 | role << 20 |

@@ -185,10 +185,11 @@ size_t prefill_atom_bytes(int max_rows, int C, int terms);
 // unit counters) zeroed
 cudaError_t launch_quant_rows_e2m1(const float* x, int T, int D, int k, const int32_t* rows, const int32_t* inv,
                                    const int32_t* counts, const int32_t* basep, int E, int max_rows, uint8_t* aq,
-                                   uint8_t* asf, float* y, int2* segs, int* ctr, Launch L);
+                                   uint8_t* asf, float* y, int2* segs, int* ctr, int* status, Launch L);
 // h's bucket rows (float [max_rows][F]) as kPrefillHTerms E2M1 terms
 cudaError_t launch_quant_h_e2m1(const float* hf, int F, const int32_t* rows, const int32_t* counts,
-                                const int32_t* basep, int E, int max_rows, uint8_t* hq, uint8_t* hsf, Launch L);
+                                const int32_t* basep, int E, int max_rows, uint8_t* hq, uint8_t* hsf, int* status,
+                                Launch L);
 cudaError_t launch_grouped_mx4(const GroupedMX4Args& a, Launch L);
 
 // ---- grouped_mm.cu ----
@@ -210,6 +211,7 @@ struct GroupedMMArgs {
   float alpha, limit;
   void* out;
   int64_t out_ld;
+  int64_t out_rows = 0;  // rows of out (scatter: tokens; row stores: max_rows), for the checked build; 0: unknown
   int* status;
   int rs = 1;  // nmat 2: 1 = separate planes; 2 = gate/up rows interleaved in one plane (w_qs[1], w_sc[1],
                // bias[1] point one row or one element past w_qs[0], w_sc[0], bias[0])

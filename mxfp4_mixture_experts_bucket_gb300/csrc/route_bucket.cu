@@ -466,8 +466,10 @@ __global__ void __launch_bounds__(kBucketThreads) bucket_kernel(const int32_t* _
     const uint32_t ballot = __ballot_sync(0xffffffffu, match);
     if (match) {
       const int p = p0 + __popc(ballot & ((1u << lane) - 1u));
-      rows[p] = a;
-      inv[a] = p;
+      if (MOE_IN_BOUNDS(status, p < max_rows)) {
+        rows[p] = a;
+        inv[a] = p;
+      }
     }
     p0 += __popc(ballot);
   }
