@@ -51,7 +51,7 @@ MOE_STAGE_PROLOGUE = 1
 MOE_STAGE_GATEUP = 2
 MOE_STAGE_DOWN = 4
 MOE_GEMV_MAX_T = 8
-MOE_AUTO_GEMV_MAX_T = 3
+MOE_AUTO_GEMV_MAX_T = 8
 MOE_AUTO_MX_MAX_T = 320
 MOE_AUTO_DECODE_MX_MAX_T = 2
 MOE_MM_TILE = 128

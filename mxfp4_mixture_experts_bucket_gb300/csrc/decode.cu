@@ -679,8 +679,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_expert_kernel(const Dec
 // ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
-// Shared memory: stages (an equal number per team, 2..4) first, then the split
-// vectors if they still fit, then the down kernel's per-team row results.
+// Shared memory: stages (an equal number per team, 1..4) first, then the split
+// vectors if they still fit (gate/up: with as little as one stage per team),
+// then the down kernel's per-team row results.
 static cudaError_t decode_plan(int KIND, int C, int nvec, int TK, DecodeArgs& A, size_t& smem) {
   constexpr size_t kBudget = 216 * 1024;  // with the kernel's static shared memory, under 227 KB
   const int nb = C >> 5;
@@ -692,7 +693,9 @@ static cudaError_t decode_plan(int KIND, int C, int nvec, int TK, DecodeArgs& A,
   const size_t vec = (size_t)nvec * nb * (128 + 4);
   const size_t so = KIND == 1 ? (size_t)nteams * TK * kDecRows * 4 : 0;
   int spt = 0, staged = 0;
-  for (int s = 4; s >= 2 && !spt; --s)
+  // staged split vectors first (the gate/up kernel's tensor-core path needs them: down to one
+  // stage per team there)
+  for (int s = 4; s >= (KIND == 0 ? 1 : 2) && !spt; --s)
     if ((size_t)nteams * s * stage + vec + so <= kBudget) spt = s, staged = 1;
   for (int s = 4; s >= 2 && !spt; --s)
     if ((size_t)nteams * s * stage + so <= kBudget) spt = s;
