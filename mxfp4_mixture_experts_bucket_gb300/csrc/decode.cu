@@ -1,5 +1,5 @@
-// Decode rail: the fused routed-expert chain for T <= 8 tokens on the CUDA
-// cores, two kernels after the router logits.
+// Decode rail: the fused routed-expert chain for T <= 8 tokens, two kernels
+// after the router logits.
 //
 // Stage 0 (gate/up + bias + swiglu) and stage 1 (down + bias + router-weighted
 // combine in slot order) follow the fused decode expert chain of "dasLLAMA
@@ -15,7 +15,16 @@
 //    into a ring of shared-memory stages; twelve consumer warps form teams of
 //    TW = ceil(C/1024) warps, and each lane of a team owns one 32-column MXFP4
 //    block of the row (16 bytes = one 128-bit shared load per row).
-//  * The input vector's block stays in the lane's registers, split into f16
+//  * Gate/up with the split vectors in shared memory (always at T = 1): each
+//    warp of a team takes a third of the row's blocks and runs the products on
+//    the tensor pipe, mma.sync m16n8k16 with the sub-task's 8 gate and 8 up
+//    rows (decoded to f16 by the hardware conversion) as A and up to four
+//    tokens' high and low f16 parts as the B columns; each block's two k16
+//    products are scaled by the activation and weight block factors and added
+//    in fp32, and the team adds its warps' partials.
+//  * Otherwise (and always in the down kernel, whose 8-row sub-tasks would
+//    leave half of each m16 product unused) the CUDA cores:
+//    the input vector's block stays in the lane's registers, split into f16
 //    high and low parts under a power-of-two block factor. The E2M1 pairs go
 //    through the hardware e2m1x2 -> f16x2 conversion and meet the high part in
 //    mixed-precision f16 x f16 + f32 FMAs (no f16 -> f32 conversions, which run
@@ -693,8 +702,7 @@ static cudaError_t decode_plan(int KIND, int C, int nvec, int TK, DecodeArgs& A,
   const size_t vec = (size_t)nvec * nb * (128 + 4);
   const size_t so = KIND == 1 ? (size_t)nteams * TK * kDecRows * 4 : 0;
   int spt = 0, staged = 0;
-  // staged split vectors first (the gate/up kernel's tensor-core path needs them: down to one
-  // stage per team there)
+  // staged split vectors first (down to one stage per team for gate/up), else per-lane splits
   for (int s = 4; s >= (KIND == 0 ? 1 : 2) && !spt; --s)
     if ((size_t)nteams * s * stage + vec + so <= kBudget) spt = s, staged = 1;
   for (int s = 4; s >= 2 && !spt; --s)

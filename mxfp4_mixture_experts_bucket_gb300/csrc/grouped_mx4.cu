@@ -37,15 +37,19 @@
 // scale atoms into tensor memory with tcgen05.st once its data has landed,
 // then a signal to the MMA thread), 4..5 copy issuers (activations; weights),
 // 6 MMA issuer, 7..14 epilogue (two per lane quarter; warp 7 owns tensor
-// memory). Units are dealt round-robin to the CTAs; every role walks the same
-// unit sequence. The accumulators are freed as soon as the epilogue has read
-// them, so the epilogue's remaining work overlaps the next unit's MMAs.
-//   gate/up epilogue: bias, swiglu_oai of every (feature, row) into registers,
+// memory). Units are handed out dynamically: the activation copy issuer takes
+// each next unit index from a global counter per GEMM and publishes it in a
+// small shared-memory ring that every other role reads in order. The
+// accumulators are freed as soon as the epilogue has read them, so the
+// epilogue's remaining work overlaps the next unit's MMAs.
+//   gate/up epilogue: (first, while the first unit streams: y zeroed for the
+//     down GEMM) bias, swiglu_oai of every (feature, row) into registers,
 //     accumulators freed, then h stored as float rows (32 consecutive
 //     features per warp and row).
-//   down epilogue: y[t] += w_a * (acc + bd) for each row's assignment a (float
-//     atomics over 32 consecutive outputs per warp, as the pages' weighted
-//     scatter).
+//   down epilogue: every 16-row chunk of the accumulator read into registers,
+//     accumulator freed, then y[t] += w_a * (acc + bd) for each row's
+//     assignment a (float atomics over 32 consecutive outputs per warp, as the
+//     pages' weighted scatter).
 #include <cuda.h>
 
 #include "decode_mx.cuh"
